@@ -1,0 +1,208 @@
+"""Plain CPU oracle for the Mamba2 recurrent path -- TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package. The CUDA product path never calls it and
+shares no code with it (``mamba2_ref.c`` has its own validation, rounding and
+arithmetic).
+
+The C source follows gllm PR #85 "feat(backend): Mamba2 ops, with CPU
+reference implementations", sections "Ops" and "CPU reference": each op is the
+token-at-a-time definition in double with the SSM state rounded to fp32 after
+every token. This module only marshals torch CPU tensors into the C library
+(built on demand with gcc) and turns status codes into exceptions.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import tempfile
+import threading
+from pathlib import Path
+
+import torch
+
+_HERE = Path(__file__).resolve().parent
+_SRC = _HERE / "mamba2_ref.c"
+_HDR = _HERE / "mamba2_ref.h"
+_LIB = _HERE / "libmamba2_ref.so"
+
+F32, BF16 = 0, 1
+OK, ERR_INVALID_ARGUMENT, ERR_SLOT_OUT_OF_RANGE, ERR_SLOT_SHARED, ERR_RUNS_DONT_COVER_ROWS = range(5)
+STATUS_NAMES = {
+    OK: "OK",
+    ERR_INVALID_ARGUMENT: "INVALID_ARGUMENT",
+    ERR_SLOT_OUT_OF_RANGE: "SLOT_OUT_OF_RANGE",
+    ERR_SLOT_SHARED: "SLOT_SHARED",
+    ERR_RUNS_DONT_COVER_ROWS: "RUNS_DONT_COVER_ROWS",
+}
+
+_lock = threading.Lock()
+_lib = None
+
+
+class OracleError(RuntimeError):
+    """A non-OK status from the oracle; ``.status`` holds the code."""
+
+    def __init__(self, status: int, op: str):
+        super().__init__(f"oracle {op}: {STATUS_NAMES.get(status, status)}")
+        self.status = status
+
+
+def build(force: bool = False) -> Path:
+    """Compile ``libmamba2_ref.so`` with gcc (OpenMP, no FP contraction)."""
+    newest = max(_SRC.stat().st_mtime, _HDR.stat().st_mtime)
+    if not force and _LIB.exists() and _LIB.stat().st_mtime >= newest:
+        return _LIB
+    fd, tmp = tempfile.mkstemp(suffix=".so", dir=str(_HERE))
+    os.close(fd)
+    cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fopenmp",
+           "-ffp-contract=off", "-fno-fast-math", str(_SRC), "-o", tmp, "-lm"]
+    try:
+        subprocess.run(cmd, check=True, capture_output=True, text=True)
+        os.replace(tmp, _LIB)
+    except subprocess.CalledProcessError as e:  # pragma: no cover
+        os.unlink(tmp)
+        raise RuntimeError(f"oracle build failed:\n{e.stderr}") from e
+    return _LIB
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(str(build()))
+            i32, p, f32 = ctypes.c_int32, ctypes.c_void_p, ctypes.c_float
+            lib.mamba2_ref_validate_batch.argtypes = [i32, p, p, i32, i32]
+            lib.mamba2_ref_causal_conv1d.argtypes = [p, p, p, p, p, i32, i32, i32, i32, i32, i32, p, p, p, p]
+            lib.mamba2_ref_ssd_scan.argtypes = [p, p, p, p, p, p, p, i32, i32, i32, i32, i32, i32, i32, i32, p, p, p, p]
+            lib.mamba2_ref_gated_rmsnorm.argtypes = [p, p, p, p, i32, i32, i32, f32, i32, p]
+            lib.mamba2_ref_decode_step.argtypes = [p, p, p, p, p, p, p, p, p, p, i32, f32, p, p,
+                                                  i32, i32, i32, i32, i32, i32, i32, i32, p, p]
+            lib.mamba2_ref_state_bytes_per_layer.argtypes = [i32] * 6
+            lib.mamba2_ref_state_bytes_per_layer.restype = ctypes.c_int64
+            lib.mamba2_ref_num_threads.restype = ctypes.c_int
+            lib.mamba2_ref_set_num_threads.argtypes = [ctypes.c_int]
+            _lib = lib
+    return _lib
+
+
+# --------------------------------------------------------------------------
+# marshalling helpers
+# --------------------------------------------------------------------------
+
+def _act_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.float32:
+        return F32
+    if t.dtype == torch.bfloat16:
+        return BF16
+    raise TypeError(f"activation dtype {t.dtype} not supported")
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    assert t.device.type == "cpu" and t.is_contiguous(), "oracle wants contiguous CPU tensors"
+    return ctypes.c_void_p(t.data_ptr()) if t.numel() else ctypes.c_void_p(0)
+
+
+def _i32(seq) -> torch.Tensor:
+    return torch.as_tensor(seq, dtype=torch.int32).contiguous()
+
+
+def _u8(seq) -> torch.Tensor:
+    return torch.as_tensor(seq, dtype=torch.uint8).contiguous()
+
+
+def _check(status: int, op: str):
+    if status != OK:
+        raise OracleError(status, op)
+
+
+def num_threads() -> int:
+    return int(_load().mamba2_ref_num_threads())
+
+
+def set_num_threads(n: int) -> None:
+    _load().mamba2_ref_set_num_threads(int(n))
+
+
+# --------------------------------------------------------------------------
+# ops
+# --------------------------------------------------------------------------
+
+def validate_batch(cu_seqlens, slots, num_slots: int, rows: int) -> int:
+    """Status of a RecurrentBatch (range, then shared, then coverage)."""
+    slots_t = _i32(slots)
+    cu = _i32(cu_seqlens)
+    n = slots_t.numel()
+    return int(_load().mamba2_ref_validate_batch(n, _ptr(cu), _ptr(slots_t), num_slots, rows))
+
+
+def causal_conv1d(x, weight, bias, conv_state, cu_seqlens, slots, fresh):
+    """Depthwise causal conv + SiLU per run; ``conv_state`` updated in place.
+
+    Returns ``(dst, dst_f64)``: the act-typed output and its unrounded values.
+    """
+    rows, conv_dim = x.shape
+    kernel = weight.shape[1]
+    dst = torch.empty_like(x)
+    dst64 = torch.empty(x.shape, dtype=torch.float64)
+    cu, sl, fr = _i32(cu_seqlens), _i32(slots), _u8(fresh)
+    st = _load().mamba2_ref_causal_conv1d(
+        _ptr(dst), _ptr(x), _ptr(weight), _ptr(bias), _ptr(conv_state),
+        conv_state.shape[0], rows, conv_dim, kernel, _act_code(x), sl.numel(),
+        _ptr(cu), _ptr(sl), _ptr(fr), _ptr(dst64))
+    _check(st, "causal_conv1d")
+    return dst, dst64
+
+
+def ssd_scan(xbc, dt, A_log, dt_bias, D, ssm_state, dims, cu_seqlens, slots, fresh):
+    """Token-at-a-time selective scan; ``ssm_state`` updated in place.
+
+    ``dims`` = (heads, headdim, d_state, ngroups). Returns ``(y, y_f64)``.
+    """
+    H, P, N, G = dims
+    rows = xbc.shape[0]
+    dst = torch.empty((rows, H * P), dtype=xbc.dtype)
+    dst64 = torch.empty((rows, H * P), dtype=torch.float64)
+    cu, sl, fr = _i32(cu_seqlens), _i32(slots), _u8(fresh)
+    st = _load().mamba2_ref_ssd_scan(
+        _ptr(dst), _ptr(xbc), _ptr(dt), _ptr(A_log), _ptr(dt_bias), _ptr(D), _ptr(ssm_state),
+        ssm_state.shape[0], rows, H, P, N, G, _act_code(xbc), sl.numel(),
+        _ptr(cu), _ptr(sl), _ptr(fr), _ptr(dst64))
+    _check(st, "ssd_scan")
+    return dst, dst64
+
+
+def gated_rmsnorm(x, z, weight, groups: int, eps: float):
+    """rmsnorm(x * silu(z)) * weight per group. Returns ``(out, out_f64)``."""
+    rows, dim = x.shape
+    dst = torch.empty_like(x)
+    dst64 = torch.empty(x.shape, dtype=torch.float64)
+    st = _load().mamba2_ref_gated_rmsnorm(
+        _ptr(dst), _ptr(x), _ptr(z), _ptr(weight), rows, dim, groups, float(eps),
+        _act_code(x), _ptr(dst64))
+    _check(st, "gated_rmsnorm")
+    return dst, dst64
+
+
+def decode_step(xBC, z, dt, conv_w, conv_b, A_log, dt_bias, D, norm_w, norm_groups, eps,
+                conv_state, ssm_state, dims, slots, fresh):
+    """One token per sequence through conv -> scan -> norm; states in place."""
+    H, P, N, G = dims
+    n = xBC.shape[0]
+    dst = torch.empty((n, H * P), dtype=xBC.dtype)
+    sl, fr = _i32(slots), _u8(fresh)
+    st = _load().mamba2_ref_decode_step(
+        _ptr(dst), _ptr(xBC), _ptr(z), _ptr(dt), _ptr(conv_w), _ptr(conv_b), _ptr(A_log),
+        _ptr(dt_bias), _ptr(D), _ptr(norm_w), norm_groups, float(eps), _ptr(conv_state),
+        _ptr(ssm_state), ssm_state.shape[0], H, P, N, G, conv_w.shape[1], _act_code(xBC),
+        sl.numel(), _ptr(sl), _ptr(fr))
+    _check(st, "decode_step")
+    return dst
+
+
+def state_bytes_per_layer(heads, headdim, d_state, ngroups, conv_kernel, conv_act=BF16) -> int:
+    return int(_load().mamba2_ref_state_bytes_per_layer(heads, headdim, d_state, ngroups,
+                                                        conv_kernel, conv_act))
