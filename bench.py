@@ -1,0 +1,445 @@
+"""Benchmark of the Mamba2 recurrent hot path on GB300.
+
+One step = the long-prefill-with-continuation workload: one packed prefill of
+65 536 tokens (conv -> chunked scan -> gated norm, 48 heads x 64, d_state 128,
+bf16, fresh slot) followed by 64 one-token decode steps on the resulting state.
+``value`` is prefill tokens/s; the batched decode workload (256 sequences x 128
+steps against a 512-slot pool) is timed in the same run and reported under
+``decode``. Inputs are seeded synthetic tensors with the workload's
+distributions, resident in HBM before the timed region and larger than L2.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun every rank runs its own independent replica (weak scaling);
+the reported time is the maximum over ranks. ``--impl reference`` times the
+CPU oracle on the host cores (rank 0 only) on a bounded sample of the same
+workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+from pathlib import Path
+
+import torch
+
+ROOT = Path(__file__).resolve().parent
+sys.path.insert(0, str(ROOT))
+
+import workloads as W  # noqa: E402
+
+METRIC = "Mamba2 layer prefill tokens/s + decode step us; % of HBM/tensor roofline"
+WORKLOAD = "long prefill 1x65536 tok + 64 decode steps, 48 heads x 64, d_state 128, 1 group, conv 4, bf16"
+TOKENS = 65536
+DECODE_TAIL = 64
+
+
+def peaks():
+    f = ROOT / "MEASURED_PEAKS.json"
+    if f.exists():
+        d = json.loads(f.read_text())
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), float(d["bf16_tflops_sustained"]), "measured"
+    return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+# --------------------------------------------------------------------------
+# algorithmic bytes / flops per launch (bf16 activations, fp32 state)
+# --------------------------------------------------------------------------
+
+def conv_bytes(T, d: W.Dims, act_b=2):
+    return 2 * T * d.conv_dim * act_b
+
+
+def scan_bytes(T, d: W.Dims, act_b=2, state_rw=1):
+    return T * (d.conv_dim + d.heads + d.d_inner) * act_b + state_rw * d.heads * d.headdim * d.d_state * 4
+
+
+def scan_flops(T, d: W.Dims, Q=64):
+    per_tok = d.heads * 2 * (Q * d.headdim + 2 * d.headdim * d.d_state) + 2 * d.ngroups * Q * d.d_state
+    return T * per_tok
+
+
+def norm_bytes(T, d: W.Dims, act_b=2):
+    return 3 * T * d.d_inner * act_b
+
+
+def decode_bytes_per_seq(d: W.Dims, act_b=2):
+    return (2 * d.heads * d.headdim * d.d_state * 4 + 2 * (d.conv_kernel - 1) * d.conv_dim * act_b
+            + d.conv_dim * act_b + 2 * d.d_inner * act_b + d.heads * act_b)
+
+
+# --------------------------------------------------------------------------
+# clocks sampled during the timed region
+# --------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=self.fh, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.fh.close()
+
+    def summary(self):
+        if self.proc is None or not self.path:
+            return None
+        rows = []
+        for line in Path(self.path).read_text().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((float(parts[1]), float(parts[2]), parts[5:9]))
+            except ValueError:
+                continue
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i, v in enumerate(r[2]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": reasons, "samples": len(rows)}
+
+
+# --------------------------------------------------------------------------
+# our arm
+# --------------------------------------------------------------------------
+
+class Prefill:
+    """Device-resident long-prefill workload and its op sequence."""
+
+    def __init__(self, wl: W.Workload, dev):
+        import selective_scan_gb300 as ss
+        self.ss = ss
+        self.wl = wl
+        p, d, b = wl.params, wl.dims, wl.batch
+        self.dev = dev
+        self.x = wl.xBC.to(dev)
+        self.z = wl.z.to(dev)
+        self.dt = wl.dt.to(dev)
+        self.pw = [t.to(dev) for t in (p.conv_w, p.conv_b, p.A_log, p.dt_bias, p.D, p.norm_w)]
+        self.conv = wl.conv_state.to(dev)
+        self.ssm = wl.ssm_state.to(dev)
+        self.xbc = torch.empty_like(self.x)
+        self.y = torch.empty((b.rows, d.d_inner), dtype=wl.act, device=dev)
+        self.out = torch.empty_like(self.y)
+        need = ss.ssd_scan_workspace_bytes(d, b.rows, b.cu_seqlens, b.slots, b.fresh)
+        self.ws = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+        self.scan_launches = 2 if need > 0 else 1
+        self.dec_x = wl.dec_xBC.to(dev)
+        self.dec_z = wl.dec_z.to(dev)
+        self.dec_dt = wl.dec_dt.to(dev)
+        self.dec_out = torch.empty((1, d.d_inner), dtype=wl.act, device=dev)
+
+    def prefill(self, x=None, z=None, dt=None, out=None, ev=None):
+        ss, wl = self.ss, self.wl
+        p, d, b = wl.params, wl.dims, wl.batch
+        cw, cb, A, dtb, D, nw = self.pw
+        x = self.x if x is None else x
+        z = self.z if z is None else z
+        dt = self.dt if dt is None else dt
+        out = self.out if out is None else out
+        if ev:
+            ev[0].record()
+        ss.causal_conv1d(self.xbc, x, cw, cb, self.conv, b.cu_seqlens, b.slots, b.fresh)
+        if ev:
+            ev[1].record()
+        ss.ssd_scan(self.y, self.xbc, dt, A, dtb, D, self.ssm, d, b.cu_seqlens, b.slots, b.fresh,
+                    workspace=self.ws)
+        if ev:
+            ev[2].record()
+        ss.gated_rmsnorm(out, self.y, z, nw, p.norm_groups, p.eps)
+        if ev:
+            ev[3].record()
+
+    def decode_tail(self, ev=None):
+        ss, wl = self.ss, self.wl
+        p, d = wl.params, wl.dims
+        cw, cb, A, dtb, D, nw = self.pw
+        for t in range(self.dec_x.shape[0]):
+            ss.decode_step(self.dec_out, self.dec_x[t], self.dec_z[t], self.dec_dt[t], cw, cb, A, dtb, D, nw,
+                           p.norm_groups, p.eps, self.conv, self.ssm, d, [0], [0])
+        if ev:
+            ev.record()
+
+
+def time_decode_batch(dev, reps, warm):
+    """256 sequences x 128 carried steps; returns (us/step, events-based)."""
+    import selective_scan_gb300 as ss
+    wl = W.decode_batch()
+    p, d, b = wl.params, wl.dims, wl.batch
+    pw = [t.to(dev) for t in (p.conv_w, p.conv_b, p.A_log, p.dt_bias, p.D, p.norm_w)]
+    conv, ssm = wl.conv_state.to(dev), wl.ssm_state.to(dev)
+    xs, zs, dts = wl.dec_xBC.to(dev), wl.dec_z.to(dev), wl.dec_dt.to(dev)
+    out = torch.empty((b.num_seqs, d.d_inner), dtype=wl.act, device=dev)
+    steps = xs.shape[0]
+
+    def run():
+        for t in range(steps):
+            ss.decode_step(out, xs[t], zs[t], dts[t], *pw, p.norm_groups, p.eps, conv, ssm, d, b.slots, b.fresh)
+
+    for _ in range(warm):
+        run()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        run()
+    e1.record()
+    torch.cuda.synchronize()
+    us = e0.elapsed_time(e1) * 1e3 / (reps * steps)
+    return us, b.num_seqs, decode_bytes_per_seq(d) * b.num_seqs, reps * steps
+
+
+def cpu_baseline(target_s=12.0):
+    """The oracle, as it stands, on a bounded prefix of the same workload."""
+    import oracle
+    oracle.build()
+    cores = oracle.num_threads()
+
+    def run(tokens):
+        wl = W.long_prefill(tokens=tokens, decode_steps=1)
+        p, b, d = wl.params, wl.batch, wl.dims
+        conv, ssm = wl.conv_state.clone(), wl.ssm_state.clone()
+        t0 = time.perf_counter()
+        xbc, _ = oracle.causal_conv1d(wl.xBC, p.conv_w, p.conv_b, conv, b.cu_seqlens, b.slots, b.fresh)
+        y, _ = oracle.ssd_scan(xbc, wl.dt, p.A_log, p.dt_bias, p.D, ssm, d.tuple4(), b.cu_seqlens, b.slots,
+                               b.fresh)
+        oracle.gated_rmsnorm(y, wl.z, p.norm_w, p.norm_groups, p.eps)
+        return time.perf_counter() - t0
+
+    probe = 1024
+    t = run(probe)
+    tokens = int(min(TOKENS, max(probe, (target_s / max(t, 1e-3)) * probe)) // 1024 * 1024)
+    t = run(tokens)
+    return {"value": tokens / t, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"prefill of the first {tokens} of the {TOKENS} tokens (conv -> scan -> norm, "
+                      f"48 heads), {t:.1f} s"}
+
+
+def run_ours(args, rank, world, local_rank):
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    hbm, tf_burst, tf_sus, peak_kind = peaks()
+    wl = W.long_prefill(seed=4 + rank)
+    pf = Prefill(wl, dev)
+    d = wl.dims
+
+    def step(evs=None):
+        pf.prefill(ev=evs[:4] if evs else None)
+        pf.decode_tail(ev=evs[4] if evs else None)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    e_start, e_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local_rank) as clk:
+        torch.cuda.synchronize()
+        e_start.record()
+        for k in range(args.steps):
+            step(evs[k])
+        e_end.record()
+        torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    total_ms = e_start.elapsed_time(e_end)
+    t_conv = sum(e[0].elapsed_time(e[1]) for e in evs) / args.steps
+    t_scan = sum(e[1].elapsed_time(e[2]) for e in evs) / args.steps
+    t_norm = sum(e[2].elapsed_time(e[3]) for e in evs) / args.steps
+    t_tail = sum(e[3].elapsed_time(e[4]) for e in evs) / args.steps
+    t_prefill = t_conv + t_scan + t_norm
+    if world > 1:
+        tt = torch.tensor([total_ms, t_prefill], device=dev)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        total_ms, t_prefill = tt.tolist()
+
+    T = TOKENS
+    gb = lambda nbytes, ms: nbytes / (ms * 1e-3) / 1e9  # noqa: E731
+    kern = {
+        "conv": {"ms": t_conv, "bytes": conv_bytes(T, d), "GB/s": gb(conv_bytes(T, d), t_conv)},
+        "scan": {"ms": t_scan, "bytes": scan_bytes(T, d), "GB/s": gb(scan_bytes(T, d), t_scan),
+                 "TFLOP/s": scan_flops(T, d) / (t_scan * 1e-3) / 1e12, "flops": scan_flops(T, d)},
+        "norm": {"ms": t_norm, "bytes": norm_bytes(T, d), "GB/s": gb(norm_bytes(T, d), t_norm)},
+    }
+    for k in kern.values():
+        k["frac_hbm"] = k["GB/s"] / hbm
+    kern["scan"]["frac_tensor_sustained"] = kern["scan"]["TFLOP/s"] / tf_sus
+    dominant = max(("conv", "scan", "norm"), key=lambda n: kern[n]["ms"])
+    dk = kern[dominant]
+    prof = ROOT / "profiles" / "traffic.json"
+    traffic = None
+    if prof.exists():
+        traffic = json.loads(prof.read_text()).get(dominant)
+
+    # batched decode (256 sequences x 128 steps), timed separately
+    dec_us, dec_n, dec_bytes, dec_steps = time_decode_batch(dev, reps=max(2, args.steps // 100), warm=1)
+    dec_gbs = dec_bytes / (dec_us * 1e-6) / 1e9
+
+    # end to end through the public API: pinned host inputs in, output back, every step
+    hx = torch.empty_like(pf.x, device="cpu").pin_memory()
+    hz = torch.empty_like(pf.z, device="cpu").pin_memory()
+    hdt = torch.empty_like(pf.dt, device="cpu").pin_memory()
+    hx.copy_(wl.xBC)
+    hz.copy_(wl.z)
+    hdt.copy_(wl.dt)
+    hout = torch.empty_like(pf.out, device="cpu").pin_memory()
+    dx, dz, ddt = torch.empty_like(pf.x), torch.empty_like(pf.z), torch.empty_like(pf.dt)
+    e2e_steps = max(3, args.steps // 20)
+
+    def e2e_step():
+        dx.copy_(hx, non_blocking=True)
+        dz.copy_(hz, non_blocking=True)
+        ddt.copy_(hdt, non_blocking=True)
+        pf.prefill(x=dx, z=dz, dt=ddt)
+        hout.copy_(pf.out, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a0.record()
+    for _ in range(e2e_steps):
+        e2e_step()
+    a1.record()
+    torch.cuda.synchronize()
+    e2e_ms = a0.elapsed_time(a1) / e2e_steps
+    if world > 1:
+        tt = torch.tensor([e2e_ms], device=dev)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        e2e_ms = tt.item()
+
+    line = {
+        "metric": METRIC,
+        "value": world * T / (t_prefill * 1e-3),
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": total_ms / args.steps,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) activations, workload distributions)",
+        "config": {"workload": WORKLOAD, "tokens": T, "heads": d.heads, "headdim": d.headdim,
+                   "d_state": d.d_state, "ngroups": d.ngroups, "conv_kernel": d.conv_kernel,
+                   "decode_tail_steps": DECODE_TAIL, "chunk": 64,
+                   "l2": "inputs larger than L2 (no flush)", "parallelism": f"replicas x{world}"},
+        "prefill_ms": t_prefill,
+        "decode_tail_us_per_step": t_tail * 1e3 / DECODE_TAIL,
+        "kernels": kern,
+        "roofline": {"kernel": dominant, "bound": "hbm", "achieved": dk["GB/s"], "peak": hbm, "unit": "GB/s",
+                     "frac": dk["GB/s"] / hbm, "traffic": traffic, "peak_kind": peak_kind},
+        "decode": {"workload": "256 seqs x 1 token, 128 carried steps, 512-slot pool, 48 heads x 64, d_state 128",
+                   "us_per_step": dec_us, "tokens_per_s": dec_n / (dec_us * 1e-6), "GB/s": dec_gbs,
+                   "roofline_frac": dec_gbs / hbm, "roofline_frac_8TBs": dec_gbs / 8000.0,
+                   "bytes_per_step": dec_bytes, "steps_timed": dec_steps},
+        "e2e": {"value": world * T / (e2e_ms * 1e-3), "unit": "tokens/s",
+                "h2d_bytes_per_step": hx.numel() * 2 + hz.numel() * 2 + hdt.numel() * 2,
+                "d2h_bytes_per_step": hout.numel() * 2},
+        "gpu_launches": args.steps * (1 + pf.scan_launches + 1 + DECODE_TAIL),
+        "clocks": clk.summary(),
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline()
+    return line
+
+
+# --------------------------------------------------------------------------
+# reference arm: the oracle on the host cores
+# --------------------------------------------------------------------------
+
+def run_reference(args):
+    import oracle
+    oracle.build()
+    sample = 2048
+    wl = W.long_prefill(tokens=sample, decode_steps=1)
+    p, b, d = wl.params, wl.batch, wl.dims
+
+    def step():
+        conv, ssm = wl.conv_state.clone(), wl.ssm_state.clone()
+        xbc, _ = oracle.causal_conv1d(wl.xBC, p.conv_w, p.conv_b, conv, b.cu_seqlens, b.slots, b.fresh)
+        y, _ = oracle.ssd_scan(xbc, wl.dt, p.A_log, p.dt_bias, p.D, ssm, d.tuple4(), b.cu_seqlens, b.slots,
+                               b.fresh)
+        oracle.gated_rmsnorm(y, wl.z, p.norm_w, p.norm_groups, p.eps)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = (time.perf_counter() - t0) / args.steps
+    v = sample / dt
+    cores = oracle.num_threads()
+    return {
+        "impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "tokens": TOKENS, "sample_tokens_per_step": sample},
+        "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                         "sample": f"prefill of the first {sample} of the {TOKENS} tokens per step"},
+        "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)), flush=True)
+        return
+    if args.warmup < 3:
+        raise SystemExit("--warmup must be >= 3")
+    if world > 1:
+        torch.cuda.set_device(local_rank)
+        torch.distributed.init_process_group("nccl")
+    line = run_ours(args, rank, world, local_rank)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

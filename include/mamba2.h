@@ -1,0 +1,209 @@
+/*
+ * libmamba2 — C ABI of the Mamba2 layer's recurrent hot path on one
+ * NVIDIA GB300 (sm_103a).
+ *
+ * The four operations are the ones gllm PR #85 "feat(backend): Mamba2 ops,
+ * with CPU reference implementations" defines in its section "Ops":
+ * CausalConv1D, SSMScan and GatedRMSNorm, plus one fused decode step that
+ * chains the three for a single token per sequence (the per-token recurrence
+ * over conv and SSM cache state that the page "Granite Mamba2 Inference
+ * Optimization" names as the decode path). The stateful calls take a
+ * RecurrentBatch: per sequence a run of rows, a state slot and a fresh flag.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Device buffers are caller-owned device pointers, row-major and
+ *    contiguous, 16-byte aligned. The library allocates no device memory and
+ *    keeps no state between calls; only `dst`, the named slots of the state
+ *    pools and a caller-provided workspace are written.
+ *  - Batch metadata (mamba2_recurrent_batch) is HOST memory. It is validated
+ *    on the host and passed to the kernels by value in their launch
+ *    parameters, so the host arrays may be reused as soon as the call returns.
+ *  - `stream` is a cudaStream_t (NULL = the legacy default stream). Calls are
+ *    asynchronous and ordered on that stream; the current CUDA device must be
+ *    the one owning the buffers.
+ *  - Activations (`act`) are fp32 or bf16. Conv weight/bias, A_log, dt_bias,
+ *    D and the norm weight are fp32; the SSM state pool is fp32; the conv
+ *    state pool holds activations.
+ *  - Errors: every check runs on the host before anything is enqueued, so a
+ *    non-OK status means no buffer was touched. Checks run in this order:
+ *    arguments, slot range, shared slots, run coverage. MAMBA2_ERR_CUDA
+ *    reports a failed launch (nothing else can fail after validation).
+ *  - A fresh sequence starts from zero state and never reads its slot; its
+ *    slot is written with the sequence's end state.
+ */
+#ifndef MAMBA2_H
+#define MAMBA2_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum mamba2_dtype {
+  MAMBA2_F32 = 0,
+  MAMBA2_BF16 = 1
+} mamba2_dtype;
+
+typedef enum mamba2_status {
+  MAMBA2_OK = 0,
+  MAMBA2_ERR_INVALID_ARGUMENT = 1,     /* null/misaligned pointer, bad size */
+  MAMBA2_ERR_SLOT_OUT_OF_RANGE = 2,    /* slot < 0 or slot >= num_slots */
+  MAMBA2_ERR_SLOT_SHARED = 3,          /* two sequences name one slot */
+  MAMBA2_ERR_RUNS_DONT_COVER_ROWS = 4, /* cu_seqlens not 0..rows, monotone */
+  MAMBA2_ERR_NOT_IMPLEMENTED = 5,      /* shape outside the built kernels */
+  MAMBA2_ERR_CUDA = 6,                 /* a kernel launch failed */
+  MAMBA2_ERR_WORKSPACE_TOO_SMALL = 7   /* scan workspace below the query */
+} mamba2_status;
+
+/* Most sequences one call accepts (the batch travels in launch parameters). */
+#define MAMBA2_MAX_SEQS 1024
+
+/*
+ * RecurrentBatch (gllm PR #85, section "Ops"): sequence i owns packed rows
+ * [cu_seqlens[i], cu_seqlens[i+1]) and state slot slots[i]; fresh[i] != 0
+ * means it starts from zero state and never reads its slot. All arrays are
+ * host memory; num_seqs <= MAMBA2_MAX_SEQS. cu_seqlens must start at 0, be
+ * non-decreasing and end at the call's row count (zero-length runs are
+ * allowed: a fresh one zeroes its slot, a resuming one leaves it unchanged).
+ */
+typedef struct mamba2_recurrent_batch {
+  int32_t num_seqs;
+  const int32_t* cu_seqlens; /* [num_seqs + 1] */
+  const int32_t* slots;      /* [num_seqs] */
+  const uint8_t* fresh;      /* [num_seqs] */
+} mamba2_recurrent_batch;
+
+/* Layer shape: heads x headdim = d_inner; ngroups B/C groups of d_state;
+ * head h reads group h / (heads / ngroups). conv_dim = d_inner +
+ * 2 * ngroups * d_state. */
+typedef struct mamba2_dims {
+  int32_t heads;
+  int32_t headdim;
+  int32_t d_state;
+  int32_t ngroups;
+  int32_t conv_kernel;
+} mamba2_dims;
+
+/*
+ * CausalConv1D (gllm PR #85, section "Ops"): for each sequence, with u its
+ * slot's kernel-1 previous inputs (zeros when fresh) followed by its rows of
+ * x, row t of dst is silu(bias + sum_k weight[:, k] * u[t + k]); the last tap
+ * weight[:, kernel-1] multiplies the current row. Afterwards the slot holds
+ * the last kernel-1 rows of u, oldest first (a bit copy of the inputs).
+ *
+ *   dst        [rows, conv_dim] act      output (must not alias x)
+ *   x          [rows, conv_dim] act      packed inputs (xBC columns)
+ *   weight     [conv_dim, kernel] f32    depthwise taps, oldest first
+ *   bias       [conv_dim] f32
+ *   conv_state [num_slots, kernel-1, conv_dim] act, updated in place
+ *   kernel     1..4; conv_dim * sizeof(act) must be a multiple of 16.
+ */
+mamba2_status mamba2_causal_conv1d(void* dst, const void* x,
+                                   const float* weight, const float* bias,
+                                   void* conv_state, int32_t num_slots,
+                                   int32_t rows, int32_t conv_dim,
+                                   int32_t kernel, mamba2_dtype act,
+                                   const mamba2_recurrent_batch* rb,
+                                   void* stream);
+
+/*
+ * Bytes of device workspace mamba2_ssd_scan needs for this batch on the
+ * current device (0 when none). Query with the same dims, rows and batch as
+ * the scan call. Returns 0 for arguments the scan would reject.
+ */
+size_t mamba2_ssd_scan_workspace_bytes(const mamba2_dims* dims, int32_t rows,
+                                       const mamba2_recurrent_batch* rb);
+
+/*
+ * SSMScan (gllm PR #85, section "Ops"): per sequence and head h (group
+ * g = h / (heads/ngroups)), per row t:
+ *   dt'  = softplus(dt[t, h] + dt_bias[h])          (no dt clamp)
+ *   h    = h * exp(-exp(A_log[h]) * dt') + dt' * B[t, g] (outer) x[t, h]
+ *   y    = h . C[t, g] + D[h] * x[t, h]
+ * seeded from the sequence's slot (zero when fresh) and written back to it.
+ * x, B and C are read from xbc at fixed column offsets: x at h*headdim,
+ * B at d_inner + g*d_state, C at d_inner + ngroups*d_state + g*d_state.
+ * Long runs are computed as a chunked scan on the tensor cores.
+ *
+ *   dst        [rows, heads*headdim] act     y
+ *   xbc        [rows, conv_dim] act          the conv output
+ *   dt         [rows, heads] act
+ *   A_log, dt_bias, D  [heads] f32
+ *   ssm_state  [num_slots, heads, headdim, d_state] f32, updated in place
+ *   workspace  device scratch of at least
+ *              mamba2_ssd_scan_workspace_bytes(...) bytes (may be NULL when
+ *              that is 0); its contents need no initialisation.
+ * Built shapes: any heads/ngroups with headdim x d_state of 16x16 or 64x128
+ * (bf16 or fp32 activations) or any shape up to headdim 1024, d_state 256 on
+ * the token-serial kernel; others return MAMBA2_ERR_NOT_IMPLEMENTED.
+ */
+mamba2_status mamba2_ssd_scan(void* dst, const void* xbc, const void* dt,
+                              const float* A_log, const float* dt_bias,
+                              const float* D, float* ssm_state,
+                              int32_t num_slots, int32_t rows,
+                              const mamba2_dims* dims, mamba2_dtype act,
+                              const mamba2_recurrent_batch* rb,
+                              void* workspace, size_t workspace_bytes,
+                              void* stream);
+
+/*
+ * GatedRMSNorm (gllm PR #85, section "Ops"): per row and per group of
+ * dim/groups consecutive channels, v = x * silu(z) and
+ * dst = v / sqrt(mean(v^2) + eps) * weight (the gate is applied before the
+ * norm). x, z, dst: [rows, dim] act; weight: [dim] f32. dim % groups == 0
+ * and (dim/groups) * sizeof(act) a multiple of 16.
+ */
+mamba2_status mamba2_gated_rmsnorm(void* dst, const void* x, const void* z,
+                                   const float* weight, int32_t rows,
+                                   int32_t dim, int32_t groups, float eps,
+                                   mamba2_dtype act, void* stream);
+
+/*
+ * One decode step: conv -> scan -> gated norm for exactly one new token per
+ * sequence, fused in one kernel, with the same rounding points as the three
+ * ops above (conv output and y rounded to act). Every run length must be 1:
+ * rb->cu_seqlens may be NULL (meaning 0, 1, ..., num_seqs) or must equal
+ * that, else MAMBA2_ERR_INVALID_ARGUMENT.
+ *
+ *   dst   [n, heads*headdim] act     normed output
+ *   xBC   [n, conv_dim] act          the token's conv inputs
+ *   z     [n, heads*headdim] act     gate
+ *   dt    [n, heads] act
+ *   conv_w [conv_dim, conv_kernel], conv_b [conv_dim], A_log/dt_bias/D
+ *   [heads], norm_w [heads*headdim]: f32
+ *   conv_state, ssm_state: the pools, updated in place at rb->slots.
+ */
+mamba2_status mamba2_decode_step(void* dst, const void* xBC, const void* z,
+                                 const void* dt, const float* conv_w,
+                                 const float* conv_b, const float* A_log,
+                                 const float* dt_bias, const float* D,
+                                 const float* norm_w, int32_t norm_groups,
+                                 float eps, void* conv_state, float* ssm_state,
+                                 int32_t num_slots, const mamba2_dims* dims,
+                                 mamba2_dtype act,
+                                 const mamba2_recurrent_batch* rb,
+                                 void* stream);
+
+/*
+ * Bytes of recurrent state one sequence holds in one layer: the fp32 SSM
+ * state plus conv_kernel-1 history rows of conv_dim channels at
+ * conv_state_dtype (InfiniLM PR #575 "feat(mamba2): integrate model loading
+ * and recurrent inference", section "Motivation": about 18.25 MiB per
+ * request for mamba2-130m over its 24 layers). -1 for invalid dims.
+ */
+int64_t mamba2_state_bytes_per_layer(const mamba2_dims* dims,
+                                     mamba2_dtype conv_state_dtype);
+
+/* Static description of a status code. */
+const char* mamba2_status_string(mamba2_status status);
+
+/* Text of the CUDA error behind the calling thread's last MAMBA2_ERR_CUDA. */
+const char* mamba2_last_cuda_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MAMBA2_H */

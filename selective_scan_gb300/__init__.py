@@ -1,0 +1,227 @@
+"""Python binding of libmamba2, the GB300 (sm_103a) Mamba2 recurrent hot path.
+
+Argument marshalling only: every step runs in the CUDA kernels behind the C ABI
+declared in ``include/mamba2.h``. Tensors are torch CUDA tensors (device memory
+and streams come from PyTorch); batch metadata (``cu_seqlens``, ``slots``,
+``fresh``) are host sequences. There is no fallback: importing the package
+without the built library raises.
+
+Entry points (same names as the C ABI without the ``mamba2_`` prefix):
+``causal_conv1d``, ``ssd_scan`` (+ ``ssd_scan_workspace_bytes``),
+``gated_rmsnorm``, ``decode_step``, ``state_bytes_per_layer``.
+"""
+from __future__ import annotations
+
+import ctypes
+from pathlib import Path
+from typing import Optional, Sequence
+
+_PKG = Path(__file__).resolve().parent
+LIB_PATH = _PKG / "libmamba2.so"
+
+F32, BF16 = 0, 1
+(OK, ERR_INVALID_ARGUMENT, ERR_SLOT_OUT_OF_RANGE, ERR_SLOT_SHARED, ERR_RUNS_DONT_COVER_ROWS,
+ ERR_NOT_IMPLEMENTED, ERR_CUDA, ERR_WORKSPACE_TOO_SMALL) = range(8)
+MAX_SEQS = 1024
+
+
+class Mamba2Error(RuntimeError):
+    """A non-OK status from libmamba2; ``.status`` holds the code."""
+
+    def __init__(self, status: int, op: str, detail: str = ""):
+        msg = f"{op}: {_lib().mamba2_status_string(status).decode()}"
+        if detail:
+            msg += f" ({detail})"
+        super().__init__(msg)
+        self.status = status
+
+
+class RecurrentBatch(ctypes.Structure):
+    _fields_ = [("num_seqs", ctypes.c_int32),
+                ("cu_seqlens", ctypes.POINTER(ctypes.c_int32)),
+                ("slots", ctypes.POINTER(ctypes.c_int32)),
+                ("fresh", ctypes.POINTER(ctypes.c_uint8))]
+
+
+class Dims(ctypes.Structure):
+    _fields_ = [("heads", ctypes.c_int32), ("headdim", ctypes.c_int32), ("d_state", ctypes.c_int32),
+                ("ngroups", ctypes.c_int32), ("conv_kernel", ctypes.c_int32)]
+
+
+_LIB = None
+
+
+def _lib():
+    global _LIB
+    if _LIB is None:
+        if not LIB_PATH.exists():
+            raise ImportError(f"{LIB_PATH} is not built; run selective_scan_gb300/build.py (nvcc, sm_103a)")
+        lib = ctypes.CDLL(str(LIB_PATH))
+        p, i32, f32, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_float, ctypes.c_size_t
+        rb, dims = ctypes.POINTER(RecurrentBatch), ctypes.POINTER(Dims)
+        lib.mamba2_causal_conv1d.argtypes = [p, p, p, p, p, i32, i32, i32, i32, ctypes.c_int, rb, p]
+        lib.mamba2_ssd_scan_workspace_bytes.argtypes = [dims, i32, rb]
+        lib.mamba2_ssd_scan_workspace_bytes.restype = sz
+        lib.mamba2_ssd_scan.argtypes = [p, p, p, p, p, p, p, i32, i32, dims, ctypes.c_int, rb, p, sz, p]
+        lib.mamba2_gated_rmsnorm.argtypes = [p, p, p, p, i32, i32, i32, f32, ctypes.c_int, p]
+        lib.mamba2_decode_step.argtypes = [p, p, p, p, p, p, p, p, p, p, i32, f32, p, p, i32, dims,
+                                           ctypes.c_int, rb, p]
+        lib.mamba2_state_bytes_per_layer.argtypes = [dims, ctypes.c_int]
+        lib.mamba2_state_bytes_per_layer.restype = ctypes.c_int64
+        lib.mamba2_status_string.argtypes = [ctypes.c_int]
+        lib.mamba2_status_string.restype = ctypes.c_char_p
+        lib.mamba2_last_cuda_error.restype = ctypes.c_char_p
+        for name in ("mamba2_causal_conv1d", "mamba2_ssd_scan", "mamba2_gated_rmsnorm", "mamba2_decode_step"):
+            getattr(lib, name).restype = ctypes.c_int
+        _LIB = lib
+    return _LIB
+
+
+def library():
+    """The loaded ctypes library (raises ImportError if it is not built)."""
+    return _lib()
+
+
+# --------------------------------------------------------------------------
+# marshalling
+# --------------------------------------------------------------------------
+
+def _dt(t) -> int:
+    import torch
+    if t.dtype == torch.bfloat16:
+        return BF16
+    if t.dtype == torch.float32:
+        return F32
+    raise TypeError(f"unsupported activation dtype {t.dtype}")
+
+
+def _ptr(t) -> Optional[int]:
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    if not t.is_contiguous():
+        raise ValueError("tensors must be contiguous")
+    return t.data_ptr()
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+class _Batch:
+    """Keeps the ctypes arrays of one RecurrentBatch alive for a call."""
+
+    def __init__(self, cu_seqlens: Optional[Sequence[int]], slots: Sequence[int], fresh: Sequence[int]):
+        n = len(slots)
+        self.slots = (ctypes.c_int32 * max(n, 1))(*[int(s) for s in slots])
+        self.fresh = (ctypes.c_uint8 * max(n, 1))(*[1 if f else 0 for f in fresh])
+        self.cu = None
+        if cu_seqlens is not None:
+            self.cu = (ctypes.c_int32 * (len(cu_seqlens)))(*[int(c) for c in cu_seqlens])
+        self.rb = RecurrentBatch(
+            n, ctypes.cast(self.cu, ctypes.POINTER(ctypes.c_int32)) if self.cu is not None else None,
+            ctypes.cast(self.slots, ctypes.POINTER(ctypes.c_int32)),
+            ctypes.cast(self.fresh, ctypes.POINTER(ctypes.c_uint8)))
+
+    def ref(self):
+        return ctypes.byref(self.rb)
+
+
+def _dims(d) -> Dims:
+    if isinstance(d, Dims):
+        return d
+    return Dims(int(d.heads), int(d.headdim), int(d.d_state), int(d.ngroups), int(d.conv_kernel))
+
+
+def _check(st: int, op: str):
+    if st != OK:
+        detail = _lib().mamba2_last_cuda_error().decode() if st == ERR_CUDA else ""
+        raise Mamba2Error(st, op, detail)
+
+
+# --------------------------------------------------------------------------
+# entry points
+# --------------------------------------------------------------------------
+
+def causal_conv1d(dst, x, weight, bias, conv_state, cu_seqlens, slots, fresh, stream=None, check=True) -> int:
+    """``mamba2_causal_conv1d``: dst = silu(depthwise causal conv) per run; conv_state updated."""
+    rows, conv_dim = x.shape
+    b = _Batch(cu_seqlens, slots, fresh)
+    st = _lib().mamba2_causal_conv1d(_ptr(dst), _ptr(x), _ptr(weight), _ptr(bias), _ptr(conv_state),
+                                     conv_state.shape[0], rows, conv_dim, weight.shape[1], _dt(x), b.ref(),
+                                     _stream(stream))
+    if check:
+        _check(st, "mamba2_causal_conv1d")
+    return st
+
+
+def ssd_scan_workspace_bytes(dims, rows, cu_seqlens, slots, fresh) -> int:
+    """``mamba2_ssd_scan_workspace_bytes`` for this batch on the current device."""
+    b = _Batch(cu_seqlens, slots, fresh)
+    d = _dims(dims)
+    return int(_lib().mamba2_ssd_scan_workspace_bytes(ctypes.byref(d), int(rows), b.ref()))
+
+
+def ssd_scan(dst, xbc, dt, A_log, dt_bias, D, ssm_state, dims, cu_seqlens, slots, fresh,
+             workspace=None, stream=None, check=True) -> int:
+    """``mamba2_ssd_scan``: chunked selective scan; ssm_state updated at the slots.
+
+    ``workspace`` is a device tensor of at least ``ssd_scan_workspace_bytes`` bytes
+    (allocated here with torch when None and needed).
+    """
+    import torch
+    rows = xbc.shape[0]
+    d = _dims(dims)
+    b = _Batch(cu_seqlens, slots, fresh)
+    if workspace is None:
+        need = int(_lib().mamba2_ssd_scan_workspace_bytes(ctypes.byref(d), rows, b.ref()))
+        if need > 0:
+            workspace = torch.empty(need, dtype=torch.uint8, device=xbc.device)
+    ws_ptr = _ptr(workspace) if workspace is not None else None
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    st = _lib().mamba2_ssd_scan(_ptr(dst), _ptr(xbc), _ptr(dt), _ptr(A_log), _ptr(dt_bias), _ptr(D),
+                                _ptr(ssm_state), ssm_state.shape[0], rows, ctypes.byref(d), _dt(xbc), b.ref(),
+                                ws_ptr, ws_bytes, _stream(stream))
+    if check:
+        _check(st, "mamba2_ssd_scan")
+    return st
+
+
+def gated_rmsnorm(dst, x, z, weight, groups, eps, stream=None, check=True) -> int:
+    """``mamba2_gated_rmsnorm``: dst = rmsnorm(x * silu(z)) * weight per group."""
+    rows, dim = x.shape
+    st = _lib().mamba2_gated_rmsnorm(_ptr(dst), _ptr(x), _ptr(z), _ptr(weight), rows, dim, int(groups),
+                                     float(eps), _dt(x), _stream(stream))
+    if check:
+        _check(st, "mamba2_gated_rmsnorm")
+    return st
+
+
+def decode_step(dst, xBC, z, dt, conv_w, conv_b, A_log, dt_bias, D, norm_w, norm_groups, eps,
+                conv_state, ssm_state, dims, slots, fresh, cu_seqlens=None, stream=None, check=True) -> int:
+    """``mamba2_decode_step``: fused conv -> scan -> gated norm for one token per sequence."""
+    d = _dims(dims)
+    b = _Batch(cu_seqlens, slots, fresh)
+    st = _lib().mamba2_decode_step(_ptr(dst), _ptr(xBC), _ptr(z), _ptr(dt), _ptr(conv_w), _ptr(conv_b),
+                                   _ptr(A_log), _ptr(dt_bias), _ptr(D), _ptr(norm_w), int(norm_groups),
+                                   float(eps), _ptr(conv_state), _ptr(ssm_state), ssm_state.shape[0],
+                                   ctypes.byref(d), _dt(xBC), b.ref(), _stream(stream))
+    if check:
+        _check(st, "mamba2_decode_step")
+    return st
+
+
+def state_bytes_per_layer(dims, conv_dtype: int = BF16) -> int:
+    """``mamba2_state_bytes_per_layer``: fp32 SSM state + conv history per sequence per layer."""
+    d = _dims(dims)
+    return int(_lib().mamba2_state_bytes_per_layer(ctypes.byref(d), int(conv_dtype)))
+
+
+def status_string(status: int) -> str:
+    return _lib().mamba2_status_string(int(status)).decode()

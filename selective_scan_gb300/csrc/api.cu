@@ -1,0 +1,329 @@
+// C ABI of libmamba2: host-side validation of every argument and of the
+// RecurrentBatch, then kernel launches on the caller's stream.
+//
+// RecurrentBatch rules: gllm PR #85 "feat(backend): Mamba2 ops, with CPU
+// reference implementations", section "Ops": a slot out of range, a slot
+// shared by two sequences, or run lengths that do not cover the rows are
+// rejected before anything is written. All checks here run before the first
+// launch, so a non-OK status leaves every buffer untouched.
+#include <algorithm>
+#include <cstdio>
+#include <cstring>
+#include <vector>
+
+#include "kernels.h"
+
+namespace mamba2 {
+namespace {
+
+thread_local char g_cuda_error[256] = "";
+
+mamba2_status cuda_fail(cudaError_t e) {
+  std::snprintf(g_cuda_error, sizeof g_cuda_error, "%s: %s", cudaGetErrorName(e), cudaGetErrorString(e));
+  return MAMBA2_ERR_CUDA;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+size_t act_size(mamba2_dtype a) { return a == MAMBA2_F32 ? 4 : 2; }
+bool act_ok(mamba2_dtype a) { return a == MAMBA2_F32 || a == MAMBA2_BF16; }
+
+// Slot range, then shared slots, then coverage of [0, rows).
+mamba2_status validate_batch(const mamba2_recurrent_batch* rb, int32_t num_slots, int32_t rows,
+                             bool need_cu) {
+  if (!rb || rb->num_seqs < 0 || rb->num_seqs > MAMBA2_MAX_SEQS || num_slots < 0 || rows < 0)
+    return MAMBA2_ERR_INVALID_ARGUMENT;
+  const int n = rb->num_seqs;
+  if (n == 0) return rows == 0 ? MAMBA2_OK : MAMBA2_ERR_RUNS_DONT_COVER_ROWS;
+  if (!rb->slots || !rb->fresh || (need_cu && !rb->cu_seqlens)) return MAMBA2_ERR_INVALID_ARGUMENT;
+  for (int i = 0; i < n; ++i)
+    if (rb->slots[i] < 0 || rb->slots[i] >= num_slots) return MAMBA2_ERR_SLOT_OUT_OF_RANGE;
+  std::vector<int32_t> sorted(rb->slots, rb->slots + n);
+  std::sort(sorted.begin(), sorted.end());
+  for (int i = 1; i < n; ++i)
+    if (sorted[i] == sorted[i - 1]) return MAMBA2_ERR_SLOT_SHARED;
+  if (rb->cu_seqlens) {
+    const int32_t* cu = rb->cu_seqlens;
+    if (cu[0] != 0) return MAMBA2_ERR_RUNS_DONT_COVER_ROWS;
+    for (int i = 0; i < n; ++i)
+      if (cu[i + 1] < cu[i]) return MAMBA2_ERR_RUNS_DONT_COVER_ROWS;
+    if (cu[n] != rows) return MAMBA2_ERR_RUNS_DONT_COVER_ROWS;
+  }
+  return MAMBA2_OK;
+}
+
+// Fill cu and slot/fresh; tiles are set by the caller.
+void fill_table(SeqTable& t, const mamba2_recurrent_batch* rb) {
+  t.n = rb->num_seqs;
+  t.cu[0] = 0;
+  for (int i = 0; i < t.n; ++i) {
+    t.cu[i + 1] = rb->cu_seqlens ? rb->cu_seqlens[i + 1] : i + 1;
+    t.slot_fresh[i] = (uint32_t)rb->slots[i] | (rb->fresh[i] ? 0x80000000u : 0u);
+  }
+}
+
+int device_sm_count() {
+  static int cache[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+  if (dev >= 0 && dev < 64 && cache[dev] > 0) return cache[dev];
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+  if (dev >= 0 && dev < 64) cache[dev] = n;
+  return n;
+}
+
+bool dims_ok(const mamba2_dims* d) {
+  return d && d->heads > 0 && d->headdim > 0 && d->d_state > 0 && d->ngroups > 0 &&
+         d->heads % d->ngroups == 0 && d->conv_kernel >= 1 && d->conv_kernel <= 4 &&
+         (int64_t)d->heads * d->headdim + 2LL * d->ngroups * d->d_state < (1LL << 30);
+}
+
+// Segmentation of the chunked scan: every sequence is cut into segments of
+// seg_chunks chunks, sized so the grid has a few CTAs per SM.
+struct ScanPlan {
+  bool chunked = false;
+  int seg_chunks = 1;
+  int total_segs = 0;
+  bool segmented = false;
+  size_t ws_state_floats = 0;
+  size_t ws_bytes = 0;
+};
+
+ScanPlan plan_scan(const mamba2_dims* d, mamba2_dtype act, const mamba2_recurrent_batch* rb) {
+  ScanPlan p;
+  p.chunked = scan_chunked_supported(act, d->headdim, d->d_state);
+  const int n = rb->num_seqs;
+  if (!p.chunked) {
+    p.total_segs = n;
+    return p;
+  }
+  int64_t total_chunks = 0;
+  for (int i = 0; i < n; ++i) {
+    const int64_t T = rb->cu_seqlens[i + 1] - rb->cu_seqlens[i];
+    total_chunks += (T + kChunk - 1) / kChunk;
+  }
+  const int64_t target = 4LL * device_sm_count();  // CTAs wanted (2 resident per SM, ~2 waves)
+  int64_t sc = (total_chunks * d->heads + target - 1) / std::max<int64_t>(1, target);
+  p.seg_chunks = (int)std::max<int64_t>(1, sc);
+  p.total_segs = 0;
+  for (int i = 0; i < n; ++i) {
+    const int64_t T = rb->cu_seqlens[i + 1] - rb->cu_seqlens[i];
+    const int64_t ch = (T + kChunk - 1) / kChunk;
+    const int segs = (int)std::max<int64_t>(1, (ch + p.seg_chunks - 1) / p.seg_chunks);
+    p.segmented |= segs > 1;
+    p.total_segs += segs;
+  }
+  if (p.segmented) {
+    p.ws_state_floats = (size_t)p.total_segs * d->heads * d->headdim * d->d_state;
+    const size_t decay_off = (p.ws_state_floats * 4 + 255) / 256 * 256;
+    p.ws_bytes = decay_off + (size_t)p.total_segs * d->heads * 4;
+  }
+  return p;
+}
+
+void fill_scan_tiles(SeqTable& t, const ScanPlan& p) {
+  t.tile[0] = 0;
+  for (int i = 0; i < t.n; ++i) {
+    int segs = 1;
+    if (p.chunked) {
+      const int64_t ch = ((int64_t)t.cu[i + 1] - t.cu[i] + kChunk - 1) / kChunk;
+      segs = (int)std::max<int64_t>(1, (ch + p.seg_chunks - 1) / p.seg_chunks);
+    }
+    t.tile[i + 1] = t.tile[i] + segs;
+  }
+}
+
+}  // namespace
+}  // namespace mamba2
+
+using namespace mamba2;
+
+extern "C" {
+
+const char* mamba2_status_string(mamba2_status s) {
+  switch (s) {
+    case MAMBA2_OK: return "MAMBA2_OK";
+    case MAMBA2_ERR_INVALID_ARGUMENT: return "MAMBA2_ERR_INVALID_ARGUMENT";
+    case MAMBA2_ERR_SLOT_OUT_OF_RANGE: return "MAMBA2_ERR_SLOT_OUT_OF_RANGE";
+    case MAMBA2_ERR_SLOT_SHARED: return "MAMBA2_ERR_SLOT_SHARED";
+    case MAMBA2_ERR_RUNS_DONT_COVER_ROWS: return "MAMBA2_ERR_RUNS_DONT_COVER_ROWS";
+    case MAMBA2_ERR_NOT_IMPLEMENTED: return "MAMBA2_ERR_NOT_IMPLEMENTED";
+    case MAMBA2_ERR_CUDA: return "MAMBA2_ERR_CUDA";
+    case MAMBA2_ERR_WORKSPACE_TOO_SMALL: return "MAMBA2_ERR_WORKSPACE_TOO_SMALL";
+  }
+  return "MAMBA2_ERR_UNKNOWN";
+}
+
+const char* mamba2_last_cuda_error(void) { return g_cuda_error; }
+
+int64_t mamba2_state_bytes_per_layer(const mamba2_dims* d, mamba2_dtype conv_dtype) {
+  if (!dims_ok(d) || !act_ok(conv_dtype)) return -1;
+  const int64_t conv_dim = (int64_t)d->heads * d->headdim + 2LL * d->ngroups * d->d_state;
+  return (int64_t)d->heads * d->headdim * d->d_state * 4 +
+         conv_dim * (d->conv_kernel - 1) * (int64_t)act_size(conv_dtype);
+}
+
+mamba2_status mamba2_causal_conv1d(void* dst, const void* x, const float* weight, const float* bias,
+                                   void* conv_state, int32_t num_slots, int32_t rows, int32_t conv_dim,
+                                   int32_t kernel, mamba2_dtype act, const mamba2_recurrent_batch* rb,
+                                   void* stream) {
+  if (!act_ok(act) || conv_dim <= 0 || kernel < 1 || rows < 0) return MAMBA2_ERR_INVALID_ARGUMENT;
+  if (kernel > 4) return MAMBA2_ERR_NOT_IMPLEMENTED;
+  if (((size_t)conv_dim * act_size(act)) % 16 != 0) return MAMBA2_ERR_NOT_IMPLEMENTED;
+  if (rb && rb->num_seqs > 0) {
+    if (!weight || !bias || (kernel > 1 && !conv_state)) return MAMBA2_ERR_INVALID_ARGUMENT;
+    if ((kernel > 1 && !aligned16(conv_state))) return MAMBA2_ERR_INVALID_ARGUMENT;
+  }
+  if (rows > 0 && (!dst || !x || !aligned16(dst) || !aligned16(x))) return MAMBA2_ERR_INVALID_ARGUMENT;
+  if (rows > 0 && dst == x) return MAMBA2_ERR_INVALID_ARGUMENT;
+  mamba2_status st = validate_batch(rb, num_slots, rows, true);
+  if (st != MAMBA2_OK) return st;
+  if (rb->num_seqs == 0) return MAMBA2_OK;
+
+  ConvArgs a;
+  std::memset(&a, 0, sizeof a);
+  a.x = x;
+  a.dst = dst;
+  a.weight = weight;
+  a.bias = bias;
+  a.conv_state = conv_state;
+  a.conv_dim = conv_dim;
+  fill_table(a.tab, rb);
+  a.tab.tile[0] = 0;
+  for (int i = 0; i < a.tab.n; ++i) {
+    const int T = a.tab.cu[i + 1] - a.tab.cu[i];
+    a.tab.tile[i + 1] = a.tab.tile[i] + std::max(1, (T + kConvRows - 1) / kConvRows);
+  }
+  cudaError_t e = launch_conv1d(a, act, kernel, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? MAMBA2_OK : cuda_fail(e);
+}
+
+size_t mamba2_ssd_scan_workspace_bytes(const mamba2_dims* dims, int32_t rows, const mamba2_recurrent_batch* rb) {
+  if (!dims_ok(dims)) return 0;
+  if (!rb || rb->num_seqs <= 0 || rb->num_seqs > MAMBA2_MAX_SEQS || !rb->cu_seqlens) return 0;
+  if (rb->cu_seqlens[0] != 0 || rb->cu_seqlens[rb->num_seqs] != rows) return 0;
+  for (int i = 0; i < rb->num_seqs; ++i)
+    if (rb->cu_seqlens[i + 1] < rb->cu_seqlens[i]) return 0;
+  return plan_scan(dims, MAMBA2_BF16, rb).ws_bytes;
+}
+
+mamba2_status mamba2_ssd_scan(void* dst, const void* xbc, const void* dt, const float* A_log,
+                              const float* dt_bias, const float* D, float* ssm_state, int32_t num_slots,
+                              int32_t rows, const mamba2_dims* dims, mamba2_dtype act,
+                              const mamba2_recurrent_batch* rb, void* workspace, size_t workspace_bytes,
+                              void* stream) {
+  if (!act_ok(act) || !dims_ok(dims) || rows < 0) return MAMBA2_ERR_INVALID_ARGUMENT;
+  const bool chunked = scan_chunked_supported(act, dims->headdim, dims->d_state);
+  if (!chunked && (dims->headdim > kSerialMaxP || dims->d_state > kSerialMaxN))
+    return MAMBA2_ERR_NOT_IMPLEMENTED;
+  if (rb && rb->num_seqs > 0 && (!ssm_state || !A_log || !dt_bias || !D || !aligned16(ssm_state)))
+    return MAMBA2_ERR_INVALID_ARGUMENT;
+  if (rows > 0 && (!dst || !xbc || !dt || !aligned16(dst) || !aligned16(xbc)))
+    return MAMBA2_ERR_INVALID_ARGUMENT;
+  mamba2_status st = validate_batch(rb, num_slots, rows, true);
+  if (st != MAMBA2_OK) return st;
+  if (rb->num_seqs == 0) return MAMBA2_OK;
+
+  const ScanPlan plan = plan_scan(dims, act, rb);
+  if (plan.ws_bytes > 0 && (!workspace || workspace_bytes < plan.ws_bytes))
+    return MAMBA2_ERR_WORKSPACE_TOO_SMALL;
+  if (plan.ws_bytes > 0 && (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return MAMBA2_ERR_INVALID_ARGUMENT;
+
+  ScanArgs a;
+  std::memset(&a, 0, sizeof a);
+  a.dst = dst;
+  a.xbc = xbc;
+  a.dt = dt;
+  a.A_log = A_log;
+  a.dt_bias = dt_bias;
+  a.D = D;
+  a.ssm_state = ssm_state;
+  a.heads = dims->heads;
+  a.headdim = dims->headdim;
+  a.d_state = dims->d_state;
+  a.ngroups = dims->ngroups;
+  a.conv_dim = dims->heads * dims->headdim + 2 * dims->ngroups * dims->d_state;
+  a.seg_chunks = plan.seg_chunks;
+  if (plan.ws_bytes > 0) {
+    a.ws_state = static_cast<float*>(workspace);
+    a.ws_decay = reinterpret_cast<float*>(static_cast<char*>(workspace) +
+                                          (plan.ws_state_floats * 4 + 255) / 256 * 256);
+  }
+  fill_table(a.tab, rb);
+  fill_scan_tiles(a.tab, plan);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = plan.chunked ? launch_scan_chunked(a, s) : launch_scan_serial(a, act, s);
+  return e == cudaSuccess ? MAMBA2_OK : cuda_fail(e);
+}
+
+mamba2_status mamba2_gated_rmsnorm(void* dst, const void* x, const void* z, const float* weight, int32_t rows,
+                                   int32_t dim, int32_t groups, float eps, mamba2_dtype act, void* stream) {
+  if (!act_ok(act) || rows < 0 || dim <= 0 || groups <= 0 || dim % groups != 0 || !(eps >= 0.0f))
+    return MAMBA2_ERR_INVALID_ARGUMENT;
+  if (((size_t)(dim / groups) * act_size(act)) % 16 != 0) return MAMBA2_ERR_NOT_IMPLEMENTED;
+  if (rows == 0) return MAMBA2_OK;
+  if (!dst || !x || !z || !weight || !aligned16(dst) || !aligned16(x) || !aligned16(z) || !aligned16(weight))
+    return MAMBA2_ERR_INVALID_ARGUMENT;
+  NormArgs a{dst, x, z, weight, rows, dim, groups, eps};
+  cudaError_t e = launch_gated_rmsnorm(a, act, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? MAMBA2_OK : cuda_fail(e);
+}
+
+mamba2_status mamba2_decode_step(void* dst, const void* xBC, const void* z, const void* dt, const float* conv_w,
+                                 const float* conv_b, const float* A_log, const float* dt_bias, const float* D,
+                                 const float* norm_w, int32_t norm_groups, float eps, void* conv_state,
+                                 float* ssm_state, int32_t num_slots, const mamba2_dims* dims, mamba2_dtype act,
+                                 const mamba2_recurrent_batch* rb, void* stream) {
+  if (!act_ok(act) || !dims_ok(dims) || !(eps >= 0.0f) || norm_groups <= 0) return MAMBA2_ERR_INVALID_ARGUMENT;
+  if (!decode_supported(act, *dims, norm_groups)) return MAMBA2_ERR_NOT_IMPLEMENTED;
+  if (!rb) return MAMBA2_ERR_INVALID_ARGUMENT;
+  const int n = rb->num_seqs;
+  if (n > 0) {
+    const void* ptrs[] = {dst, xBC, z, dt, conv_w, conv_b, A_log, dt_bias, D, norm_w, ssm_state};
+    for (const void* p : ptrs)
+      if (!p) return MAMBA2_ERR_INVALID_ARGUMENT;
+    if (dims->conv_kernel > 1 && !conv_state) return MAMBA2_ERR_INVALID_ARGUMENT;
+    if (!aligned16(dst) || !aligned16(xBC) || !aligned16(z) || !aligned16(ssm_state) ||
+        (dims->conv_kernel > 1 && !aligned16(conv_state)) || !aligned16(norm_w))
+      return MAMBA2_ERR_INVALID_ARGUMENT;
+  }
+  mamba2_status st = validate_batch(rb, num_slots, n, false);
+  if (st != MAMBA2_OK) return st;
+  if (rb->cu_seqlens)
+    for (int i = 0; i <= n; ++i)
+      if (rb->cu_seqlens[i] != i) return MAMBA2_ERR_INVALID_ARGUMENT;
+  if (n == 0) return MAMBA2_OK;
+
+  DecodeArgs a;
+  std::memset(&a, 0, sizeof a);
+  a.dst = dst;
+  a.xBC = xBC;
+  a.z = z;
+  a.dt = dt;
+  a.conv_w = conv_w;
+  a.conv_b = conv_b;
+  a.A_log = A_log;
+  a.dt_bias = dt_bias;
+  a.D = D;
+  a.norm_w = norm_w;
+  a.conv_state = conv_state;
+  a.ssm_state = ssm_state;
+  a.heads = dims->heads;
+  a.headdim = dims->headdim;
+  a.d_state = dims->d_state;
+  a.ngroups = dims->ngroups;
+  a.conv_kernel = dims->conv_kernel;
+  a.norm_groups = norm_groups;
+  a.eps = eps;
+  const int cl = std::min(kDecodeMaxCluster, dims->heads);
+  a.heads_per_cta = (dims->heads + cl - 1) / cl;
+  a.cluster = (dims->heads + a.heads_per_cta - 1) / a.heads_per_cta;
+  fill_table(a.tab, rb);
+  for (int i = 0; i <= n; ++i) a.tab.tile[i] = i;
+  cudaError_t e = launch_decode(a, act, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? MAMBA2_OK : cuda_fail(e);
+}
+
+}  // extern "C"

@@ -1,0 +1,156 @@
+// Depthwise causal conv1d + SiLU over packed variable-length runs, with the
+// conv-state slot read and rewritten in the same kernel.
+//
+// Semantics: gllm PR #85 "feat(backend): Mamba2 ops, with CPU reference
+// implementations", section "Ops" (CausalConv1D): row t of a run is
+// silu(bias + sum_k w[:, k] * u[t + k]) with u = slot history (zeros when
+// fresh) followed by the run's inputs; the slot then holds u's last kernel-1
+// rows.
+//
+// Layout and work split: every thread owns one 16-byte channel vector (8 bf16
+// or 4 fp32 channels) over a tile of kRows consecutive rows of ONE sequence.
+// Tiles never straddle sequences (the host numbers tiles per sequence), so a
+// thread keeps the kernel-1 previous inputs in registers as a sliding window.
+// Only tile 0 of a sequence reads the slot (kRows >= kernel-1), and that same
+// thread writes the new history for its channels at the end: no other thread
+// touches those slot bytes, so no ordering between CTAs is needed. A
+// zero-length sequence still gets one (empty) tile for its slot update.
+//
+// Memory: each input row is read once by its tile plus kernel-1 window rows
+// read again by the next tile (L2 hits); each output row written once. The
+// kernel is HBM-bound: 2 * conv_dim * sizeof(act) bytes per row.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace mamba2 {
+
+template <typename T, int K>
+__global__ void __launch_bounds__(kConvThreads)
+conv1d_silu_kernel(const __grid_constant__ ConvArgs a) {
+  constexpr int V = Vec16<T>::n;
+  constexpr int H = K - 1;  // history rows
+  const int nvec = a.conv_dim / V;
+  const int64_t item = (int64_t)blockIdx.x * kConvThreads + threadIdx.x;
+  const int64_t total = (int64_t)a.tab.tile[a.tab.n] * nvec;
+  if (item >= total) return;
+  const int tile = (int)(item / nvec);
+  const int cv = (int)(item - (int64_t)tile * nvec);
+  const int s = find_tile_seq(a.tab, tile);
+  const int local_tile = tile - a.tab.tile[s];
+  const int row0 = a.tab.cu[s];
+  const int T_len = a.tab.cu[s + 1] - row0;
+  const int q0 = local_tile * kConvRows;
+  const int nrows = min(kConvRows, T_len - q0);
+  const bool fresh = seq_fresh(a.tab, s);
+  const int64_t slot_base = (int64_t)seq_slot(a.tab, s) * H * a.conv_dim;
+  const int c0 = cv * V;
+  const T* x = static_cast<const T*>(a.x);
+  T* dst = static_cast<T*>(a.dst);
+  T* cst = static_cast<T*>(a.conv_state);
+
+  // taps and bias for this thread's channels
+  float w[K][V], b[V];
+#pragma unroll
+  for (int j = 0; j < V; ++j) {
+    b[j] = a.bias[c0 + j];
+#pragma unroll
+    for (int k = 0; k < K; ++k) w[k][j] = a.weight[(int64_t)(c0 + j) * K + k];
+  }
+
+  // window = u[q0 .. q0 + H - 1] = conv inputs at positions q0 - H .. q0 - 1
+  uint4 raw_hist[H > 0 ? H : 1];
+  float win[H > 0 ? H : 1][V];
+#pragma unroll
+  for (int i = 0; i < H; ++i) {
+    const int pos = q0 - H + i;
+    uint4 r;
+    if (pos >= 0) {
+      r = *reinterpret_cast<const uint4*>(x + (int64_t)(row0 + pos) * a.conv_dim + c0);
+    } else if (fresh) {
+      r = make_uint4(0u, 0u, 0u, 0u);
+    } else {
+      r = *reinterpret_cast<const uint4*>(cst + slot_base + (int64_t)(H + pos) * a.conv_dim + c0);
+    }
+    raw_hist[i] = r;
+    Vec16<T>::load(reinterpret_cast<const T*>(&r), win[i]);
+  }
+
+  // the tile's rows: loads first, then the K-tap dot products
+  uint4 in[kConvRows];
+#pragma unroll
+  for (int r = 0; r < kConvRows; ++r)
+    if (r < nrows)
+      in[r] = *reinterpret_cast<const uint4*>(x + (int64_t)(row0 + q0 + r) * a.conv_dim + c0);
+#pragma unroll
+  for (int r = 0; r < kConvRows; ++r) {
+    if (r < nrows) {
+      float cur[V], out[V];
+      Vec16<T>::load(reinterpret_cast<const T*>(&in[r]), cur);
+#pragma unroll
+      for (int j = 0; j < V; ++j) {
+        float acc = b[j];
+#pragma unroll
+        for (int k = 0; k < H; ++k) acc = fmaf(w[k][j], win[k][j], acc);
+        acc = fmaf(w[H][j], cur[j], acc);
+        out[j] = silu_f(acc);
+      }
+      Vec16<T>::store(dst + (int64_t)(row0 + q0 + r) * a.conv_dim + c0, out);
+#pragma unroll
+      for (int k = 0; k + 1 < H; ++k)
+#pragma unroll
+        for (int j = 0; j < V; ++j) win[k][j] = win[k + 1][j];
+      if (H > 0)
+#pragma unroll
+        for (int j = 0; j < V; ++j) win[H > 0 ? H - 1 : 0][j] = cur[j];
+    }
+  }
+
+  // slot update by tile 0: new history = u[T .. T + H - 1] (bit copies)
+  if (local_tile == 0) {
+#pragma unroll
+    for (int j = 0; j < H; ++j) {
+      const int upos = T_len + j;  // index into u
+      uint4 r = make_uint4(0u, 0u, 0u, 0u);
+      if (upos >= H) {
+        r = *reinterpret_cast<const uint4*>(x + (int64_t)(row0 + upos - H) * a.conv_dim + c0);
+      } else {
+        // old history (zeros when fresh); only when the run is shorter than H
+#pragma unroll
+        for (int i = 0; i < H; ++i)
+          if (i == upos) r = raw_hist[i];
+      }
+      *reinterpret_cast<uint4*>(cst + slot_base + (int64_t)j * a.conv_dim + c0) = r;
+    }
+  }
+}
+
+template <typename T, int K>
+static cudaError_t launch_conv_t(const ConvArgs& a, cudaStream_t st) {
+  const int nvec = a.conv_dim / Vec16<T>::n;
+  const int64_t total = (int64_t)a.tab.tile[a.tab.n] * nvec;
+  if (total == 0) return cudaSuccess;
+  const int64_t blocks = (total + kConvThreads - 1) / kConvThreads;
+  conv1d_silu_kernel<T, K><<<(unsigned)blocks, kConvThreads, 0, st>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_conv1d(const ConvArgs& a, mamba2_dtype act, int kernel, cudaStream_t st) {
+  if (act == MAMBA2_BF16) {
+    switch (kernel) {
+      case 1: return launch_conv_t<__nv_bfloat16, 1>(a, st);
+      case 2: return launch_conv_t<__nv_bfloat16, 2>(a, st);
+      case 3: return launch_conv_t<__nv_bfloat16, 3>(a, st);
+      case 4: return launch_conv_t<__nv_bfloat16, 4>(a, st);
+    }
+  } else {
+    switch (kernel) {
+      case 1: return launch_conv_t<float, 1>(a, st);
+      case 2: return launch_conv_t<float, 2>(a, st);
+      case 3: return launch_conv_t<float, 3>(a, st);
+      case 4: return launch_conv_t<float, 4>(a, st);
+    }
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace mamba2

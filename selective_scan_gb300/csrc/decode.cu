@@ -1,0 +1,315 @@
+// One decode step: conv (one token) -> selective scan (one token) -> gated
+// RMSNorm, fused in one kernel for a batch of sequences.
+//
+// Semantics: the three ops of gllm PR #85 "feat(backend): Mamba2 ops, with
+// CPU reference implementations", section "Ops", applied to a single token per
+// sequence, with the conv output and y rounded to the activation type exactly
+// where the unfused ops store them. The page "Granite Mamba2 Inference
+// Optimization" describes decode as a per-token recurrence over conv and SSM
+// cache state; InfiniLM PR #575 "feat(mamba2): integrate model loading and
+// recurrent inference" (section "Summary") runs it as indexed recurrent decode
+// over a state pool.
+//
+// Work split: a thread-block cluster per sequence; CTA r of the cluster owns
+// heads [r*hpc, (r+1)*hpc). Each CTA
+//   1. computes the conv for its heads' x channels and for all B/C channels
+//      (B/C recomputed per CTA: 2*G*N channels, tiny), writes the new conv
+//      history of its own x channels (no other CTA touches them);
+//   2. streams its heads' fp32 SSM state once: 16-byte loads along d_state,
+//      h = h*decay + dt'*x*B, y = h.C + D*x (warp-shuffle reduction), store;
+//   3. forms g = y*silu(z) and a deterministic partial sum of g^2 per norm
+//      group in shared memory;
+//   4. cluster barrier; CTA 0 then writes the B/C conv history (every CTA has
+//      read the old one by now); each CTA sums the partials of all CTAs in
+//      rank order through distributed shared memory and writes its normed
+//      outputs; a final cluster barrier keeps shared memory alive until every
+//      CTA has read it.
+// HBM traffic per sequence: SSM state read + write (H*P*N*4 bytes each), conv
+// history read + write, the token's inputs and outputs. The state stream is
+// the roofline term.
+#include <type_traits>
+
+#include "common.cuh"
+
+namespace mamba2 {
+
+constexpr int kDecodeWarps = kDecodeThreads / 32;
+constexpr int kDecodeUnroll = 8;  // rows of state in flight per lane
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n" ::: "memory");
+  asm volatile("barrier.cluster.wait.acquire.aligned;\n" ::: "memory");
+}
+
+__device__ __forceinline__ float ld_dsmem_f32(const float* local, uint32_t rank) {
+  uint32_t remote;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_addr(local)), "r"(rank));
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
+  return v;
+}
+
+template <typename T, int K>
+__global__ void __launch_bounds__(kDecodeThreads)
+decode_step_kernel(const __grid_constant__ DecodeArgs a) {
+  constexpr int V = Vec16<T>::n;
+  constexpr int HIST = K - 1;
+  extern __shared__ __align__(16) float dsm[];
+
+  const int rank = blockIdx.x;  // cluster spans grid.x exactly
+  const int s = blockIdx.y;
+  const int H = a.heads, P = a.headdim, N = a.d_state, G = a.ngroups;
+  const int d_inner = H * P;
+  const int conv_dim = d_inner + 2 * G * N;
+  const int h0 = rank * a.heads_per_cta;
+  const int h1 = min(H, h0 + a.heads_per_cta);
+  const int nh = max(0, h1 - h0);
+  const int rows = nh * P;  // state rows owned by this CTA
+  const bool fresh = seq_fresh(a.tab, s);
+  const int64_t slot = seq_slot(a.tab, s);
+
+  float* xs = dsm;                           // [heads_per_cta * P] conv output x
+  float* ys = xs + a.heads_per_cta * P;      // [heads_per_cta * P] y, then g
+  float* bc = ys + a.heads_per_cta * P;      // [2 * G * N] conv output B, C
+  float* hdt = bc + 2 * G * N;               // [heads_per_cta] dt'
+  float* hdec = hdt + a.heads_per_cta;       // [heads_per_cta] decay
+  float* hD = hdec + a.heads_per_cta;        // [heads_per_cta] D
+  float* part = hD + a.heads_per_cta;        // [kDecodeMaxNormGroups]
+  float* wsum = part + kDecodeMaxNormGroups; // [kDecodeWarps]
+
+  const T* xBC = static_cast<const T*>(a.xBC) + (int64_t)s * conv_dim;
+  T* cst = static_cast<T*>(a.conv_state) + slot * HIST * conv_dim;
+
+  for (int i = threadIdx.x; i < kDecodeMaxNormGroups; i += kDecodeThreads) part[i] = 0.0f;
+
+  // ---- 1. conv for own x channels and all B/C channels -------------------
+  const int nxv = rows / V;
+  const int nbcv = 2 * G * N / V;
+  for (int i = threadIdx.x; i < nxv + nbcv; i += kDecodeThreads) {
+    const bool is_x = i < nxv;
+    const int c0 = is_x ? h0 * P + i * V : d_inner + (i - nxv) * V;
+    uint4 hraw[HIST > 0 ? HIST : 1];
+    float hist[HIST > 0 ? HIST : 1][V], cur[V], out[V];
+#pragma unroll
+    for (int j = 0; j < HIST; ++j) {
+      hraw[j] = fresh ? make_uint4(0u, 0u, 0u, 0u)
+                      : *reinterpret_cast<const uint4*>(cst + (int64_t)j * conv_dim + c0);
+      Vec16<T>::load(reinterpret_cast<const T*>(&hraw[j]), hist[j]);
+    }
+    const uint4 craw = *reinterpret_cast<const uint4*>(xBC + c0);
+    Vec16<T>::load(reinterpret_cast<const T*>(&craw), cur);
+#pragma unroll
+    for (int j = 0; j < V; ++j) {
+      float wk[K], uk[K];
+#pragma unroll
+      for (int k = 0; k < K; ++k) {
+        wk[k] = a.conv_w[(int64_t)(c0 + j) * K + k];
+        uk[k] = k < HIST ? hist[k < HIST ? k : 0][j] : cur[j];
+      }
+      if constexpr (std::is_same<T, __nv_bfloat16>::value) {
+        out[j] = conv_silu_bf16_exact<K>(a.conv_b[c0 + j], wk, uk);
+      } else {
+        float acc = a.conv_b[c0 + j];
+#pragma unroll
+        for (int k = 0; k < K; ++k) acc = fmaf(wk[k], uk[k], acc);
+        out[j] = silu_f(acc);
+      }
+    }
+    float* o = is_x ? xs + i * V : bc + (c0 - d_inner);
+#pragma unroll
+    for (int j = 0; j < V; ++j) o[j] = out[j];
+    if (is_x) {  // own channels: shift the history now
+#pragma unroll
+      for (int j = 0; j + 1 < HIST; ++j)
+        *reinterpret_cast<uint4*>(cst + (int64_t)j * conv_dim + c0) = hraw[j + 1];
+      if (HIST > 0)
+        *reinterpret_cast<uint4*>(cst + (int64_t)(HIST > 0 ? HIST - 1 : 0) * conv_dim + c0) = craw;
+    }
+  }
+  if (threadIdx.x < nh) {
+    const int h = h0 + threadIdx.x;
+    const float v = Act<T>::to_f(static_cast<const T*>(a.dt)[(int64_t)s * H + h]) + a.dt_bias[h];
+    const float dtp = softplus_f(v);
+    hdt[threadIdx.x] = dtp;
+    hdec[threadIdx.x] = expf(-expf(a.A_log[h]) * dtp);
+    hD[threadIdx.x] = a.D[h];
+  }
+  __syncthreads();
+
+  // ---- 2. state stream: h = h*decay + dt'*x*B; y = h.C + D*x -------------
+  {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int nq = N / 4;                  // float4 per state row
+    const int lpr = nq < 32 ? nq : 32;     // lanes per row
+    const int rpp = 32 / lpr;              // rows per warp pass
+    const int qpl = (nq + lpr - 1) / lpr;  // float4 per lane per row
+    const int q0 = lane % lpr, rs = lane / lpr;
+    float4* st = reinterpret_cast<float4*>(a.ssm_state + (slot * H + h0) * (int64_t)P * N);
+    const int hpg = H / G;
+    for (int base = warp * rpp * kDecodeUnroll; base < rows; base += kDecodeWarps * rpp * kDecodeUnroll) {
+      for (int qq = 0; qq < qpl; ++qq) {
+        const int q = q0 + qq * lpr;
+        float4 hv[kDecodeUnroll];
+#pragma unroll
+        for (int u = 0; u < kDecodeUnroll; ++u) {
+          const int r = base + u * rpp + rs;
+          hv[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (!fresh && r < rows && q < nq) hv[u] = __ldcs(st + (int64_t)r * nq + q);
+        }
+#pragma unroll
+        for (int u = 0; u < kDecodeUnroll; ++u) {
+          const int r = base + u * rpp + rs;
+          float acc = 0.0f;
+          if (r < rows && q < nq) {
+            const int hl = r / P;
+            const int g = (h0 + hl) / hpg;
+            const float xv = xs[r], dtp = hdt[hl], dec = hdec[hl];
+            const float4 b4 = *reinterpret_cast<const float4*>(bc + g * N + 4 * q);
+            const float4 c4 = *reinterpret_cast<const float4*>(bc + G * N + g * N + 4 * q);
+            float4 h = hv[u];
+            h.x = fmaf(h.x, dec, dtp * b4.x * xv);
+            h.y = fmaf(h.y, dec, dtp * b4.y * xv);
+            h.z = fmaf(h.z, dec, dtp * b4.z * xv);
+            h.w = fmaf(h.w, dec, dtp * b4.w * xv);
+            __stcs(st + (int64_t)r * nq + q, h);
+            acc = h.x * c4.x;
+            acc = fmaf(h.y, c4.y, acc);
+            acc = fmaf(h.z, c4.z, acc);
+            acc = fmaf(h.w, c4.w, acc);
+          }
+          for (int o = lpr >> 1; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+          if (qq == 0) {
+            if (q0 == 0 && r < rows) ys[r] = acc;
+          } else if (q0 == 0 && r < rows) {
+            ys[r] += acc;
+          }
+        }
+      }
+    }
+  }
+  __syncthreads();
+
+  // ---- 3. g = round(y) * silu(z); partial sums of g^2 per norm group -----
+  const int gs = d_inner / a.norm_groups;
+  const T* zrow = static_cast<const T*>(a.z) + (int64_t)s * d_inner;
+  for (int r = threadIdx.x; r < rows; r += kDecodeThreads) {
+    const int hl = r / P;
+    const float y = round_act<T>(ys[r] + hD[hl] * xs[r]);
+    ys[r] = y * silu_f(Act<T>::to_f(zrow[h0 * P + r]));
+  }
+  __syncthreads();
+  if (rows > 0) {
+    const int c_lo = h0 * P, c_hi = h0 * P + rows;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int grp = c_lo / gs; grp * gs < c_hi; ++grp) {
+      const int lo = max(c_lo, grp * gs) - c_lo, hi = min(c_hi, (grp + 1) * gs) - c_lo;
+      float ss = 0.0f;
+      for (int r = lo + threadIdx.x; r < hi; r += kDecodeThreads) ss = fmaf(ys[r], ys[r], ss);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+      if (lane == 0) wsum[warp] = ss;
+      __syncthreads();
+      if (threadIdx.x == 0) {
+        float t = 0.0f;
+        for (int w = 0; w < kDecodeWarps; ++w) t += wsum[w];
+        part[grp] = t;
+      }
+      __syncthreads();
+    }
+  }
+
+  // ---- 4. cluster: B/C history, group totals, normed output --------------
+  cluster_sync_all();
+  if (rank == 0) {
+    for (int i = threadIdx.x; i < nbcv; i += kDecodeThreads) {
+      const int c0 = d_inner + i * V;
+      const uint4 craw = *reinterpret_cast<const uint4*>(xBC + c0);
+#pragma unroll
+      for (int j = 0; j + 1 < HIST; ++j) {
+        const uint4 nxt = fresh ? make_uint4(0u, 0u, 0u, 0u)
+                                : *reinterpret_cast<const uint4*>(cst + (int64_t)(j + 1) * conv_dim + c0);
+        *reinterpret_cast<uint4*>(cst + (int64_t)j * conv_dim + c0) = nxt;
+      }
+      if (HIST > 0)
+        *reinterpret_cast<uint4*>(cst + (int64_t)(HIST > 0 ? HIST - 1 : 0) * conv_dim + c0) = craw;
+    }
+  }
+  if (rows > 0) {
+    T* orow = static_cast<T*>(a.dst) + (int64_t)s * d_inner + h0 * P;
+    for (int i = threadIdx.x; i < rows / V; i += kDecodeThreads) {
+      const int c0 = h0 * P + i * V;
+      const int grp = c0 / gs;  // V divides gs, so a vector sits in one group
+      float tot = 0.0f;
+      for (int r2 = 0; r2 < a.cluster; ++r2) tot += ld_dsmem_f32(part + grp, (uint32_t)r2);
+      const float inv = rsqrtf(tot / (float)gs + a.eps);
+      float o[V];
+#pragma unroll
+      for (int j = 0; j < V; ++j) o[j] = ys[i * V + j] * inv * a.norm_w[c0 + j];
+      Vec16<T>::store(orow + i * V, o);
+    }
+  }
+  cluster_sync_all();
+}
+
+bool decode_supported(mamba2_dtype act, const mamba2_dims& d, int norm_groups) {
+  const int V = act == MAMBA2_BF16 ? 8 : 4;
+  const int nq = d.d_state / 4;
+  if (d.d_state % 4 != 0 || nq == 0) return false;
+  if (nq < 32 && (nq & (nq - 1)) != 0) return false;
+  if (d.headdim % V != 0 || (2 * d.ngroups * d.d_state) % V != 0) return false;
+  if (d.conv_kernel < 1 || d.conv_kernel > 4) return false;
+  if (norm_groups < 1 || norm_groups > kDecodeMaxNormGroups) return false;
+  const int d_inner = d.heads * d.headdim;
+  if (d_inner % norm_groups != 0 || (d_inner / norm_groups) % V != 0) return false;
+  return true;
+}
+
+template <typename T, int K>
+static cudaError_t launch_decode_t(const DecodeArgs& a, cudaStream_t st) {
+  const size_t smem = sizeof(float) * (2 * (size_t)a.heads_per_cta * a.headdim + 2 * (size_t)a.ngroups * a.d_state +
+                                       3 * (size_t)a.heads_per_cta + kDecodeMaxNormGroups + kDecodeWarps);
+  auto kern = decode_step_kernel<T, K>;
+  if (smem > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)a.cluster, (unsigned)a.tab.n, 1);
+  cfg.blockDim = dim3(kDecodeThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)a.cluster;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, a);
+}
+
+cudaError_t launch_decode(const DecodeArgs& a, mamba2_dtype act, cudaStream_t st) {
+  if (a.tab.n == 0) return cudaSuccess;
+  if (act == MAMBA2_BF16) {
+    switch (a.conv_kernel) {
+      case 1: return launch_decode_t<__nv_bfloat16, 1>(a, st);
+      case 2: return launch_decode_t<__nv_bfloat16, 2>(a, st);
+      case 3: return launch_decode_t<__nv_bfloat16, 3>(a, st);
+      case 4: return launch_decode_t<__nv_bfloat16, 4>(a, st);
+    }
+  } else {
+    switch (a.conv_kernel) {
+      case 1: return launch_decode_t<float, 1>(a, st);
+      case 2: return launch_decode_t<float, 2>(a, st);
+      case 3: return launch_decode_t<float, 3>(a, st);
+      case 4: return launch_decode_t<float, 4>(a, st);
+    }
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace mamba2

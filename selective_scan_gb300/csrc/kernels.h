@@ -1,0 +1,108 @@
+// Kernel argument blocks and launchers (internal to libmamba2).
+//
+// Every kernel takes one argument block by value (__grid_constant__), so the
+// batch table travels in the launch parameters: no device metadata buffers and
+// no host->device copies per call.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/mamba2.h"
+
+namespace mamba2 {
+
+// Batch table. Sequence i owns rows [cu[i], cu[i+1]); its slot is
+// slot_fresh[i] & 0x7fffffff and it is fresh when bit 31 is set. tile[i] is
+// the index of the sequence's first work tile (tile[n] = total tiles); each
+// kernel defines what a tile is (conv: kConvRows rows; scan: one segment).
+struct SeqTable {
+  int32_t n;
+  int32_t cu[MAMBA2_MAX_SEQS + 1];
+  uint32_t slot_fresh[MAMBA2_MAX_SEQS];
+  int32_t tile[MAMBA2_MAX_SEQS + 1];
+};
+
+// ---------------------------------------------------------------- conv ----
+constexpr int kConvThreads = 256;
+constexpr int kConvRows = 16;  // rows per work tile (>= kernel - 1)
+
+struct ConvArgs {
+  const void* x;
+  void* dst;
+  const float* weight;
+  const float* bias;
+  void* conv_state;
+  int32_t conv_dim;
+  SeqTable tab;
+};
+cudaError_t launch_conv1d(const ConvArgs& a, mamba2_dtype act, int kernel, cudaStream_t st);
+
+// ---------------------------------------------------------------- scan ----
+constexpr int kChunk = 64;  // tokens per chunk of the chunked scan
+
+struct ScanArgs {
+  void* dst;
+  const void* xbc;
+  const void* dt;
+  const float* A_log;
+  const float* dt_bias;
+  const float* D;
+  float* ssm_state;
+  float* ws_state;  // [segments, heads, P, N] (null when unsegmented)
+  float* ws_decay;  // [segments, heads]
+  int32_t heads, headdim, d_state, ngroups, conv_dim;
+  int32_t seg_chunks;  // chunks per segment (tile = segment)
+  SeqTable tab;
+};
+// True when the chunked tensor-core kernel covers this shape.
+bool scan_chunked_supported(mamba2_dtype act, int headdim, int d_state);
+// Chunked scan: state pass over all but the last segment of each sequence,
+// then the full pass. The serial kernel is the token-at-a-time fallback.
+cudaError_t launch_scan_chunked(const ScanArgs& a, cudaStream_t st);
+cudaError_t launch_scan_serial(const ScanArgs& a, mamba2_dtype act, cudaStream_t st);
+constexpr int kSerialMaxN = 256;
+constexpr int kSerialMaxP = 1024;
+
+// ---------------------------------------------------------------- norm ----
+struct NormArgs {
+  void* dst;
+  const void* x;
+  const void* z;
+  const float* weight;
+  int32_t rows;
+  int32_t dim;
+  int32_t groups;
+  float eps;
+};
+cudaError_t launch_gated_rmsnorm(const NormArgs& a, mamba2_dtype act, cudaStream_t st);
+
+// -------------------------------------------------------------- decode ----
+constexpr int kDecodeThreads = 256;
+constexpr int kDecodeMaxCluster = 8;
+constexpr int kDecodeMaxNormGroups = 64;
+
+struct DecodeArgs {
+  void* dst;
+  const void* xBC;
+  const void* z;
+  const void* dt;
+  const float* conv_w;
+  const float* conv_b;
+  const float* A_log;
+  const float* dt_bias;
+  const float* D;
+  const float* norm_w;
+  void* conv_state;
+  float* ssm_state;
+  int32_t heads, headdim, d_state, ngroups, conv_kernel;
+  int32_t norm_groups;
+  float eps;
+  int32_t cluster;         // CTAs per sequence
+  int32_t heads_per_cta;
+  SeqTable tab;
+};
+bool decode_supported(mamba2_dtype act, const mamba2_dims& d, int norm_groups);
+cudaError_t launch_decode(const DecodeArgs& a, mamba2_dtype act, cudaStream_t st);
+
+}  // namespace mamba2

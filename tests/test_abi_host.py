@@ -1,0 +1,117 @@
+"""Host-side checks of the C ABI (no GPU needed): the library loads, exports
+every function include/mamba2.h declares, and rejects malformed
+RecurrentBatches before touching any device pointer, with the same status the
+oracle returns (gllm PR #85 "feat(backend): Mamba2 ops, with CPU reference
+implementations", section "Ops": out-of-range slot, shared slot, runs that do
+not cover the rows)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import oracle
+import selective_scan_gb300 as ss
+import workloads as W
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(__file__)), "include", "mamba2.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(mamba2_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_exports_every_declared_symbol(product_lib):
+    names = declared_functions()
+    for op in ("mamba2_causal_conv1d", "mamba2_ssd_scan", "mamba2_gated_rmsnorm", "mamba2_decode_step"):
+        assert op in names
+    missing = [n for n in names if not hasattr(product_lib, n)]
+    assert not missing, missing
+
+
+def test_status_strings(product_lib):
+    for code in range(8):
+        s = ss.status_string(code)
+        assert s.startswith("MAMBA2_")
+    assert ss.status_string(ss.ERR_SLOT_SHARED) == "MAMBA2_ERR_SLOT_SHARED"
+
+
+def test_state_bytes_match_oracle_and_page(product_lib):
+    d = W.Dims(24, 64, 128, 1, 4)
+    per_layer = ss.state_bytes_per_layer(d, ss.BF16)
+    assert per_layer == oracle.state_bytes_per_layer(24, 64, 128, 1, 4, oracle.BF16)
+    assert round(24 * per_layer / 2 ** 20, 2) == 18.25
+    assert ss.state_bytes_per_layer(W.Dims(0, 64, 128, 1, 4)) == -1
+
+
+# fake, 16-byte aligned device addresses: a rejected call must never touch them
+FAKE = [0x10000 * (i + 1) for i in range(16)]
+
+BAD = [
+    ("slot out of range", [0, 3, 7], [0, 5], ss.ERR_SLOT_OUT_OF_RANGE),
+    ("negative slot", [0, 3, 7], [-1, 0], ss.ERR_SLOT_OUT_OF_RANGE),
+    ("shared slot", [0, 3, 7], [2, 2], ss.ERR_SLOT_SHARED),
+    ("runs short", [0, 3, 6], [0, 1], ss.ERR_RUNS_DONT_COVER_ROWS),
+    ("runs long", [0, 3, 9], [0, 1], ss.ERR_RUNS_DONT_COVER_ROWS),
+    ("non-monotone", [0, 5, 4], [0, 1], ss.ERR_RUNS_DONT_COVER_ROWS),
+    ("nonzero start", [2, 3, 7], [0, 1], ss.ERR_RUNS_DONT_COVER_ROWS),
+    ("range before shared", [0, 3, 7], [9, 9], ss.ERR_SLOT_OUT_OF_RANGE),
+]
+
+
+@pytest.mark.parametrize("name,cu,slots,status", BAD, ids=[b[0] for b in BAD])
+def test_rejections_match_oracle(product_lib, name, cu, slots, status):
+    num_slots, rows = 4, 7
+    assert oracle.validate_batch(cu, slots, num_slots, rows) == status
+    lib = product_lib
+    b = ss._Batch(cu, slots, [0] * len(slots))
+    st = lib.mamba2_causal_conv1d(FAKE[0], FAKE[1], FAKE[2], FAKE[3], FAKE[4], num_slots, rows, 128, 4,
+                                  ss.BF16, b.ref(), None)
+    assert st == status
+    d = ss.Dims(4, 16, 16, 2, 4)
+    st = lib.mamba2_ssd_scan(FAKE[0], FAKE[1], FAKE[2], FAKE[3], FAKE[4], FAKE[5], FAKE[6], num_slots, rows,
+                             ctypes.byref(d), ss.BF16, b.ref(), None, 0, None)
+    assert st == status
+
+
+def test_decode_rejections(product_lib):
+    lib = product_lib
+    d = ss.Dims(4, 16, 16, 2, 4)
+
+    def call(slots, cu=None, num_slots=4):
+        b = ss._Batch(cu, slots, [0] * len(slots))
+        return lib.mamba2_decode_step(*FAKE[:10], 2, 1e-5, FAKE[10], FAKE[11], num_slots, ctypes.byref(d),
+                                      ss.BF16, b.ref(), None)
+
+    assert call([0, 4]) == ss.ERR_SLOT_OUT_OF_RANGE
+    assert call([1, 1]) == ss.ERR_SLOT_SHARED
+    assert call([0, 1], cu=[0, 1, 3]) == ss.ERR_RUNS_DONT_COVER_ROWS  # 3 rows != 2 sequences
+    assert call([0, 1], cu=[0, 2, 2]) == ss.ERR_INVALID_ARGUMENT  # a run of 2 tokens
+
+
+def test_argument_checks(product_lib):
+    lib = product_lib
+    b = ss._Batch([0, 4], [0], [1])
+    # conv_dim * 2 bytes not a multiple of 16
+    assert lib.mamba2_causal_conv1d(FAKE[0], FAKE[1], FAKE[2], FAKE[3], FAKE[4], 1, 4, 100, 4, ss.BF16,
+                                    b.ref(), None) == ss.ERR_NOT_IMPLEMENTED
+    # misaligned activation pointer
+    assert lib.mamba2_causal_conv1d(FAKE[0], FAKE[1] + 2, FAKE[2], FAKE[3], FAKE[4], 1, 4, 128, 4, ss.BF16,
+                                    b.ref(), None) == ss.ERR_INVALID_ARGUMENT
+    # dst aliasing x
+    assert lib.mamba2_causal_conv1d(FAKE[1], FAKE[1], FAKE[2], FAKE[3], FAKE[4], 1, 4, 128, 4, ss.BF16,
+                                    b.ref(), None) == ss.ERR_INVALID_ARGUMENT
+    # heads not a multiple of ngroups
+    d = ss.Dims(3, 16, 16, 2, 4)
+    assert lib.mamba2_ssd_scan(*FAKE[:7], 1, 4, ctypes.byref(d), ss.BF16, b.ref(), None, 0,
+                               None) == ss.ERR_INVALID_ARGUMENT
+    # too many sequences for one call
+    n = ss.MAX_SEQS + 1
+    big = ss._Batch(list(range(n + 1)), list(range(n)), [1] * n)
+    assert lib.mamba2_causal_conv1d(FAKE[0], FAKE[1], FAKE[2], FAKE[3], FAKE[4], n, n, 128, 4, ss.BF16,
+                                    big.ref(), None) == ss.ERR_INVALID_ARGUMENT
+    # norm: groups must divide dim
+    assert lib.mamba2_gated_rmsnorm(FAKE[0], FAKE[1], FAKE[2], FAKE[3], 2, 64, 3, 1e-5, ss.BF16,
+                                    None) == ss.ERR_INVALID_ARGUMENT
