@@ -250,7 +250,7 @@ def run_ours(args, rank, world, local_rank):
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
     hbm, tf_burst, tf_sus, peak_kind = peaks()
-    wl = W.long_prefill(seed=4 + rank)
+    wl = W.long_prefill(seed=4 + rank, tokens=args.tokens)
     pf = Prefill(wl, dev)
     d = wl.dims
 
@@ -285,7 +285,7 @@ def run_ours(args, rank, world, local_rank):
         torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
         total_ms, t_prefill = tt.tolist()
 
-    T = TOKENS
+    T = args.tokens
     gb = lambda nbytes, ms: nbytes / (ms * 1e-3) / 1e9  # noqa: E731
     kern = {
         "conv": {"ms": t_conv, "bytes": conv_bytes(T, d), "GB/s": gb(conv_bytes(T, d), t_conv)},
@@ -352,7 +352,7 @@ def run_ours(args, rank, world, local_rank):
         "vs_baseline": None,
         "dtype": "bf16",
         "data": "synthetic (seeded N(0,1) activations, workload distributions)",
-        "config": {"workload": WORKLOAD, "tokens": T, "heads": d.heads, "headdim": d.headdim,
+        "config": {"workload": WORKLOAD if T == TOKENS else WORKLOAD.replace(str(TOKENS), str(T)), "tokens": T, "heads": d.heads, "headdim": d.headdim,
                    "d_state": d.d_state, "ngroups": d.ngroups, "conv_kernel": d.conv_kernel,
                    "decode_tail_steps": DECODE_TAIL, "chunk": 64,
                    "l2": "inputs larger than L2 (no flush)", "parallelism": f"replicas x{world}"},
@@ -420,6 +420,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--tokens", type=int, default=TOKENS, help="prefill length (profiling captures use less)")
     args = ap.parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

@@ -173,6 +173,7 @@ mamba2_status mamba2_causal_conv1d(void* dst, const void* x, const float* weight
   if (((size_t)conv_dim * act_size(act)) % 16 != 0) return MAMBA2_ERR_NOT_IMPLEMENTED;
   if (rb && rb->num_seqs > 0) {
     if (!weight || !bias || (kernel > 1 && !conv_state)) return MAMBA2_ERR_INVALID_ARGUMENT;
+    if (!aligned16(weight) || !aligned16(bias)) return MAMBA2_ERR_INVALID_ARGUMENT;
     if ((kernel > 1 && !aligned16(conv_state))) return MAMBA2_ERR_INVALID_ARGUMENT;
   }
   if (rows > 0 && (!dst || !x || !aligned16(dst) || !aligned16(x))) return MAMBA2_ERR_INVALID_ARGUMENT;

@@ -102,27 +102,31 @@ template <> struct Vec16<__nv_bfloat16> {
   }
 };
 
-__device__ __forceinline__ float silu_f(float v) { return v / (1.0f + __expf(-v)); }
+// silu(v) = v * sigmoid(v) with the fast exponential and reciprocal (a few ulp).
+__device__ __forceinline__ float silu_f(float v) { return __fdividef(v, 1.0f + __expf(-v)); }
 
 // softplus(v) = max(v, 0) + log1p(exp(-|v|)), no clamp.
 __device__ __forceinline__ float softplus_f(float v) {
   return fmaxf(v, 0.0f) + log1pf(__expf(-fabsf(v)));
 }
 
-// ---------------------------------------------------------------------------
-// Conv output rounded to bf16 as the double-precision definition rounds it.
-//
-// The value silu(bias + sum_k w_k u_k) is computed in fp32 together with a
-// bound on its error; when the fp32 value lies farther than that bound from
-// the bf16 rounding boundary nearest to it, its bf16 rounding equals that of
-// the exact value rounded first to fp32 and then to bf16. Otherwise (about
-// one element in a thousand) the value is recomputed in fp64 with separately
-// rounded multiplies and adds in tap order, and rounded double -> fp32 ->
-// bf16. This is Ziv's rounding test; it keeps the conv output, and so the
-// state it feeds, independent of fp32 rounding noise.
-// ---------------------------------------------------------------------------
+// fp64 evaluation of silu(bias + sum_k w_k u_k) with separately rounded
+// multiplies and adds in tap order, rounded double -> fp32 -> bf16.
 template <int K>
-__device__ __forceinline__ float conv_silu_bf16_exact(float bias, const float (&w)[K], const float (&u)[K]) {
+__device__ __forceinline__ float conv_silu_bf16_fp64(float bias, const float* w, const float* u) {
+  double pd = (double)bias;
+#pragma unroll
+  for (int k = 0; k < K; ++k) pd = __dadd_rn(pd, __dmul_rn((double)w[k], (double)u[k]));
+  const double vd = __ddiv_rn(pd, __dadd_rn(1.0, exp(-pd)));
+  return __bfloat162float(__float2bfloat16_rn(__double2float_rn(vd)));
+}
+
+// Fast half of the rounding test: the fp32 value rounded to bf16, with
+// `retry` set when the value lies within its error bound of a bf16 rounding
+// boundary (then only the fp64 evaluation decides the rounding).
+template <int K>
+__device__ __forceinline__ float conv_silu_bf16_fast(float bias, const float (&w)[K], const float (&u)[K],
+                                                     bool& retry) {
   float pre = bias;
   float mag = fabsf(bias);
 #pragma unroll
@@ -139,12 +143,38 @@ __device__ __forceinline__ float conv_silu_bf16_exact(float bias, const float (&
   const uint32_t bits = __float_as_uint(v);
   const float ulp = fmaxf(__uint_as_float(bits & 0x7f800000u) * 0x1p-23f, 0x1p-149f);
   const float dist = fabsf((float)((int)(bits & 0xffffu) - 0x8000)) * ulp;
-  if (dist > err + 2.0f * ulp && isfinite(v)) return __bfloat162float(__float2bfloat16_rn(v));
-  double pd = (double)bias;
+  retry = !(dist > err + 2.0f * ulp && isfinite(v));
+  return __bfloat162float(__float2bfloat16_rn(v));
+}
+
+// Conv output rounded to bf16 as the double-precision definition rounds it.
+//
+// The value silu(bias + sum_k w_k u_k) is computed in fp32 together with a
+// bound on its error; when the fp32 value lies farther than that bound from
+// the bf16 rounding boundary nearest to it, its bf16 rounding equals that of
+// the exact value rounded first to fp32 and then to bf16. Otherwise (about
+// one element in a thousand) the value is recomputed in fp64. This is Ziv's
+// rounding test; it keeps the conv output, and so the state it feeds,
+// independent of fp32 rounding noise.
+template <int K>
+__device__ __forceinline__ float conv_silu_bf16_exact(float bias, const float (&w)[K], const float (&u)[K]) {
+  bool retry;
+  const float v = conv_silu_bf16_fast<K>(bias, w, u, retry);
+  return retry ? conv_silu_bf16_fp64<K>(bias, w, u) : v;
+}
+
+// Conv output for one channel at the activation type: bf16 through the exact
+// rounding test, fp32 as computed.
+template <typename T, int K>
+__device__ __forceinline__ float conv_silu_act(float bias, const float (&w)[K], const float (&u)[K]) {
+  if constexpr (Act<T>::code == MAMBA2_BF16) {
+    return conv_silu_bf16_exact<K>(bias, w, u);
+  } else {
+    float acc = bias;
 #pragma unroll
-  for (int k = 0; k < K; ++k) pd = __dadd_rn(pd, __dmul_rn((double)w[k], (double)u[k]));
-  const double vd = __ddiv_rn(pd, __dadd_rn(1.0, exp(-pd)));
-  return __bfloat162float(__float2bfloat16_rn(__double2float_rn(vd)));
+    for (int k = 0; k < K; ++k) acc = fmaf(w[k], u[k], acc);
+    return silu_f(acc);
+  }
 }
 
 }  // namespace mamba2

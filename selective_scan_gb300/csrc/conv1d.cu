@@ -19,13 +19,18 @@
 // Memory: each input row is read once by its tile plus kernel-1 window rows
 // read again by the next tile (L2 hits); each output row written once. The
 // kernel is HBM-bound: 2 * conv_dim * sizeof(act) bytes per row.
+//
+// Rounding: bf16 outputs are rounded exactly as the double-precision
+// definition rounds them (Ziv's test with an fp64 retry, conv_silu_act), so
+// the scan downstream sees the same conv output whether or not the conv ran
+// here.
 #include "common.cuh"
 #include "kernels.h"
 
 namespace mamba2 {
 
 template <typename T, int K>
-__global__ void __launch_bounds__(kConvThreads)
+__global__ void __launch_bounds__(kConvThreads, 2)
 conv1d_silu_kernel(const __grid_constant__ ConvArgs a) {
   constexpr int V = Vec16<T>::n;
   constexpr int H = K - 1;  // history rows
@@ -48,61 +53,90 @@ conv1d_silu_kernel(const __grid_constant__ ConvArgs a) {
   T* dst = static_cast<T*>(a.dst);
   T* cst = static_cast<T*>(a.conv_state);
 
-  // taps and bias for this thread's channels
+  // taps and bias for this thread's channels (16-byte loads: V*K floats are
+  // contiguous and 16-byte aligned since V*4 bytes is)
   float w[K][V], b[V];
+  {
+    const float4* wp = reinterpret_cast<const float4*>(a.weight + (int64_t)c0 * K);
 #pragma unroll
-  for (int j = 0; j < V; ++j) {
-    b[j] = a.bias[c0 + j];
+    for (int q = 0; q < V * K / 4; ++q) {
+      const float4 f = __ldg(wp + q);
+      const float e[4] = {f.x, f.y, f.z, f.w};
 #pragma unroll
-    for (int k = 0; k < K; ++k) w[k][j] = a.weight[(int64_t)(c0 + j) * K + k];
+      for (int i = 0; i < 4; ++i) w[(4 * q + i) % K][(4 * q + i) / K] = e[i];
+    }
+    const float4* bp = reinterpret_cast<const float4*>(a.bias + c0);
+#pragma unroll
+    for (int q = 0; q < V / 4; ++q) {
+      const float4 f = __ldg(bp + q);
+      b[4 * q] = f.x; b[4 * q + 1] = f.y; b[4 * q + 2] = f.z; b[4 * q + 3] = f.w;
+    }
   }
 
-  // window = u[q0 .. q0 + H - 1] = conv inputs at positions q0 - H .. q0 - 1
-  uint4 raw_hist[H > 0 ? H : 1];
-  float win[H > 0 ? H : 1][V];
+  // raw conv inputs u[q0 .. q0 + H + kConvRows - 1] (positions q0 - H ..): the
+  // H window rows before the tile, then the tile's rows; tap k of tile row r is
+  // rows[r + k]. Loads first, then the K-tap dot products.
+  uint4 rows[H + kConvRows];
 #pragma unroll
   for (int i = 0; i < H; ++i) {
     const int pos = q0 - H + i;
-    uint4 r;
     if (pos >= 0) {
-      r = *reinterpret_cast<const uint4*>(x + (int64_t)(row0 + pos) * a.conv_dim + c0);
+      rows[i] = *reinterpret_cast<const uint4*>(x + (int64_t)(row0 + pos) * a.conv_dim + c0);
     } else if (fresh) {
-      r = make_uint4(0u, 0u, 0u, 0u);
+      rows[i] = make_uint4(0u, 0u, 0u, 0u);
     } else {
-      r = *reinterpret_cast<const uint4*>(cst + slot_base + (int64_t)(H + pos) * a.conv_dim + c0);
+      rows[i] = *reinterpret_cast<const uint4*>(cst + slot_base + (int64_t)(H + pos) * a.conv_dim + c0);
     }
-    raw_hist[i] = r;
-    Vec16<T>::load(reinterpret_cast<const T*>(&r), win[i]);
   }
-
-  // the tile's rows: loads first, then the K-tap dot products
-  uint4 in[kConvRows];
 #pragma unroll
   for (int r = 0; r < kConvRows; ++r)
     if (r < nrows)
-      in[r] = *reinterpret_cast<const uint4*>(x + (int64_t)(row0 + q0 + r) * a.conv_dim + c0);
+      rows[H + r] = *reinterpret_cast<const uint4*>(x + (int64_t)(row0 + q0 + r) * a.conv_dim + c0);
+  uint64_t retry_mask = 0;  // (row, channel) outputs the fast rounding test could not decide
+  static_assert(kConvRows * V <= 64, "retry mask width");
 #pragma unroll
   for (int r = 0; r < kConvRows; ++r) {
     if (r < nrows) {
-      float cur[V], out[V];
-      Vec16<T>::load(reinterpret_cast<const T*>(&in[r]), cur);
+      float u[K][V], out[V];
+#pragma unroll
+      for (int k = 0; k < K; ++k) Vec16<T>::load(reinterpret_cast<const T*>(&rows[r + k]), u[k]);
 #pragma unroll
       for (int j = 0; j < V; ++j) {
-        float acc = b[j];
+        float wk[K], uk[K];
 #pragma unroll
-        for (int k = 0; k < H; ++k) acc = fmaf(w[k][j], win[k][j], acc);
-        acc = fmaf(w[H][j], cur[j], acc);
-        out[j] = silu_f(acc);
+        for (int k = 0; k < K; ++k) {
+          wk[k] = w[k][j];
+          uk[k] = u[k][j];
+        }
+        if constexpr (Act<T>::code == MAMBA2_BF16) {
+          bool retry;
+          out[j] = conv_silu_bf16_fast<K>(b[j], wk, uk, retry);
+          if (retry) retry_mask |= 1ull << (r * V + j);
+        } else {
+          out[j] = conv_silu_act<T, K>(b[j], wk, uk);
+        }
       }
       Vec16<T>::store(dst + (int64_t)(row0 + q0 + r) * a.conv_dim + c0, out);
-#pragma unroll
-      for (int k = 0; k + 1 < H; ++k)
-#pragma unroll
-        for (int j = 0; j < V; ++j) win[k][j] = win[k + 1][j];
-      if (H > 0)
-#pragma unroll
-        for (int j = 0; j < V; ++j) win[H > 0 ? H - 1 : 0][j] = cur[j];
     }
+  }
+
+  // fp64 retry of the undecided outputs (about one in a thousand); inputs are
+  // re-read from memory (the slot is still unmodified here)
+  while (retry_mask) {
+    const int i = __ffsll((long long)retry_mask) - 1;
+    retry_mask &= retry_mask - 1;
+    const int r = i / V, j = i % V, c = c0 + j;
+    float wk[K], uk[K];
+#pragma unroll
+    for (int k = 0; k < K; ++k) {
+      wk[k] = a.weight[(int64_t)c * K + k];
+      const int pos = q0 + r - H + k;  // conv input position of tap k
+      float uv = 0.0f;
+      if (pos >= 0) uv = Act<T>::to_f(x[(int64_t)(row0 + pos) * a.conv_dim + c]);
+      else if (!fresh) uv = Act<T>::to_f(cst[slot_base + (int64_t)(H + pos) * a.conv_dim + c]);
+      uk[k] = uv;
+    }
+    dst[(int64_t)(row0 + q0 + r) * a.conv_dim + c] = Act<T>::from_f(conv_silu_bf16_fp64<K>(a.bias[c], wk, uk));
   }
 
   // slot update by tile 0: new history = u[T .. T + H - 1] (bit copies)
@@ -113,11 +147,10 @@ conv1d_silu_kernel(const __grid_constant__ ConvArgs a) {
       uint4 r = make_uint4(0u, 0u, 0u, 0u);
       if (upos >= H) {
         r = *reinterpret_cast<const uint4*>(x + (int64_t)(row0 + upos - H) * a.conv_dim + c0);
-      } else {
-        // old history (zeros when fresh); only when the run is shorter than H
-#pragma unroll
-        for (int i = 0; i < H; ++i)
-          if (i == upos) r = raw_hist[i];
+      } else if (!fresh) {
+        // old history row upos (only when the run is shorter than H); rows
+        // below j are already rewritten, but upos > j, so row upos is not
+        r = *reinterpret_cast<const uint4*>(cst + slot_base + (int64_t)upos * a.conv_dim + c0);
       }
       *reinterpret_cast<uint4*>(cst + slot_base + (int64_t)j * a.conv_dim + c0) = r;
     }

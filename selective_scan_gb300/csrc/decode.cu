@@ -27,8 +27,6 @@
 // HBM traffic per sequence: SSM state read + write (H*P*N*4 bytes each), conv
 // history read + write, the token's inputs and outputs. The state stream is
 // the roofline term.
-#include <type_traits>
-
 #include "common.cuh"
 
 namespace mamba2 {
@@ -110,14 +108,7 @@ decode_step_kernel(const __grid_constant__ DecodeArgs a) {
         wk[k] = a.conv_w[(int64_t)(c0 + j) * K + k];
         uk[k] = k < HIST ? hist[k < HIST ? k : 0][j] : cur[j];
       }
-      if constexpr (std::is_same<T, __nv_bfloat16>::value) {
-        out[j] = conv_silu_bf16_exact<K>(a.conv_b[c0 + j], wk, uk);
-      } else {
-        float acc = a.conv_b[c0 + j];
-#pragma unroll
-        for (int k = 0; k < K; ++k) acc = fmaf(wk[k], uk[k], acc);
-        out[j] = silu_f(acc);
-      }
+      out[j] = conv_silu_act<T, K>(a.conv_b[c0 + j], wk, uk);
     }
     float* o = is_x ? xs + i * V : bc + (c0 - d_inner);
 #pragma unroll

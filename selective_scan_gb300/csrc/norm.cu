@@ -4,27 +4,29 @@
 // implementations", section "Ops" (GatedRMSNorm, the gate applied before the
 // norm, the RMS taken per group).
 //
-// One warp per (row, group). Each lane holds up to kMaxVec 16-byte vectors of
-// the group in registers (x * silu(z) in fp32), so x and z are read from HBM
-// exactly once and the output written once: 3 * dim * sizeof(act) bytes per
-// row, HBM-bound. Groups wider than 32 * kMaxVec vectors are streamed twice
-// (the second pass mostly hits L2).
+// One CTA of kNormThreads per (row, group). Each thread holds up to kVPT
+// 16-byte vectors of the group in registers (x * silu(z) in fp32), so x and z
+// are read from HBM exactly once and the output written once:
+// 3 * dim * sizeof(act) bytes per row, HBM-bound. The sum of squares is
+// reduced warp by warp and then across the CTA's warps in a fixed order
+// (deterministic). Groups wider than kNormThreads * kVPT vectors stream the
+// remainder twice (the second pass mostly hits L2).
 #include "common.cuh"
 
 namespace mamba2 {
 
-constexpr int kNormWarps = 8;
-constexpr int kMaxVec = 12;
+constexpr int kNormThreads = 128;
+constexpr int kVPT = 4;  // 16-byte vectors per thread kept in registers
 
 template <typename T>
-__global__ void __launch_bounds__(kNormWarps * 32)
+__global__ void __launch_bounds__(kNormThreads)
 gated_rmsnorm_kernel(const NormArgs a) {
   constexpr int V = Vec16<T>::n;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t item = (int64_t)blockIdx.x * kNormWarps + warp;
-  if (item >= (int64_t)a.rows * a.groups) return;
+  __shared__ float wsum[kNormThreads / 32];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int64_t item = blockIdx.x;  // (row, group)
   const int gs = a.dim / a.groups;
-  const int nv = gs / V;  // vectors in the group
+  const int nv = gs / V;
   const int64_t row = item / a.groups;
   const int grp = (int)(item - row * a.groups);
   const int64_t base = row * a.dim + (int64_t)grp * gs;
@@ -33,15 +35,24 @@ gated_rmsnorm_kernel(const NormArgs a) {
   T* out = static_cast<T*>(a.dst) + base;
   const float* w = a.weight + (int64_t)grp * gs;
 
-  float v[kMaxVec][V];
+  uint4 xr[kVPT], zr[kVPT];
+#pragma unroll
+  for (int i = 0; i < kVPT; ++i) {
+    const int vi = tid + kNormThreads * i;
+    if (vi < nv) {
+      xr[i] = __ldcs(reinterpret_cast<const uint4*>(x + vi * V));
+      zr[i] = __ldcs(reinterpret_cast<const uint4*>(z + vi * V));
+    }
+  }
+  float v[kVPT][V];
   float ss = 0.0f;
 #pragma unroll
-  for (int i = 0; i < kMaxVec; ++i) {
-    const int vi = lane + 32 * i;
+  for (int i = 0; i < kVPT; ++i) {
+    const int vi = tid + kNormThreads * i;
     if (vi < nv) {
       float xv[V], zv[V];
-      Vec16<T>::load_stream(x + vi * V, xv);
-      Vec16<T>::load_stream(z + vi * V, zv);
+      Vec16<T>::load(reinterpret_cast<const T*>(&xr[i]), xv);
+      Vec16<T>::load(reinterpret_cast<const T*>(&zr[i]), zv);
 #pragma unroll
       for (int j = 0; j < V; ++j) {
         v[i][j] = xv[j] * silu_f(zv[j]);
@@ -49,7 +60,7 @@ gated_rmsnorm_kernel(const NormArgs a) {
       }
     }
   }
-  for (int vi = lane + 32 * kMaxVec; vi < nv; vi += 32) {  // wide groups
+  for (int vi = tid + kNormThreads * kVPT; vi < nv; vi += kNormThreads) {  // wide groups
     float xv[V], zv[V];
     Vec16<T>::load(x + vi * V, xv);
     Vec16<T>::load(z + vi * V, zv);
@@ -61,11 +72,16 @@ gated_rmsnorm_kernel(const NormArgs a) {
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-  const float inv = rsqrtf(ss / (float)gs + a.eps);
+  if (lane == 0) wsum[warp] = ss;
+  __syncthreads();
+  float tot = 0.0f;
+#pragma unroll
+  for (int i = 0; i < kNormThreads / 32; ++i) tot += wsum[i];
+  const float inv = rsqrtf(tot / (float)gs + a.eps);
 
 #pragma unroll
-  for (int i = 0; i < kMaxVec; ++i) {
-    const int vi = lane + 32 * i;
+  for (int i = 0; i < kVPT; ++i) {
+    const int vi = tid + kNormThreads * i;
     if (vi < nv) {
       float o[V];
       const float4* wp = reinterpret_cast<const float4*>(w + vi * V);
@@ -80,7 +96,7 @@ gated_rmsnorm_kernel(const NormArgs a) {
       Vec16<T>::store_stream(out + vi * V, o);
     }
   }
-  for (int vi = lane + 32 * kMaxVec; vi < nv; vi += 32) {
+  for (int vi = tid + kNormThreads * kVPT; vi < nv; vi += kNormThreads) {
     float xv[V], zv[V], o[V];
     Vec16<T>::load(x + vi * V, xv);
     Vec16<T>::load(z + vi * V, zv);
@@ -93,11 +109,11 @@ gated_rmsnorm_kernel(const NormArgs a) {
 cudaError_t launch_gated_rmsnorm(const NormArgs& a, mamba2_dtype act, cudaStream_t st) {
   const int64_t items = (int64_t)a.rows * a.groups;
   if (items == 0) return cudaSuccess;
-  const int64_t blocks = (items + kNormWarps - 1) / kNormWarps;
+  if (items > 0x7fffffffLL) return cudaErrorInvalidValue;
   if (act == MAMBA2_BF16)
-    gated_rmsnorm_kernel<__nv_bfloat16><<<(unsigned)blocks, kNormWarps * 32, 0, st>>>(a);
+    gated_rmsnorm_kernel<__nv_bfloat16><<<(unsigned)items, kNormThreads, 0, st>>>(a);
   else
-    gated_rmsnorm_kernel<float><<<(unsigned)blocks, kNormWarps * 32, 0, st>>>(a);
+    gated_rmsnorm_kernel<float><<<(unsigned)items, kNormThreads, 0, st>>>(a);
   return cudaGetLastError();
 }
 

@@ -20,17 +20,20 @@
 // direction (<= 0), so nothing overflows for any decay.
 //
 // CTA = (sequence segment, head), 4 warps. Warp w owns token rows
-// [16w, 16w+16) of the chunk for y, and a 16-row block of the state for the
-// chunk-state product. Per chunk (m16n8k16 bf16 MMAs, fp32 accumulate):
-//   Y  = C . H^T            (H = running state, kept as a bf16 copy in smem)
-//   Y *= exp(s_t)
-//   CB = C . B^T            (only the causal column blocks)
-//   M  = CB o exp(s_t - s_j) dt'_j  (in registers: accumulator -> A operand)
-//   Y += M . X ;  y = Y + D x  -> bf16
-//   H  = exp(s_{Q-1}) H + (X o w)^T . B,  w_j = exp(s_{Q-1} - s_j) dt'_j
+// [16w, 16w+16) of the chunk for y, and state rows p in [16w, 16w+16) (all
+// d_state columns, fp32 registers) for the state products. Per chunk
+// (m16n8k16 bf16 MMAs, fp32 accumulate):
+//   Yoff^T = H . C^T             (state-row warps; A = H straight from the
+//                                 accumulator registers, scaled by exp(s_t),
+//                                 staged in smem as fp32)
+//   CB     = C . B^T             (token-row warps, causal column blocks only)
+//   M      = CB o exp(s_t - s_j) dt'_j   (accumulator -> A operand in registers)
+//   Y      = M . X ;  y = Y + Yoff + D x  -> bf16
+//   H      = exp(s_{Q-1}) H + (X o w)^T . B,  w_j = exp(s_{Q-1} - s_j) dt'_j
 // The running state H stays in fp32 registers across chunks (it never goes
-// to HBM between chunks). (X o w) is split into bf16 hi + lo parts (two MMAs)
-// so the state product keeps ~16 mantissa bits.
+// to HBM between chunks). Every fp32 operand (H, M, X o w) is split into bf16
+// hi + lo parts (two MMAs), which keeps ~16 mantissa bits: the sums feeding y
+// can cancel strongly, and plain bf16 operands then lose the output.
 //
 // Long runs are cut into segments of seg_chunks chunks so enough CTAs run.
 // A state pass (kFull = false) computes each segment's end state from zero
@@ -99,7 +102,7 @@ struct ScanSmem {
   __nv_bfloat16 x[2][kQ][XS];
   __nv_bfloat16 b[2][kQ][BS];
   __nv_bfloat16 c[2][kQ][BS];
-  __nv_bfloat16 h[P][BS];  // bf16 copy of the running state (operand of C.H^T)
+  float yoff[kQ][P + 4];   // exp(s_t) * C_t . H (fp32), token-major
   float s[kQ];             // inclusive cumulative log-decay within the chunk
   float dtp[kQ];           // dt'
   float w[kQ];             // exp(s_{Q-1} - s_j) * dt'_j
@@ -110,12 +113,10 @@ template <int P, int N, bool kFull>
 __global__ void __launch_bounds__(kThreads, 2)
 ssd_chunk_kernel(const __grid_constant__ ScanArgs a) {
   using Sm = ScanSmem<P, N>;
-  constexpr int NT = N / 8;                          // 8-wide state column tiles
-  constexpr int PB = P / 16;                         // 16-row state blocks
-  constexpr int TILES = PB * NT;
-  constexpr int TPW = (TILES + kWarps - 1) / kWarps; // state tiles per warp
-  static_assert(P % 16 == 0 && N % 16 == 0, "tile shape");
-  static_assert(NT % TPW == 0 || TPW == 1, "a warp's state tiles share one row block");
+  constexpr int NT = N / 8;   // 8-wide state column tiles
+  constexpr int PB = P / 16;  // 16-row state blocks, one per warp
+  constexpr int TPW = NT;     // state tiles per owning warp (a full row block)
+  static_assert(P % 16 == 0 && N % 16 == 0 && PB <= kWarps, "tile shape");
 
   extern __shared__ __align__(128) unsigned char smem_raw[];
   Sm& sm = *reinterpret_cast<Sm*>(smem_raw);
@@ -146,11 +147,10 @@ ssd_chunk_kernel(const __grid_constant__ ScanArgs a) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int gq = lane >> 2, tq = lane & 3;
 
-  // ---- state tiles owned by this warp: rows pb*16 + {gq, gq+8}, cols nt*8 + 2tq + {0,1}
-  const int tile0 = warp * TPW;
-  const int pb = (tile0 < TILES) ? tile0 / NT : 0;
-  const int nt0 = (tile0 < TILES) ? tile0 % NT : 0;
-  const bool owns = tile0 < TILES;
+  // ---- state rows owned by this warp: rows pb*16 + {gq, gq+8}, cols nt*8 + 2tq + {0,1}
+  const int pb = warp;
+  const int nt0 = 0;
+  const bool owns = warp < PB;
   float hreg[TPW][4];
 
   const int64_t head_off = (int64_t)h * P * N;
@@ -175,15 +175,6 @@ ssd_chunk_kernel(const __grid_constant__ ScanArgs a) {
       const int r0 = pb * 16 + gq, cn = (nt0 + i) * 8 + 2 * tq;
       *reinterpret_cast<float2*>(dst + (int64_t)r0 * N + cn) = make_float2(hreg[i][0], hreg[i][1]);
       *reinterpret_cast<float2*>(dst + (int64_t)(r0 + 8) * N + cn) = make_float2(hreg[i][2], hreg[i][3]);
-    }
-  };
-  auto state_to_smem = [&]() {
-    if (!owns) return;
-#pragma unroll
-    for (int i = 0; i < TPW; ++i) {
-      const int r0 = pb * 16 + gq, cn = (nt0 + i) * 8 + 2 * tq;
-      *reinterpret_cast<uint32_t*>(&sm.h[r0][cn]) = pack_bf16(hreg[i][0], hreg[i][1]);
-      *reinterpret_cast<uint32_t*>(&sm.h[r0 + 8][cn]) = pack_bf16(hreg[i][2], hreg[i][3]);
     }
   };
 
@@ -213,7 +204,6 @@ ssd_chunk_kernel(const __grid_constant__ ScanArgs a) {
       }
     }
   }
-  if (kFull) state_to_smem();
 
   // ---- chunk loads (cp.async, zero-filled past the run's end)
   auto issue_chunk = [&](int c, int buf) {
@@ -258,7 +248,7 @@ ssd_chunk_kernel(const __grid_constant__ ScanArgs a) {
     const int buf = (c - c_begin) & 1;
     const int len = min(kQ, T - c * kQ);
     cp_async_wait_all();
-    __syncthreads();  // chunk c staged; previous chunk's readers of buf^1 and of sm.h are done
+    __syncthreads();  // chunk c staged; the previous chunk's readers of buf^1 and sm.yoff are done
     if (c + 1 < c_end) issue_chunk(c + 1, buf ^ 1);
 
     // dt', inclusive cumulative log-decay, and the state weights w
@@ -290,40 +280,59 @@ ssd_chunk_kernel(const __grid_constant__ ScanArgs a) {
     __syncthreads();
 
     if (kFull) {
-      // ---------------- y for rows [16*warp, 16*warp + 16) ----------------
+      // ---------------- Yoff^T = H . C^T on the state-row warps --------------
+      // A = H rows [16 pb, 16 pb + 16) x n, straight from the accumulator
+      // registers (hi + lo bf16); B = C^T (n x t) from sm.c rows t.
+      if (owns) {
+        float yo[kQ / 8][4];
+#pragma unroll
+        for (int i = 0; i < kQ / 8; ++i) yo[i][0] = yo[i][1] = yo[i][2] = yo[i][3] = 0.f;
+#pragma unroll
+        for (int kk = 0; kk < N / 16; ++kk) {
+          uint32_t ahi[4], alo[4];
+          const float hv[4][2] = {{hreg[2 * kk][0], hreg[2 * kk][1]},
+                                  {hreg[2 * kk][2], hreg[2 * kk][3]},
+                                  {hreg[2 * kk + 1][0], hreg[2 * kk + 1][1]},
+                                  {hreg[2 * kk + 1][2], hreg[2 * kk + 1][3]}};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            ahi[e] = pack_bf16(hv[e][0], hv[e][1]);
+            alo[e] = pack_bf16(hv[e][0] - bf16_lo(ahi[e]), hv[e][1] - bf16_hi(ahi[e]));
+          }
+#pragma unroll
+          for (int tp = 0; tp < kQ / 16; ++tp) {
+            uint32_t bf[4];
+            const int rr = tp * 16 + (lane & 7) + ((lane >> 4) << 3);
+            const int cc = kk * 16 + ((lane >> 3) & 1) * 8;
+            ldsm_x4(smem_u32(&sm.c[buf][rr][cc]), bf);
+            mma_bf16(yo[2 * tp], ahi, bf[0], bf[1]);
+            mma_bf16(yo[2 * tp], alo, bf[0], bf[1]);
+            mma_bf16(yo[2 * tp + 1], ahi, bf[2], bf[3]);
+            mma_bf16(yo[2 * tp + 1], alo, bf[2], bf[3]);
+          }
+        }
+        // scale column t by exp(s_t) and stage token-major in smem
+#pragma unroll
+        for (int i = 0; i < kQ / 8; ++i) {
+          const int t0 = i * 8 + 2 * tq;
+          const float e0 = __expf(sm.s[t0]), e1 = __expf(sm.s[t0 + 1]);
+          const int p0 = pb * 16 + gq;
+          sm.yoff[t0][p0] = yo[i][0] * e0;
+          sm.yoff[t0 + 1][p0] = yo[i][1] * e1;
+          sm.yoff[t0][p0 + 8] = yo[i][2] * e0;
+          sm.yoff[t0 + 1][p0 + 8] = yo[i][3] * e1;
+        }
+      }
+
+      // ---------------- y for token rows [16 warp, 16 warp + 16) --------------
       constexpr int PT = P / 8;  // 8-wide column tiles of y
       float yacc[PT][4];
 #pragma unroll
       for (int i = 0; i < PT; ++i) yacc[i][0] = yacc[i][1] = yacc[i][2] = yacc[i][3] = 0.f;
       const int m0 = warp * 16;
       const int lrow = lane & 15, lcol8 = (lane >> 4) * 8;  // A-operand ldmatrix lane address
-      // Y = C . H^T
-#pragma unroll
-      for (int kk = 0; kk < N / 16; ++kk) {
-        uint32_t af[4];
-        ldsm_x4(smem_u32(&sm.c[buf][m0 + lrow][kk * 16 + lcol8]), af);
-        if constexpr (PT >= 2) {
-#pragma unroll
-          for (int pt = 0; pt < PT; pt += 2) {
-            uint32_t bf[4];
-            const int rr = pt * 8 + (lane & 7) + ((lane >> 4) << 3);
-            const int cc = kk * 16 + ((lane >> 3) & 1) * 8;
-            ldsm_x4(smem_u32(&sm.h[rr][cc]), bf);
-            mma_bf16(yacc[pt], af, bf[0], bf[1]);
-            mma_bf16(yacc[pt + 1], af, bf[2], bf[3]);
-          }
-        }
-      }
       const int t_lo = m0 + gq, t_hi = t_lo + 8;
       const float st_lo = sm.s[t_lo], st_hi = sm.s[t_hi];
-      {
-        const float e_lo = __expf(st_lo), e_hi = __expf(st_hi);
-#pragma unroll
-        for (int i = 0; i < PT; ++i) {
-          yacc[i][0] *= e_lo; yacc[i][1] *= e_lo;
-          yacc[i][2] *= e_hi; yacc[i][3] *= e_hi;
-        }
-      }
       // CB = C . B^T for causal column blocks j < 16*(warp+1)
       float cb[kQ / 8][4];
 #pragma unroll
@@ -344,38 +353,43 @@ ssd_chunk_kernel(const __grid_constant__ ScanArgs a) {
           }
         }
       }
-      // M = CB o exp(s_t - s_j) dt'_j (j <= t), then Y += M . X
+      // M = CB o exp(s_t - s_j) dt'_j (j <= t) as hi + lo A operands; Y = M . X
 #pragma unroll
       for (int kk = 0; kk < kQ / 16; ++kk) {
         if (kk <= warp) {
-          uint32_t af[4];
+          float mv[4][2];  // {row lo k 0-7, row hi k 0-7, row lo k 8-15, row hi k 8-15}
 #pragma unroll
           for (int half = 0; half < 2; ++half) {
             const int jt = 2 * kk + half;
             const int j0 = jt * 8 + 2 * tq;
             const float sj0 = sm.s[j0], sj1 = sm.s[j0 + 1];
             const float dj0 = sm.dtp[j0], dj1 = sm.dtp[j0 + 1];
-            const float m00 = j0 <= t_lo ? cb[jt][0] * __expf(st_lo - sj0) * dj0 : 0.f;
-            const float m01 = j0 + 1 <= t_lo ? cb[jt][1] * __expf(st_lo - sj1) * dj1 : 0.f;
-            const float m10 = j0 <= t_hi ? cb[jt][2] * __expf(st_hi - sj0) * dj0 : 0.f;
-            const float m11 = j0 + 1 <= t_hi ? cb[jt][3] * __expf(st_hi - sj1) * dj1 : 0.f;
-            af[2 * half + 0] = pack_bf16(m00, m01);
-            af[2 * half + 1] = pack_bf16(m10, m11);
+            mv[2 * half][0] = j0 <= t_lo ? cb[jt][0] * __expf(st_lo - sj0) * dj0 : 0.f;
+            mv[2 * half][1] = j0 + 1 <= t_lo ? cb[jt][1] * __expf(st_lo - sj1) * dj1 : 0.f;
+            mv[2 * half + 1][0] = j0 <= t_hi ? cb[jt][2] * __expf(st_hi - sj0) * dj0 : 0.f;
+            mv[2 * half + 1][1] = j0 + 1 <= t_hi ? cb[jt][3] * __expf(st_hi - sj1) * dj1 : 0.f;
           }
-          // af order for m16n8k16: {row lo k 0-7, row hi k 0-7, row lo k 8-15, row hi k 8-15}
-          uint32_t a4[4] = {af[0], af[1], af[2], af[3]};
+          uint32_t ahi[4], alo[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            ahi[e] = pack_bf16(mv[e][0], mv[e][1]);
+            alo[e] = pack_bf16(mv[e][0] - bf16_lo(ahi[e]), mv[e][1] - bf16_hi(ahi[e]));
+          }
 #pragma unroll
           for (int pt = 0; pt < PT; pt += 2) {
             uint32_t bf[4];
             const int rr = kk * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
             const int cc = pt * 8 + (lane >> 4) * 8;
             ldsm_x4_t(smem_u32(&sm.x[buf][rr][cc]), bf);
-            mma_bf16(yacc[pt], a4, bf[0], bf[1]);
-            mma_bf16(yacc[pt + 1], a4, bf[2], bf[3]);
+            mma_bf16(yacc[pt], ahi, bf[0], bf[1]);
+            mma_bf16(yacc[pt], alo, bf[0], bf[1]);
+            mma_bf16(yacc[pt + 1], ahi, bf[2], bf[3]);
+            mma_bf16(yacc[pt + 1], alo, bf[2], bf[3]);
           }
         }
       }
-      // y = Y + D x, rounded to bf16
+      __syncthreads();  // sm.yoff complete
+      // y = Y + Yoff + D x, rounded to bf16
       __nv_bfloat16* yout = static_cast<__nv_bfloat16*>(a.dst);
       const int64_t ldy = (int64_t)H * P;
 #pragma unroll
@@ -383,14 +397,14 @@ ssd_chunk_kernel(const __grid_constant__ ScanArgs a) {
         const int p = pt * 8 + 2 * tq;
         if (t_lo < len) {
           const __nv_bfloat162 xv = *reinterpret_cast<const __nv_bfloat162*>(&sm.x[buf][t_lo][p]);
-          const float y0 = fmaf(Dh, __low2float(xv), yacc[pt][0]);
-          const float y1 = fmaf(Dh, __high2float(xv), yacc[pt][1]);
+          const float y0 = fmaf(Dh, __low2float(xv), yacc[pt][0] + sm.yoff[t_lo][p]);
+          const float y1 = fmaf(Dh, __high2float(xv), yacc[pt][1] + sm.yoff[t_lo][p + 1]);
           *reinterpret_cast<uint32_t*>(yout + (row0 + (int64_t)c * kQ + t_lo) * ldy + x_col + p) = pack_bf16(y0, y1);
         }
         if (t_hi < len) {
           const __nv_bfloat162 xv = *reinterpret_cast<const __nv_bfloat162*>(&sm.x[buf][t_hi][p]);
-          const float y0 = fmaf(Dh, __low2float(xv), yacc[pt][2]);
-          const float y1 = fmaf(Dh, __high2float(xv), yacc[pt][3]);
+          const float y0 = fmaf(Dh, __low2float(xv), yacc[pt][2] + sm.yoff[t_hi][p]);
+          const float y1 = fmaf(Dh, __high2float(xv), yacc[pt][3] + sm.yoff[t_hi][p + 1]);
           *reinterpret_cast<uint32_t*>(yout + (row0 + (int64_t)c * kQ + t_hi) * ldy + x_col + p) = pack_bf16(y0, y1);
         }
       }
@@ -447,10 +461,6 @@ ssd_chunk_kernel(const __grid_constant__ ScanArgs a) {
         }
       }
       if (!kFull) seg_logdecay += tot;
-    }
-    if (kFull) {
-      __syncthreads();  // every warp is done reading sm.h for this chunk
-      state_to_smem();
     }
   }
 

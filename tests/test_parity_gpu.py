@@ -16,7 +16,8 @@ import oracle
 import selective_scan_gb300 as ss
 import workloads as W
 from tests.gpu_util import device, gpu_conv, gpu_norm, gpu_scan, oracle_prefill, slot_rel_l2
-from tests.util import (STATE_DECODE_REL_L2, STATE_PREFILL_REL_L2, assert_bits_equal, check_act, rel_l2)
+from tests.util import (STATE_DECODE_REL_L2, STATE_PREFILL_REL_L2, assert_bits_equal, check_act,
+                        bf16_ulp, norm_gain, rel_l2)
 
 pytestmark = pytest.mark.gpu
 
@@ -49,11 +50,20 @@ def _prefill_parity(wl):
     out = gpu_norm(wl, dev, ref["y"])
     torch.cuda.synchronize()
     check_act(out.cpu(), ref["out64"], "norm output")
-    # chained: conv -> scan -> norm entirely on the GPU
+    # chained: conv -> scan -> norm entirely on the GPU. y is a rounding point
+    # of both pipelines: the norm carries the y difference (within the y
+    # tolerance, plus one bf16 step where the two round apart) to the output,
+    # scaled by its local gain d out / d y.
     y2, ssm2 = gpu_scan(wl, dev, xbc)
     out2 = gpu_norm(wl, dev, y2)
     torch.cuda.synchronize()
-    check_act(out2.cpu(), ref["out64"], "chained output")
+    if wl.act == torch.bfloat16:
+        check_act(y2.cpu(), ref["y64"], "chained scan output")
+        gain = norm_gain(ref["y"], wl.z, wl.params.norm_w, wl.params.norm_groups, wl.params.eps)
+        dy = (y2.cpu().double() - ref["y"].double()).abs() + bf16_ulp(ref["y"])
+        check_act(out2.cpu(), ref["out64"], "chained output", extra=gain * dy)
+    else:
+        check_act(out2.cpu(), ref["out64"], "chained output")
     rl2 = slot_rel_l2(ssm2, ref["ssm"], b.slots)
     assert rl2 <= STATE_PREFILL_REL_L2, f"chained ssm state rel L2 {rl2:.3g}"
     return ref, dict(xbc=xbc, y=y2, out=out2, ssm=ssm2, conv=conv)
@@ -132,7 +142,8 @@ def test_split_equals_whole_gpu():
     torch.cuda.synchronize()
     assert_bits_equal(torch.cat(xs).cpu(), xbc_w.cpu(), "conv output split vs whole")
     assert_bits_equal(conv_s.cpu(), conv_w.cpu(), "conv state split vs whole")
-    assert rel_l2(ssm_s.cpu()[1], ssm_w.cpu()[1]) <= 1e-6
+    # the cuts are not chunk-aligned, so the chunking differs: operand precision ~2^-17
+    assert rel_l2(ssm_s.cpu()[1], ssm_w.cpu()[1]) <= 1e-5
     assert rel_l2(torch.cat(ys).cpu(), y_w.cpu()) <= 1e-3
 
 

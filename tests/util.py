@@ -26,14 +26,17 @@ def rel_l2(got: torch.Tensor, ref: torch.Tensor) -> float:
 
 
 def check_act(got: torch.Tensor, ref64: torch.Tensor, what: str = "",
-              abs_tol: float = ABS_TOL, rel_ulp: float = REL_ULP, rel_l2_tol: float = REL_L2):
-    """Elementwise |g - r| <= abs_tol + rel_ulp*|r| and rel-L2 <= rel_l2_tol."""
+              abs_tol: float = ABS_TOL, rel_ulp: float = REL_ULP, rel_l2_tol: float = REL_L2,
+              extra: torch.Tensor = None):
+    """Elementwise |g - r| <= abs_tol + rel_ulp*|r| (+ extra) and rel-L2 <= rel_l2_tol."""
     g = got.double().cpu()
     r = ref64.double().cpu()
     assert g.shape == r.shape, (what, g.shape, r.shape)
     assert torch.isfinite(g).all(), f"{what}: non-finite output"
     err = (g - r).abs()
     bound = abs_tol + rel_ulp * r.abs()
+    if extra is not None:
+        bound = bound + extra.double().cpu()
     bad = err > bound
     if bad.any():
         idx = bad.nonzero()[0].tolist()
@@ -62,3 +65,20 @@ def assert_bits_equal(a: torch.Tensor, b: torch.Tensor, what: str = ""):
     if not torch.equal(a, b):
         diff = (a != b).nonzero()
         raise AssertionError(f"{what}: {diff.shape[0]} elements differ bitwise; first at {diff[0].tolist()}")
+
+
+def bf16_ulp(v: torch.Tensor) -> torch.Tensor:
+    """Spacing of bf16 values at |v| (8 significant bits)."""
+    a = v.double().abs().clamp_min(2.0 ** -126)
+    return torch.exp2(torch.floor(torch.log2(a)) - 7)
+
+
+def norm_gain(y: torch.Tensor, z: torch.Tensor, weight: torch.Tensor, groups: int, eps: float) -> torch.Tensor:
+    """|d out_i / d y_i| for out = rmsnorm(y * silu(z)) * weight (diagonal term):
+    how strongly the normed output follows its input y."""
+    yd, zd = y.double(), z.double()
+    gate = torch.nn.functional.silu(zd)
+    g = (yd * gate).view(y.shape[0], groups, -1)
+    inv = 1.0 / torch.sqrt((g * g).mean(dim=2, keepdim=True) + eps)
+    inv = inv.expand_as(g).reshape(y.shape)
+    return (gate * inv * weight.double()).abs()
