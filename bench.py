@@ -159,6 +159,9 @@ class Prefill:
         self.dec_z = wl.dec_z.to(dev)
         self.dec_dt = wl.dec_dt.to(dev)
         self.dec_out = torch.empty((1, d.d_inner), dtype=wl.act, device=dev)
+        self.batch = ss.Batch(b.cu_seqlens, b.slots, b.fresh)
+        self.dec_batch = ss.Batch(None, [b.slots[0]], [0])
+        self.dims = ss.Dims(d.heads, d.headdim, d.d_state, d.ngroups, d.conv_kernel)
 
     def prefill(self, x=None, z=None, dt=None, out=None, ev=None):
         ss, wl = self.ss, self.wl
@@ -170,11 +173,10 @@ class Prefill:
         out = self.out if out is None else out
         if ev:
             ev[0].record()
-        ss.causal_conv1d(self.xbc, x, cw, cb, self.conv, b.cu_seqlens, b.slots, b.fresh)
+        ss.causal_conv1d(self.xbc, x, cw, cb, self.conv, batch=self.batch)
         if ev:
             ev[1].record()
-        ss.ssd_scan(self.y, self.xbc, dt, A, dtb, D, self.ssm, d, b.cu_seqlens, b.slots, b.fresh,
-                    workspace=self.ws)
+        ss.ssd_scan(self.y, self.xbc, dt, A, dtb, D, self.ssm, self.dims, workspace=self.ws, batch=self.batch)
         if ev:
             ev[2].record()
         ss.gated_rmsnorm(out, self.y, z, nw, p.norm_groups, p.eps)
@@ -187,7 +189,7 @@ class Prefill:
         cw, cb, A, dtb, D, nw = self.pw
         for t in range(self.dec_x.shape[0]):
             ss.decode_step(self.dec_out, self.dec_x[t], self.dec_z[t], self.dec_dt[t], cw, cb, A, dtb, D, nw,
-                           p.norm_groups, p.eps, self.conv, self.ssm, d, [0], [0])
+                           p.norm_groups, p.eps, self.conv, self.ssm, self.dims, batch=self.dec_batch)
         if ev:
             ev.record()
 
@@ -202,10 +204,12 @@ def time_decode_batch(dev, reps, warm):
     xs, zs, dts = wl.dec_xBC.to(dev), wl.dec_z.to(dev), wl.dec_dt.to(dev)
     out = torch.empty((b.num_seqs, d.d_inner), dtype=wl.act, device=dev)
     steps = xs.shape[0]
+    batch = ss.Batch(None, b.slots, b.fresh)
+    dims = ss.Dims(d.heads, d.headdim, d.d_state, d.ngroups, d.conv_kernel)
 
     def run():
         for t in range(steps):
-            ss.decode_step(out, xs[t], zs[t], dts[t], *pw, p.norm_groups, p.eps, conv, ssm, d, b.slots, b.fresh)
+            ss.decode_step(out, xs[t], zs[t], dts[t], *pw, p.norm_groups, p.eps, conv, ssm, dims, batch=batch)
 
     for _ in range(warm):
         run()

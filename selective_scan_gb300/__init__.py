@@ -114,8 +114,9 @@ def _stream(stream) -> Optional[int]:
     return stream.cuda_stream
 
 
-class _Batch:
-    """Keeps the ctypes arrays of one RecurrentBatch alive for a call."""
+class Batch:
+    """A RecurrentBatch marshalled once (host arrays kept alive); pass it as
+    ``batch=`` to reuse it across calls instead of cu_seqlens/slots/fresh."""
 
     def __init__(self, cu_seqlens: Optional[Sequence[int]], slots: Sequence[int], fresh: Sequence[int]):
         n = len(slots)
@@ -131,6 +132,13 @@ class _Batch:
 
     def ref(self):
         return ctypes.byref(self.rb)
+
+
+_Batch = Batch
+
+
+def _batch(cu_seqlens, slots, fresh, batch):
+    return batch if batch is not None else Batch(cu_seqlens, slots, fresh)
 
 
 def _dims(d) -> Dims:
@@ -149,10 +157,11 @@ def _check(st: int, op: str):
 # entry points
 # --------------------------------------------------------------------------
 
-def causal_conv1d(dst, x, weight, bias, conv_state, cu_seqlens, slots, fresh, stream=None, check=True) -> int:
+def causal_conv1d(dst, x, weight, bias, conv_state, cu_seqlens=None, slots=None, fresh=None, stream=None,
+                  check=True, batch=None) -> int:
     """``mamba2_causal_conv1d``: dst = silu(depthwise causal conv) per run; conv_state updated."""
     rows, conv_dim = x.shape
-    b = _Batch(cu_seqlens, slots, fresh)
+    b = _batch(cu_seqlens, slots, fresh, batch)
     st = _lib().mamba2_causal_conv1d(_ptr(dst), _ptr(x), _ptr(weight), _ptr(bias), _ptr(conv_state),
                                      conv_state.shape[0], rows, conv_dim, weight.shape[1], _dt(x), b.ref(),
                                      _stream(stream))
@@ -161,15 +170,15 @@ def causal_conv1d(dst, x, weight, bias, conv_state, cu_seqlens, slots, fresh, st
     return st
 
 
-def ssd_scan_workspace_bytes(dims, rows, cu_seqlens, slots, fresh) -> int:
+def ssd_scan_workspace_bytes(dims, rows, cu_seqlens=None, slots=None, fresh=None, batch=None) -> int:
     """``mamba2_ssd_scan_workspace_bytes`` for this batch on the current device."""
-    b = _Batch(cu_seqlens, slots, fresh)
+    b = _batch(cu_seqlens, slots, fresh, batch)
     d = _dims(dims)
     return int(_lib().mamba2_ssd_scan_workspace_bytes(ctypes.byref(d), int(rows), b.ref()))
 
 
-def ssd_scan(dst, xbc, dt, A_log, dt_bias, D, ssm_state, dims, cu_seqlens, slots, fresh,
-             workspace=None, stream=None, check=True) -> int:
+def ssd_scan(dst, xbc, dt, A_log, dt_bias, D, ssm_state, dims, cu_seqlens=None, slots=None, fresh=None,
+             workspace=None, stream=None, check=True, batch=None) -> int:
     """``mamba2_ssd_scan``: chunked selective scan; ssm_state updated at the slots.
 
     ``workspace`` is a device tensor of at least ``ssd_scan_workspace_bytes`` bytes
@@ -178,7 +187,7 @@ def ssd_scan(dst, xbc, dt, A_log, dt_bias, D, ssm_state, dims, cu_seqlens, slots
     import torch
     rows = xbc.shape[0]
     d = _dims(dims)
-    b = _Batch(cu_seqlens, slots, fresh)
+    b = _batch(cu_seqlens, slots, fresh, batch)
     if workspace is None:
         need = int(_lib().mamba2_ssd_scan_workspace_bytes(ctypes.byref(d), rows, b.ref()))
         if need > 0:
@@ -204,10 +213,11 @@ def gated_rmsnorm(dst, x, z, weight, groups, eps, stream=None, check=True) -> in
 
 
 def decode_step(dst, xBC, z, dt, conv_w, conv_b, A_log, dt_bias, D, norm_w, norm_groups, eps,
-                conv_state, ssm_state, dims, slots, fresh, cu_seqlens=None, stream=None, check=True) -> int:
+                conv_state, ssm_state, dims, slots=None, fresh=None, cu_seqlens=None, stream=None, check=True,
+                batch=None) -> int:
     """``mamba2_decode_step``: fused conv -> scan -> gated norm for one token per sequence."""
     d = _dims(dims)
-    b = _Batch(cu_seqlens, slots, fresh)
+    b = _batch(cu_seqlens, slots, fresh, batch)
     st = _lib().mamba2_decode_step(_ptr(dst), _ptr(xBC), _ptr(z), _ptr(dt), _ptr(conv_w), _ptr(conv_b),
                                    _ptr(A_log), _ptr(dt_bias), _ptr(D), _ptr(norm_w), int(norm_groups),
                                    float(eps), _ptr(conv_state), _ptr(ssm_state), ssm_state.shape[0],

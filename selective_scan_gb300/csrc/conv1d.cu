@@ -20,10 +20,13 @@
 // read again by the next tile (L2 hits); each output row written once. The
 // kernel is HBM-bound: 2 * conv_dim * sizeof(act) bytes per row.
 //
-// Rounding: bf16 outputs are rounded exactly as the double-precision
-// definition rounds them (Ziv's test with an fp64 retry, conv_silu_act), so
-// the scan downstream sees the same conv output whether or not the conv ran
-// here.
+// Rounding: outputs are computed in fp32 (taps in order, fast exponential and
+// reciprocal for SiLU) and rounded once to the activation type, so a value
+// within a few fp32 ulps of a bf16 rounding boundary may land one bf16 step
+// from the double-precision definition. (The fused decode kernel rounds
+// exactly instead: there the conv output feeds a state whose tolerance is
+// tighter than one such step; for the 16x more outputs of a prefill the fp64
+// retries of that test cost more than the whole conv.)
 #include "common.cuh"
 #include "kernels.h"
 
@@ -92,51 +95,30 @@ conv1d_silu_kernel(const __grid_constant__ ConvArgs a) {
   for (int r = 0; r < kConvRows; ++r)
     if (r < nrows)
       rows[H + r] = *reinterpret_cast<const uint4*>(x + (int64_t)(row0 + q0 + r) * a.conv_dim + c0);
-  uint64_t retry_mask = 0;  // (row, channel) outputs the fast rounding test could not decide
-  static_assert(kConvRows * V <= 64, "retry mask width");
+  // unpack each row once; tap k of tile row r is u[r + k]
+  float u[H + kConvRows][V];
+#pragma unroll
+  for (int i = 0; i < H; ++i) Vec16<T>::load(reinterpret_cast<const T*>(&rows[i]), u[i]);
 #pragma unroll
   for (int r = 0; r < kConvRows; ++r) {
     if (r < nrows) {
-      float u[K][V], out[V];
-#pragma unroll
-      for (int k = 0; k < K; ++k) Vec16<T>::load(reinterpret_cast<const T*>(&rows[r + k]), u[k]);
+      Vec16<T>::load(reinterpret_cast<const T*>(&rows[H + r]), u[H + r]);
+      float out[V];
 #pragma unroll
       for (int j = 0; j < V; ++j) {
         float wk[K], uk[K];
 #pragma unroll
         for (int k = 0; k < K; ++k) {
           wk[k] = w[k][j];
-          uk[k] = u[k][j];
+          uk[k] = u[r + k][j];
         }
-        if constexpr (Act<T>::code == MAMBA2_BF16) {
-          bool retry;
-          out[j] = conv_silu_bf16_fast<K>(b[j], wk, uk, retry);
-          if (retry) retry_mask |= 1ull << (r * V + j);
-        } else {
-          out[j] = conv_silu_act<T, K>(b[j], wk, uk);
-        }
+        float acc = b[j];
+#pragma unroll
+        for (int k = 0; k < K; ++k) acc = fmaf(wk[k], uk[k], acc);
+        out[j] = silu_f(acc);
       }
       Vec16<T>::store(dst + (int64_t)(row0 + q0 + r) * a.conv_dim + c0, out);
     }
-  }
-
-  // fp64 retry of the undecided outputs (about one in a thousand); inputs are
-  // re-read from memory (the slot is still unmodified here)
-  while (retry_mask) {
-    const int i = __ffsll((long long)retry_mask) - 1;
-    retry_mask &= retry_mask - 1;
-    const int r = i / V, j = i % V, c = c0 + j;
-    float wk[K], uk[K];
-#pragma unroll
-    for (int k = 0; k < K; ++k) {
-      wk[k] = a.weight[(int64_t)c * K + k];
-      const int pos = q0 + r - H + k;  // conv input position of tap k
-      float uv = 0.0f;
-      if (pos >= 0) uv = Act<T>::to_f(x[(int64_t)(row0 + pos) * a.conv_dim + c]);
-      else if (!fresh) uv = Act<T>::to_f(cst[slot_base + (int64_t)(H + pos) * a.conv_dim + c]);
-      uk[k] = uv;
-    }
-    dst[(int64_t)(row0 + q0 + r) * a.conv_dim + c] = Act<T>::from_f(conv_silu_bf16_fp64<K>(a.bias[c], wk, uk));
   }
 
   // slot update by tile 0: new history = u[T .. T + H - 1] (bit copies)

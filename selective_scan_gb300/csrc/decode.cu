@@ -32,7 +32,7 @@
 namespace mamba2 {
 
 constexpr int kDecodeWarps = kDecodeThreads / 32;
-constexpr int kDecodeUnroll = 8;  // rows of state in flight per lane
+constexpr int kDecodeUnroll = 16;  // state rows in flight per lane (16-byte loads)
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
   return (uint32_t)__cvta_generic_to_shared(p);
@@ -52,7 +52,7 @@ __device__ __forceinline__ float ld_dsmem_f32(const float* local, uint32_t rank)
 }
 
 template <typename T, int K>
-__global__ void __launch_bounds__(kDecodeThreads)
+__global__ void __launch_bounds__(kDecodeThreads, 2)
 decode_step_kernel(const __grid_constant__ DecodeArgs a) {
   constexpr int V = Vec16<T>::n;
   constexpr int HIST = K - 1;
@@ -84,6 +84,29 @@ decode_step_kernel(const __grid_constant__ DecodeArgs a) {
 
   for (int i = threadIdx.x; i < kDecodeMaxNormGroups; i += kDecodeThreads) part[i] = 0.0f;
 
+  // ---- state-stream geometry; the first batch of state loads is issued now
+  // so it is in flight while the conv phase below waits on its own inputs
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nq = N / 4;                  // float4 per state row
+  const int lpr = nq < 32 ? nq : 32;     // lanes per row
+  const int rpp = 32 / lpr;              // rows per warp pass
+  const int qpl = (nq + lpr - 1) / lpr;  // float4 per lane per row
+  const int q0 = lane % lpr, rs = lane / lpr;
+  float4* st = reinterpret_cast<float4*>(a.ssm_state + (slot * H + h0) * (int64_t)P * N);
+  const int base0 = warp * rpp * kDecodeUnroll;
+  const int bstep = kDecodeWarps * rpp * kDecodeUnroll;
+  float4 hv[kDecodeUnroll];
+  auto load_rows = [&](int base, int qq) {
+    const int q = q0 + qq * lpr;
+#pragma unroll
+    for (int u = 0; u < kDecodeUnroll; ++u) {
+      const int r = base + u * rpp + rs;
+      hv[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (!fresh && r < rows && q < nq) hv[u] = __ldcs(st + (int64_t)r * nq + q);
+    }
+  };
+  load_rows(base0, 0);
+
   // ---- 1. conv for own x channels and all B/C channels -------------------
   const int nxv = rows / V;
   const int nbcv = 2 * G * N / V;
@@ -100,19 +123,55 @@ decode_step_kernel(const __grid_constant__ DecodeArgs a) {
     }
     const uint4 craw = *reinterpret_cast<const uint4*>(xBC + c0);
     Vec16<T>::load(reinterpret_cast<const T*>(&craw), cur);
+    float wv[V * K], bv[V];
+    {
+      const float4* wp = reinterpret_cast<const float4*>(a.conv_w + (int64_t)c0 * K);
+#pragma unroll
+      for (int q = 0; q < V * K / 4; ++q) {
+        const float4 f = __ldg(wp + q);
+        wv[4 * q] = f.x; wv[4 * q + 1] = f.y; wv[4 * q + 2] = f.z; wv[4 * q + 3] = f.w;
+      }
+      const float4* bp = reinterpret_cast<const float4*>(a.conv_b + c0);
+#pragma unroll
+      for (int q = 0; q < V / 4; ++q) {
+        const float4 f = __ldg(bp + q);
+        bv[4 * q] = f.x; bv[4 * q + 1] = f.y; bv[4 * q + 2] = f.z; bv[4 * q + 3] = f.w;
+      }
+    }
+    uint32_t retry_mask = 0;
 #pragma unroll
     for (int j = 0; j < V; ++j) {
       float wk[K], uk[K];
 #pragma unroll
       for (int k = 0; k < K; ++k) {
-        wk[k] = a.conv_w[(int64_t)(c0 + j) * K + k];
+        wk[k] = wv[j * K + k];
         uk[k] = k < HIST ? hist[k < HIST ? k : 0][j] : cur[j];
       }
-      out[j] = conv_silu_act<T, K>(a.conv_b[c0 + j], wk, uk);
+      if constexpr (Act<T>::code == MAMBA2_BF16) {
+        bool retry;
+        out[j] = conv_silu_bf16_fast<K>(bv[j], wk, uk, retry);
+        if (retry) retry_mask |= 1u << j;
+      } else {
+        out[j] = conv_silu_act<T, K>(bv[j], wk, uk);
+      }
     }
     float* o = is_x ? xs + i * V : bc + (c0 - d_inner);
 #pragma unroll
     for (int j = 0; j < V; ++j) o[j] = out[j];
+    // fp64 retry of the outputs the fast rounding test could not decide
+    // (inputs re-read; this thread has not yet rewritten its history rows)
+    while (retry_mask) {
+      const int j = __ffs(retry_mask) - 1;
+      retry_mask &= retry_mask - 1;
+      const int c = c0 + j;
+      float wk[K], uk[K];
+#pragma unroll
+      for (int k = 0; k < K; ++k) {
+        wk[k] = a.conv_w[(int64_t)c * K + k];
+        uk[k] = k < HIST ? (fresh ? 0.f : Act<T>::to_f(cst[(int64_t)k * conv_dim + c])) : Act<T>::to_f(xBC[c]);
+      }
+      o[j] = conv_silu_bf16_fp64<K>(a.conv_b[c], wk, uk);
+    }
     if (is_x) {  // own channels: shift the history now
 #pragma unroll
       for (int j = 0; j + 1 < HIST; ++j)
@@ -133,24 +192,11 @@ decode_step_kernel(const __grid_constant__ DecodeArgs a) {
 
   // ---- 2. state stream: h = h*decay + dt'*x*B; y = h.C + D*x -------------
   {
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int nq = N / 4;                  // float4 per state row
-    const int lpr = nq < 32 ? nq : 32;     // lanes per row
-    const int rpp = 32 / lpr;              // rows per warp pass
-    const int qpl = (nq + lpr - 1) / lpr;  // float4 per lane per row
-    const int q0 = lane % lpr, rs = lane / lpr;
-    float4* st = reinterpret_cast<float4*>(a.ssm_state + (slot * H + h0) * (int64_t)P * N);
     const int hpg = H / G;
-    for (int base = warp * rpp * kDecodeUnroll; base < rows; base += kDecodeWarps * rpp * kDecodeUnroll) {
+    for (int base = base0; base < rows; base += bstep) {
       for (int qq = 0; qq < qpl; ++qq) {
         const int q = q0 + qq * lpr;
-        float4 hv[kDecodeUnroll];
-#pragma unroll
-        for (int u = 0; u < kDecodeUnroll; ++u) {
-          const int r = base + u * rpp + rs;
-          hv[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-          if (!fresh && r < rows && q < nq) hv[u] = __ldcs(st + (int64_t)r * nq + q);
-        }
+        if (base != base0 || qq != 0) load_rows(base, qq);
 #pragma unroll
         for (int u = 0; u < kDecodeUnroll; ++u) {
           const int r = base + u * rpp + rs;
@@ -195,7 +241,6 @@ decode_step_kernel(const __grid_constant__ DecodeArgs a) {
   __syncthreads();
   if (rows > 0) {
     const int c_lo = h0 * P, c_hi = h0 * P + rows;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     for (int grp = c_lo / gs; grp * gs < c_hi; ++grp) {
       const int lo = max(c_lo, grp * gs) - c_lo, hi = min(c_hi, (grp + 1) * gs) - c_lo;
       float ss = 0.0f;

@@ -66,19 +66,3 @@ def assert_bits_equal(a: torch.Tensor, b: torch.Tensor, what: str = ""):
         diff = (a != b).nonzero()
         raise AssertionError(f"{what}: {diff.shape[0]} elements differ bitwise; first at {diff[0].tolist()}")
 
-
-def bf16_ulp(v: torch.Tensor) -> torch.Tensor:
-    """Spacing of bf16 values at |v| (8 significant bits)."""
-    a = v.double().abs().clamp_min(2.0 ** -126)
-    return torch.exp2(torch.floor(torch.log2(a)) - 7)
-
-
-def norm_gain(y: torch.Tensor, z: torch.Tensor, weight: torch.Tensor, groups: int, eps: float) -> torch.Tensor:
-    """|d out_i / d y_i| for out = rmsnorm(y * silu(z)) * weight (diagonal term):
-    how strongly the normed output follows its input y."""
-    yd, zd = y.double(), z.double()
-    gate = torch.nn.functional.silu(zd)
-    g = (yd * gate).view(y.shape[0], groups, -1)
-    inv = 1.0 / torch.sqrt((g * g).mean(dim=2, keepdim=True) + eps)
-    inv = inv.expand_as(g).reshape(y.shape)
-    return (gate * inv * weight.double()).abs()
