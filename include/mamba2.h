@@ -150,6 +150,47 @@ mamba2_status mamba2_ssd_scan(void* dst, const void* xbc, const void* dt,
                               void* stream);
 
 /*
+ * Bytes of the library's built-in scan scratch (see
+ * mamba2_ssd_scan_static_scratch).
+ */
+#define MAMBA2_STATIC_SCAN_SCRATCH_BYTES (32u << 20)
+
+/*
+ * mamba2_ssd_scan without a caller-provided workspace. The paper has no
+ * counterpart to this entry point; it exists for callers that cannot
+ * allocate device memory when they call the scan: a server whose allocator
+ * has handed all device memory to its state and cache pools, a plugin host
+ * that gives its kernels only their input and output buffers, or a latency-
+ * critical loop where an allocation's implicit synchronisation is not
+ * acceptable.
+ *
+ * The scratch is a fixed array of MAMBA2_STATIC_SCAN_SCRATCH_BYTES (32 MiB)
+ * in the library's own device memory; every GPU that loads the library holds
+ * it until the process exits. This call allocates nothing: no cudaMalloc, no
+ * cudaFree, no allocating library routine. The first call on each device
+ * looks up the array's device address once (cudaGetSymbolAddress with that
+ * device current); make that first call before any stream capture.
+ *
+ * Arguments, semantics, results and errors are those of mamba2_ssd_scan, plus
+ * MAMBA2_ERR_WORKSPACE_TOO_SMALL when the batch needs more scratch than the
+ * array holds (mamba2_ssd_scan_workspace_bytes gives the need; long runs
+ * split into many segments and batches of many sequences need more), in
+ * which case nothing is enqueued.
+ *
+ * All calls share the one array and it keeps the last call's contents;
+ * nothing in it needs to start at zero (every entry a call reads, the same
+ * call wrote first). Calls whose work overlaps on the GPU (different streams,
+ * or several host threads) race on it and must be serialised by the caller.
+ */
+mamba2_status mamba2_ssd_scan_static_scratch(void* dst, const void* xbc, const void* dt,
+                                             const float* A_log, const float* dt_bias,
+                                             const float* D, float* ssm_state,
+                                             int32_t num_slots, int32_t rows,
+                                             const mamba2_dims* dims, mamba2_dtype act,
+                                             const mamba2_recurrent_batch* rb,
+                                             void* stream);
+
+/*
  * GatedRMSNorm (gllm PR #85, section "Ops"): per row and per group of
  * dim/groups consecutive channels, v = x * silu(z) and
  * dst = v / sqrt(mean(v^2) + eps) * weight (the gate is applied before the

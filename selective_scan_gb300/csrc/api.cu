@@ -328,3 +328,60 @@ mamba2_status mamba2_decode_step(void* dst, const void* xBC, const void* z, cons
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Scan with the library's own scratch, for callers that cannot allocate.
+// ---------------------------------------------------------------------------
+#include <mutex>
+
+namespace mamba2 {
+namespace {
+
+// The built-in scan scratch: one fixed array in every device that loads the
+// library. Host code must not use its name as an address (on the host it is
+// only a stand-in); the device address comes from cudaGetSymbolAddress.
+static __device__ __align__(256) unsigned char g_scan_scratch[MAMBA2_STATIC_SCAN_SCRATCH_BYTES];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_scratch_mutex;
+void* g_scratch_addr[kMaxDevices] = {};
+
+// Device address of g_scan_scratch on the current device, looked up once per
+// device (with that device current).
+mamba2_status scan_scratch_address(void** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (dev < 0 || dev >= kMaxDevices) return MAMBA2_ERR_INVALID_ARGUMENT;
+  std::lock_guard<std::mutex> lock(g_scratch_mutex);
+  if (!g_scratch_addr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_scan_scratch);
+    if (e != cudaSuccess) return cuda_fail(e);
+    g_scratch_addr[dev] = p;
+  }
+  *out = g_scratch_addr[dev];
+  return MAMBA2_OK;
+}
+
+}  // namespace
+}  // namespace mamba2
+
+extern "C" mamba2_status mamba2_ssd_scan_static_scratch(void* dst, const void* xbc, const void* dt,
+                                                        const float* A_log, const float* dt_bias, const float* D,
+                                                        float* ssm_state, int32_t num_slots, int32_t rows,
+                                                        const mamba2_dims* dims, mamba2_dtype act,
+                                                        const mamba2_recurrent_batch* rb, void* stream) {
+  // Scratch this batch needs (arguments the scan rejects need none; the scan
+  // below then reports them).
+  size_t need = 0;
+  if (act_ok(act) && dims_ok(dims) && rows >= 0 && validate_batch(rb, num_slots, rows, true) == MAMBA2_OK &&
+      rb->num_seqs > 0)
+    need = plan_scan(dims, act, rb).ws_bytes;
+  if (need > MAMBA2_STATIC_SCAN_SCRATCH_BYTES) return MAMBA2_ERR_WORKSPACE_TOO_SMALL;
+  void* scratch = nullptr;
+  const mamba2_status st = scan_scratch_address(&scratch);
+  if (st != MAMBA2_OK) return st;
+  return mamba2_ssd_scan(dst, xbc, dt, A_log, dt_bias, D, ssm_state, num_slots, rows, dims, act, rb, scratch,
+                         MAMBA2_STATIC_SCAN_SCRATCH_BYTES, stream);
+}
