@@ -183,13 +183,31 @@ class Prefill:
         if ev:
             ev[3].record()
 
-    def decode_tail(self, ev=None):
+    def _decode_steps(self):
         ss, wl = self.ss, self.wl
-        p, d = wl.params, wl.dims
+        p = wl.params
         cw, cb, A, dtb, D, nw = self.pw
         for t in range(self.dec_x.shape[0]):
             ss.decode_step(self.dec_out, self.dec_x[t], self.dec_z[t], self.dec_dt[t], cw, cb, A, dtb, D, nw,
                            p.norm_groups, p.eps, self.conv, self.ssm, self.dims, batch=self.dec_batch)
+
+    def capture_decode(self):
+        """Capture the 64 decode steps into a CUDA graph (the batch table is in
+        the launch parameters, so the launches replay as they were recorded)."""
+        self.graph = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            self._decode_steps()
+        torch.cuda.current_stream().wait_stream(side)
+        with torch.cuda.graph(self.graph):
+            self._decode_steps()
+
+    def decode_tail(self, ev=None):
+        if getattr(self, "graph", None) is not None:
+            self.graph.replay()
+        else:
+            self._decode_steps()
         if ev:
             ev.record()
 
@@ -207,12 +225,17 @@ def time_decode_batch(dev, reps, warm):
     batch = ss.Batch(None, b.slots, b.fresh)
     dims = ss.Dims(d.heads, d.headdim, d.d_state, d.ngroups, d.conv_kernel)
 
-    def run():
+    def run_eager():
         for t in range(steps):
             ss.decode_step(out, xs[t], zs[t], dts[t], *pw, p.norm_groups, p.eps, conv, ssm, dims, batch=batch)
 
     for _ in range(warm):
-        run()
+        run_eager()
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        run_eager()
+    run = graph.replay
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record()
@@ -256,6 +279,7 @@ def run_ours(args, rank, world, local_rank):
     hbm, tf_burst, tf_sus, peak_kind = peaks()
     wl = W.long_prefill(seed=4 + rank, tokens=args.tokens)
     pf = Prefill(wl, dev)
+    pf.capture_decode()
     d = wl.dims
 
     def step(evs=None):
@@ -362,10 +386,12 @@ def run_ours(args, rank, world, local_rank):
                    "l2": "inputs larger than L2 (no flush)", "parallelism": f"replicas x{world}"},
         "prefill_ms": t_prefill,
         "decode_tail_us_per_step": t_tail * 1e3 / DECODE_TAIL,
+        "decode_tail_launch": "CUDA graph of the 64 steps",
         "kernels": kern,
         "roofline": {"kernel": dominant, "bound": "hbm", "achieved": dk["GB/s"], "peak": hbm, "unit": "GB/s",
                      "frac": dk["GB/s"] / hbm, "traffic": traffic, "peak_kind": peak_kind},
         "decode": {"workload": "256 seqs x 1 token, 128 carried steps, 512-slot pool, 48 heads x 64, d_state 128",
+                   "launch": "CUDA graph of the 128 steps",
                    "us_per_step": dec_us, "tokens_per_s": dec_n / (dec_us * 1e-6), "GB/s": dec_gbs,
                    "roofline_frac": dec_gbs / hbm, "roofline_frac_8TBs": dec_gbs / 8000.0,
                    "bytes_per_step": dec_bytes, "steps_timed": dec_steps},

@@ -33,6 +33,7 @@ namespace mamba2 {
 
 constexpr int kDecodeWarps = kDecodeThreads / 32;
 constexpr int kDecodeUnroll = 16;  // state rows in flight per lane (16-byte loads)
+static_assert(kDecodeUnroll == 16, "the d_state = 128 path reduces 16 rows by recursive halving");
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
   return (uint32_t)__cvta_generic_to_shared(p);
@@ -78,6 +79,7 @@ decode_step_kernel(const __grid_constant__ DecodeArgs a) {
   float* hD = hdec + a.heads_per_cta;        // [heads_per_cta] D
   float* part = hD + a.heads_per_cta;        // [kDecodeMaxNormGroups]
   float* wsum = part + kDecodeMaxNormGroups; // [kDecodeWarps]
+  float* zs = wsum + kDecodeWarps;           // [heads_per_cta * P] silu(z) of own channels
 
   const T* xBC = static_cast<const T*>(a.xBC) + (int64_t)s * conv_dim;
   T* cst = static_cast<T*>(a.conv_state) + slot * HIST * conv_dim;
@@ -123,6 +125,12 @@ decode_step_kernel(const __grid_constant__ DecodeArgs a) {
     }
     const uint4 craw = *reinterpret_cast<const uint4*>(xBC + c0);
     Vec16<T>::load(reinterpret_cast<const T*>(&craw), cur);
+    if (is_x) {  // the gate of the same channels, for the norm
+      float zv[V];
+      Vec16<T>::load(static_cast<const T*>(a.z) + (int64_t)s * d_inner + c0, zv);
+#pragma unroll
+      for (int j = 0; j < V; ++j) zs[i * V + j] = silu_f(zv[j]);
+    }
     float wv[V * K], bv[V];
     {
       const float4* wp = reinterpret_cast<const float4*>(a.conv_w + (int64_t)c0 * K);
@@ -191,7 +199,53 @@ decode_step_kernel(const __grid_constant__ DecodeArgs a) {
   __syncthreads();
 
   // ---- 2. state stream: h = h*decay + dt'*x*B; y = h.C + D*x -------------
-  {
+  if (lpr == 32 && qpl == 1) {
+    // d_state = 128: one float4 per lane per row, rows of a 16-row batch all
+    // in one head (P % 16 == 0), so B and C are loaded once per batch; the 16
+    // row sums are reduced across the warp by recursive halving (16 shuffles
+    // per lane instead of 5 per row).
+    const int hpg = H / G;
+    for (int base = base0; base < rows; base += bstep) {
+      if (base != base0) load_rows(base, 0);
+      const int hl = base / P;
+      const int g = (h0 + hl) / hpg;
+      const float dtp = hdt[hl], dec = hdec[hl];
+      const float4 b4 = *reinterpret_cast<const float4*>(bc + g * N + 4 * lane);
+      const float4 c4 = *reinterpret_cast<const float4*>(bc + G * N + g * N + 4 * lane);
+      float acc[kDecodeUnroll];
+#pragma unroll
+      for (int u = 0; u < kDecodeUnroll; ++u) {
+        const int r = base + u;
+        acc[u] = 0.0f;
+        if (r < rows) {
+          const float xd = dtp * xs[r];
+          float4 h = hv[u];
+          h.x = fmaf(h.x, dec, xd * b4.x);
+          h.y = fmaf(h.y, dec, xd * b4.y);
+          h.z = fmaf(h.z, dec, xd * b4.z);
+          h.w = fmaf(h.w, dec, xd * b4.w);
+          __stcs(st + (int64_t)r * nq + lane, h);
+          float t = h.x * c4.x;
+          t = fmaf(h.y, c4.y, t);
+          t = fmaf(h.z, c4.z, t);
+          acc[u] = fmaf(h.w, c4.w, t);
+        }
+      }
+#pragma unroll
+      for (int d = 16, m = kDecodeUnroll; d >= 2; d >>= 1, m >>= 1) {
+        const bool upper = (lane & d) != 0;
+#pragma unroll
+        for (int i = 0; i < m / 2; ++i) {
+          const float send = upper ? acc[i] : acc[i + m / 2];
+          const float keep = upper ? acc[i + m / 2] : acc[i];
+          acc[i] = keep + __shfl_xor_sync(0xffffffffu, send, d);
+        }
+      }
+      acc[0] += __shfl_xor_sync(0xffffffffu, acc[0], 1);
+      const int rl = ((lane >> 4) & 1) * 8 + ((lane >> 3) & 1) * 4 + ((lane >> 2) & 1) * 2 + ((lane >> 1) & 1);
+      if ((lane & 1) == 0 && base + rl < rows) ys[base + rl] = acc[0];
+    }
+  } else {
     const int hpg = H / G;
     for (int base = base0; base < rows; base += bstep) {
       for (int qq = 0; qq < qpl; ++qq) {
@@ -232,11 +286,10 @@ decode_step_kernel(const __grid_constant__ DecodeArgs a) {
 
   // ---- 3. g = round(y) * silu(z); partial sums of g^2 per norm group -----
   const int gs = d_inner / a.norm_groups;
-  const T* zrow = static_cast<const T*>(a.z) + (int64_t)s * d_inner;
   for (int r = threadIdx.x; r < rows; r += kDecodeThreads) {
     const int hl = r / P;
     const float y = round_act<T>(ys[r] + hD[hl] * xs[r]);
-    ys[r] = y * silu_f(Act<T>::to_f(zrow[h0 * P + r]));
+    ys[r] = y * zs[r];
   }
   __syncthreads();
   if (rows > 0) {
@@ -306,7 +359,7 @@ bool decode_supported(mamba2_dtype act, const mamba2_dims& d, int norm_groups) {
 
 template <typename T, int K>
 static cudaError_t launch_decode_t(const DecodeArgs& a, cudaStream_t st) {
-  const size_t smem = sizeof(float) * (2 * (size_t)a.heads_per_cta * a.headdim + 2 * (size_t)a.ngroups * a.d_state +
+  const size_t smem = sizeof(float) * (3 * (size_t)a.heads_per_cta * a.headdim + 2 * (size_t)a.ngroups * a.d_state +
                                        3 * (size_t)a.heads_per_cta + kDecodeMaxNormGroups + kDecodeWarps);
   auto kern = decode_step_kernel<T, K>;
   if (smem > 48 * 1024) {
