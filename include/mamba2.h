@@ -136,9 +136,11 @@ size_t mamba2_ssd_scan_workspace_bytes(const mamba2_dims* dims, int32_t rows,
  *   workspace  device scratch of at least
  *              mamba2_ssd_scan_workspace_bytes(...) bytes (may be NULL when
  *              that is 0); its contents need no initialisation.
- * Built shapes: any heads/ngroups with headdim x d_state of 16x16 or 64x128
- * (bf16 or fp32 activations) or any shape up to headdim 1024, d_state 256 on
- * the token-serial kernel; others return MAMBA2_ERR_NOT_IMPLEMENTED.
+ * Built shapes (any heads, ngroups): bf16 headdim 64 x d_state 128 runs on
+ * the tcgen05 chunked kernel (128-token chunks), bf16 16 x 16 on the mma.sync
+ * chunked kernel (64-token chunks); fp32 activations and other shapes up to
+ * headdim 1024, d_state 256 run on the token-serial kernel; larger shapes
+ * return MAMBA2_ERR_NOT_IMPLEMENTED.
  */
 mamba2_status mamba2_ssd_scan(void* dst, const void* xbc, const void* dt,
                               const float* A_log, const float* dt_bias,
@@ -243,6 +245,15 @@ const char* mamba2_status_string(mamba2_status status);
 
 /* Text of the CUDA error behind the calling thread's last MAMBA2_ERR_CUDA. */
 const char* mamba2_last_cuda_error(void);
+
+/*
+ * Failure detection: how many tensor-core scan CTAs on the current device gave
+ * up waiting for their MMA completion barrier (each wait is bounded; a CTA
+ * that gives up writes nothing further, frees its tensor memory and exits).
+ * Always 0 on a healthy GPU. Synchronous (reads a device counter);
+ * 0xffffffff if the read fails.
+ */
+unsigned int mamba2_device_timeouts(void);
 
 #ifdef __cplusplus
 }

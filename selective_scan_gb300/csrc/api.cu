@@ -98,10 +98,11 @@ ScanPlan plan_scan(const mamba2_dims* d, mamba2_dtype act, const mamba2_recurren
     p.total_segs = n;
     return p;
   }
+  const int Q = scan_chunk_tokens(d->headdim, d->d_state);
   int64_t total_chunks = 0;
   for (int i = 0; i < n; ++i) {
     const int64_t T = rb->cu_seqlens[i + 1] - rb->cu_seqlens[i];
-    total_chunks += (T + kChunk - 1) / kChunk;
+    total_chunks += (T + Q - 1) / Q;
   }
   const int64_t target = 4LL * device_sm_count();  // CTAs wanted (2 resident per SM, ~2 waves)
   int64_t sc = (total_chunks * d->heads + target - 1) / std::max<int64_t>(1, target);
@@ -109,7 +110,7 @@ ScanPlan plan_scan(const mamba2_dims* d, mamba2_dtype act, const mamba2_recurren
   p.total_segs = 0;
   for (int i = 0; i < n; ++i) {
     const int64_t T = rb->cu_seqlens[i + 1] - rb->cu_seqlens[i];
-    const int64_t ch = (T + kChunk - 1) / kChunk;
+    const int64_t ch = (T + Q - 1) / Q;
     const int segs = (int)std::max<int64_t>(1, (ch + p.seg_chunks - 1) / p.seg_chunks);
     p.segmented |= segs > 1;
     p.total_segs += segs;
@@ -122,12 +123,12 @@ ScanPlan plan_scan(const mamba2_dims* d, mamba2_dtype act, const mamba2_recurren
   return p;
 }
 
-void fill_scan_tiles(SeqTable& t, const ScanPlan& p) {
+void fill_scan_tiles(SeqTable& t, const ScanPlan& p, int Q) {
   t.tile[0] = 0;
   for (int i = 0; i < t.n; ++i) {
     int segs = 1;
     if (p.chunked) {
-      const int64_t ch = ((int64_t)t.cu[i + 1] - t.cu[i] + kChunk - 1) / kChunk;
+      const int64_t ch = ((int64_t)t.cu[i + 1] - t.cu[i] + Q - 1) / Q;
       segs = (int)std::max<int64_t>(1, (ch + p.seg_chunks - 1) / p.seg_chunks);
     }
     t.tile[i + 1] = t.tile[i] + segs;
@@ -156,6 +157,8 @@ const char* mamba2_status_string(mamba2_status s) {
 }
 
 const char* mamba2_last_cuda_error(void) { return g_cuda_error; }
+
+unsigned int mamba2_device_timeouts(void) { return read_device_timeouts(); }
 
 int64_t mamba2_state_bytes_per_layer(const mamba2_dims* d, mamba2_dtype conv_dtype) {
   if (!dims_ok(d) || !act_ok(conv_dtype)) return -1;
@@ -253,7 +256,7 @@ mamba2_status mamba2_ssd_scan(void* dst, const void* xbc, const void* dt, const 
                                           (plan.ws_state_floats * 4 + 255) / 256 * 256);
   }
   fill_table(a.tab, rb);
-  fill_scan_tiles(a.tab, plan);
+  fill_scan_tiles(a.tab, plan, scan_chunk_tokens(dims->headdim, dims->d_state));
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e = plan.chunked ? launch_scan_chunked(a, s) : launch_scan_serial(a, act, s);
   return e == cudaSuccess ? MAMBA2_OK : cuda_fail(e);

@@ -55,8 +55,15 @@ struct ScanArgs {
   int32_t seg_chunks;  // chunks per segment (tile = segment)
   SeqTable tab;
 };
-// True when the chunked tensor-core kernel covers this shape.
+// True when the chunked tensor-core kernels cover this shape: tcgen05 for
+// headdim 64 x d_state 128 (chunks of kChunkTc tokens), mma.sync for 16 x 16.
 bool scan_chunked_supported(mamba2_dtype act, int headdim, int d_state);
+constexpr int kChunkTc = 128;
+inline int scan_chunk_tokens(int headdim, int d_state) {
+  return (headdim == 64 && d_state == 128) ? kChunkTc : kChunk;
+}
+cudaError_t launch_scan_tc(const ScanArgs& a, cudaStream_t st);
+unsigned int read_device_timeouts();
 // Chunked scan: state pass over all but the last segment of each sequence,
 // then the full pass. The serial kernel is the token-at-a-time fallback.
 cudaError_t launch_scan_chunked(const ScanArgs& a, cudaStream_t st);

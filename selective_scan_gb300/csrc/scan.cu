@@ -548,7 +548,7 @@ bool scan_chunked_supported(mamba2_dtype act, int headdim, int d_state) {
 }
 
 cudaError_t launch_scan_chunked(const ScanArgs& a, cudaStream_t st) {
-  if (a.headdim == 64 && a.d_state == 128) return launch_chunked_pn<64, 128>(a, st);
+  if (a.headdim == 64 && a.d_state == 128) return launch_scan_tc(a, st);
   if (a.headdim == 16 && a.d_state == 16) return launch_chunked_pn<16, 16>(a, st);
   return cudaErrorInvalidValue;
 }
