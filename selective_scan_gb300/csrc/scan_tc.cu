@@ -19,7 +19,7 @@
 // (or state row n). Per chunk, with every tile in its natural load layout
 // (a [rows][cols] bf16 tile stored with the 128-byte swizzle in 64-column
 // blocks is both the K-major and the MN-major tcgen05 operand):
-//   MMA batch 1 (one issuing thread):
+//   MMA batch 1:
 //     CB      = C . B^T                       M=128 N=128 K=128 (C, B K-major)
 //     Yoff    = C . H^T                       M=128 N=64  K=128 (H^T MN-major)
 //     dH^T    = B^T . (X o w)  (hi + lo)      M=128 N=64  K=128 (both MN-major)
@@ -245,8 +245,8 @@ ssd_tc_kernel(const __grid_constant__ ScanArgs a) {
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
   }
   if (tid == 0) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" :: "r"(mbar1));
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" :: "r"(mbar2));
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" :: "r"(mbar1), "r"(kFull ? 2 : 1));
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 2;" :: "r"(mbar2));
     asm volatile("fence.mbarrier_init.release.cluster;");
   }
 
@@ -314,45 +314,37 @@ ssd_tc_kernel(const __grid_constant__ ScanArgs a) {
     }
     asm volatile("cp.async.commit_group;\n" ::);
   };
-  // ---- dt of a chunk (warp 0; lane l: tokens 4l .. 4l+3)
-  float dt_raw4[4] = {0.f, 0.f, 0.f, 0.f};
+  // ---- dt of a chunk: warps 0, 4, 8, 12 (TMEM lane quarter 0, the lightest M
+  // share), warp 4k taking the 32-block k (lane l: token 32 k + l)
+  const bool dt_warp = (warp & 3) == 0;
+  const int dblk = warp >> 2;
+  float* s_btot = reinterpret_cast<float*>(smem + kOffMisc + 32);  // [2][4] block totals of the log2 decay
+  // raw bf16 bits: the load stays in flight until the next chunk's dt phase converts it
+  unsigned short dt_raw = 0;
   auto load_dt = [&](int c) {
-    const int len = min(TQ, T - c * TQ);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int t = 4 * lane + i;
-      dt_raw4[i] = t < len ? __bfloat162float(dtg[(row0 + (int64_t)c * TQ + t) * H + h]) : 0.f;
-    }
+    const int t = 32 * dblk + lane;
+    dt_raw = t < min(TQ, T - c * TQ) ? reinterpret_cast<const unsigned short*>(dtg)[(row0 + (int64_t)c * TQ + t) * H + h]
+                                     : (unsigned short)0;
   };
   // dt', log2-scaled cumulative decay S and block-relative factors v of chunk c into buffer sb
   auto dt_phase = [&](int c, int sb) {
-    const int len = min(TQ, T - c * TQ);
-    float dp[4], S[4];
-    float run = 0.f;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int t = 4 * lane + i;
-      dp[i] = t < len ? softplus_f(dt_raw4[i] + dtb) : 0.f;
-      run -= A2 * dp[i];
-      S[i] = run;
-    }
-    float incl = run;
+    const int t = 32 * dblk + lane;
+    const float dp = t < min(TQ, T - c * TQ) ? softplus_f(__uint_as_float((uint32_t)dt_raw << 16) + dtb) : 0.f;
+    float incl = -A2 * dp;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const float v = __shfl_up_sync(0xffffffffu, incl, o);
       if (lane >= o) incl += v;
     }
-    const float excl = incl - run;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) S[i] += excl;
-    const float Se = __shfl_sync(0xffffffffu, S[3], (lane & ~7) | 7);  // S at the end of this 32-block
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int t = 4 * lane + i;
-      s_s2[sb * TQ + t] = S[i];
-      s_dtp[sb * TQ + t] = dp[i];
-      s_v[sb * TQ + t] = ex2(Se - S[i]) * dp[i];
-    }
+    if (lane == 31) s_btot[sb * 4 + dblk] = incl;
+    asm volatile("bar.sync 1, 128;" ::: "memory");  // the four dt warps
+    float pre = 0.f;
+    for (int k2 = 0; k2 < dblk; ++k2) pre += s_btot[sb * 4 + k2];
+    const float S = pre + incl;
+    const float Se = __shfl_sync(0xffffffffu, S, 31);  // S at the end of this 32-block
+    s_s2[sb * TQ + t] = S;
+    s_dtp[sb * TQ + t] = dp;
+    s_v[sb * TQ + t] = ex2(Se - S) * dp;
   };
   // (X o w) hi + lo of the chunk in `stage`, row j = row, columns [16 cg, +16)
   auto xw_phase = [&](int stage, int sb) {
@@ -371,35 +363,45 @@ ssd_tc_kernel(const __grid_constant__ ScanArgs a) {
       *reinterpret_cast<uint4*>(smem + kOffXWlo + o) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
     }
   };
-  // ---- MMA issue (thread 0)
+  // ---- MMA issue. Four independent streams, each from lane 0 of a warp whose
+  // M share is the lightest (TMEM lane quarter 0): an issuing thread waits out each
+  // MMA, so separate issuers let the streams overlap on the tensor pipe.
+  // Descriptors are precomputed bases plus constant offsets (a descriptor's address
+  // field is the byte address / 16, and shared addresses stay below 2^18).
   uint32_t tmem = 0;  // TMEM base, read after the allocation barrier below
-  auto issue_cb_dh = [&](int stage) {  // CB = C . B^T (full pass), dH^T = B^T . (X o w)
-    const uint32_t sC = sbase + kOffIn + stage * kStage, sB = sC + kTileC;
-    if (kFull) {
-      for (int s2 = 0; s2 < TN / 16; ++s2) {
-        const uint32_t ko = (s2 >> 2) * TQ * 128 + (s2 & 3) * 32;
-        mma_ss(tmem + kColCB, sdesc(sC + ko, 16, 1024), sdesc(sB + ko, 16, 1024), idesc128(128, 0, 0), s2 > 0);
-      }
+  constexpr int kIssYd = 0, kIssYo = 128, kIssCB = 256, kIssDH = 384;  // issuing threads
+  auto stage_addr = [&](int stage) { return sbase + kOffIn + stage * kStage; };
+  auto issue_cb = [&](int stage) {  // CB = C . B^T
+    const uint64_t a0 = sdesc(stage_addr(stage), 16, 1024), b0 = sdesc(stage_addr(stage) + kTileC, 16, 1024);
+#pragma unroll
+    for (int s2 = 0; s2 < TN / 16; ++s2) {
+      const uint32_t ko = ((s2 >> 2) * TQ * 128 + (s2 & 3) * 32) >> 4;
+      mma_ss(tmem + kColCB, a0 + ko, b0 + ko, idesc128(128, 0, 0), s2 > 0);
     }
+  };
+  auto issue_dh = [&](int stage) {  // dH^T = B^T . (X o w), hi then lo
+    const uint64_t bt0 = sdesc(stage_addr(stage) + kTileC, TQ * 128, 1024);
+    const uint64_t hi0 = sdesc(sbase + kOffXWhi, TQ * 128, 1024), lo0 = sdesc(sbase + kOffXWlo, TQ * 128, 1024);
+#pragma unroll
     for (int s2 = 0; s2 < TQ / 16; ++s2) {
-      const uint32_t jk = s2 * 2048;  // 16 rows of the [j][*] tiles
-      const uint64_t bt = sdesc(sB + jk, TQ * 128, 1024);
-      mma_ss(tmem + kColDH, bt, sdesc(sbase + kOffXWhi + jk, TQ * 128, 1024), idesc128(64, 1, 1), s2 > 0);
-      mma_ss(tmem + kColDH, bt, sdesc(sbase + kOffXWlo + jk, TQ * 128, 1024), idesc128(64, 1, 1), 1);
+      const uint32_t jk = (s2 * 2048) >> 4;  // 16 rows of the [j][*] tiles
+      mma_ss(tmem + kColDH, bt0 + jk, hi0 + jk, idesc128(64, 1, 1), s2 > 0);
+      mma_ss(tmem + kColDH, bt0 + jk, lo0 + jk, idesc128(64, 1, 1), 1);
     }
   };
   auto issue_yo = [&](int stage, int yb) {  // Yoff = C . H^T into Yo buffer yb
-    const uint32_t sC = sbase + kOffIn + stage * kStage;
+    const uint64_t a0 = sdesc(stage_addr(stage), 16, 1024), h0 = sdesc(sbase + kOffHT, TN * 128, 1024);
+#pragma unroll
     for (int s2 = 0; s2 < TN / 16; ++s2) {
-      const uint32_t ko = (s2 >> 2) * TQ * 128 + (s2 & 3) * 32;
-      mma_ss(tmem + kColYo + 64 * yb, sdesc(sC + ko, 16, 1024), sdesc(sbase + kOffHT + s2 * 2048, TN * 128, 1024),
-             idesc128(64, 0, 1), s2 > 0);
+      const uint32_t ko = ((s2 >> 2) * TQ * 128 + (s2 & 3) * 32) >> 4;
+      mma_ss(tmem + kColYo + 64 * yb, a0 + ko, h0 + ((s2 * 2048) >> 4), idesc128(64, 0, 1), s2 > 0);
     }
   };
   auto issue_yd = [&](int stage) {  // Y = M . X (A = M hi, lo from TMEM)
-    const uint32_t sX = sbase + kOffIn + stage * kStage + kTileC + kTileB;
+    const uint64_t x0 = sdesc(stage_addr(stage) + kTileC + kTileB, TQ * 128, 1024);
+#pragma unroll
     for (int s2 = 0; s2 < TQ / 16; ++s2) {
-      const uint64_t xd = sdesc(sX + s2 * 2048, TQ * 128, 1024);
+      const uint64_t xd = x0 + ((s2 * 2048) >> 4);
       mma_ts(tmem + kColYd, tmem + kColMhi + s2 * 8, xd, idesc128(64, 0, 1), s2 > 0);
       mma_ts(tmem + kColYd, tmem + kColMlo + s2 * 8, xd, idesc128(64, 0, 1), 1);
     }
@@ -425,7 +427,7 @@ ssd_tc_kernel(const __grid_constant__ ScanArgs a) {
   if (c_begin < c_end) {
     issue_chunk(c_begin, 0);
     if (c_begin + 1 < c_end) issue_chunk(c_begin + 1, 1);
-    if (warp == 0) {
+    if (dt_warp) {
       load_dt(c_begin);
       dt_phase(c_begin, 0);
       if (c_begin + 1 < c_end) load_dt(c_begin + 1);
@@ -436,11 +438,15 @@ ssd_tc_kernel(const __grid_constant__ ScanArgs a) {
     __syncthreads();
     xw_phase(0, 0);
     tc_sync();
-    if (tid == 0) {
-      issue_cb_dh(0);
-      if (kFull) issue_yo(0, 0);
+    if (kFull && tid == kIssCB) {
+      issue_cb(0);
       mma_commit(mbar1);
     }
+    if (tid == kIssDH) {
+      issue_dh(0);
+      mma_commit(mbar1);
+    }
+    if (kFull && tid == kIssYo) issue_yo(0, 0);  // completion covered by this thread's next commit
   }
 
   for (int c = c_begin; c < c_end; ++c) {
@@ -457,7 +463,7 @@ ssd_tc_kernel(const __grid_constant__ ScanArgs a) {
     tc_fence_after();
     const float tot2 = s_s2[st * TQ + TQ - 1];
 
-    // (2) M(c) into TMEM; H(c) = exp(total) H(c-1) + dH(c); warp 0 also prepares chunk c+1's decays
+    // (2) M(c) into TMEM; H(c) = exp(total) H(c-1) + dH(c); the dt warps also prepare chunk c+1's decays
     if (kFull) {
       // M = CB o exp(s_t - s_j) dt'_j (j <= t) for row t = row. This thread takes
       // columns 32 bb + 8 cg .. +7 of each 32-column block bb, so every warp gets
@@ -529,7 +535,7 @@ ssd_tc_kernel(const __grid_constant__ ScanArgs a) {
       if (kFull) state_to_smem();
       else seg_logdecay += tot2 * 0.6931471805599453f;
     }
-    if (warp == 0 && more) {
+    if (dt_warp && more) {
       dt_phase(c + 1, st ^ 1);
       if (c + 2 < c_end) load_dt(c + 2);
     }
@@ -538,19 +544,24 @@ ssd_tc_kernel(const __grid_constant__ ScanArgs a) {
     tc_sync();
 
     // (3) MMAs: Y(c) = M(c) . X(c); Yoff(c+1) = C(c+1) . H(c)^T
-    if (tid == 0) {
-      if (kFull) {
-        issue_yd(st);
-        if (more) issue_yo(st ^ 1, st ^ 1);
-        mma_commit(mbar2);
-      }
+    if (kFull && tid == kIssYd) {
+      issue_yd(st);
+      mma_commit(mbar2);
+    }
+    if (kFull && tid == kIssYo) {
+      if (more) issue_yo(st ^ 1, st ^ 1);
+      mma_commit(mbar2);
     }
     // (4) chunk c+1's (X o w), then its CB and dH MMAs
     if (more) {
       xw_phase(st ^ 1, st ^ 1);
       tc_sync();
-      if (tid == 0) {
-        issue_cb_dh(st ^ 1);
+      if (kFull && tid == kIssCB) {
+        issue_cb(st ^ 1);
+        mma_commit(mbar1);
+      }
+      if (tid == kIssDH) {
+        issue_dh(st ^ 1);
         mma_commit(mbar1);
       }
     }
