@@ -7,6 +7,7 @@
 // rejected before anything is written. All checks here run before the first
 // launch, so a non-OK status leaves every buffer untouched.
 #include <algorithm>
+#include <functional>
 #include <cstdio>
 #include <cstring>
 #include <vector>
@@ -99,14 +100,28 @@ ScanPlan plan_scan(const mamba2_dims* d, mamba2_dtype act, const mamba2_recurren
     return p;
   }
   const int Q = scan_chunk_tokens(d->headdim, d->d_state);
-  int64_t total_chunks = 0;
-  for (int i = 0; i < n; ++i) {
-    const int64_t T = rb->cu_seqlens[i + 1] - rb->cu_seqlens[i];
-    total_chunks += (T + Q - 1) / Q;
+  // Chunks per segment: both passes run one CTA per SM, so pick the segment
+  // length that minimises whole waves x chunks per CTA, counting a state-pass
+  // chunk (one product, no output) at about a third of a full-pass chunk and
+  // about two chunks of fill and drain per CTA.
+  std::vector<int64_t> ch(n);
+  for (int i = 0; i < n; ++i) ch[i] = (rb->cu_seqlens[i + 1] - rb->cu_seqlens[i] + Q - 1) / Q;
+  std::sort(ch.begin(), ch.end(), std::greater<int64_t>());
+  const int64_t nsm = std::max(1, device_sm_count());
+  const int64_t max_ch = n > 0 ? std::max<int64_t>(1, ch[0]) : 1;
+  double best = 1e300;
+  p.seg_chunks = (int)max_ch;
+  for (int64_t sc = 1; sc <= std::min<int64_t>(max_ch, 4096); ++sc) {
+    int64_t extra = 0;  // segments beyond one per sequence = state-pass CTAs per head
+    for (int i = 0; i < n && ch[i] > sc; ++i) extra += (ch[i] + sc - 1) / sc - 1;
+    const int64_t full_waves = (d->heads * (n + extra) + nsm - 1) / nsm;
+    const int64_t state_waves = (d->heads * extra + nsm - 1) / nsm;
+    const double cost = (double)full_waves * (double)(std::min(sc, max_ch) + 2) + (double)state_waves * (0.35 * sc + 1.0);
+    if (cost < best - 1e-9) {
+      best = cost;
+      p.seg_chunks = (int)sc;
+    }
   }
-  const int64_t target = 4LL * device_sm_count();  // CTAs wanted (2 resident per SM, ~2 waves)
-  int64_t sc = (total_chunks * d->heads + target - 1) / std::max<int64_t>(1, target);
-  p.seg_chunks = (int)std::max<int64_t>(1, sc);
   p.total_segs = 0;
   for (int i = 0; i < n; ++i) {
     const int64_t T = rb->cu_seqlens[i + 1] - rb->cu_seqlens[i];

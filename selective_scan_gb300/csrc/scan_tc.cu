@@ -1,5 +1,5 @@
-// Chunked selective scan on the 5th-generation tensor cores (tcgen05, TMEM)
-// for headdim 64 x d_state 128 with bf16 activations.
+// Chunked selective scan on the 5th-generation tensor cores (tcgen05 MMAs with
+// TMEM accumulators, TMA tile loads) for headdim 64 x d_state 128, bf16.
 //
 // Semantics: gllm PR #85 "feat(backend): Mamba2 ops, with CPU reference
 // implementations", section "Ops" (SSMScan): per token
@@ -11,36 +11,50 @@
 // Optimization" describes long prefill as a chunked parallel scan.
 //
 // Chunk of Q = 128 tokens, a_t = -exp(A_log) dt'_t, s_t = a_0 + ... + a_t:
-//   y_t   = exp(s_t) C_t . h_in + sum_{j<=t} (C_t . B_j) exp(s_t - s_j) dt'_j x_j + D x_t
+//   y_t   = exp(s_t) C_t . h_in + sum_{j<=t} M[t][j] x_j,
+//           M[t][j] = (C_t . B_j) exp(s_t - s_j) dt'_j  (+ D when j = t)
 //   h_out = exp(s_{Q-1}) h_in + sum_j exp(s_{Q-1} - s_j) dt'_j x_j (x) B_j
 // (every exponent a difference taken in the <= 0 direction).
 //
-// One CTA of 8 warps per (sequence segment, head); TMEM lane t = token row t
-// (or state row n). Per chunk, with every tile in its natural load layout
-// (a [rows][cols] bf16 tile stored with the 128-byte swizzle in 64-column
-// blocks is both the K-major and the MN-major tcgen05 operand):
-//   MMA batch 1:
-//     CB      = C . B^T                       M=128 N=128 K=128 (C, B K-major)
-//     Yoff    = C . H^T                       M=128 N=64  K=128 (H^T MN-major)
-//     dH^T    = B^T . (X o w)  (hi + lo)      M=128 N=64  K=128 (both MN-major)
-//   threads: M = CB o exp(s_t - s_j) dt'_j (j <= t), split bf16 hi + lo into
-//            TMEM (A operand); H^T = exp(s_{Q-1}) H^T + dH^T kept in fp32
-//            registers, its bf16 copy written to smem for the next chunk
-//   MMA batch 2:  Y = M . X  (A from TMEM)    M=128 N=64  K=128 (X MN-major)
-//   threads: y = Y + exp(s_t) Yoff + D x  -> bf16 -> HBM
+// Full pass: one CTA per (sequence segment, head), 20 warps in fixed roles
+// that hand work to each other through mbarriers (no CTA-wide barrier in the
+// chunk loop):
+//   warps 0-15  element-wise work; TMEM lane t = token row t (or state row n).
+//               Per chunk i: state through chunk i-1 (H = exp(total) H + dH,
+//               fp32 in registers, bf16 copy of H^T to smem); X o w for chunk i
+//               (bf16 hi + lo); M(i) = CB o decay (+ D on the diagonal), bf16
+//               hi + lo written over CB in TMEM; output of chunk i-1,
+//               y = Y + exp(s_t) Yoff, stored straight from registers.
+//   warp 16     CB = C . B^T                M=128 N=128 K=128; before it, the
+//               chunk's dt' = softplus(dt + dt_bias), cumulative log-decay and
+//               block factors (up to four chunks ahead of the element-wise warps)
+//   warp 17     Yoff = C . H^T              M=128 N=64  K=128 (H^T MN-major)
+//   warp 18     dH^T = B^T . (X o w)        M=128 N=64  K=128 (hi and lo);
+//               also loads the C and B tiles of chunk i+2
+//   warp 19     Y = M . X (A from TMEM)     M=128 N=64  K=128 (hi and lo);
+//               also loads the X tile of chunk i+2
+// An MMA-issuing thread waits out each MMA it issues (about 100 cycles per
+// instruction at any N), so the four products run as four concurrent streams
+// from four warps. A [rows][cols] bf16 tile stored with the 128-byte swizzle
+// in 64-column blocks (the TMA box layout) is both the K-major and the
+// MN-major tcgen05 operand, so every tile is used in its load layout.
 // M and X o w are carried as bf16 hi + lo (about 16 mantissa bits): with a
 // single bf16 M the worst y error reaches 1.4x its tolerance, and a single
 // bf16 X o w gives a state error of 1.7e-3 against a 1e-3 tolerance
-// (measured on the 130m, varlen and 65 536-token workloads). A single bf16
-// copy of H costs y less than 5 % of its tolerance, so H is not split.
+// (measured on the 130m, varlen and 65 536-token workloads); a single bf16
+// copy of H costs y less than 5 % of its tolerance.
 //
-// Long runs are cut into segments; a state pass (kFull = false: only the
-// dH^T products) computes each segment's end state from zero and its total
-// log-decay, and the full pass seeds segment k by folding the earlier
-// segments' entries (see the scan entry point). Waits on the MMA-completion
-// mbarriers are bounded: on a timeout the kernel records it in a device
-// counter (mamba2_device_timeouts), stops issuing work, frees its TMEM and
+// Long runs are cut into segments. The state pass computes, per segment but
+// the last, the end state from zero (the first segment from the slot's state)
+// and the total log-decay, walking the chunks from last to first so that every
+// token's weight exp(s_end - s_j) dt'_j is known when its chunk is read: the
+// products B^T . (X o w) of all chunks then accumulate in TMEM with no per-chunk
+// state update. The full pass seeds segment k by folding the earlier segments'
+// entries. Every wait is bounded: on a timeout the CTA records it in a device
+// counter (mamba2_device_timeouts), drains what it issued, frees its TMEM and
 // returns.
+#include <cuda.h>
+
 #include "common.cuh"
 
 namespace mamba2 {
@@ -52,38 +66,56 @@ namespace {
 constexpr int TQ = 128;  // tokens per chunk
 constexpr int TP = 64;   // headdim
 constexpr int TN = 128;  // d_state
-constexpr int kTcThreads = 512;  // 16 warps: 4 per TMEM lane quarter
-constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kWaitLimit = 1u << 22;  // try_wait rounds before giving up (far above a healthy MMA batch)
+constexpr int kMathWarps = 16;
+constexpr int kMathThreads = 32 * kMathWarps;
+constexpr int kFullThreads = kMathThreads + 4 * 32;   // + CB (and dt), Yoff, dH, Y issuers
+constexpr int kStateThreads = kMathThreads + 3 * 32;  // + loader, dH hi and dH lo issuers
+constexpr uint32_t kWaitLimit = 1u << 22;  // try_wait rounds before giving up (about a second at the backoff)
+constexpr uint32_t kSuspendNs = 1000;      // a waiting thread sleeps up to this long per try_wait round
 
-// TMEM column map (128 lanes each)
-constexpr uint32_t kColCB = 0;     // [0,128)   C . B^T (fp32)
-constexpr uint32_t kColMhi = 128;  // [128,192) M hi (bf16 pairs)
-constexpr uint32_t kColMlo = 192;  // [192,256) M lo
-constexpr uint32_t kColYo = 256;   // [256,384) C . H^T (fp32), two buffers of 64 (chunk parity)
-constexpr uint32_t kColDH = 384;   // [384,448) B^T . (X o w) (fp32, lane = n)
-constexpr uint32_t kColYd = 448;   // [448,512) M . X (fp32)
+// ---- full pass: TMEM columns (128 lanes each)
+constexpr uint32_t kColCB = 0;     // [0,256): CB of chunk parity b at 128 b; M hi | M lo replace it
+constexpr uint32_t kColYo = 256;   // [256,384): C . H^T of chunk parity b at 256 + 64 b
+constexpr uint32_t kColDH = 384;   // [384,448): B^T . (X o w), lane = n
+constexpr uint32_t kColYd = 448;   // [448,512): M . X
 
-// Shared memory plan (bytes). Operand tiles are 1024-byte aligned.
-constexpr uint32_t kTileC = TQ * TN * 2;  // 32 KB  [t][n]
-constexpr uint32_t kTileB = TQ * TN * 2;  // 32 KB  [j][n]
-constexpr uint32_t kTileX = TQ * TP * 2;  // 16 KB  [j][p]
-constexpr uint32_t kStage = kTileC + kTileB + kTileX;  // 80 KB per input stage
-constexpr uint32_t kOffIn = 0;                          // 2 stages; a spent C tile stages y
-constexpr uint32_t kOffXWhi = 2 * kStage;               // (X o w) hi [j][p]
+// ---- full pass: shared memory (operand tiles 1024-byte aligned)
+constexpr uint32_t kTileC = TQ * TN * 2;  // 32 KB [t][n]
+constexpr uint32_t kTileB = TQ * TN * 2;  // 32 KB [j][n]
+constexpr uint32_t kTileX = TQ * TP * 2;  // 16 KB [j][p]
+constexpr uint32_t kStage = kTileC + kTileB + kTileX;  // chunk parity b at b * kStage
+constexpr uint32_t kOffXWhi = 2 * kStage;
 constexpr uint32_t kOffXWlo = kOffXWhi + kTileX;
-constexpr uint32_t kOffHT = kOffXWlo + kTileX;          // H^T (bf16) [n][p]
-constexpr uint32_t kOffS = kOffHT + TN * TP * 2;        // float s2[2][TQ]  (log2e * cumulative log-decay)
-constexpr uint32_t kOffDtp = kOffS + 2 * TQ * 4;        // float dtp[2][TQ]
-constexpr uint32_t kOffV = kOffDtp + 2 * TQ * 4;        // float v[2][TQ]
-constexpr uint32_t kOffMisc = kOffV + 2 * TQ * 4;       // mbarriers, tmem base
-constexpr uint32_t kSmemBytes = kOffMisc + 64 + 1024;  // + slack to align the base to 1024 bytes
-static_assert(kSmemBytes <= 232448, "shared memory plan exceeds 227 KB");
+constexpr uint32_t kOffHT = kOffXWlo + kTileX;         // H^T bf16 [n][p]
+constexpr int kDtRing = 4;                              // dt buffers (chunk i in i % 4)
+constexpr uint32_t kOffDt = kOffHT + TN * TP * 2;      // kDtRing buffers of {s2, dt', v}[TQ] floats
+constexpr uint32_t kDtBuf = 3 * TQ * 4;
+constexpr uint32_t kOffBar = kOffDt + kDtRing * kDtBuf;
+enum FullBar : int {  // + chunk % 2 (+ chunk % 4 for kEpiDone)
+  kFullCB = 0, kFullX = 2, kCBDone = 4, kYoDone = 6, kDHDone = 8, kYdDone = 10,
+  kHDone = 12, kXWReady = 14, kMReady = 16, kDtReady = 18, kEpiDone = 20, kNumFullBars = 24
+};
+constexpr uint32_t kOffMisc = kOffBar + 8 * kNumFullBars;  // TMEM base, abort flag
+constexpr uint32_t kFullSmem = kOffMisc + 16 + 1024;        // + slack to align the base to 1024
+static_assert(kFullSmem <= 232448, "full-pass shared memory plan exceeds 227 KB");
+
+// ---- state pass: shared memory (3 stages of B, X), TMEM D hi [0,64), D lo [64,128)
+constexpr int kStStages = 3;
+constexpr uint32_t kStStage = kTileB + kTileX;
+constexpr uint32_t kStOffXW = kStStages * kStStage;   // [2][hi, lo] X o w tiles
+constexpr uint32_t kStOffW = kStOffXW + 4 * kTileX;   // [2][TQ] token weights
+constexpr uint32_t kStOffBtot = kStOffW + 2 * TQ * 4; // [2][4]
+constexpr uint32_t kStOffR = kStOffBtot + 32;         // total log2 decay of the segment
+constexpr uint32_t kStOffBar = kStOffR + 16;
+enum StateBar : int { kStFull = 0, kStDHDone = 3, kStXWReady = 6, kNumStateBars = 8 };
+constexpr uint32_t kStOffMisc = kStOffBar + 8 * kNumStateBars;
+constexpr uint32_t kStateSmem = kStOffMisc + 16 + 1024;
+static_assert(kStateSmem <= 232448, "state-pass shared memory plan exceeds 227 KB");
 
 __device__ __forceinline__ uint32_t su32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
 
 // byte offset of element (r, c) in a [R][cols] bf16 tile, 128-byte swizzle,
-// 64-column blocks of R rows each
+// 64-column blocks of R rows each (the layout a TMA box of 64 x R lands in)
 __device__ __forceinline__ uint32_t tile_off(int r, int c, int R) {
   return (uint32_t)((c >> 6) * R * 128 + r * 128 + ((((c & 63) >> 3) ^ (r & 7)) << 4) + (c & 7) * 2);
 }
@@ -110,20 +142,61 @@ __device__ __forceinline__ void mma_ts(uint32_t d, uint32_t a_tmem, uint64_t b, 
 __device__ __forceinline__ void mma_commit(uint32_t mbar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" :: "r"(mbar) : "memory");
 }
-// Bounded wait for the mbarrier phase; false on timeout.
-__device__ __forceinline__ bool mbar_wait(uint32_t mbar, uint32_t phase) {
-  for (uint32_t it = 0; it < kWaitLimit; ++it) {
-    uint32_t done;
-    asm volatile("{\n.reg .pred P;\nmbarrier.try_wait.parity.shared::cta.b64 P, [%1], %2;\nselp.u32 %0, 1, 0, P;\n}\n"
-                 : "=r"(done) : "r"(mbar), "r"(phase) : "memory");
-    if (done) return true;
-  }
-  return false;
-}
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
+// ---- mbarriers
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" :: "r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" :: "r"(bar) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" :: "r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile("{\n.reg .pred P;\nmbarrier.try_wait.parity.shared::cta.b64 P, [%1], %2, %3;\nselp.u32 %0, 1, 0, P;\n}\n"
+               : "=r"(done) : "r"(bar), "r"(parity), "r"(kSuspendNs) : "memory");
+  return done != 0;
+}
+// Bounded wait for the completion of the barrier phase with this parity; after
+// a few rounds the thread sleeps between polls, so waiting warps leave the
+// issue slots to the working ones. Gives up when the CTA's abort flag is
+// raised, and raises it itself on a timeout.
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile uint32_t* abort_flag) {
+  for (uint32_t it = 0; it < kWaitLimit; ++it) {
+    if (mbar_test(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (it >= 2) __nanosleep(it < 32 ? 32 : 128);  // back off: a polling warp takes issue slots
+  }
+  *abort_flag = 1u;
+  return false;
+}
+// The same, decided for the whole warp (every lane waits; all get the same
+// answer), for warps whose lanes then run .sync.aligned or __syncwarp code.
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile uint32_t* abort_flag) {
+  return __all_sync(0xffffffffu, wait_bar(bar, parity, abort_flag));
+}
+// Bounded wait that ignores the abort flag (draining work already issued).
+__device__ __forceinline__ void drain_bar(uint32_t bar, uint32_t parity) {
+  for (uint32_t it = 0; it < kWaitLimit; ++it)
+    if (mbar_test(bar, parity)) return;
+}
+// named barrier over `count` threads; returns the OR of `pred` over them
+__device__ __forceinline__ bool bar_or(int id, int count, bool pred) {
+  uint32_t r;
+  asm volatile("{\n.reg .pred p, q;\nsetp.ne.u32 p, %1, 0;\nbar.red.or.pred q, %2, %3, p;\nselp.u32 %0, 1, 0, q;\n}\n"
+               : "=r"(r) : "r"((uint32_t)pred), "r"(id), "r"(count) : "memory");
+  return r != 0;
+}
+__device__ __forceinline__ void bar_sync(int id, int count) {
+  asm volatile("bar.sync %0, %1;" :: "r"(id), "r"(count) : "memory");
+}
+
+// ---- TMEM loads / stores (32 lanes x 32 bit)
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
   uint32_t r[16];
   asm volatile("tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
@@ -133,48 +206,6 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
   for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
-}
-__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
-  asm volatile("tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};"
-               :: "r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
-                  "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
-               : "memory");
-}
-
-// 2^x with the hardware approximation (flushes subnormal results to zero)
-__device__ __forceinline__ float ex2(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
-
-__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
-  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
-  return *reinterpret_cast<uint32_t*>(&v);
-}
-// fp32 pair -> (hi, lo) bf16 pairs with hi + lo ~ v to ~2^-17
-__device__ __forceinline__ void split2(float a, float b, uint32_t& hi, uint32_t& lo) {
-  hi = pack2(a, b);
-  lo = pack2(a - __uint_as_float(hi << 16), b - __uint_as_float(hi & 0xffff0000u));
-}
-
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool valid) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src), "r"(valid ? 16 : 0));
-}
-
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
-  uint32_t r[32];
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
-        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
-        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-      : "r"(taddr));
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 // two 16-column loads, one wait
 __device__ __forceinline__ void tmem_ld16x2(uint32_t ta, uint32_t tb, float (&va)[16], float (&vb)[16]) {
@@ -196,436 +227,768 @@ __device__ __forceinline__ void tmem_ld16x2(uint32_t ta, uint32_t tb, float (&va
   }
 }
 
-template <bool kFull>
-__global__ void __launch_bounds__(kTcThreads, 1)
-ssd_tc_kernel(const __grid_constant__ ScanArgs a) {
+// 2^x with the hardware approximation (flushes subnormal results to zero)
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+// fp32 pair -> (hi, lo) bf16 pairs with hi + lo ~ v to ~2^-17
+__device__ __forceinline__ void split2(float a, float b, uint32_t& hi, uint32_t& lo) {
+  hi = pack2(a, b);
+  lo = pack2(a - __uint_as_float(hi << 16), b - __uint_as_float(hi & 0xffff0000u));
+}
+
+// ---- tile loads
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool valid) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src), "r"(valid ? 16 : 0));
+}
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* tm, int x, int y, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
+      :: "r"(dst), "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(bar) : "memory");
+}
+
+// Where one chunk's tiles come from: xbc rows [rb, rb + len), 1 <= len <= TQ.
+struct ChunkSrc {
+  const __nv_bfloat16* xbc;
+  int64_t ld;  // row stride (conv_dim)
+  int64_t rb;
+  int len;
+};
+
+// One [TQ][ncols] tile (64-column blocks, 128-byte swizzle) of columns
+// [col0, col0 + ncols), by the whole calling warp: a TMA box per 64 columns
+// when the chunk is whole, else 16-byte cp.async pieces with the rows past the
+// run zero-filled. Arms `bar` with the bytes (TMA) or arrives on it once the
+// copies are visible to the tensor cores (cp.async): one arrival per call, so
+// a barrier shared by two tiles is initialised with count 2.
+__device__ __forceinline__ void load_tile(uint32_t dst, const ChunkSrc& s, const CUtensorMap* tm, bool use_tma,
+                                          int col0, int ncols, uint32_t bar, int lane) {
+  if (use_tma && s.len == TQ) {
+    if (lane == 0) {
+      mbar_expect_tx(bar, (uint32_t)(TQ * ncols * 2));
+      for (int b = 0; b < ncols / 64; ++b) tma_load_2d(dst + b * TQ * 128, tm, col0 + 64 * b, (int)s.rb, bar);
+    }
+  } else {
+    const int pieces = ncols / 8;
+    for (int i = lane; i < TQ * pieces; i += 32) {
+      const int t = i / pieces, pc = i - t * pieces;
+      const bool ok = t < s.len;
+      const int64_t grow = ok ? s.rb + t : s.rb;
+      cp_async16(dst + tile_off(t, pc * 8, TQ), s.xbc + grow * s.ld + col0 + pc * 8, ok);
+    }
+    asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;\n" ::: "memory");
+    fence_async_smem();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar);
+  }
+}
+
+// What one CTA works on: head h of segment k of sequence sq, chunks [c_begin, c_end).
+struct Cta {
+  int sq, seg0, k, nseg, h, row0, T, c_begin, c_end, n;
+  bool fresh;
+  int x_col, b_col, c_col;
+  float A2, dtb, Dh;  // decay rate in log2 units, dt bias, skip weight
+};
+__device__ __forceinline__ Cta cta_info(const ScanArgs& a) {
+  Cta c;
+  const int seg = blockIdx.x;
+  c.h = blockIdx.y;
+  c.sq = find_tile_seq(a.tab, seg);
+  c.seg0 = a.tab.tile[c.sq];
+  c.k = seg - c.seg0;
+  c.nseg = a.tab.tile[c.sq + 1] - c.seg0;
+  const int H = a.heads, G = a.ngroups;
+  const int g = c.h / (H / G);
+  c.row0 = a.tab.cu[c.sq];
+  c.T = a.tab.cu[c.sq + 1] - c.row0;
+  const int nchunks = (c.T + TQ - 1) / TQ;
+  c.c_begin = c.k * a.seg_chunks;
+  c.c_end = min(nchunks, c.c_begin + a.seg_chunks);
+  c.n = max(0, c.c_end - c.c_begin);
+  c.fresh = seq_fresh(a.tab, c.sq);
+  c.x_col = c.h * TP;
+  c.b_col = H * TP + g * TN;
+  c.c_col = H * TP + G * TN + g * TN;
+  c.A2 = expf(a.A_log[c.h]) * 1.4426950408889634f;
+  c.dtb = a.dt_bias[c.h];
+  c.Dh = a.D[c.h];
+  return c;
+}
+
+// dt'_t = softplus(dt_t + dt_bias) of token t of chunk c (0 past the run), from raw bf16 bits
+__device__ __forceinline__ float dt_prime(unsigned short raw, bool valid, float dtb) {
+  return valid ? softplus_f(__uint_as_float((uint32_t)raw << 16) + dtb) : 0.f;
+}
+// inclusive warp scan
+__device__ __forceinline__ float warp_incl_sum(float v, int lane) {
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const float u = __shfl_up_sync(0xffffffffu, v, o);
+    if (lane >= o) v += u;
+  }
+  return v;
+}
+
+__global__ void __launch_bounds__(kFullThreads, 1)
+ssd_tc_full(const __grid_constant__ ScanArgs a, const __grid_constant__ CUtensorMap tm, const int use_tma) {
   extern __shared__ unsigned char smem_raw[];
   // operand tiles need a 1024-byte aligned base (the swizzle keys on address bits 7-9)
   const uint32_t raw_base = su32(smem_raw);
   unsigned char* smem = smem_raw + (((raw_base + 1023u) & ~1023u) - raw_base);
   const uint32_t sbase = su32(smem);
-  float* s_s2 = reinterpret_cast<float*>(smem + kOffS);    // [2][TQ] log2e * cumulative log-decay
-  float* s_dtp = reinterpret_cast<float*>(smem + kOffDtp); // [2][TQ] dt'
-  float* s_v = reinterpret_cast<float*>(smem + kOffV);     // [2][TQ] exp(s_e - s_j) dt'_j, e = end of j's 32-block
-  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + kOffMisc + 8);
-  const uint32_t mbar1 = sbase + kOffMisc + 16, mbar2 = sbase + kOffMisc + 24;
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + kOffMisc);
+  volatile uint32_t* s_abort = reinterpret_cast<volatile uint32_t*>(smem + kOffMisc + 4);
+  auto bar = [&](int id) { return sbase + kOffBar + 8u * (uint32_t)id; };
+  auto par = [](int i) { return (uint32_t)((i >> 1) & 1); };  // phase parity of chunk i on a [2] barrier
+  auto stage = [&](int i) { return sbase + (uint32_t)(i & 1) * kStage; };
 
-  const int seg = blockIdx.x, h = blockIdx.y;
-  const int sq = find_tile_seq(a.tab, seg);
-  const int seg0 = a.tab.tile[sq];
-  const int k = seg - seg0;
-  const int nseg = a.tab.tile[sq + 1] - seg0;
-  if (!kFull && k == nseg - 1) return;  // the state pass skips last segments
-
-  const int H = a.heads, G = a.ngroups;
-  const int g = h / (H / G);
-  const int row0 = a.tab.cu[sq];
-  const int T = a.tab.cu[sq + 1] - row0;
-  const int nchunks = (T + TQ - 1) / TQ;
-  const int c_begin = k * a.seg_chunks;
-  const int c_end = min(nchunks, c_begin + a.seg_chunks);
-  const bool fresh = seq_fresh(a.tab, sq);
-  const int64_t ld = a.conv_dim;
-  const __nv_bfloat16* xbc = static_cast<const __nv_bfloat16*>(a.xbc);
-  const __nv_bfloat16* dtg = static_cast<const __nv_bfloat16*>(a.dt);
-  const int x_col = h * TP, b_col = H * TP + g * TN, c_col = H * TP + G * TN + g * TN;
-  const float A2 = expf(a.A_log[h]) * 1.4426950408889634f;  // decay rate in log2 units
-  const float dtb = a.dt_bias[h];
-  const float Dh = a.D[h];
-
+  const Cta ci = cta_info(a);
+  const int n = ci.n;
+  const int H = a.heads;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int row = tid & 127;   // TMEM lane = tile row this thread works on
-  const int cg = tid >> 7;     // column group 0..3 (warps 4 cg .. 4 cg + 3)
-  const int qrt = warp & 3;    // TMEM lane quarter = 32-row block of `row`
-  const uint32_t lane_off = (uint32_t)(qrt * 32) << 16;
+  const __nv_bfloat16* xbc = static_cast<const __nv_bfloat16*>(a.xbc);
 
-  // ---- TMEM allocation (warp 0), barriers (thread 0)
+  // ---- TMEM (warp 0) and barriers
   if (warp == 0) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" :: "r"(su32(s_tmem)), "r"(kTmemCols));
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;" :: "r"(su32(s_tmem)));
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
   }
-  if (tid == 0) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" :: "r"(mbar1), "r"(kFull ? 2 : 1));
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], 2;" :: "r"(mbar2));
-    asm volatile("fence.mbarrier_init.release.cluster;");
+  if (tid == kMathThreads) {
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(bar(kFullCB + b), 2);  // C tile, B tile
+      mbar_init(bar(kFullX + b), 1);
+      mbar_init(bar(kCBDone + b), 1);
+      mbar_init(bar(kYoDone + b), 1);
+      mbar_init(bar(kDHDone + b), 1);
+      mbar_init(bar(kYdDone + b), 1);
+      mbar_init(bar(kHDone + b), kMathWarps);
+      mbar_init(bar(kXWReady + b), kMathWarps);
+      mbar_init(bar(kMReady + b), kMathWarps);
+      mbar_init(bar(kDtReady + b), 1);
+    }
+    for (int b = 0; b < 4; ++b) mbar_init(bar(kEpiDone + b), kMathWarps);
+    *s_abort = 0u;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-
-  // ---- running state: this thread holds H^T[n = row][p], p in [16 cg, 16 cg + 16)
-  const int64_t head_off = (int64_t)h * TP * TN;
-  float* slot_ptr = a.ssm_state + (int64_t)seq_slot(a.tab, sq) * H * TP * TN + head_off;
-  auto ws_entry = [&](int segidx) -> float* { return a.ws_state + (int64_t)segidx * H * TP * TN + head_off; };
-  float hst[16];
-  auto load_state = [&](const float* src) {
-#pragma unroll
-    for (int i = 0; i < 16; ++i) hst[i] = src ? src[(int64_t)(16 * cg + i) * TN + row] : 0.0f;
-  };
-  auto store_state = [&](float* dst) {
-#pragma unroll
-    for (int i = 0; i < 16; ++i) dst[(int64_t)(16 * cg + i) * TN + row] = hst[i];
-  };
-  if (k == 0) {
-    const float* src = fresh ? nullptr : ((kFull && nseg > 1) ? ws_entry(seg0 + nseg - 1) : slot_ptr);
-    load_state(src);
-    if (!kFull && !fresh) store_state(ws_entry(seg0 + nseg - 1));  // seed copy for the full pass
-  } else if (!kFull) {
-    load_state(nullptr);
-  } else {
-    load_state(ws_entry(seg0));
-    for (int j = 1; j < k; ++j) {
-      const float d = __expf(a.ws_decay[(int64_t)(seg0 + j) * H + h]);
-      const float* e = ws_entry(seg0 + j);
-      float ev[16];
-#pragma unroll
-      for (int i = 0; i < 16; ++i) ev[i] = e[(int64_t)(16 * cg + i) * TN + row];
-#pragma unroll
-      for (int i = 0; i < 16; ++i) hst[i] = fmaf(d, hst[i], ev[i]);
-    }
-  }
-  // bf16 copy of H^T (B operand of C . H^T): row n, columns [16 cg, +16)
-  auto state_to_smem = [&]() {
-#pragma unroll
-    for (int q = 0; q < 2; ++q) {
-      uint32_t hw[4];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) hw[e] = pack2(hst[8 * q + 2 * e], hst[8 * q + 2 * e + 1]);
-      *reinterpret_cast<uint4*>(smem + kOffHT + tile_off(row, 16 * cg + 8 * q, TN)) =
-          make_uint4(hw[0], hw[1], hw[2], hw[3]);
-    }
-  };
-
-  // ---- chunk loads: cp.async 16-byte pieces into the swizzled tiles (zero past the run)
-  auto issue_chunk = [&](int c, int stage) {
-    const int len = min(TQ, T - c * TQ);
-    const int64_t rb = row0 + (int64_t)c * TQ;
-    const uint32_t st = sbase + kOffIn + stage * kStage;
-    for (int i = tid; i < TQ * (TN / 8); i += kTcThreads) {  // B and C: 16 pieces per row
-      const int t = i >> 4, pc = i & 15;
-      const bool ok = t < len;
-      const int64_t grow = ok ? rb + t : row0;
-      const uint32_t o = tile_off(t, pc * 8, TQ);
-      cp_async16(st + kTileC + o, xbc + grow * ld + b_col + pc * 8, ok);
-      if (kFull) cp_async16(st + o, xbc + grow * ld + c_col + pc * 8, ok);
-    }
-    for (int i = tid; i < TQ * (TP / 8); i += kTcThreads) {  // x: 8 pieces per row
-      const int t = i >> 3, pc = i & 7;
-      const bool ok = t < len;
-      const int64_t grow = ok ? rb + t : row0;
-      cp_async16(st + kTileC + kTileB + tile_off(t, pc * 8, TQ), xbc + grow * ld + x_col + pc * 8, ok);
-    }
-    asm volatile("cp.async.commit_group;\n" ::);
-  };
-  // ---- dt of a chunk: warps 0, 4, 8, 12 (TMEM lane quarter 0, the lightest M
-  // share), warp 4k taking the 32-block k (lane l: token 32 k + l)
-  const bool dt_warp = (warp & 3) == 0;
-  const int dblk = warp >> 2;
-  float* s_btot = reinterpret_cast<float*>(smem + kOffMisc + 32);  // [2][4] block totals of the log2 decay
-  // raw bf16 bits: the load stays in flight until the next chunk's dt phase converts it
-  unsigned short dt_raw = 0;
-  auto load_dt = [&](int c) {
-    const int t = 32 * dblk + lane;
-    dt_raw = t < min(TQ, T - c * TQ) ? reinterpret_cast<const unsigned short*>(dtg)[(row0 + (int64_t)c * TQ + t) * H + h]
-                                     : (unsigned short)0;
-  };
-  // dt', log2-scaled cumulative decay S and block-relative factors v of chunk c into buffer sb
-  auto dt_phase = [&](int c, int sb) {
-    const int t = 32 * dblk + lane;
-    const float dp = t < min(TQ, T - c * TQ) ? softplus_f(__uint_as_float((uint32_t)dt_raw << 16) + dtb) : 0.f;
-    float incl = -A2 * dp;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const float v = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += v;
-    }
-    if (lane == 31) s_btot[sb * 4 + dblk] = incl;
-    asm volatile("bar.sync 1, 128;" ::: "memory");  // the four dt warps
-    float pre = 0.f;
-    for (int k2 = 0; k2 < dblk; ++k2) pre += s_btot[sb * 4 + k2];
-    const float S = pre + incl;
-    const float Se = __shfl_sync(0xffffffffu, S, 31);  // S at the end of this 32-block
-    s_s2[sb * TQ + t] = S;
-    s_dtp[sb * TQ + t] = dp;
-    s_v[sb * TQ + t] = ex2(Se - S) * dp;
-  };
-  // (X o w) hi + lo of the chunk in `stage`, row j = row, columns [16 cg, +16)
-  auto xw_phase = [&](int stage, int sb) {
-    const float tot2 = s_s2[sb * TQ + TQ - 1];
-    const float wj = ex2(tot2 - s_s2[sb * TQ + row]) * s_dtp[sb * TQ + row];
-#pragma unroll
-    for (int q = 0; q < 2; ++q) {
-      const uint32_t o = tile_off(row, 16 * cg + 8 * q, TQ);
-      const uint4 xv = *reinterpret_cast<const uint4*>(smem + kOffIn + stage * kStage + kTileC + kTileB + o);
-      const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
-      uint32_t hi[4], lo[4];
-#pragma unroll
-      for (int e = 0; e < 4; ++e)
-        split2(__uint_as_float(xw[e] << 16) * wj, __uint_as_float(xw[e] & 0xffff0000u) * wj, hi[e], lo[e]);
-      *reinterpret_cast<uint4*>(smem + kOffXWhi + o) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-      *reinterpret_cast<uint4*>(smem + kOffXWlo + o) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-    }
-  };
-  // ---- MMA issue. Four independent streams, each from lane 0 of a warp whose
-  // M share is the lightest (TMEM lane quarter 0): an issuing thread waits out each
-  // MMA, so separate issuers let the streams overlap on the tensor pipe.
-  // Descriptors are precomputed bases plus constant offsets (a descriptor's address
-  // field is the byte address / 16, and shared addresses stay below 2^18).
-  uint32_t tmem = 0;  // TMEM base, read after the allocation barrier below
-  constexpr int kIssYd = 0, kIssYo = 128, kIssCB = 256, kIssDH = 384;  // issuing threads
-  auto stage_addr = [&](int stage) { return sbase + kOffIn + stage * kStage; };
-  auto issue_cb = [&](int stage) {  // CB = C . B^T
-    const uint64_t a0 = sdesc(stage_addr(stage), 16, 1024), b0 = sdesc(stage_addr(stage) + kTileC, 16, 1024);
-#pragma unroll
-    for (int s2 = 0; s2 < TN / 16; ++s2) {
-      const uint32_t ko = ((s2 >> 2) * TQ * 128 + (s2 & 3) * 32) >> 4;
-      mma_ss(tmem + kColCB, a0 + ko, b0 + ko, idesc128(128, 0, 0), s2 > 0);
-    }
-  };
-  auto issue_dh = [&](int stage) {  // dH^T = B^T . (X o w), hi then lo
-    const uint64_t bt0 = sdesc(stage_addr(stage) + kTileC, TQ * 128, 1024);
-    const uint64_t hi0 = sdesc(sbase + kOffXWhi, TQ * 128, 1024), lo0 = sdesc(sbase + kOffXWlo, TQ * 128, 1024);
-#pragma unroll
-    for (int s2 = 0; s2 < TQ / 16; ++s2) {
-      const uint32_t jk = (s2 * 2048) >> 4;  // 16 rows of the [j][*] tiles
-      mma_ss(tmem + kColDH, bt0 + jk, hi0 + jk, idesc128(64, 1, 1), s2 > 0);
-      mma_ss(tmem + kColDH, bt0 + jk, lo0 + jk, idesc128(64, 1, 1), 1);
-    }
-  };
-  auto issue_yo = [&](int stage, int yb) {  // Yoff = C . H^T into Yo buffer yb
-    const uint64_t a0 = sdesc(stage_addr(stage), 16, 1024), h0 = sdesc(sbase + kOffHT, TN * 128, 1024);
-#pragma unroll
-    for (int s2 = 0; s2 < TN / 16; ++s2) {
-      const uint32_t ko = ((s2 >> 2) * TQ * 128 + (s2 & 3) * 32) >> 4;
-      mma_ss(tmem + kColYo + 64 * yb, a0 + ko, h0 + ((s2 * 2048) >> 4), idesc128(64, 0, 1), s2 > 0);
-    }
-  };
-  auto issue_yd = [&](int stage) {  // Y = M . X (A = M hi, lo from TMEM)
-    const uint64_t x0 = sdesc(stage_addr(stage) + kTileC + kTileB, TQ * 128, 1024);
-#pragma unroll
-    for (int s2 = 0; s2 < TQ / 16; ++s2) {
-      const uint64_t xd = x0 + ((s2 * 2048) >> 4);
-      mma_ts(tmem + kColYd, tmem + kColMhi + s2 * 8, xd, idesc128(64, 0, 1), s2 > 0);
-      mma_ts(tmem + kColYd, tmem + kColMlo + s2 * 8, xd, idesc128(64, 0, 1), 1);
-    }
-  };
-  // block-wide barrier with the TMEM / async-proxy fences around it
-  auto tc_sync = [&]() {
-    fence_async_smem();
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-  };
-
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  tmem = *s_tmem;
+  const uint32_t tmem = *s_tmem;
 
-  float seg_logdecay = 0.f;
-  uint32_t ph1 = 0, ph2 = 0;
-  bool ok_run = true;
+  auto chunk_src = [&](int i) {
+    ChunkSrc s;
+    const int c = ci.c_begin + i;
+    s.xbc = xbc;
+    s.ld = a.conv_dim;
+    s.rb = ci.row0 + (int64_t)c * TQ;
+    s.len = min(TQ, ci.T - c * TQ);
+    return s;
+  };
 
-  // ---- prologue: chunk c_begin's loads, dt, (X o w), and its first MMAs
-  if (c_begin < c_end) {
-    issue_chunk(c_begin, 0);
-    if (c_begin + 1 < c_end) issue_chunk(c_begin + 1, 1);
-    if (dt_warp) {
-      load_dt(c_begin);
-      dt_phase(c_begin, 0);
-      if (c_begin + 1 < c_end) load_dt(c_begin + 1);
-    }
-    if (kFull) state_to_smem();
-    if (c_begin + 1 < c_end) asm volatile("cp.async.wait_group 1;\n" ::: "memory");
-    else asm volatile("cp.async.wait_group 0;\n" ::: "memory");
-    __syncthreads();
-    xw_phase(0, 0);
-    tc_sync();
-    if (kFull && tid == kIssCB) {
-      issue_cb(0);
-      mma_commit(mbar1);
-    }
-    if (tid == kIssDH) {
-      issue_dh(0);
-      mma_commit(mbar1);
-    }
-    if (kFull && tid == kIssYo) issue_yo(0, 0);  // completion covered by this thread's next commit
-  }
+  if (warp < kMathWarps) {
+    // =================== element-wise warps
+    const int row = tid & 127;  // TMEM lane = tile row this thread works on
+    const int cg = tid >> 7;    // column group 0..3
+    const int qrt = warp & 3;   // TMEM lane quarter = 32-row block of `row`
+    const uint32_t lane_off = (uint32_t)(qrt * 32) << 16;
+    auto dtbuf = [&](int i) { return reinterpret_cast<float*>(smem + kOffDt + (uint32_t)(i % kDtRing) * kDtBuf); };
 
-  for (int c = c_begin; c < c_end; ++c) {
-    const int st = (c - c_begin) & 1;  // stage, decay-array buffer and Yo buffer of chunk c
-    const int len = min(TQ, T - c * TQ);
-    const bool more = c + 1 < c_end;
-    // (1) CB(c), dH(c) (and Yoff(c)) complete
-    if (!__syncthreads_and(mbar_wait(mbar1, ph1))) {
-      if (tid == 0) atomicAdd(&g_tc_timeouts, 1u);
-      ok_run = false;
-      break;
-    }
-    ph1 ^= 1u;
-    tc_fence_after();
-    const float tot2 = s_s2[st * TQ + TQ - 1];
-
-    // (2) M(c) into TMEM; H(c) = exp(total) H(c-1) + dH(c); the dt warps also prepare chunk c+1's decays
-    if (kFull) {
-      // M = CB o exp(s_t - s_j) dt'_j (j <= t) for row t = row. This thread takes
-      // columns 32 bb + 8 cg .. +7 of each 32-column block bb, so every warp gets
-      // the same mix of blocks: above the diagonal all zero; below it
-      // exp(s_t - s_j) = exp(s_t - s_e) exp(s_e - s_j) with e the block's last
-      // token (both factors <= 1, the second times dt'_j being v_j); the
-      // diagonal block exponentiates each pair.
-      const float* S2 = s_s2 + st * TQ;
-      const float* DP = s_dtp + st * TQ;
-      const float* VV = s_v + st * TQ;
-      float cbv[4][8];
+    // running state: this thread holds H^T[n = row][p], p in [16 cg, 16 cg + 16)
+    const int64_t head_off = (int64_t)ci.h * TP * TN;
+    float* slot_ptr = a.ssm_state + (int64_t)seq_slot(a.tab, ci.sq) * H * TP * TN + head_off;
+    auto ws_entry = [&](int segidx) -> float* { return a.ws_state + (int64_t)segidx * H * TP * TN + head_off; };
+    float hst[16];
+    auto load_state = [&](const float* src) {
 #pragma unroll
-      for (int bb = 0; bb < 4; ++bb) {
-        if (bb <= qrt) {
-          uint32_t r[8];
-          asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
-                       : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
-                       : "r"(tmem + lane_off + kColCB + 32 * bb + 8 * cg));
+      for (int i = 0; i < 16; ++i) hst[i] = src ? src[(int64_t)(16 * cg + i) * TN + row] : 0.0f;
+    };
+    if (ci.k == 0) {
+      // the first segment starts from the slot (from the state pass's copy when the
+      // last segment will overwrite the slot in this same launch)
+      load_state(ci.fresh ? nullptr : (ci.nseg > 1 ? ws_entry(ci.seg0 + ci.nseg - 1) : slot_ptr));
+    } else {
+      load_state(ws_entry(ci.seg0));
+      for (int j = 1; j < ci.k; ++j) {
+        const float d = __expf(a.ws_decay[(int64_t)(ci.seg0 + j) * H + ci.h]);
+        const float* e = ws_entry(ci.seg0 + j);
+        float ev[16];
 #pragma unroll
-          for (int i = 0; i < 8; ++i) cbv[bb][i] = __uint_as_float(r[i]);
-        }
-      }
-      asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-      const float St = S2[row];
+        for (int i = 0; i < 16; ++i) ev[i] = e[(int64_t)(16 * cg + i) * TN + row];
 #pragma unroll
-      for (int bb = 0; bb < 4; ++bb) {
-        uint32_t hi[4], lo[4];
-        const int j0 = 32 * bb + 8 * cg;
-        if (bb > qrt) {
-#pragma unroll
-          for (int e = 0; e < 4; ++e) hi[e] = lo[e] = 0u;
-        } else if (bb < qrt) {
-          const float u = ex2(St - S2[32 * bb + 31]);
-#pragma unroll
-          for (int e = 0; e < 4; ++e)
-            split2(cbv[bb][2 * e] * u * VV[j0 + 2 * e], cbv[bb][2 * e + 1] * u * VV[j0 + 2 * e + 1], hi[e], lo[e]);
-        } else {
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int ja = j0 + 2 * e, jb = ja + 1;
-            const float ma = ja <= row ? cbv[bb][2 * e] * ex2(St - S2[ja]) * DP[ja] : 0.f;
-            const float mb = jb <= row ? cbv[bb][2 * e + 1] * ex2(St - S2[jb]) * DP[jb] : 0.f;
-            split2(ma, mb, hi[e], lo[e]);
-          }
-        }
-        const uint32_t pc = (uint32_t)(j0 >> 1);  // packed bf16-pair column
-        asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1,%2,%3,%4};"
-                     :: "r"(tmem + lane_off + kColMhi + pc), "r"(hi[0]), "r"(hi[1]), "r"(hi[2]), "r"(hi[3]) : "memory");
-        asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1,%2,%3,%4};"
-                     :: "r"(tmem + lane_off + kColMlo + pc), "r"(lo[0]), "r"(lo[1]), "r"(lo[2]), "r"(lo[3]) : "memory");
+        for (int i = 0; i < 16; ++i) hst[i] = fmaf(d, hst[i], ev[i]);
       }
     }
-    {
-      const float decay = ex2(tot2);
+
+    // bf16 H^T (B operand of C . H^T): row n, columns [16 cg, +16)
+    auto write_ht = [&]() {
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {
+        uint32_t hw[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) hw[e] = pack2(hst[8 * q + 2 * e], hst[8 * q + 2 * e + 1]);
+        *reinterpret_cast<uint4*>(smem + kOffHT + tile_off(row, 16 * cg + 8 * q, TN)) =
+            make_uint4(hw[0], hw[1], hw[2], hw[3]);
+      }
+    };
+    auto state_update = [&](int j) {  // H = exp(total_j) H + dH(j)
       float dv[16];
-      {
-        uint32_t r[16];
-        asm volatile("tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
-                     : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-                       "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
-                       "=r"(r[15])
-                     : "r"(tmem + lane_off + kColDH + 16 * cg));
-        asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-        for (int i = 0; i < 16; ++i) dv[i] = __uint_as_float(r[i]);
-      }
+      tmem_ld16(tmem + lane_off + kColDH + 16 * cg, dv);
+      const float decay = ex2(dtbuf(j)[TQ - 1]);
 #pragma unroll
       for (int i = 0; i < 16; ++i) hst[i] = fmaf(decay, hst[i], dv[i]);
-      if (kFull) state_to_smem();
-      else seg_logdecay += tot2 * 0.6931471805599453f;
-    }
-    if (dt_warp && more) {
-      dt_phase(c + 1, st ^ 1);
-      if (c + 2 < c_end) load_dt(c + 2);
-    }
-    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-    if (more) asm volatile("cp.async.wait_group 0;\n" ::: "memory");  // chunk c+1's tiles
-    tc_sync();
+    };
 
-    // (3) MMAs: Y(c) = M(c) . X(c); Yoff(c+1) = C(c+1) . H(c)^T
-    if (kFull && tid == kIssYd) {
-      issue_yd(st);
-      mma_commit(mbar2);
-    }
-    if (kFull && tid == kIssYo) {
-      if (more) issue_yo(st ^ 1, st ^ 1);
-      mma_commit(mbar2);
-    }
-    // (4) chunk c+1's (X o w), then its CB and dH MMAs
-    if (more) {
-      xw_phase(st ^ 1, st ^ 1);
-      tc_sync();
-      if (kFull && tid == kIssCB) {
-        issue_cb(st ^ 1);
-        mma_commit(mbar1);
-      }
-      if (tid == kIssDH) {
-        issue_dh(st ^ 1);
-        mma_commit(mbar1);
-      }
-    }
-    if (kFull) {
-      // (5) epilogue of chunk c: y = Y + exp(s_t) Yoff + D x, staged in the spent
-      // C tile of this stage, then written as whole rows
-      if (!__syncthreads_and(mbar_wait(mbar2, ph2))) {
-        if (tid == 0) atomicAdd(&g_tc_timeouts, 1u);
-        ok_run = false;
+    bool live = true;
+    for (int i = 0; i <= n; ++i) {
+      // all element-wise warps done with chunk i-1's steps; uniform abort decision
+      if (bar_or(2, kMathThreads, *s_abort != 0u)) {
+        live = false;
         break;
       }
-      ph2 ^= 1u;
-      tc_fence_after();
-      unsigned char* stage_p = smem + kOffIn + st * kStage;
-      {
-        const float et = ex2(s_s2[st * TQ + row]);
-        float yd[16], yo[16];
-        tmem_ld16x2(tmem + lane_off + kColYd + 16 * cg, tmem + lane_off + kColYo + 64 * st + 16 * cg, yd, yo);
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const uint32_t o = tile_off(row, 16 * cg + 8 * e, TQ);
-          const uint4 xv = *reinterpret_cast<const uint4*>(stage_p + kTileC + kTileB + o);
-          const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
-          uint32_t outw[4];
-#pragma unroll
-          for (int f = 0; f < 4; ++f) {
-            const int i = 8 * e + 2 * f;
-            const float y0 = fmaf(Dh, __uint_as_float(xw[f] << 16), fmaf(et, yo[i], yd[i]));
-            const float y1 = fmaf(Dh, __uint_as_float(xw[f] & 0xffff0000u), fmaf(et, yo[i + 1], yd[i + 1]));
-            outw[f] = pack2(y0, y1);
+      if (i < n) {
+        const float* D0 = dtbuf(i);
+        // (a) state through chunk i-1 -> H^T for C . H^T(i); releases the dH accumulator
+        bool ok = true;
+        if (i > 0) {
+          ok = warp_wait(bar(kDHDone + ((i - 1) & 1)), par(i - 1), s_abort) &&
+               warp_wait(bar(kYoDone + ((i - 1) & 1)), par(i - 1), s_abort);  // C . H^T(i-1) has read H^T
+          if (ok) {
+            tc_fence_after();
+            state_update(i - 1);
           }
-          *reinterpret_cast<uint4*>(stage_p + o) = make_uint4(outw[0], outw[1], outw[2], outw[3]);
         }
+        if (ok) write_ht();
+        fence_async_smem();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(kHDone + (i & 1)));
+
+        // (b) X o w of chunk i (bf16 hi + lo), w_j = exp(s_end - s_j) dt'_j
+        ok = warp_wait(bar(kDtReady + (i & 1)), par(i), s_abort) && warp_wait(bar(kFullX + (i & 1)), par(i), s_abort);
+        if (ok) {
+          const float w = ex2(D0[TQ - 1] - D0[row]) * D0[TQ + row];
+          const unsigned char* xt = smem + (uint32_t)(i & 1) * kStage + kTileC + kTileB;
+#pragma unroll
+          for (int q = 0; q < 2; ++q) {
+            const uint32_t o = tile_off(row, 16 * cg + 8 * q, TQ);
+            const uint4 xv = *reinterpret_cast<const uint4*>(xt + o);
+            const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
+            uint32_t hi[4], lo[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              split2(__uint_as_float(xw[e] << 16) * w, __uint_as_float(xw[e] & 0xffff0000u) * w, hi[e], lo[e]);
+            *reinterpret_cast<uint4*>(smem + kOffXWhi + o) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+            *reinterpret_cast<uint4*>(smem + kOffXWlo + o) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+          }
+        }
+        fence_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(kXWReady + (i & 1)));
+
+        // (c) M(i) = CB o exp(s_t - s_j) dt'_j (j <= t), + D on the diagonal, written
+        // over CB(i) as bf16 hi (columns [0,64)) and lo ([64,128)) packed pairs. This
+        // thread takes columns 32 bb + 8 cg .. +7 of each 32-column block bb: above
+        // the diagonal all zero; below it exp(s_t - s_j) = exp(s_t - s_e) exp(s_e - s_j)
+        // with e the block's last token (the second factor times dt'_j being v_j);
+        // the diagonal block exponentiates each pair.
+        ok = warp_wait(bar(kCBDone + (i & 1)), par(i), s_abort);
+        const uint32_t cbt = tmem + lane_off + kColCB + 128u * (uint32_t)(i & 1);
+        float cbv[4][8];
+        if (ok) {
+          tc_fence_after();
+#pragma unroll
+          for (int bb = 0; bb < 4; ++bb) {
+            if (bb <= qrt) {
+              uint32_t r[8];
+              asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                           : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+                             "=r"(r[7])
+                           : "r"(cbt + 32 * bb + 8 * cg));
+#pragma unroll
+              for (int e = 0; e < 8; ++e) cbv[bb][e] = __uint_as_float(r[e]);
+            }
+          }
+          asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+        }
+        bar_sync(3 + qrt, 128);  // this lane quarter's four warps have read CB(i)
+        if (ok) {
+          const float St = D0[row];
+#pragma unroll
+          for (int bb = 0; bb < 4; ++bb) {
+            uint32_t hi[4], lo[4];
+            const int j0 = 32 * bb + 8 * cg;
+            if (bb > qrt) {
+#pragma unroll
+              for (int e = 0; e < 4; ++e) hi[e] = lo[e] = 0u;
+            } else if (bb < qrt) {
+              const float u = ex2(St - D0[32 * bb + 31]);
+              float v[8];
+              *reinterpret_cast<float4*>(v) = *reinterpret_cast<const float4*>(D0 + 2 * TQ + j0);
+              *reinterpret_cast<float4*>(v + 4) = *reinterpret_cast<const float4*>(D0 + 2 * TQ + j0 + 4);
+#pragma unroll
+              for (int e = 0; e < 4; ++e)
+                split2(cbv[bb][2 * e] * (u * v[2 * e]), cbv[bb][2 * e + 1] * (u * v[2 * e + 1]), hi[e], lo[e]);
+            } else {
+              float sj[8], dj[8];
+              *reinterpret_cast<float4*>(sj) = *reinterpret_cast<const float4*>(D0 + j0);
+              *reinterpret_cast<float4*>(sj + 4) = *reinterpret_cast<const float4*>(D0 + j0 + 4);
+              *reinterpret_cast<float4*>(dj) = *reinterpret_cast<const float4*>(D0 + TQ + j0);
+              *reinterpret_cast<float4*>(dj + 4) = *reinterpret_cast<const float4*>(D0 + TQ + j0 + 4);
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const int ja = j0 + 2 * e, jb = ja + 1;
+                float ma = ja <= row ? cbv[bb][2 * e] * ex2(St - sj[2 * e]) * dj[2 * e] : 0.f;
+                float mb = jb <= row ? cbv[bb][2 * e + 1] * ex2(St - sj[2 * e + 1]) * dj[2 * e + 1] : 0.f;
+                if (ja == row) ma += ci.Dh;
+                if (jb == row) mb += ci.Dh;
+                split2(ma, mb, hi[e], lo[e]);
+              }
+            }
+            const uint32_t pc = (uint32_t)(j0 >> 1);  // packed bf16-pair column
+            asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1,%2,%3,%4};"
+                         :: "r"(cbt + pc), "r"(hi[0]), "r"(hi[1]), "r"(hi[2]), "r"(hi[3]) : "memory");
+            asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1,%2,%3,%4};"
+                         :: "r"(cbt + 64 + pc), "r"(lo[0]), "r"(lo[1]), "r"(lo[2]), "r"(lo[3]) : "memory");
+          }
+          asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(kMReady + (i & 1)));
       }
-      tc_fence_before();
-      __syncthreads();
-      {
-        __nv_bfloat16* yout = static_cast<__nv_bfloat16*>(a.dst);
-        for (int i = tid; i < TQ * (TP / 8); i += kTcThreads) {
-          const int t = i >> 3, pc = i & 7;
-          if (t < len) {
-            const uint4 v = *reinterpret_cast<const uint4*>(stage_p + tile_off(t, pc * 8, TQ));
-            *reinterpret_cast<uint4*>(yout + (row0 + (int64_t)c * TQ + t) * (int64_t)(H * TP) + x_col + pc * 8) = v;
+      if (i > 0) {
+        // (d) output of chunk j = i-1: y = M . X + exp(s_t) C . H^T, straight to HBM
+        const int j = i - 1;
+        bool ok = warp_wait(bar(kYdDone + (j & 1)), par(j), s_abort);
+        if (i == n) ok = ok && warp_wait(bar(kYoDone + (j & 1)), par(j), s_abort);
+        if (ok) {
+          tc_fence_after();
+          float yd[16], yo[16];
+          tmem_ld16x2(tmem + lane_off + kColYd + 16 * cg, tmem + lane_off + kColYo + 64u * (uint32_t)(j & 1) + 16 * cg,
+                      yd, yo);
+          const float et = ex2(dtbuf(j)[row]);
+          const int c = ci.c_begin + j;
+          if (row < min(TQ, ci.T - c * TQ)) {
+            uint32_t o[8];
+#pragma unroll
+            for (int f = 0; f < 8; ++f) o[f] = pack2(fmaf(et, yo[2 * f], yd[2 * f]), fmaf(et, yo[2 * f + 1], yd[2 * f + 1]));
+            // one full 32-byte sector per thread (y rows and the 16-column groups are 32-byte aligned)
+            __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(a.dst) + (ci.row0 + (int64_t)c * TQ + row) * (int64_t)(H * TP) +
+                                 ci.x_col + 16 * cg;
+            asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(dst), "r"(o[0]), "r"(o[1]), "r"(o[2]),
+                         "r"(o[3]), "r"(o[4]), "r"(o[5]), "r"(o[6]), "r"(o[7])
+                         : "memory");
           }
         }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(kEpiDone + (j & 3)));
       }
     }
-    __syncthreads();  // this stage's tiles are spent
-    if (c + 2 < c_end) issue_chunk(c + 2, st);
+    // ---- state after the last chunk
+    if (live) {
+      bool ok = true;
+      if (n > 0) {
+        ok = warp_wait(bar(kDHDone + ((n - 1) & 1)), par(n - 1), s_abort);
+        if (ok) {
+          tc_fence_after();
+          state_update(n - 1);
+        }
+      }
+      if (ok && ci.k == ci.nseg - 1) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) slot_ptr[(int64_t)(16 * cg + i) * TN + row] = hst[i];
+      }
+    }
+  } else if (warp == 16) {
+    // =================== per chunk i: dt' = softplus(dt + dt_bias), log2-scaled
+    // cumulative decay S and block factors v into dt buffer i % 4 (lane l: tokens
+    // 4l .. 4l+3; the buffer last served chunk i-4, whose readers are done once
+    // chunk i-3's output is written); then CB = C . B^T (lane 0)
+    unsigned short raw[4] = {0, 0, 0, 0};  // raw bf16 bits: the loads stay in flight until used
+    auto load_raw = [&](int i) {
+      const int c = ci.c_begin + i, len = min(TQ, ci.T - c * TQ);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int t = 4 * lane + e;
+        raw[e] = t < len ? reinterpret_cast<const unsigned short*>(a.dt)[(ci.row0 + (int64_t)c * TQ + t) * H + ci.h]
+                         : (unsigned short)0;
+      }
+    };
+    if (n > 0) load_raw(0);
+    int last = -1;
+    for (int i = 0; i < n; ++i) {
+      if (i >= 3 && !warp_wait(bar(kEpiDone + ((i - 3) & 3)), (uint32_t)(((i - 3) >> 2) & 1), s_abort)) break;
+      {
+        const int c = ci.c_begin + i, len = min(TQ, ci.T - c * TQ);
+        float dp[4], S[4], run = 0.f;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          dp[e] = dt_prime(raw[e], 4 * lane + e < len, ci.dtb);
+          run -= ci.A2 * dp[e];
+          S[e] = run;
+        }
+        if (i + 1 < n) load_raw(i + 1);
+        const float excl = warp_incl_sum(run, lane) - run;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) S[e] += excl;
+        const float Se = __shfl_sync(0xffffffffu, S[3], (lane & ~7) | 7);  // S at the end of this 32-block
+        float* D0 = reinterpret_cast<float*>(smem + kOffDt + (uint32_t)(i % kDtRing) * kDtBuf);
+        *reinterpret_cast<float4*>(D0 + 4 * lane) = make_float4(S[0], S[1], S[2], S[3]);
+        *reinterpret_cast<float4*>(D0 + TQ + 4 * lane) = make_float4(dp[0], dp[1], dp[2], dp[3]);
+        *reinterpret_cast<float4*>(D0 + 2 * TQ + 4 * lane) =
+            make_float4(ex2(Se - S[0]) * dp[0], ex2(Se - S[1]) * dp[1], ex2(Se - S[2]) * dp[2], ex2(Se - S[3]) * dp[3]);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(kDtReady + (i & 1)));
+      }
+      if (!warp_wait(bar(kFullCB + (i & 1)), par(i), s_abort)) break;
+      if (i >= 2 && !warp_wait(bar(kYdDone + (i & 1)), par(i - 2), s_abort)) break;  // M(i-2) consumed
+      tc_fence_after();
+      if (lane == 0) {
+        const uint64_t a0 = sdesc(stage(i), 16, 1024), b0 = sdesc(stage(i) + kTileC, 16, 1024);
+#pragma unroll
+        for (int s2 = 0; s2 < TN / 16; ++s2) {
+          const uint32_t ko = ((s2 >> 2) * TQ * 128 + (s2 & 3) * 32) >> 4;
+          mma_ss(tmem + kColCB + 128u * (uint32_t)(i & 1), a0 + ko, b0 + ko, idesc128(128, 0, 0), s2 > 0);
+        }
+        mma_commit(bar(kCBDone + (i & 1)));
+      }
+      __syncwarp();
+      last = i;
+    }
+    if (lane == 0 && last >= 0) drain_bar(bar(kCBDone + (last & 1)), par(last));
+  } else if (warp == 17) {
+    // =================== Yoff = C . H^T
+    if (lane == 0) {
+      int last = -1;
+      for (int i = 0; i < n; ++i) {
+        if (!wait_bar(bar(kFullCB + (i & 1)), par(i), s_abort)) break;
+        if (!wait_bar(bar(kHDone + (i & 1)), par(i), s_abort)) break;  // H^T through chunk i-1 written
+        if (i >= 2 && !wait_bar(bar(kEpiDone + ((i - 2) & 3)), (uint32_t)(((i - 2) >> 2) & 1), s_abort)) break;  // Yoff buffer read
+        tc_fence_after();
+        const uint64_t a0 = sdesc(stage(i), 16, 1024), h0 = sdesc(sbase + kOffHT, TN * 128, 1024);
+#pragma unroll
+        for (int s2 = 0; s2 < TN / 16; ++s2) {
+          const uint32_t ko = ((s2 >> 2) * TQ * 128 + (s2 & 3) * 32) >> 4;
+          mma_ss(tmem + kColYo + 64u * (uint32_t)(i & 1), a0 + ko, h0 + ((s2 * 2048) >> 4), idesc128(64, 0, 1), s2 > 0);
+        }
+        mma_commit(bar(kYoDone + (i & 1)));
+        last = i;
+      }
+      if (last >= 0) drain_bar(bar(kYoDone + (last & 1)), par(last));
+    }
+  } else if (warp == 18) {
+    // =================== dH^T = B^T . (X o w); C and B tile loads
+    auto load_cb = [&](int i) {
+      const ChunkSrc s = chunk_src(i);
+      load_tile(stage(i), s, &tm, use_tma != 0, ci.c_col, TN, bar(kFullCB + (i & 1)), lane);
+      load_tile(stage(i) + kTileC, s, &tm, use_tma != 0, ci.b_col, TN, bar(kFullCB + (i & 1)), lane);
+    };
+    int loaded = min(n, 2), last = -1;
+    for (int i = 0; i < loaded; ++i) load_cb(i);
+    for (int i = 0; i < n; ++i) {
+      const bool ok = warp_wait(bar(kFullCB + (i & 1)), par(i), s_abort) &&
+                      warp_wait(bar(kHDone + (i & 1)), par(i), s_abort) &&  // dH accumulator read
+                      warp_wait(bar(kXWReady + (i & 1)), par(i), s_abort);
+      if (!ok) break;
+      tc_fence_after();
+      if (lane == 0) {
+        const uint64_t bt0 = sdesc(stage(i) + kTileC, TQ * 128, 1024);
+        const uint64_t hi0 = sdesc(sbase + kOffXWhi, TQ * 128, 1024), lo0 = sdesc(sbase + kOffXWlo, TQ * 128, 1024);
+#pragma unroll
+        for (int s2 = 0; s2 < TQ / 16; ++s2) {
+          const uint32_t jk = (s2 * 2048) >> 4;  // 16 rows of the [j][*] tiles
+          mma_ss(tmem + kColDH, bt0 + jk, hi0 + jk, idesc128(64, 1, 1), s2 > 0);
+          mma_ss(tmem + kColDH, bt0 + jk, lo0 + jk, idesc128(64, 1, 1), 1);
+        }
+        mma_commit(bar(kDHDone + (i & 1)));
+      }
+      __syncwarp();
+      last = i;
+      if (i + 2 < n) {
+        // chunk i's C and B tiles are spent once its three products are done
+        if (!(warp_wait(bar(kDHDone + (i & 1)), par(i), s_abort) && warp_wait(bar(kCBDone + (i & 1)), par(i), s_abort) &&
+              warp_wait(bar(kYoDone + (i & 1)), par(i), s_abort)))
+          break;
+        load_cb(i + 2);
+        loaded = i + 3;
+      }
+    }
+    if (lane == 0 && last >= 0) drain_bar(bar(kDHDone + (last & 1)), par(last));
+    if (lane == 0 && *s_abort)
+      for (int i = max(0, loaded - 2); i < loaded; ++i) drain_bar(bar(kFullCB + (i & 1)), par(i));
+  } else if (warp == kMathWarps + 3) {
+    // =================== Y = M . X (A = M hi, lo from TMEM); X tile loads
+    auto load_x = [&](int i) {
+      load_tile(stage(i) + kTileC + kTileB, chunk_src(i), &tm, use_tma != 0, ci.x_col, TP, bar(kFullX + (i & 1)), lane);
+    };
+    int loaded = min(n, 2), last = -1;
+    for (int i = 0; i < loaded; ++i) load_x(i);
+    for (int i = 0; i < n; ++i) {
+      bool ok = warp_wait(bar(kMReady + (i & 1)), par(i), s_abort);
+      if (ok && i >= 1) ok = warp_wait(bar(kEpiDone + ((i - 1) & 3)), (uint32_t)(((i - 1) >> 2) & 1), s_abort);  // Y accumulator read
+      if (ok) ok = warp_wait(bar(kFullX + (i & 1)), par(i), s_abort);
+      if (!ok) break;
+      tc_fence_after();
+      if (lane == 0) {
+        const uint64_t x0 = sdesc(stage(i) + kTileC + kTileB, TQ * 128, 1024);
+        const uint32_t m = tmem + kColCB + 128u * (uint32_t)(i & 1);
+#pragma unroll
+        for (int s2 = 0; s2 < TQ / 16; ++s2) {
+          const uint64_t xd = x0 + ((s2 * 2048) >> 4);
+          mma_ts(tmem + kColYd, m + 8 * s2, xd, idesc128(64, 0, 1), s2 > 0);
+          mma_ts(tmem + kColYd, m + 64 + 8 * s2, xd, idesc128(64, 0, 1), 1);
+        }
+        mma_commit(bar(kYdDone + (i & 1)));
+      }
+      __syncwarp();
+      last = i;
+      if (i + 2 < n) {
+        if (!warp_wait(bar(kYdDone + (i & 1)), par(i), s_abort)) break;  // chunk i's X tile spent
+        load_x(i + 2);
+        loaded = i + 3;
+      }
+    }
+    if (lane == 0 && last >= 0) drain_bar(bar(kYdDone + (last & 1)), par(last));
+    if (lane == 0 && *s_abort)
+      for (int i = max(0, loaded - 2); i < loaded; ++i) drain_bar(bar(kFullX + (i & 1)), par(i));
   }
 
-  // ---- results
-  if (ok_run) {
-    if (kFull) {
-      if (k == nseg - 1) store_state(slot_ptr);
-    } else {
-      store_state(ws_entry(seg));
-      if (tid == 0) a.ws_decay[(int64_t)seg * H + h] = seg_logdecay;
-    }
-  }
-  asm volatile("cp.async.wait_group 0;\n" ::: "memory");
+  // ---- teardown: every role has drained what it issued
   tc_fence_before();
   __syncthreads();
-  if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" :: "r"(tmem), "r"(kTmemCols));
+  if (tid == 0 && *s_abort) atomicAdd(&g_tc_timeouts, 1u);
+  if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;" :: "r"(tmem));
+}
+
+// State pass: end state (from zero; the first segment from the slot's state)
+// and total log-decay of every segment but the last. Chunks are read last to
+// first; with R the log2 decay of the chunks already read, token j's weight is
+// w_j = 2^(R + S_end - S_j) dt'_j (S the chunk's cumulative log2 decay), so
+// B^T . (X o w) of every chunk accumulates into the same TMEM columns.
+//   warps 0-15  dt' and weights (warps 0, 4, 8, 12), X o w (bf16 hi + lo)
+//   warp 16     B and X tile loads (three stages)
+//   warp 17/18  dH^T += B^T . (X o w) hi / lo, each into its own accumulator
+__global__ void __launch_bounds__(kStateThreads, 1)
+ssd_tc_state(const __grid_constant__ ScanArgs a, const __grid_constant__ CUtensorMap tm, const int use_tma) {
+  const Cta ci = cta_info(a);
+  if (ci.k == ci.nseg - 1) return;  // the last segment has no entry (the full pass ends it)
+  extern __shared__ unsigned char smem_raw[];
+  const uint32_t raw_base = su32(smem_raw);
+  unsigned char* smem = smem_raw + (((raw_base + 1023u) & ~1023u) - raw_base);
+  const uint32_t sbase = su32(smem);
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + kStOffMisc);
+  volatile uint32_t* s_abort = reinterpret_cast<volatile uint32_t*>(smem + kStOffMisc + 4);
+  auto bar = [&](int id) { return sbase + kStOffBar + 8u * (uint32_t)id; };
+  auto stg = [&](int i) { return sbase + (uint32_t)(i % kStStages) * kStStage; };
+  auto p3 = [](int i) { return (uint32_t)((i / kStStages) & 1); };  // phase parity on a [3] barrier
+  auto p2 = [](int i) { return (uint32_t)((i >> 1) & 1); };         // phase parity on a [2] barrier
+
+  const int n = ci.n;  // >= 1 for every segment but the last
+  const int H = a.heads;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 128;" :: "r"(su32(s_tmem)));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+  }
+  if (tid == kMathThreads) {
+    for (int s = 0; s < kStStages; ++s) {
+      mbar_init(bar(kStFull + s), 2);    // B tile, X tile
+      mbar_init(bar(kStDHDone + s), 2);  // hi and lo issuers
+    }
+    for (int b = 0; b < 2; ++b) mbar_init(bar(kStXWReady + b), kMathWarps);
+    *s_abort = 0u;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *s_tmem;
+
+  // local chunk i is chunk c_end - 1 - i
+  auto chunk_src = [&](int i) {
+    ChunkSrc s;
+    const int c = ci.c_end - 1 - i;
+    s.xbc = static_cast<const __nv_bfloat16*>(a.xbc);
+    s.ld = a.conv_dim;
+    s.rb = ci.row0 + (int64_t)c * TQ;
+    s.len = min(TQ, ci.T - c * TQ);
+    return s;
+  };
+
+  if (warp < kMathWarps) {
+    const int row = tid & 127, cg = tid >> 7, qrt = warp & 3;
+    const uint32_t lane_off = (uint32_t)(qrt * 32) << 16;
+    const bool dt_warp = qrt == 0;
+    const int dblk = warp >> 2;
+    float* s_w = reinterpret_cast<float*>(smem + kStOffW);
+    float* s_btot = reinterpret_cast<float*>(smem + kStOffBtot);
+    float* s_R = reinterpret_cast<float*>(smem + kStOffR);
+    const int64_t head_off = (int64_t)ci.h * TP * TN;
+    auto ws_entry = [&](int segidx) -> float* { return a.ws_state + (int64_t)segidx * H * TP * TN + head_off; };
+
+    // the first segment starts from the slot's state: keep it, and leave a copy
+    // for the full pass (whose last segment overwrites the slot)
+    float h0[16];
+    const bool seeded = ci.k == 0 && !ci.fresh;
+    if (seeded) {
+      const float* slot_ptr = a.ssm_state + (int64_t)seq_slot(a.tab, ci.sq) * H * TP * TN + head_off;
+      float* copy = ws_entry(ci.seg0 + ci.nseg - 1);
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        h0[i] = slot_ptr[(int64_t)(16 * cg + i) * TN + row];
+        copy[(int64_t)(16 * cg + i) * TN + row] = h0[i];
+      }
+    }
+
+    unsigned short dt_raw = 0;
+    float R = 0.f;  // log2 decay from the end of the chunks already read to the segment end
+    auto load_dt = [&](int i) {
+      const int c = ci.c_end - 1 - i, t = 32 * dblk + lane;
+      dt_raw = t < min(TQ, ci.T - c * TQ)
+                   ? reinterpret_cast<const unsigned short*>(a.dt)[(ci.row0 + (int64_t)c * TQ + t) * H + ci.h]
+                   : (unsigned short)0;
+    };
+    auto dt_phase = [&](int i) {
+      const int c = ci.c_end - 1 - i, t = 32 * dblk + lane;
+      const float dp = dt_prime(dt_raw, t < min(TQ, ci.T - c * TQ), ci.dtb);
+      const float incl = warp_incl_sum(-ci.A2 * dp, lane);
+      float* bt = s_btot + (i & 1) * 4;
+      if (lane == 31) bt[dblk] = incl;
+      bar_sync(1, 128);  // the four dt warps
+      float pre = 0.f;
+      for (int k2 = 0; k2 < dblk; ++k2) pre += bt[k2];
+      const float tot = (bt[0] + bt[1]) + (bt[2] + bt[3]);
+      s_w[(i & 1) * TQ + t] = ex2(R + (tot - (pre + incl))) * dp;
+      R += tot;
+      if (i == n - 1 && warp == 0 && lane == 0) *s_R = R;
+    };
+
+    bool live = true;
+    if (dt_warp) {
+      load_dt(0);
+      dt_phase(0);
+      if (n > 1) load_dt(1);
+    }
+    for (int i = 0; i < n; ++i) {
+      if (bar_or(2, kMathThreads, *s_abort != 0u)) {
+        live = false;
+        break;
+      }
+      bool ok = warp_wait(bar(kStFull + i % kStStages), p3(i), s_abort);
+      if (ok && i >= 2) ok = warp_wait(bar(kStDHDone + (i - 2) % kStStages), p3(i - 2), s_abort);  // X o w buffer read
+      if (ok) {
+        const float w = s_w[(i & 1) * TQ + row];
+        const unsigned char* xt = smem + (uint32_t)(i % kStStages) * kStStage + kTileB;
+        unsigned char* xw = smem + kStOffXW + (uint32_t)(i & 1) * 2 * kTileX;
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+          const uint32_t o = tile_off(row, 16 * cg + 8 * q, TQ);
+          const uint4 xv = *reinterpret_cast<const uint4*>(xt + o);
+          const uint32_t xr[4] = {xv.x, xv.y, xv.z, xv.w};
+          uint32_t hi[4], lo[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            split2(__uint_as_float(xr[e] << 16) * w, __uint_as_float(xr[e] & 0xffff0000u) * w, hi[e], lo[e]);
+          *reinterpret_cast<uint4*>(xw + o) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+          *reinterpret_cast<uint4*>(xw + kTileX + o) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+        }
+      }
+      fence_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(kStXWReady + (i & 1)));
+      if (dt_warp && i + 1 < n) {
+        dt_phase(i + 1);
+        if (i + 2 < n) load_dt(i + 2);
+      }
+    }
+    if (live && warp_wait(bar(kStDHDone + (n - 1) % kStStages), p3(n - 1), s_abort)) {
+      tc_fence_after();
+      float dhi[16], dlo[16];
+      tmem_ld16x2(tmem + lane_off + 16 * cg, tmem + lane_off + 64 + 16 * cg, dhi, dlo);
+      const float Rt = *s_R;  // written before this loop's last barrier
+      const float d = ex2(Rt);
+      float* dst = ws_entry(blockIdx.x);
+#pragma unroll
+      for (int i = 0; i < 16; ++i)
+        dst[(int64_t)(16 * cg + i) * TN + row] = seeded ? fmaf(d, h0[i], dhi[i] + dlo[i]) : dhi[i] + dlo[i];
+      if (tid == 0) a.ws_decay[(int64_t)blockIdx.x * H + ci.h] = Rt * 0.6931471805599453f;
+    }
+  } else if (warp == kMathWarps) {
+    // =================== B and X tile loads
+    int loaded = 0;
+    for (int i = 0; i < n; ++i) {
+      if (i >= kStStages && !warp_wait(bar(kStDHDone + i % kStStages), p3(i - kStStages), s_abort)) break;
+      const ChunkSrc s = chunk_src(i);
+      load_tile(stg(i), s, &tm, use_tma != 0, ci.b_col, TN, bar(kStFull + i % kStStages), lane);
+      load_tile(stg(i) + kTileB, s, &tm, use_tma != 0, ci.x_col, TP, bar(kStFull + i % kStStages), lane);
+      loaded = i + 1;
+    }
+    if (lane == 0 && *s_abort)
+      for (int i = max(0, loaded - kStStages); i < loaded; ++i) drain_bar(bar(kStFull + i % kStStages), p3(i));
+  } else {
+    // =================== dH^T += B^T . (X o w) hi (warp 17) / lo (warp 18)
+    if (lane == 0) {
+      const uint32_t part = warp == kMathWarps + 1 ? 0u : 1u;
+      int last = -1;
+      for (int i = 0; i < n; ++i) {
+        if (!wait_bar(bar(kStFull + i % kStStages), p3(i), s_abort)) break;
+        if (!wait_bar(bar(kStXWReady + (i & 1)), p2(i), s_abort)) break;
+        tc_fence_after();
+        const uint64_t bt0 = sdesc(stg(i), TQ * 128, 1024);
+        const uint64_t xw0 = sdesc(sbase + kStOffXW + (uint32_t)(i & 1) * 2 * kTileX + part * kTileX, TQ * 128, 1024);
+#pragma unroll
+        for (int s2 = 0; s2 < TQ / 16; ++s2) {
+          const uint32_t jk = (s2 * 2048) >> 4;
+          mma_ss(tmem + 64u * part, bt0 + jk, xw0 + jk, idesc128(64, 1, 1), (i > 0 || s2 > 0) ? 1u : 0u);
+        }
+        mma_commit(bar(kStDHDone + i % kStStages));
+        last = i;
+      }
+      if (last >= 0) drain_bar(bar(kStDHDone + last % kStStages), p3(last));
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (tid == 0 && *s_abort) atomicAdd(&g_tc_timeouts, 1u);
+  if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 128;" :: "r"(tmem));
+}
+
+// Tensor map over xbc [rows][conv_dim] bf16: boxes of 64 columns x TQ rows,
+// 128-byte swizzle. False when TMA cannot address it (base not 16-byte
+// aligned, row stride not a multiple of 16 bytes, or no driver entry point):
+// the kernels then load every tile with cp.async.
+bool make_xbc_map(CUtensorMap* tm, const ScanArgs& a) {
+  using Encode = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                              const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                              CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+  static Encode encode = []() -> Encode {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return nullptr;
+    return reinterpret_cast<Encode>(fn);
+  }();
+  const uint64_t rows = (uint64_t)a.tab.cu[a.tab.n];
+  if (!encode || rows == 0 || (reinterpret_cast<uintptr_t>(a.xbc) & 15u) != 0 || (a.conv_dim * 2) % 16 != 0) return false;
+  const cuuint64_t dims[2] = {(cuuint64_t)a.conv_dim, rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)a.conv_dim * 2};
+  const cuuint32_t box[2] = {64, TQ};
+  const cuuint32_t estr[2] = {1, 1};
+  return encode(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(a.xbc), dims, strides, box, estr,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 }  // namespace
@@ -639,21 +1002,22 @@ unsigned int read_device_timeouts() {
 cudaError_t launch_scan_tc(const ScanArgs& a, cudaStream_t st) {
   const int segs = a.tab.tile[a.tab.n];
   if (segs == 0) return cudaSuccess;
+  CUtensorMap tm;
+  memset(&tm, 0, sizeof tm);
+  const int use_tma = make_xbc_map(&tm, a) ? 1 : 0;
   const dim3 grid((unsigned)segs, (unsigned)a.heads);
   bool segmented = false;
   for (int i = 0; i < a.tab.n; ++i) segmented |= (a.tab.tile[i + 1] - a.tab.tile[i]) > 1;
   if (segmented) {
-    cudaError_t e = cudaFuncSetAttribute(ssd_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)kSmemBytes);
+    cudaError_t e = cudaFuncSetAttribute(ssd_tc_state, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kStateSmem);
     if (e != cudaSuccess) return e;
-    ssd_tc_kernel<false><<<grid, kTcThreads, kSmemBytes, st>>>(a);
+    ssd_tc_state<<<grid, kStateThreads, kStateSmem, st>>>(a, tm, use_tma);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
-  cudaError_t e = cudaFuncSetAttribute(ssd_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)kSmemBytes);
+  cudaError_t e = cudaFuncSetAttribute(ssd_tc_full, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kFullSmem);
   if (e != cudaSuccess) return e;
-  ssd_tc_kernel<true><<<grid, kTcThreads, kSmemBytes, st>>>(a);
+  ssd_tc_full<<<grid, kFullThreads, kFullSmem, st>>>(a, tm, use_tma);
   return cudaGetLastError();
 }
 
