@@ -19,17 +19,19 @@
 // Full pass: one CTA per (sequence segment, head), 20 warps in fixed roles
 // that hand work to each other through mbarriers (no CTA-wide barrier in the
 // chunk loop):
-//   warps 0-15  element-wise work; TMEM lane t = token row t (or state row n).
-//               Per chunk i: state through chunk i-1 (H = exp(total) H + dH,
-//               fp32 in registers, bf16 copy of H^T to smem); X o w for chunk i
-//               (bf16 hi + lo); M(i) = CB o decay (+ D on the diagonal), bf16
-//               hi + lo written over CB in TMEM; output of chunk i-1,
-//               y = Y + exp(s_t) Yoff, stored straight from registers.
+//   warps 0-7   M(i) = CB o decay (+ D on the diagonal), bf16 hi + lo written
+//               over CB in TMEM (TMEM lane t = token row t)
+//   warps 8-15  per chunk i: X o w (bf16 hi + lo); the state through chunk
+//               i-1 (H = exp(total) H + dH, fp32 in registers, bf16 copy of
+//               H^T to smem; TMEM lane n = state row n); the output of chunk
+//               i-1, y = Y + exp(s_t) Yoff, stored from registers
+//               (two warps per TMEM lane quarter in each group, so M and the
+//               state / output work run side by side on every sub-partition)
 //   warp 16     CB = C . B^T                M=128 N=128 K=128; before it, the
 //               chunk's dt' = softplus(dt + dt_bias), cumulative log-decay and
 //               block factors (up to four chunks ahead of the element-wise warps)
 //   warp 17     Yoff = C . H^T              M=128 N=64  K=128 (H^T MN-major)
-//   warp 18     dH^T = B^T . (X o w)        M=128 N=64  K=128 (hi and lo);
+//   warp 18     dH^T = B^T . [X o w hi | lo]  M=128 N=128 K=128;
 //               also loads the C and B tiles of chunk i+2
 //   warp 19     Y = M . X (A from TMEM)     M=128 N=64  K=128 (hi and lo);
 //               also loads the X tile of chunk i+2
@@ -75,8 +77,8 @@ constexpr uint32_t kSuspendNs = 1000;      // a waiting thread sleeps up to this
 
 // ---- full pass: TMEM columns (128 lanes each)
 constexpr uint32_t kColCB = 0;     // [0,256): CB of chunk parity b at 128 b; M hi | M lo replace it
-constexpr uint32_t kColYo = 256;   // [256,384): C . H^T of chunk parity b at 256 + 64 b
-constexpr uint32_t kColDH = 384;   // [384,448): B^T . (X o w), lane = n
+constexpr uint32_t kColYo = 256;   // [256,320): C . H^T
+constexpr uint32_t kColDH = 320;   // [320,448): B^T . (X o w) hi | lo, lane = n
 constexpr uint32_t kColYd = 448;   // [448,512): M . X
 
 // ---- full pass: shared memory (operand tiles 1024-byte aligned)
@@ -162,11 +164,13 @@ __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
                : "=r"(done) : "r"(bar), "r"(parity), "r"(kSuspendNs) : "memory");
   return done != 0;
 }
+// (The waits are out of line: one copy of the polling loop instead of one per
+// call site keeps the kernels' hot code small in the instruction cache.)
 // Bounded wait for the completion of the barrier phase with this parity; after
 // a few rounds the thread sleeps between polls, so waiting warps leave the
 // issue slots to the working ones. Gives up when the CTA's abort flag is
 // raised, and raises it itself on a timeout.
-__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile uint32_t* abort_flag) {
+__device__ __noinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile uint32_t* abort_flag) {
   for (uint32_t it = 0; it < kWaitLimit; ++it) {
     if (mbar_test(bar, parity)) return true;
     if (*abort_flag) return false;
@@ -177,7 +181,7 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile
 }
 // The same, decided for the whole warp (every lane waits; all get the same
 // answer), for warps whose lanes then run .sync.aligned or __syncwarp code.
-__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile uint32_t* abort_flag) {
+__device__ __noinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile uint32_t* abort_flag) {
   return __all_sync(0xffffffffu, wait_bar(bar, parity, abort_flag));
 }
 // Bounded wait that ignores the abort flag (draining work already issued).
@@ -369,12 +373,12 @@ ssd_tc_full(const __grid_constant__ ScanArgs a, const __grid_constant__ CUtensor
       mbar_init(bar(kYoDone + b), 1);
       mbar_init(bar(kDHDone + b), 1);
       mbar_init(bar(kYdDone + b), 1);
-      mbar_init(bar(kHDone + b), kMathWarps);
-      mbar_init(bar(kXWReady + b), kMathWarps);
-      mbar_init(bar(kMReady + b), kMathWarps);
+      mbar_init(bar(kHDone + b), kMathWarps / 2);
+      mbar_init(bar(kXWReady + b), kMathWarps / 2);
+      mbar_init(bar(kMReady + b), kMathWarps / 2);
       mbar_init(bar(kDtReady + b), 1);
     }
-    for (int b = 0; b < 4; ++b) mbar_init(bar(kEpiDone + b), kMathWarps);
+    for (int b = 0; b < 4; ++b) mbar_init(bar(kEpiDone + b), kMathWarps / 2);
     *s_abort = 0u;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -394,169 +398,76 @@ ssd_tc_full(const __grid_constant__ ScanArgs a, const __grid_constant__ CUtensor
   };
 
   if (warp < kMathWarps) {
-    // =================== element-wise warps
-    const int row = tid & 127;  // TMEM lane = tile row this thread works on
-    const int cg = tid >> 7;    // column group 0..3
-    const int qrt = warp & 3;   // TMEM lane quarter = 32-row block of `row`
+    // =================== element-wise warps: two groups of eight, two warps per
+    // TMEM lane quarter each, so that M and the state / output work of a chunk
+    // run side by side on every SM sub-partition
+    const int qrt = warp & 3;   // TMEM lane quarter = 32-row block
+    const int row = qrt * 32 + lane;
+    const int half = (warp >> 2) & 1;  // which 16 columns of each 32-block (M) / which 32 columns (state, y)
     const uint32_t lane_off = (uint32_t)(qrt * 32) << 16;
     auto dtbuf = [&](int i) { return reinterpret_cast<float*>(smem + kOffDt + (uint32_t)(i % kDtRing) * kDtBuf); };
 
-    // running state: this thread holds H^T[n = row][p], p in [16 cg, 16 cg + 16)
-    const int64_t head_off = (int64_t)ci.h * TP * TN;
-    float* slot_ptr = a.ssm_state + (int64_t)seq_slot(a.tab, ci.sq) * H * TP * TN + head_off;
-    auto ws_entry = [&](int segidx) -> float* { return a.ws_state + (int64_t)segidx * H * TP * TN + head_off; };
-    float hst[16];
-    auto load_state = [&](const float* src) {
-#pragma unroll
-      for (int i = 0; i < 16; ++i) hst[i] = src ? src[(int64_t)(16 * cg + i) * TN + row] : 0.0f;
-    };
-    if (ci.k == 0) {
-      // the first segment starts from the slot (from the state pass's copy when the
-      // last segment will overwrite the slot in this same launch)
-      load_state(ci.fresh ? nullptr : (ci.nseg > 1 ? ws_entry(ci.seg0 + ci.nseg - 1) : slot_ptr));
-    } else {
-      load_state(ws_entry(ci.seg0));
-      for (int j = 1; j < ci.k; ++j) {
-        const float d = __expf(a.ws_decay[(int64_t)(ci.seg0 + j) * H + ci.h]);
-        const float* e = ws_entry(ci.seg0 + j);
-        float ev[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) ev[i] = e[(int64_t)(16 * cg + i) * TN + row];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) hst[i] = fmaf(d, hst[i], ev[i]);
-      }
-    }
-
-    // bf16 H^T (B operand of C . H^T): row n, columns [16 cg, +16)
-    auto write_ht = [&]() {
-#pragma unroll
-      for (int q = 0; q < 2; ++q) {
-        uint32_t hw[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) hw[e] = pack2(hst[8 * q + 2 * e], hst[8 * q + 2 * e + 1]);
-        *reinterpret_cast<uint4*>(smem + kOffHT + tile_off(row, 16 * cg + 8 * q, TN)) =
-            make_uint4(hw[0], hw[1], hw[2], hw[3]);
-      }
-    };
-    auto state_update = [&](int j) {  // H = exp(total_j) H + dH(j)
-      float dv[16];
-      tmem_ld16(tmem + lane_off + kColDH + 16 * cg, dv);
-      const float decay = ex2(dtbuf(j)[TQ - 1]);
-#pragma unroll
-      for (int i = 0; i < 16; ++i) hst[i] = fmaf(decay, hst[i], dv[i]);
-    };
-
-    bool live = true;
-    for (int i = 0; i <= n; ++i) {
-      // all element-wise warps done with chunk i-1's steps; uniform abort decision
-      if (bar_or(2, kMathThreads, *s_abort != 0u)) {
-        live = false;
-        break;
-      }
-      if (i < n) {
-        const float* D0 = dtbuf(i);
-        // (a) state through chunk i-1 -> H^T for C . H^T(i); releases the dH accumulator
-        bool ok = true;
-        if (i > 0) {
-          ok = warp_wait(bar(kDHDone + ((i - 1) & 1)), par(i - 1), s_abort) &&
-               warp_wait(bar(kYoDone + ((i - 1) & 1)), par(i - 1), s_abort);  // C . H^T(i-1) has read H^T
-          if (ok) {
-            tc_fence_after();
-            state_update(i - 1);
-          }
-        }
-        if (ok) write_ht();
-        fence_async_smem();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar(kHDone + (i & 1)));
-
-        // (b) X o w of chunk i (bf16 hi + lo), w_j = exp(s_end - s_j) dt'_j
-        ok = warp_wait(bar(kDtReady + (i & 1)), par(i), s_abort) && warp_wait(bar(kFullX + (i & 1)), par(i), s_abort);
-        if (ok) {
-          const float w = ex2(D0[TQ - 1] - D0[row]) * D0[TQ + row];
-          const unsigned char* xt = smem + (uint32_t)(i & 1) * kStage + kTileC + kTileB;
-#pragma unroll
-          for (int q = 0; q < 2; ++q) {
-            const uint32_t o = tile_off(row, 16 * cg + 8 * q, TQ);
-            const uint4 xv = *reinterpret_cast<const uint4*>(xt + o);
-            const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
-            uint32_t hi[4], lo[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e)
-              split2(__uint_as_float(xw[e] << 16) * w, __uint_as_float(xw[e] & 0xffff0000u) * w, hi[e], lo[e]);
-            *reinterpret_cast<uint4*>(smem + kOffXWhi + o) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-            *reinterpret_cast<uint4*>(smem + kOffXWlo + o) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-          }
-        }
-        fence_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar(kXWReady + (i & 1)));
-
-        // (c) M(i) = CB o exp(s_t - s_j) dt'_j (j <= t), + D on the diagonal, written
-        // over CB(i) as bf16 hi (columns [0,64)) and lo ([64,128)) packed pairs. This
-        // thread takes columns 32 bb + 8 cg .. +7 of each 32-column block bb: above
-        // the diagonal all zero; below it exp(s_t - s_j) = exp(s_t - s_e) exp(s_e - s_j)
-        // with e the block's last token (the second factor times dt'_j being v_j);
-        // the diagonal block exponentiates each pair.
-        ok = warp_wait(bar(kCBDone + (i & 1)), par(i), s_abort);
-        const uint32_t cbt = tmem + lane_off + kColCB + 128u * (uint32_t)(i & 1);
-        float cbv[4][8];
+    if (warp < kMathWarps / 2) {
+      // ---------- group M: M(i) = CB o exp(s_t - s_j) dt'_j (j <= t), + D on the
+      // diagonal. This thread takes columns j in [32 bb + 16 half, +16) of every
+      // 32-block bb and writes, over exactly those CB columns, the 16 values as
+      // bf16 hi (8 packed pairs) then lo (8 packed pairs), so the Y product reads
+      // hi and lo as two K=16 steps against the same 16 rows of X. Above the
+      // diagonal all zero; below it exp(s_t - s_j) = exp(s_t - s_e) exp(s_e - s_j)
+      // with e the block's last token (the second factor times dt'_j being v_j);
+      // the diagonal block exponentiates each pair.
+      for (int i = 0; i < n; ++i) {
+        if (bar_or(2, kMathThreads / 2, *s_abort != 0u)) break;
+        const bool ok = warp_wait(bar(kDtReady + (i & 1)), par(i), s_abort) &&
+                        warp_wait(bar(kCBDone + (i & 1)), par(i), s_abort);
         if (ok) {
           tc_fence_after();
-#pragma unroll
-          for (int bb = 0; bb < 4; ++bb) {
-            if (bb <= qrt) {
-              uint32_t r[8];
-              asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
-                           : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-                             "=r"(r[7])
-                           : "r"(cbt + 32 * bb + 8 * cg));
-#pragma unroll
-              for (int e = 0; e < 8; ++e) cbv[bb][e] = __uint_as_float(r[e]);
-            }
-          }
-          asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-        }
-        bar_sync(3 + qrt, 128);  // this lane quarter's four warps have read CB(i)
-        if (ok) {
+          const float* D0 = dtbuf(i);
           const float St = D0[row];
-#pragma unroll
-          for (int bb = 0; bb < 4; ++bb) {
-            uint32_t hi[4], lo[4];
-            const int j0 = 32 * bb + 8 * cg;
+          const uint32_t cbt = tmem + lane_off + kColCB + 128u * (uint32_t)(i & 1);
+#pragma unroll 1
+          for (int bb = 0; bb < 4; ++bb) {  // not unrolled: keeps the loop body small in the instruction cache
+            const int j0 = 32 * bb + 16 * half;
+            uint32_t hi[8], lo[8];
             if (bb > qrt) {
 #pragma unroll
-              for (int e = 0; e < 4; ++e) hi[e] = lo[e] = 0u;
-            } else if (bb < qrt) {
-              const float u = ex2(St - D0[32 * bb + 31]);
-              float v[8];
-              *reinterpret_cast<float4*>(v) = *reinterpret_cast<const float4*>(D0 + 2 * TQ + j0);
-              *reinterpret_cast<float4*>(v + 4) = *reinterpret_cast<const float4*>(D0 + 2 * TQ + j0 + 4);
-#pragma unroll
-              for (int e = 0; e < 4; ++e)
-                split2(cbv[bb][2 * e] * (u * v[2 * e]), cbv[bb][2 * e + 1] * (u * v[2 * e + 1]), hi[e], lo[e]);
+              for (int e = 0; e < 8; ++e) hi[e] = lo[e] = 0u;
             } else {
-              float sj[8], dj[8];
-              *reinterpret_cast<float4*>(sj) = *reinterpret_cast<const float4*>(D0 + j0);
-              *reinterpret_cast<float4*>(sj + 4) = *reinterpret_cast<const float4*>(D0 + j0 + 4);
-              *reinterpret_cast<float4*>(dj) = *reinterpret_cast<const float4*>(D0 + TQ + j0);
-              *reinterpret_cast<float4*>(dj + 4) = *reinterpret_cast<const float4*>(D0 + TQ + j0 + 4);
+              float cb[16];
+              tmem_ld16(cbt + j0, cb);
+              if (bb < qrt) {
+                const float u = ex2(St - D0[32 * bb + 31]);
+                float v[16];
 #pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                const int ja = j0 + 2 * e, jb = ja + 1;
-                float ma = ja <= row ? cbv[bb][2 * e] * ex2(St - sj[2 * e]) * dj[2 * e] : 0.f;
-                float mb = jb <= row ? cbv[bb][2 * e + 1] * ex2(St - sj[2 * e + 1]) * dj[2 * e + 1] : 0.f;
-                if (ja == row) ma += ci.Dh;
-                if (jb == row) mb += ci.Dh;
-                split2(ma, mb, hi[e], lo[e]);
+                for (int e = 0; e < 4; ++e)
+                  *reinterpret_cast<float4*>(v + 4 * e) = *reinterpret_cast<const float4*>(D0 + 2 * TQ + j0 + 4 * e);
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                  split2(cb[2 * e] * (u * v[2 * e]), cb[2 * e + 1] * (u * v[2 * e + 1]), hi[e], lo[e]);
+              } else {
+                float sj[16], dj[16];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                  *reinterpret_cast<float4*>(sj + 4 * e) = *reinterpret_cast<const float4*>(D0 + j0 + 4 * e);
+                  *reinterpret_cast<float4*>(dj + 4 * e) = *reinterpret_cast<const float4*>(D0 + TQ + j0 + 4 * e);
+                }
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                  const int ja = j0 + 2 * e, jb = ja + 1;
+                  float ma = ja <= row ? cb[2 * e] * ex2(St - sj[2 * e]) * dj[2 * e] : 0.f;
+                  float mb = jb <= row ? cb[2 * e + 1] * ex2(St - sj[2 * e + 1]) * dj[2 * e + 1] : 0.f;
+                  if (ja == row) ma += ci.Dh;
+                  if (jb == row) mb += ci.Dh;
+                  split2(ma, mb, hi[e], lo[e]);
+                }
               }
             }
-            const uint32_t pc = (uint32_t)(j0 >> 1);  // packed bf16-pair column
-            asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1,%2,%3,%4};"
-                         :: "r"(cbt + pc), "r"(hi[0]), "r"(hi[1]), "r"(hi[2]), "r"(hi[3]) : "memory");
-            asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1,%2,%3,%4};"
-                         :: "r"(cbt + 64 + pc), "r"(lo[0]), "r"(lo[1]), "r"(lo[2]), "r"(lo[3]) : "memory");
+            asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};"
+                         :: "r"(cbt + j0), "r"(hi[0]), "r"(hi[1]), "r"(hi[2]), "r"(hi[3]), "r"(hi[4]), "r"(hi[5]),
+                            "r"(hi[6]), "r"(hi[7]) : "memory");
+            asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};"
+                         :: "r"(cbt + j0 + 8), "r"(lo[0]), "r"(lo[1]), "r"(lo[2]), "r"(lo[3]), "r"(lo[4]), "r"(lo[5]),
+                            "r"(lo[6]), "r"(lo[7]) : "memory");
           }
           asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
         }
@@ -564,48 +475,150 @@ ssd_tc_full(const __grid_constant__ ScanArgs a, const __grid_constant__ CUtensor
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(kMReady + (i & 1)));
       }
-      if (i > 0) {
-        // (d) output of chunk j = i-1: y = M . X + exp(s_t) C . H^T, straight to HBM
-        const int j = i - 1;
-        bool ok = warp_wait(bar(kYdDone + (j & 1)), par(j), s_abort);
-        if (i == n) ok = ok && warp_wait(bar(kYoDone + (j & 1)), par(j), s_abort);
-        if (ok) {
-          tc_fence_after();
-          float yd[16], yo[16];
-          tmem_ld16x2(tmem + lane_off + kColYd + 16 * cg, tmem + lane_off + kColYo + 64u * (uint32_t)(j & 1) + 16 * cg,
-                      yd, yo);
-          const float et = ex2(dtbuf(j)[row]);
-          const int c = ci.c_begin + j;
-          if (row < min(TQ, ci.T - c * TQ)) {
-            uint32_t o[8];
+    } else {
+      // ---------- group S: X o w, the running state and the output
+      const int pc0 = 32 * half;  // this thread's 32 columns (p) of the state and of y
+      // running state: H^T[n = row][p], p in [pc0, pc0 + 32)
+      const int64_t head_off = (int64_t)ci.h * TP * TN;
+      float* slot_ptr = a.ssm_state + (int64_t)seq_slot(a.tab, ci.sq) * H * TP * TN + head_off;
+      auto ws_entry = [&](int segidx) -> float* { return a.ws_state + (int64_t)segidx * H * TP * TN + head_off; };
+      float hst[32];
+      auto load_state = [&](const float* src) {
 #pragma unroll
-            for (int f = 0; f < 8; ++f) o[f] = pack2(fmaf(et, yo[2 * f], yd[2 * f]), fmaf(et, yo[2 * f + 1], yd[2 * f + 1]));
-            // one full 32-byte sector per thread (y rows and the 16-column groups are 32-byte aligned)
-            __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(a.dst) + (ci.row0 + (int64_t)c * TQ + row) * (int64_t)(H * TP) +
-                                 ci.x_col + 16 * cg;
-            asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(dst), "r"(o[0]), "r"(o[1]), "r"(o[2]),
-                         "r"(o[3]), "r"(o[4]), "r"(o[5]), "r"(o[6]), "r"(o[7])
-                         : "memory");
+        for (int i = 0; i < 32; ++i) hst[i] = src ? src[(int64_t)(pc0 + i) * TN + row] : 0.0f;
+      };
+      if (ci.k == 0) {
+        // the first segment starts from the slot (from the state pass's copy when the
+        // last segment will overwrite the slot in this same launch)
+        load_state(ci.fresh ? nullptr : (ci.nseg > 1 ? ws_entry(ci.seg0 + ci.nseg - 1) : slot_ptr));
+      } else {
+        load_state(ws_entry(ci.seg0));
+        for (int j = 1; j < ci.k; ++j) {
+          const float d = __expf(a.ws_decay[(int64_t)(ci.seg0 + j) * H + ci.h]);
+          const float* e = ws_entry(ci.seg0 + j);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) hst[i] = fmaf(d, hst[i], e[(int64_t)(pc0 + i) * TN + row]);
+        }
+      }
+      auto state_update = [&](int j) {  // H = exp(total_j) H + dH(j), dH = hi part + lo part
+        const float decay = ex2(dtbuf(j)[TQ - 1]);
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {  // unrolled: hst must stay in registers
+          float dh[16], dl[16];
+          tmem_ld16x2(tmem + lane_off + kColDH + pc0 + 16 * q, tmem + lane_off + kColDH + 64 + pc0 + 16 * q, dh, dl);
+#pragma unroll
+          for (int e = 0; e < 16; ++e) hst[16 * q + e] = fmaf(decay, hst[16 * q + e], dh[e] + dl[e]);
+        }
+      };
+      // bf16 H^T (B operand of C . H^T): row n, columns [pc0, pc0 + 32)
+      auto write_ht = [&]() {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          uint32_t hw[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) hw[e] = pack2(hst[8 * q + 2 * e], hst[8 * q + 2 * e + 1]);
+          *reinterpret_cast<uint4*>(smem + kOffHT + tile_off(row, pc0 + 8 * q, TN)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+        }
+      };
+      // X o w work items: row xr, 16-column groups g0 and g0 + 2
+      const int xu = (warp - kMathWarps / 2) * 32 + lane;
+      const int xr = xu & 127, g0 = xu >> 7;
+
+      bool live = true;
+      for (int i = 0; i <= n; ++i) {
+        if (bar_or(1, kMathThreads / 2, *s_abort != 0u)) {
+          live = false;
+          break;
+        }
+        if (i < n) {
+          // (b) X o w of chunk i (bf16 hi + lo), w_j = exp(s_end - s_j) dt'_j
+          bool ok = warp_wait(bar(kDtReady + (i & 1)), par(i), s_abort) && warp_wait(bar(kFullX + (i & 1)), par(i), s_abort);
+          if (ok && i > 0) ok = warp_wait(bar(kDHDone + ((i - 1) & 1)), par(i - 1), s_abort);  // X o w buffer read
+          if (ok) {
+            const float* D0 = dtbuf(i);
+            const float w = ex2(D0[TQ - 1] - D0[xr]) * D0[TQ + xr];
+            const unsigned char* xt = smem + (uint32_t)(i & 1) * kStage + kTileC + kTileB;
+#pragma unroll 1
+            for (int gi = 0; gi < 4; ++gi) {  // 8-column pieces of groups g0 and g0 + 2
+              {
+                const uint32_t o = tile_off(xr, 16 * (g0 + 2 * (gi >> 1)) + 8 * (gi & 1), TQ);
+                const uint4 xv = *reinterpret_cast<const uint4*>(xt + o);
+                const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
+                uint32_t hi[4], lo[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                  split2(__uint_as_float(xw[e] << 16) * w, __uint_as_float(xw[e] & 0xffff0000u) * w, hi[e], lo[e]);
+                *reinterpret_cast<uint4*>(smem + kOffXWhi + o) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                *reinterpret_cast<uint4*>(smem + kOffXWlo + o) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+              }
+            }
+          }
+          fence_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(kXWReady + (i & 1)));
+
+          // (a) state through chunk i-1 -> H^T for C . H^T(i); releases the dH accumulator
+          if (i > 0) {
+            ok = warp_wait(bar(kDHDone + ((i - 1) & 1)), par(i - 1), s_abort) &&
+                 warp_wait(bar(kYoDone + ((i - 1) & 1)), par(i - 1), s_abort);  // C . H^T(i-1) has read H^T
+            if (ok) {
+              tc_fence_after();
+              state_update(i - 1);
+            }
+          } else {
+            ok = true;
+          }
+          if (ok) write_ht();
+          fence_async_smem();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(kHDone + (i & 1)));
+        }
+        if (i > 0) {
+          // (d) output of chunk j = i-1: y = M . X + exp(s_t) C . H^T, straight to HBM
+          const int j = i - 1;
+          bool ok = warp_wait(bar(kYdDone + (j & 1)), par(j), s_abort);
+          if (i == n) ok = ok && warp_wait(bar(kYoDone + (j & 1)), par(j), s_abort);
+          if (ok) {
+            tc_fence_after();
+            const float et = ex2(dtbuf(j)[row]);
+            const int c = ci.c_begin + j;
+            const bool in_run = row < min(TQ, ci.T - c * TQ);
+            __nv_bfloat16* ydst = static_cast<__nv_bfloat16*>(a.dst) + (ci.row0 + (int64_t)c * TQ + row) * (int64_t)(H * TP) +
+                                  ci.x_col + pc0;
+#pragma unroll 1
+            for (int q = 0; q < 2; ++q) {
+              float yd[16], yo[16];
+              tmem_ld16x2(tmem + lane_off + kColYd + pc0 + 16 * q, tmem + lane_off + kColYo + pc0 + 16 * q, yd, yo);
+              uint32_t o[8];
+#pragma unroll
+              for (int f = 0; f < 8; ++f) o[f] = pack2(fmaf(et, yo[2 * f], yd[2 * f]), fmaf(et, yo[2 * f + 1], yd[2 * f + 1]));
+              // one full 32-byte sector (y rows and the 16-column groups are 32-byte aligned)
+              if (in_run)
+                asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(ydst + 16 * q), "r"(o[0]), "r"(o[1]),
+                             "r"(o[2]), "r"(o[3]), "r"(o[4]), "r"(o[5]), "r"(o[6]), "r"(o[7])
+                             : "memory");
+            }
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(kEpiDone + (j & 3)));
+        }
+      }
+      // ---- state after the last chunk
+      if (live) {
+        bool ok = true;
+        if (n > 0) {
+          ok = warp_wait(bar(kDHDone + ((n - 1) & 1)), par(n - 1), s_abort);
+          if (ok) {
+            tc_fence_after();
+            state_update(n - 1);
           }
         }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar(kEpiDone + (j & 3)));
-      }
-    }
-    // ---- state after the last chunk
-    if (live) {
-      bool ok = true;
-      if (n > 0) {
-        ok = warp_wait(bar(kDHDone + ((n - 1) & 1)), par(n - 1), s_abort);
-        if (ok) {
-          tc_fence_after();
-          state_update(n - 1);
-        }
-      }
-      if (ok && ci.k == ci.nseg - 1) {
+        if (ok && ci.k == ci.nseg - 1) {
 #pragma unroll
-        for (int i = 0; i < 16; ++i) slot_ptr[(int64_t)(16 * cg + i) * TN + row] = hst[i];
+          for (int i = 0; i < 32; ++i) slot_ptr[(int64_t)(pc0 + i) * TN + row] = hst[i];
+        }
       }
     }
   } else if (warp == 16) {
@@ -672,13 +685,13 @@ ssd_tc_full(const __grid_constant__ ScanArgs a, const __grid_constant__ CUtensor
       for (int i = 0; i < n; ++i) {
         if (!wait_bar(bar(kFullCB + (i & 1)), par(i), s_abort)) break;
         if (!wait_bar(bar(kHDone + (i & 1)), par(i), s_abort)) break;  // H^T through chunk i-1 written
-        if (i >= 2 && !wait_bar(bar(kEpiDone + ((i - 2) & 3)), (uint32_t)(((i - 2) >> 2) & 1), s_abort)) break;  // Yoff buffer read
+        if (i >= 1 && !wait_bar(bar(kEpiDone + ((i - 1) & 3)), (uint32_t)(((i - 1) >> 2) & 1), s_abort)) break;  // Yoff(i-1) read
         tc_fence_after();
         const uint64_t a0 = sdesc(stage(i), 16, 1024), h0 = sdesc(sbase + kOffHT, TN * 128, 1024);
 #pragma unroll
         for (int s2 = 0; s2 < TN / 16; ++s2) {
           const uint32_t ko = ((s2 >> 2) * TQ * 128 + (s2 & 3) * 32) >> 4;
-          mma_ss(tmem + kColYo + 64u * (uint32_t)(i & 1), a0 + ko, h0 + ((s2 * 2048) >> 4), idesc128(64, 0, 1), s2 > 0);
+          mma_ss(tmem + kColYo, a0 + ko, h0 + ((s2 * 2048) >> 4), idesc128(64, 0, 1), s2 > 0);
         }
         mma_commit(bar(kYoDone + (i & 1)));
         last = i;
@@ -701,13 +714,14 @@ ssd_tc_full(const __grid_constant__ ScanArgs a, const __grid_constant__ CUtensor
       if (!ok) break;
       tc_fence_after();
       if (lane == 0) {
+        // B operand [X o w hi | X o w lo]: two 64-column blocks 16 KB apart
+        static_assert(kOffXWlo == kOffXWhi + kTileX, "X o w hi and lo must be adjacent");
         const uint64_t bt0 = sdesc(stage(i) + kTileC, TQ * 128, 1024);
-        const uint64_t hi0 = sdesc(sbase + kOffXWhi, TQ * 128, 1024), lo0 = sdesc(sbase + kOffXWlo, TQ * 128, 1024);
+        const uint64_t xw0 = sdesc(sbase + kOffXWhi, kTileX, 1024);
 #pragma unroll
         for (int s2 = 0; s2 < TQ / 16; ++s2) {
           const uint32_t jk = (s2 * 2048) >> 4;  // 16 rows of the [j][*] tiles
-          mma_ss(tmem + kColDH, bt0 + jk, hi0 + jk, idesc128(64, 1, 1), s2 > 0);
-          mma_ss(tmem + kColDH, bt0 + jk, lo0 + jk, idesc128(64, 1, 1), 1);
+          mma_ss(tmem + kColDH, bt0 + jk, xw0 + jk, idesc128(128, 1, 1), s2 > 0);
         }
         mma_commit(bar(kDHDone + (i & 1)));
       }
@@ -742,10 +756,10 @@ ssd_tc_full(const __grid_constant__ ScanArgs a, const __grid_constant__ CUtensor
         const uint64_t x0 = sdesc(stage(i) + kTileC + kTileB, TQ * 128, 1024);
         const uint32_t m = tmem + kColCB + 128u * (uint32_t)(i & 1);
 #pragma unroll
-        for (int s2 = 0; s2 < TQ / 16; ++s2) {
+        for (int s2 = 0; s2 < TQ / 16; ++s2) {  // tokens [16 s2, 16 s2 + 16): hi, then lo, same 16 rows of X
           const uint64_t xd = x0 + ((s2 * 2048) >> 4);
-          mma_ts(tmem + kColYd, m + 8 * s2, xd, idesc128(64, 0, 1), s2 > 0);
-          mma_ts(tmem + kColYd, m + 64 + 8 * s2, xd, idesc128(64, 0, 1), 1);
+          mma_ts(tmem + kColYd, m + 16 * s2, xd, idesc128(64, 0, 1), s2 > 0);
+          mma_ts(tmem + kColYd, m + 16 * s2 + 8, xd, idesc128(64, 0, 1), 1);
         }
         mma_commit(bar(kYdDone + (i & 1)));
       }
