@@ -71,7 +71,7 @@ constexpr int TN = 128;  // d_state
 constexpr int kMathWarps = 16;
 constexpr int kMathThreads = 32 * kMathWarps;
 constexpr int kFullThreads = kMathThreads + 4 * 32;   // + CB (and dt), Yoff, dH, Y issuers
-constexpr int kStateThreads = kMathThreads + 3 * 32;  // + loader, dH hi and dH lo issuers
+constexpr int kStateThreads = kMathThreads + 4 * 32;  // + loader, dH hi and dH lo issuers, weight producer
 constexpr uint32_t kWaitLimit = 1u << 22;  // try_wait rounds before giving up (about a second at the backoff)
 constexpr uint32_t kSuspendNs = 1000;      // a waiting thread sleeps up to this long per try_wait round
 
@@ -105,11 +105,12 @@ static_assert(kFullSmem <= 232448, "full-pass shared memory plan exceeds 227 KB"
 constexpr int kStStages = 3;
 constexpr uint32_t kStStage = kTileB + kTileX;
 constexpr uint32_t kStOffXW = kStStages * kStStage;   // [2][hi, lo] X o w tiles
-constexpr uint32_t kStOffW = kStOffXW + 4 * kTileX;   // [2][TQ] token weights
-constexpr uint32_t kStOffBtot = kStOffW + 2 * TQ * 4; // [2][4]
-constexpr uint32_t kStOffR = kStOffBtot + 32;         // total log2 decay of the segment
+constexpr uint32_t kStOffW = kStOffXW + 4 * kTileX;   // [4][TQ] token weights (chunk i in i % 4)
+constexpr uint32_t kStOffR = kStOffW + 4 * TQ * 4;    // total log2 decay of the segment
 constexpr uint32_t kStOffBar = kStOffR + 16;
-enum StateBar : int { kStFull = 0, kStDHDone = 3, kStXWReady = 6, kNumStateBars = 8 };
+enum StateBar : int {  // + chunk % 3 (stages) or chunk % 4 (weights)
+  kStFull = 0, kStDHDone = 3, kStXWReady = 6, kStWReady = 10, kNumStateBars = 14
+};
 constexpr uint32_t kStOffMisc = kStOffBar + 8 * kNumStateBars;
 constexpr uint32_t kStateSmem = kStOffMisc + 16 + 1024;
 static_assert(kStateSmem <= 232448, "state-pass shared memory plan exceeds 227 KB");
@@ -189,17 +190,6 @@ __device__ __forceinline__ void drain_bar(uint32_t bar, uint32_t parity) {
   for (uint32_t it = 0; it < kWaitLimit; ++it)
     if (mbar_test(bar, parity)) return;
 }
-// named barrier over `count` threads; returns the OR of `pred` over them
-__device__ __forceinline__ bool bar_or(int id, int count, bool pred) {
-  uint32_t r;
-  asm volatile("{\n.reg .pred p, q;\nsetp.ne.u32 p, %1, 0;\nbar.red.or.pred q, %2, %3, p;\nselp.u32 %0, 1, 0, q;\n}\n"
-               : "=r"(r) : "r"((uint32_t)pred), "r"(id), "r"(count) : "memory");
-  return r != 0;
-}
-__device__ __forceinline__ void bar_sync(int id, int count) {
-  asm volatile("bar.sync %0, %1;" :: "r"(id), "r"(count) : "memory");
-}
-
 // ---- TMEM loads / stores (32 lanes x 32 bit)
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
   uint32_t r[16];
@@ -417,7 +407,7 @@ ssd_tc_full(const __grid_constant__ ScanArgs a, const __grid_constant__ CUtensor
       // with e the block's last token (the second factor times dt'_j being v_j);
       // the diagonal block exponentiates each pair.
       for (int i = 0; i < n; ++i) {
-        if (bar_or(2, kMathThreads / 2, *s_abort != 0u)) break;
+        if (*s_abort) break;
         const bool ok = warp_wait(bar(kDtReady + (i & 1)), par(i), s_abort) &&
                         warp_wait(bar(kCBDone + (i & 1)), par(i), s_abort);
         if (ok) {
@@ -526,7 +516,7 @@ ssd_tc_full(const __grid_constant__ ScanArgs a, const __grid_constant__ CUtensor
 
       bool live = true;
       for (int i = 0; i <= n; ++i) {
-        if (bar_or(1, kMathThreads / 2, *s_abort != 0u)) {
+        if (*s_abort) {
           live = false;
           break;
         }
@@ -788,9 +778,10 @@ ssd_tc_full(const __grid_constant__ ScanArgs a, const __grid_constant__ CUtensor
 // first; with R the log2 decay of the chunks already read, token j's weight is
 // w_j = 2^(R + S_end - S_j) dt'_j (S the chunk's cumulative log2 decay), so
 // B^T . (X o w) of every chunk accumulates into the same TMEM columns.
-//   warps 0-15  dt' and weights (warps 0, 4, 8, 12), X o w (bf16 hi + lo)
+//   warps 0-15  X o w (bf16 hi + lo); at the end, the segment's state
 //   warp 16     B and X tile loads (three stages)
 //   warp 17/18  dH^T += B^T . (X o w) hi / lo, each into its own accumulator
+//   warp 19     dt' and the token weights, up to four chunks ahead
 __global__ void __launch_bounds__(kStateThreads, 1)
 ssd_tc_state(const __grid_constant__ ScanArgs a, const __grid_constant__ CUtensorMap tm, const int use_tma) {
   const Cta ci = cta_info(a);
@@ -801,10 +792,12 @@ ssd_tc_state(const __grid_constant__ ScanArgs a, const __grid_constant__ CUtenso
   const uint32_t sbase = su32(smem);
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + kStOffMisc);
   volatile uint32_t* s_abort = reinterpret_cast<volatile uint32_t*>(smem + kStOffMisc + 4);
+  float* s_w = reinterpret_cast<float*>(smem + kStOffW);
+  float* s_R = reinterpret_cast<float*>(smem + kStOffR);
   auto bar = [&](int id) { return sbase + kStOffBar + 8u * (uint32_t)id; };
   auto stg = [&](int i) { return sbase + (uint32_t)(i % kStStages) * kStStage; };
   auto p3 = [](int i) { return (uint32_t)((i / kStStages) & 1); };  // phase parity on a [3] barrier
-  auto p2 = [](int i) { return (uint32_t)((i >> 1) & 1); };         // phase parity on a [2] barrier
+  auto p4 = [](int i) { return (uint32_t)((i >> 2) & 1); };         // phase parity on a [4] barrier
 
   const int n = ci.n;  // >= 1 for every segment but the last
   const int H = a.heads;
@@ -819,7 +812,10 @@ ssd_tc_state(const __grid_constant__ ScanArgs a, const __grid_constant__ CUtenso
       mbar_init(bar(kStFull + s), 2);    // B tile, X tile
       mbar_init(bar(kStDHDone + s), 2);  // hi and lo issuers
     }
-    for (int b = 0; b < 2; ++b) mbar_init(bar(kStXWReady + b), kMathWarps);
+    for (int b = 0; b < 4; ++b) {
+      mbar_init(bar(kStXWReady + b), kMathWarps);
+      mbar_init(bar(kStWReady + b), 1);
+    }
     *s_abort = 0u;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -840,101 +836,61 @@ ssd_tc_state(const __grid_constant__ ScanArgs a, const __grid_constant__ CUtenso
   };
 
   if (warp < kMathWarps) {
+    // =================== X o w of every chunk, then the segment's state
     const int row = tid & 127, cg = tid >> 7, qrt = warp & 3;
     const uint32_t lane_off = (uint32_t)(qrt * 32) << 16;
-    const bool dt_warp = qrt == 0;
-    const int dblk = warp >> 2;
-    float* s_w = reinterpret_cast<float*>(smem + kStOffW);
-    float* s_btot = reinterpret_cast<float*>(smem + kStOffBtot);
-    float* s_R = reinterpret_cast<float*>(smem + kStOffR);
     const int64_t head_off = (int64_t)ci.h * TP * TN;
     auto ws_entry = [&](int segidx) -> float* { return a.ws_state + (int64_t)segidx * H * TP * TN + head_off; };
-
-    // the first segment starts from the slot's state: keep it, and leave a copy
-    // for the full pass (whose last segment overwrites the slot)
-    float h0[16];
-    const bool seeded = ci.k == 0 && !ci.fresh;
-    if (seeded) {
-      const float* slot_ptr = a.ssm_state + (int64_t)seq_slot(a.tab, ci.sq) * H * TP * TN + head_off;
-      float* copy = ws_entry(ci.seg0 + ci.nseg - 1);
-#pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        h0[i] = slot_ptr[(int64_t)(16 * cg + i) * TN + row];
-        copy[(int64_t)(16 * cg + i) * TN + row] = h0[i];
-      }
-    }
-
-    unsigned short dt_raw = 0;
-    float R = 0.f;  // log2 decay from the end of the chunks already read to the segment end
-    auto load_dt = [&](int i) {
-      const int c = ci.c_end - 1 - i, t = 32 * dblk + lane;
-      dt_raw = t < min(TQ, ci.T - c * TQ)
-                   ? reinterpret_cast<const unsigned short*>(a.dt)[(ci.row0 + (int64_t)c * TQ + t) * H + ci.h]
-                   : (unsigned short)0;
-    };
-    auto dt_phase = [&](int i) {
-      const int c = ci.c_end - 1 - i, t = 32 * dblk + lane;
-      const float dp = dt_prime(dt_raw, t < min(TQ, ci.T - c * TQ), ci.dtb);
-      const float incl = warp_incl_sum(-ci.A2 * dp, lane);
-      float* bt = s_btot + (i & 1) * 4;
-      if (lane == 31) bt[dblk] = incl;
-      bar_sync(1, 128);  // the four dt warps
-      float pre = 0.f;
-      for (int k2 = 0; k2 < dblk; ++k2) pre += bt[k2];
-      const float tot = (bt[0] + bt[1]) + (bt[2] + bt[3]);
-      s_w[(i & 1) * TQ + t] = ex2(R + (tot - (pre + incl))) * dp;
-      R += tot;
-      if (i == n - 1 && warp == 0 && lane == 0) *s_R = R;
-    };
-
     bool live = true;
-    if (dt_warp) {
-      load_dt(0);
-      dt_phase(0);
-      if (n > 1) load_dt(1);
-    }
     for (int i = 0; i < n; ++i) {
-      if (bar_or(2, kMathThreads, *s_abort != 0u)) {
+      bool ok = warp_wait(bar(kStFull + i % kStStages), p3(i), s_abort) &&
+                warp_wait(bar(kStWReady + (i & 3)), p4(i), s_abort);
+      if (ok && i >= 2) ok = warp_wait(bar(kStDHDone + (i - 2) % kStStages), p3(i - 2), s_abort);  // X o w buffer read
+      if (!ok) {
         live = false;
         break;
       }
-      bool ok = warp_wait(bar(kStFull + i % kStStages), p3(i), s_abort);
-      if (ok && i >= 2) ok = warp_wait(bar(kStDHDone + (i - 2) % kStStages), p3(i - 2), s_abort);  // X o w buffer read
-      if (ok) {
-        const float w = s_w[(i & 1) * TQ + row];
-        const unsigned char* xt = smem + (uint32_t)(i % kStStages) * kStStage + kTileB;
-        unsigned char* xw = smem + kStOffXW + (uint32_t)(i & 1) * 2 * kTileX;
+      const float w = s_w[(i & 3) * TQ + row];
+      const unsigned char* xt = smem + (uint32_t)(i % kStStages) * kStStage + kTileB;
+      unsigned char* xw = smem + kStOffXW + (uint32_t)(i & 1) * 2 * kTileX;
 #pragma unroll
-        for (int q = 0; q < 2; ++q) {
-          const uint32_t o = tile_off(row, 16 * cg + 8 * q, TQ);
-          const uint4 xv = *reinterpret_cast<const uint4*>(xt + o);
-          const uint32_t xr[4] = {xv.x, xv.y, xv.z, xv.w};
-          uint32_t hi[4], lo[4];
+      for (int q = 0; q < 2; ++q) {
+        const uint32_t o = tile_off(row, 16 * cg + 8 * q, TQ);
+        const uint4 xv = *reinterpret_cast<const uint4*>(xt + o);
+        const uint32_t xr[4] = {xv.x, xv.y, xv.z, xv.w};
+        uint32_t hi[4], lo[4];
 #pragma unroll
-          for (int e = 0; e < 4; ++e)
-            split2(__uint_as_float(xr[e] << 16) * w, __uint_as_float(xr[e] & 0xffff0000u) * w, hi[e], lo[e]);
-          *reinterpret_cast<uint4*>(xw + o) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-          *reinterpret_cast<uint4*>(xw + kTileX + o) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-        }
+        for (int e = 0; e < 4; ++e)
+          split2(__uint_as_float(xr[e] << 16) * w, __uint_as_float(xr[e] & 0xffff0000u) * w, hi[e], lo[e]);
+        *reinterpret_cast<uint4*>(xw + o) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+        *reinterpret_cast<uint4*>(xw + kTileX + o) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
       }
       fence_async_smem();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(kStXWReady + (i & 1)));
-      if (dt_warp && i + 1 < n) {
-        dt_phase(i + 1);
-        if (i + 2 < n) load_dt(i + 2);
-      }
+      if (lane == 0) mbar_arrive(bar(kStXWReady + (i & 3)));
     }
     if (live && warp_wait(bar(kStDHDone + (n - 1) % kStStages), p3(n - 1), s_abort)) {
       tc_fence_after();
       float dhi[16], dlo[16];
       tmem_ld16x2(tmem + lane_off + 16 * cg, tmem + lane_off + 64 + 16 * cg, dhi, dlo);
-      const float Rt = *s_R;  // written before this loop's last barrier
-      const float d = ex2(Rt);
+      const float Rt = *s_R;  // written before the weights of the last chunk were published
       float* dst = ws_entry(blockIdx.x);
+      if (ci.k == 0 && !ci.fresh) {
+        // the first segment starts from the slot's state: add its decayed share, and
+        // leave a copy of it for the full pass (whose last segment overwrites the slot)
+        const float d = ex2(Rt);
+        const float* slot_ptr = a.ssm_state + (int64_t)seq_slot(a.tab, ci.sq) * H * TP * TN + head_off;
+        float* copy = ws_entry(ci.seg0 + ci.nseg - 1);
 #pragma unroll
-      for (int i = 0; i < 16; ++i)
-        dst[(int64_t)(16 * cg + i) * TN + row] = seeded ? fmaf(d, h0[i], dhi[i] + dlo[i]) : dhi[i] + dlo[i];
+        for (int i = 0; i < 16; ++i) {
+          const float h0 = slot_ptr[(int64_t)(16 * cg + i) * TN + row];
+          copy[(int64_t)(16 * cg + i) * TN + row] = h0;
+          dst[(int64_t)(16 * cg + i) * TN + row] = fmaf(d, h0, dhi[i] + dlo[i]);
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) dst[(int64_t)(16 * cg + i) * TN + row] = dhi[i] + dlo[i];
+      }
       if (tid == 0) a.ws_decay[(int64_t)blockIdx.x * H + ci.h] = Rt * 0.6931471805599453f;
     }
   } else if (warp == kMathWarps) {
@@ -949,14 +905,14 @@ ssd_tc_state(const __grid_constant__ ScanArgs a, const __grid_constant__ CUtenso
     }
     if (lane == 0 && *s_abort)
       for (int i = max(0, loaded - kStStages); i < loaded; ++i) drain_bar(bar(kStFull + i % kStStages), p3(i));
-  } else {
+  } else if (warp <= kMathWarps + 2) {
     // =================== dH^T += B^T . (X o w) hi (warp 17) / lo (warp 18)
     if (lane == 0) {
       const uint32_t part = warp == kMathWarps + 1 ? 0u : 1u;
       int last = -1;
       for (int i = 0; i < n; ++i) {
         if (!wait_bar(bar(kStFull + i % kStStages), p3(i), s_abort)) break;
-        if (!wait_bar(bar(kStXWReady + (i & 1)), p2(i), s_abort)) break;
+        if (!wait_bar(bar(kStXWReady + (i & 3)), p4(i), s_abort)) break;
         tc_fence_after();
         const uint64_t bt0 = sdesc(stg(i), TQ * 128, 1024);
         const uint64_t xw0 = sdesc(sbase + kStOffXW + (uint32_t)(i & 1) * 2 * kTileX + part * kTileX, TQ * 128, 1024);
@@ -969,6 +925,42 @@ ssd_tc_state(const __grid_constant__ ScanArgs a, const __grid_constant__ CUtenso
         last = i;
       }
       if (last >= 0) drain_bar(bar(kStDHDone + last % kStStages), p3(last));
+    }
+  } else {
+    // =================== dt' and token weights of chunk i into ring slot i % 4
+    // (lane l: tokens 4l .. 4l+3); slot i % 4 last served chunk i-4
+    unsigned short raw[4] = {0, 0, 0, 0};  // raw bf16 bits: the loads stay in flight until used
+    auto load_raw = [&](int i) {
+      const int c = ci.c_end - 1 - i, len = min(TQ, ci.T - c * TQ);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int t = 4 * lane + e;
+        raw[e] = t < len ? reinterpret_cast<const unsigned short*>(a.dt)[(ci.row0 + (int64_t)c * TQ + t) * H + ci.h]
+                         : (unsigned short)0;
+      }
+    };
+    float R = 0.f;  // log2 decay from the end of the chunks already read to the segment end
+    load_raw(0);
+    for (int i = 0; i < n; ++i) {
+      if (i >= 4 && !warp_wait(bar(kStXWReady + (i & 3)), p4(i - 4), s_abort)) break;
+      const int c = ci.c_end - 1 - i, len = min(TQ, ci.T - c * TQ);
+      float dp[4], S[4], run = 0.f;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        dp[e] = dt_prime(raw[e], 4 * lane + e < len, ci.dtb);
+        run -= ci.A2 * dp[e];
+        S[e] = run;
+      }
+      if (i + 1 < n) load_raw(i + 1);
+      const float incl = warp_incl_sum(run, lane);
+      const float tot = __shfl_sync(0xffffffffu, incl, 31);
+      const float base = R + (tot - (incl - run));  // R + S_end - (S before this lane's tokens)
+      *reinterpret_cast<float4*>(s_w + (i & 3) * TQ + 4 * lane) =
+          make_float4(ex2(base - S[0]) * dp[0], ex2(base - S[1]) * dp[1], ex2(base - S[2]) * dp[2], ex2(base - S[3]) * dp[3]);
+      R += tot;
+      if (i == n - 1 && lane == 0) *s_R = R;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(kStWReady + (i & 3)));
     }
   }
 
