@@ -71,7 +71,7 @@ constexpr int TN = 128;  // d_state
 constexpr int kMathWarps = 16;
 constexpr int kMathThreads = 32 * kMathWarps;
 constexpr int kFullThreads = kMathThreads + 4 * 32;   // + CB (and dt), Yoff, dH, Y issuers
-constexpr int kStateThreads = kMathThreads + 4 * 32;  // + loader, dH hi and dH lo issuers, weight producer
+constexpr int kStateThreads = kMathThreads + 3 * 32;  // + loader, dH issuer, weight producer
 constexpr uint32_t kWaitLimit = 1u << 22;  // try_wait rounds before giving up (about a second at the backoff)
 constexpr uint32_t kSuspendNs = 1000;      // a waiting thread sleeps up to this long per try_wait round
 
@@ -101,7 +101,7 @@ constexpr uint32_t kOffMisc = kOffBar + 8 * kNumFullBars;  // TMEM base, abort f
 constexpr uint32_t kFullSmem = kOffMisc + 16 + 1024;        // + slack to align the base to 1024
 static_assert(kFullSmem <= 232448, "full-pass shared memory plan exceeds 227 KB");
 
-// ---- state pass: shared memory (3 stages of B, X), TMEM D hi [0,64), D lo [64,128)
+// ---- state pass: shared memory (3 stages of B, X), TMEM D = [hi part | lo part] in [0,128)
 constexpr int kStStages = 3;
 constexpr uint32_t kStStage = kTileB + kTileX;
 constexpr uint32_t kStOffXW = kStStages * kStStage;   // [2][hi, lo] X o w tiles
@@ -321,6 +321,10 @@ __device__ __forceinline__ Cta cta_info(const ScanArgs& a) {
 __device__ __forceinline__ float dt_prime(unsigned short raw, bool valid, float dtb) {
   return valid ? softplus_f(__uint_as_float((uint32_t)raw << 16) + dtb) : 0.f;
 }
+// Raw bf16 bits of dt for this lane's four tokens (4l .. 4l+3) of one chunk.
+struct DtRaw {
+  unsigned short v[4];
+};
 // inclusive warp scan
 __device__ __forceinline__ float warp_incl_sum(float v, int lane) {
 #pragma unroll
@@ -616,17 +620,21 @@ ssd_tc_full(const __grid_constant__ ScanArgs a, const __grid_constant__ CUtensor
     // cumulative decay S and block factors v into dt buffer i % 4 (lane l: tokens
     // 4l .. 4l+3; the buffer last served chunk i-4, whose readers are done once
     // chunk i-3's output is written); then CB = C . B^T (lane 0)
-    unsigned short raw[4] = {0, 0, 0, 0};  // raw bf16 bits: the loads stay in flight until used
+    // raw bf16 dt bits of chunks i .. i+3, loaded four chunks ahead (the loads stay
+    // in flight until used)
     auto load_raw = [&](int i) {
-      const int c = ci.c_begin + i, len = min(TQ, ci.T - c * TQ);
+      DtRaw r = {{0, 0, 0, 0}};
+      if (i < n) {
+        const int c = ci.c_begin + i, len = min(TQ, ci.T - c * TQ);
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int t = 4 * lane + e;
-        raw[e] = t < len ? reinterpret_cast<const unsigned short*>(a.dt)[(ci.row0 + (int64_t)c * TQ + t) * H + ci.h]
-                         : (unsigned short)0;
+        for (int e = 0; e < 4; ++e) {
+          const int t = 4 * lane + e;
+          if (t < len) r.v[e] = reinterpret_cast<const unsigned short*>(a.dt)[(ci.row0 + (int64_t)c * TQ + t) * H + ci.h];
+        }
       }
+      return r;
     };
-    if (n > 0) load_raw(0);
+    DtRaw r0 = load_raw(0), r1 = load_raw(1), r2 = load_raw(2), r3 = load_raw(3);
     int last = -1;
     for (int i = 0; i < n; ++i) {
       if (i >= 3 && !warp_wait(bar(kEpiDone + ((i - 3) & 3)), (uint32_t)(((i - 3) >> 2) & 1), s_abort)) break;
@@ -635,11 +643,14 @@ ssd_tc_full(const __grid_constant__ ScanArgs a, const __grid_constant__ CUtensor
         float dp[4], S[4], run = 0.f;
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          dp[e] = dt_prime(raw[e], 4 * lane + e < len, ci.dtb);
+          dp[e] = dt_prime(r0.v[e], 4 * lane + e < len, ci.dtb);
           run -= ci.A2 * dp[e];
           S[e] = run;
         }
-        if (i + 1 < n) load_raw(i + 1);
+        r0 = r1;
+        r1 = r2;
+        r2 = r3;
+        r3 = load_raw(i + 4);
         const float excl = warp_incl_sum(run, lane) - run;
 #pragma unroll
         for (int e = 0; e < 4; ++e) S[e] += excl;
@@ -780,8 +791,8 @@ ssd_tc_full(const __grid_constant__ ScanArgs a, const __grid_constant__ CUtensor
 // B^T . (X o w) of every chunk accumulates into the same TMEM columns.
 //   warps 0-15  X o w (bf16 hi + lo); at the end, the segment's state
 //   warp 16     B and X tile loads (three stages)
-//   warp 17/18  dH^T += B^T . (X o w) hi / lo, each into its own accumulator
-//   warp 19     dt' and the token weights, up to four chunks ahead
+//   warp 17     dH^T += B^T . [X o w hi | lo]  (M=128 N=128 K=128 per chunk)
+//   warp 18     dt' and the token weights, up to four chunks ahead
 __global__ void __launch_bounds__(kStateThreads, 1)
 ssd_tc_state(const __grid_constant__ ScanArgs a, const __grid_constant__ CUtensorMap tm, const int use_tma) {
   const Cta ci = cta_info(a);
@@ -810,7 +821,7 @@ ssd_tc_state(const __grid_constant__ ScanArgs a, const __grid_constant__ CUtenso
   if (tid == kMathThreads) {
     for (int s = 0; s < kStStages; ++s) {
       mbar_init(bar(kStFull + s), 2);    // B tile, X tile
-      mbar_init(bar(kStDHDone + s), 2);  // hi and lo issuers
+      mbar_init(bar(kStDHDone + s), 1);
     }
     for (int b = 0; b < 4; ++b) {
       mbar_init(bar(kStXWReady + b), kMathWarps);
@@ -905,21 +916,20 @@ ssd_tc_state(const __grid_constant__ ScanArgs a, const __grid_constant__ CUtenso
     }
     if (lane == 0 && *s_abort)
       for (int i = max(0, loaded - kStStages); i < loaded; ++i) drain_bar(bar(kStFull + i % kStStages), p3(i));
-  } else if (warp <= kMathWarps + 2) {
-    // =================== dH^T += B^T . (X o w) hi (warp 17) / lo (warp 18)
+  } else if (warp == kMathWarps + 1) {
+    // =================== dH^T += B^T . [X o w hi | X o w lo] (one N=128 product per chunk)
     if (lane == 0) {
-      const uint32_t part = warp == kMathWarps + 1 ? 0u : 1u;
       int last = -1;
       for (int i = 0; i < n; ++i) {
         if (!wait_bar(bar(kStFull + i % kStStages), p3(i), s_abort)) break;
         if (!wait_bar(bar(kStXWReady + (i & 3)), p4(i), s_abort)) break;
         tc_fence_after();
         const uint64_t bt0 = sdesc(stg(i), TQ * 128, 1024);
-        const uint64_t xw0 = sdesc(sbase + kStOffXW + (uint32_t)(i & 1) * 2 * kTileX + part * kTileX, TQ * 128, 1024);
+        const uint64_t xw0 = sdesc(sbase + kStOffXW + (uint32_t)(i & 1) * 2 * kTileX, kTileX, 1024);  // hi | lo blocks
 #pragma unroll
         for (int s2 = 0; s2 < TQ / 16; ++s2) {
           const uint32_t jk = (s2 * 2048) >> 4;
-          mma_ss(tmem + 64u * part, bt0 + jk, xw0 + jk, idesc128(64, 1, 1), (i > 0 || s2 > 0) ? 1u : 0u);
+          mma_ss(tmem, bt0 + jk, xw0 + jk, idesc128(128, 1, 1), (i > 0 || s2 > 0) ? 1u : 0u);
         }
         mma_commit(bar(kStDHDone + i % kStStages));
         last = i;
@@ -929,29 +939,35 @@ ssd_tc_state(const __grid_constant__ ScanArgs a, const __grid_constant__ CUtenso
   } else {
     // =================== dt' and token weights of chunk i into ring slot i % 4
     // (lane l: tokens 4l .. 4l+3); slot i % 4 last served chunk i-4
-    unsigned short raw[4] = {0, 0, 0, 0};  // raw bf16 bits: the loads stay in flight until used
+    // raw bf16 dt bits of chunks i .. i+3, loaded four chunks ahead
     auto load_raw = [&](int i) {
-      const int c = ci.c_end - 1 - i, len = min(TQ, ci.T - c * TQ);
+      DtRaw r = {{0, 0, 0, 0}};
+      if (i < n) {
+        const int c = ci.c_end - 1 - i, len = min(TQ, ci.T - c * TQ);
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int t = 4 * lane + e;
-        raw[e] = t < len ? reinterpret_cast<const unsigned short*>(a.dt)[(ci.row0 + (int64_t)c * TQ + t) * H + ci.h]
-                         : (unsigned short)0;
+        for (int e = 0; e < 4; ++e) {
+          const int t = 4 * lane + e;
+          if (t < len) r.v[e] = reinterpret_cast<const unsigned short*>(a.dt)[(ci.row0 + (int64_t)c * TQ + t) * H + ci.h];
+        }
       }
+      return r;
     };
     float R = 0.f;  // log2 decay from the end of the chunks already read to the segment end
-    load_raw(0);
+    DtRaw r0 = load_raw(0), r1 = load_raw(1), r2 = load_raw(2), r3 = load_raw(3);
     for (int i = 0; i < n; ++i) {
       if (i >= 4 && !warp_wait(bar(kStXWReady + (i & 3)), p4(i - 4), s_abort)) break;
       const int c = ci.c_end - 1 - i, len = min(TQ, ci.T - c * TQ);
       float dp[4], S[4], run = 0.f;
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        dp[e] = dt_prime(raw[e], 4 * lane + e < len, ci.dtb);
+        dp[e] = dt_prime(r0.v[e], 4 * lane + e < len, ci.dtb);
         run -= ci.A2 * dp[e];
         S[e] = run;
       }
-      if (i + 1 < n) load_raw(i + 1);
+      r0 = r1;
+      r1 = r2;
+      r2 = r3;
+      r3 = load_raw(i + 4);
       const float incl = warp_incl_sum(run, lane);
       const float tot = __shfl_sync(0xffffffffu, incl, 31);
       const float base = R + (tot - (incl - run));  // R + S_end - (S before this lane's tokens)
