@@ -135,7 +135,9 @@ size_t mamba2_ssd_scan_workspace_bytes(const mamba2_dims* dims, int32_t rows,
  *   ssm_state  [num_slots, heads, headdim, d_state] f32, updated in place
  *   workspace  device scratch of at least
  *              mamba2_ssd_scan_workspace_bytes(...) bytes (may be NULL when
- *              that is 0); its contents need no initialisation.
+ *              that is 0), 256-byte aligned; its contents need no
+ *              initialisation. It holds the segment states of long runs and,
+ *              on the tcgen05 path, dt' for every row and head.
  * Built shapes (any heads, ngroups): bf16 headdim 64 x d_state 128 runs on
  * the tcgen05 chunked kernel (128-token chunks), bf16 16 x 16 on the mma.sync
  * chunked kernel (64-token chunks); fp32 activations and other shapes up to

@@ -88,6 +88,9 @@ struct ScanPlan {
   int total_segs = 0;
   bool segmented = false;
   size_t ws_state_floats = 0;
+  size_t off_decay = 0;  // byte offsets in the workspace
+  size_t off_dtp = 0;
+  bool has_dtp = false;  // tcgen05 path: dt' precomputed into the workspace
   size_t ws_bytes = 0;
 };
 
@@ -130,11 +133,18 @@ ScanPlan plan_scan(const mamba2_dims* d, mamba2_dtype act, const mamba2_recurren
     p.segmented |= segs > 1;
     p.total_segs += segs;
   }
+  size_t bytes = 0;
   if (p.segmented) {
     p.ws_state_floats = (size_t)p.total_segs * d->heads * d->headdim * d->d_state;
-    const size_t decay_off = (p.ws_state_floats * 4 + 255) / 256 * 256;
-    p.ws_bytes = decay_off + (size_t)p.total_segs * d->heads * 4;
+    p.off_decay = (p.ws_state_floats * 4 + 255) / 256 * 256;
+    bytes = p.off_decay + (size_t)p.total_segs * d->heads * 4;
   }
+  p.has_dtp = scan_uses_tc(act, d->headdim, d->d_state);
+  if (p.has_dtp) {
+    p.off_dtp = (bytes + 255) / 256 * 256;
+    bytes = p.off_dtp + (size_t)rb->cu_seqlens[n] * d->heads * 4;
+  }
+  p.ws_bytes = bytes;
   return p;
 }
 
@@ -265,11 +275,11 @@ mamba2_status mamba2_ssd_scan(void* dst, const void* xbc, const void* dt, const 
   a.ngroups = dims->ngroups;
   a.conv_dim = dims->heads * dims->headdim + 2 * dims->ngroups * dims->d_state;
   a.seg_chunks = plan.seg_chunks;
-  if (plan.ws_bytes > 0) {
+  if (plan.segmented) {
     a.ws_state = static_cast<float*>(workspace);
-    a.ws_decay = reinterpret_cast<float*>(static_cast<char*>(workspace) +
-                                          (plan.ws_state_floats * 4 + 255) / 256 * 256);
+    a.ws_decay = reinterpret_cast<float*>(static_cast<char*>(workspace) + plan.off_decay);
   }
+  if (plan.has_dtp) a.dtp = reinterpret_cast<float*>(static_cast<char*>(workspace) + plan.off_dtp);
   fill_table(a.tab, rb);
   fill_scan_tiles(a.tab, plan, scan_chunk_tokens(dims->headdim, dims->d_state));
   cudaStream_t s = static_cast<cudaStream_t>(stream);

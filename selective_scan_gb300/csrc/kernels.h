@@ -51,6 +51,7 @@ struct ScanArgs {
   float* ssm_state;
   float* ws_state;  // [segments, heads, P, N] (null when unsegmented)
   float* ws_decay;  // [segments, heads]
+  float* dtp;       // [heads, rows] dt' = softplus(dt + dt_bias) (tcgen05 path; null otherwise)
   int32_t heads, headdim, d_state, ngroups, conv_dim;
   int32_t seg_chunks;  // chunks per segment (tile = segment)
   SeqTable tab;
@@ -59,6 +60,9 @@ struct ScanArgs {
 // headdim 64 x d_state 128 (chunks of kChunkTc tokens), mma.sync for 16 x 16.
 bool scan_chunked_supported(mamba2_dtype act, int headdim, int d_state);
 constexpr int kChunkTc = 128;
+inline bool scan_uses_tc(mamba2_dtype act, int headdim, int d_state) {
+  return act == MAMBA2_BF16 && headdim == 64 && d_state == 128;
+}
 inline int scan_chunk_tokens(int headdim, int d_state) {
   return (headdim == 64 && d_state == 128) ? kChunkTc : kChunk;
 }

@@ -289,7 +289,7 @@ struct Cta {
   int sq, seg0, k, nseg, h, row0, T, c_begin, c_end, n;
   bool fresh;
   int x_col, b_col, c_col;
-  float A2, dtb, Dh;  // decay rate in log2 units, dt bias, skip weight
+  float A2, Dh;  // decay rate in log2 units, skip weight
 };
 __device__ __forceinline__ Cta cta_info(const ScanArgs& a) {
   Cta c;
@@ -312,19 +312,31 @@ __device__ __forceinline__ Cta cta_info(const ScanArgs& a) {
   c.b_col = H * TP + g * TN;
   c.c_col = H * TP + G * TN + g * TN;
   c.A2 = expf(a.A_log[c.h]) * 1.4426950408889634f;
-  c.dtb = a.dt_bias[c.h];
   c.Dh = a.D[c.h];
   return c;
 }
 
-// dt'_t = softplus(dt_t + dt_bias) of token t of chunk c (0 past the run), from raw bf16 bits
-__device__ __forceinline__ float dt_prime(unsigned short raw, bool valid, float dtb) {
-  return valid ? softplus_f(__uint_as_float((uint32_t)raw << 16) + dtb) : 0.f;
-}
-// Raw bf16 bits of dt for this lane's four tokens (4l .. 4l+3) of one chunk.
-struct DtRaw {
-  unsigned short v[4];
+// dt' of this lane's four tokens (4l .. 4l+3) of one chunk, 0 past the run.
+struct DtQuad {
+  float v[4];
 };
+// dt' = softplus(dt + dt_bias) of every (row, head), transposed to [head][row]
+// so that a chunk's 128 values of one head are contiguous. 32 x 32 tiles.
+__global__ void __launch_bounds__(256) dt_prime_kernel(const __nv_bfloat16* __restrict__ dt, const float* __restrict__ dt_bias,
+                                                      float* __restrict__ dtp, int rows, int heads) {
+  __shared__ float tile[32][33];
+  const int r0 = blockIdx.x * 32, h0 = blockIdx.y * 32;
+  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
+  for (int k = ty; k < 32; k += 8) {
+    const int r = r0 + k, h = h0 + tx;
+    if (r < rows && h < heads) tile[k][tx] = softplus_f(__bfloat162float(dt[(int64_t)r * heads + h]) + dt_bias[h]);
+  }
+  __syncthreads();
+  for (int k = ty; k < 32; k += 8) {
+    const int h = h0 + k, r = r0 + tx;
+    if (r < rows && h < heads) dtp[(int64_t)h * rows + r] = tile[tx][k];
+  }
+}
 // inclusive warp scan
 __device__ __forceinline__ float warp_incl_sum(float v, int lane) {
 #pragma unroll
@@ -620,37 +632,35 @@ ssd_tc_full(const __grid_constant__ ScanArgs a, const __grid_constant__ CUtensor
     // cumulative decay S and block factors v into dt buffer i % 4 (lane l: tokens
     // 4l .. 4l+3; the buffer last served chunk i-4, whose readers are done once
     // chunk i-3's output is written); then CB = C . B^T (lane 0)
-    // raw bf16 dt bits of chunks i .. i+3, loaded four chunks ahead (the loads stay
-    // in flight until used)
-    auto load_raw = [&](int i) {
-      DtRaw r = {{0, 0, 0, 0}};
+    // dt' of chunks i .. i+3, loaded four chunks ahead (the loads stay in flight until used)
+    const int64_t rows_all = a.tab.cu[a.tab.n];
+    auto load_dtp = [&](int i) {
+      DtQuad r = {{0.f, 0.f, 0.f, 0.f}};
       if (i < n) {
         const int c = ci.c_begin + i, len = min(TQ, ci.T - c * TQ);
+        const float* src = a.dtp + (int64_t)ci.h * rows_all + ci.row0 + (int64_t)c * TQ;
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int t = 4 * lane + e;
-          if (t < len) r.v[e] = reinterpret_cast<const unsigned short*>(a.dt)[(ci.row0 + (int64_t)c * TQ + t) * H + ci.h];
-        }
+        for (int e = 0; e < 4; ++e)
+          if (4 * lane + e < len) r.v[e] = src[4 * lane + e];
       }
       return r;
     };
-    DtRaw r0 = load_raw(0), r1 = load_raw(1), r2 = load_raw(2), r3 = load_raw(3);
+    DtQuad r0 = load_dtp(0), r1 = load_dtp(1), r2 = load_dtp(2), r3 = load_dtp(3);
     int last = -1;
     for (int i = 0; i < n; ++i) {
       if (i >= 3 && !warp_wait(bar(kEpiDone + ((i - 3) & 3)), (uint32_t)(((i - 3) >> 2) & 1), s_abort)) break;
       {
-        const int c = ci.c_begin + i, len = min(TQ, ci.T - c * TQ);
         float dp[4], S[4], run = 0.f;
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          dp[e] = dt_prime(r0.v[e], 4 * lane + e < len, ci.dtb);
+          dp[e] = r0.v[e];
           run -= ci.A2 * dp[e];
           S[e] = run;
         }
         r0 = r1;
         r1 = r2;
         r2 = r3;
-        r3 = load_raw(i + 4);
+        r3 = load_dtp(i + 4);
         const float excl = warp_incl_sum(run, lane) - run;
 #pragma unroll
         for (int e = 0; e < 4; ++e) S[e] += excl;
@@ -939,35 +949,34 @@ ssd_tc_state(const __grid_constant__ ScanArgs a, const __grid_constant__ CUtenso
   } else {
     // =================== dt' and token weights of chunk i into ring slot i % 4
     // (lane l: tokens 4l .. 4l+3); slot i % 4 last served chunk i-4
-    // raw bf16 dt bits of chunks i .. i+3, loaded four chunks ahead
-    auto load_raw = [&](int i) {
-      DtRaw r = {{0, 0, 0, 0}};
+    // dt' of chunks i .. i+3, loaded four chunks ahead
+    const int64_t rows_all = a.tab.cu[a.tab.n];
+    auto load_dtp = [&](int i) {
+      DtQuad r = {{0.f, 0.f, 0.f, 0.f}};
       if (i < n) {
         const int c = ci.c_end - 1 - i, len = min(TQ, ci.T - c * TQ);
+        const float* src = a.dtp + (int64_t)ci.h * rows_all + ci.row0 + (int64_t)c * TQ;
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int t = 4 * lane + e;
-          if (t < len) r.v[e] = reinterpret_cast<const unsigned short*>(a.dt)[(ci.row0 + (int64_t)c * TQ + t) * H + ci.h];
-        }
+        for (int e = 0; e < 4; ++e)
+          if (4 * lane + e < len) r.v[e] = src[4 * lane + e];
       }
       return r;
     };
     float R = 0.f;  // log2 decay from the end of the chunks already read to the segment end
-    DtRaw r0 = load_raw(0), r1 = load_raw(1), r2 = load_raw(2), r3 = load_raw(3);
+    DtQuad r0 = load_dtp(0), r1 = load_dtp(1), r2 = load_dtp(2), r3 = load_dtp(3);
     for (int i = 0; i < n; ++i) {
       if (i >= 4 && !warp_wait(bar(kStXWReady + (i & 3)), p4(i - 4), s_abort)) break;
-      const int c = ci.c_end - 1 - i, len = min(TQ, ci.T - c * TQ);
       float dp[4], S[4], run = 0.f;
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        dp[e] = dt_prime(r0.v[e], 4 * lane + e < len, ci.dtb);
+        dp[e] = r0.v[e];
         run -= ci.A2 * dp[e];
         S[e] = run;
       }
       r0 = r1;
       r1 = r2;
       r2 = r3;
-      r3 = load_raw(i + 4);
+      r3 = load_dtp(i + 4);
       const float incl = warp_incl_sum(run, lane);
       const float tot = __shfl_sync(0xffffffffu, incl, 31);
       const float base = R + (tot - (incl - run));  // R + S_end - (S before this lane's tokens)
@@ -1027,6 +1036,13 @@ cudaError_t launch_scan_tc(const ScanArgs& a, cudaStream_t st) {
   CUtensorMap tm;
   memset(&tm, 0, sizeof tm);
   const int use_tma = make_xbc_map(&tm, a) ? 1 : 0;
+  const int rows = a.tab.cu[a.tab.n];
+  if (rows > 0) {
+    const dim3 pg((unsigned)((rows + 31) / 32), (unsigned)((a.heads + 31) / 32));
+    dt_prime_kernel<<<pg, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(a.dt), a.dt_bias, a.dtp, rows, a.heads);
+    const cudaError_t e0 = cudaGetLastError();
+    if (e0 != cudaSuccess) return e0;
+  }
   const dim3 grid((unsigned)segs, (unsigned)a.heads);
   bool segmented = false;
   for (int i = 0; i < a.tab.n; ++i) segmented |= (a.tab.tile[i + 1] - a.tab.tile[i]) > 1;
