@@ -60,7 +60,7 @@ def scan_bytes(T, d: W.Dims, act_b=2, state_rw=1):
     return T * (d.conv_dim + d.heads + d.d_inner) * act_b + state_rw * d.heads * d.headdim * d.d_state * 4
 
 
-def scan_flops(T, d: W.Dims, Q=64):
+def scan_flops(T, d: W.Dims, Q=128):
     per_tok = d.heads * 2 * (Q * d.headdim + 2 * d.headdim * d.d_state) + 2 * d.ngroups * Q * d.d_state
     return T * per_tok
 
@@ -382,7 +382,7 @@ def run_ours(args, rank, world, local_rank):
         "data": "synthetic (seeded N(0,1) activations, workload distributions)",
         "config": {"workload": WORKLOAD if T == TOKENS else WORKLOAD.replace(str(TOKENS), str(T)), "tokens": T, "heads": d.heads, "headdim": d.headdim,
                    "d_state": d.d_state, "ngroups": d.ngroups, "conv_kernel": d.conv_kernel,
-                   "decode_tail_steps": DECODE_TAIL, "chunk": 64,
+                   "decode_tail_steps": DECODE_TAIL, "chunk": 128,
                    "l2": "inputs larger than L2 (no flush)", "parallelism": f"replicas x{world}"},
         "prefill_ms": t_prefill,
         "decode_tail_us_per_step": t_tail * 1e3 / DECODE_TAIL,
