@@ -9,8 +9,10 @@
 //
 // Layout and work split: every thread owns one 16-byte channel vector (8 bf16
 // or 4 fp32 channels) over a tile of kRows consecutive rows of ONE sequence.
-// Tiles never straddle sequences (the host numbers tiles per sequence), so a
-// thread keeps the kernel-1 previous inputs in registers as a sliding window.
+// Tiles never straddle sequences (the host numbers tiles per sequence). The
+// tile's rows and the kernel-1 rows before it are copied asynchronously into
+// the thread's own shared-memory slots, so four CTAs per SM keep enough loads
+// in flight to stream at HBM speed.
 // Only tile 0 of a sequence reads the slot (kRows >= kernel-1), and that same
 // thread writes the new history for its channels at the end: no other thread
 // touches those slot bytes, so no ordering between CTAs is needed. A
@@ -33,10 +35,16 @@
 namespace mamba2 {
 
 template <typename T, int K>
-__global__ void __launch_bounds__(kConvThreads, 2)
+__global__ void __launch_bounds__(kConvThreads, 4)
 conv1d_silu_kernel(const __grid_constant__ ConvArgs a) {
   constexpr int V = Vec16<T>::n;
   constexpr int H = K - 1;  // history rows
+  constexpr int R = H + kConvRows;
+  // raw conv inputs of this thread, u[q0 - H .. q0 + kConvRows - 1], one 16-byte
+  // vector per row: [row][thread], so a warp's reads of one row are 512
+  // contiguous bytes. Copied asynchronously: the thread holds no registers for
+  // them while they are in flight (four CTAs per SM keep the loads deep).
+  __shared__ __align__(16) uint4 sm_rows[R][kConvThreads];
   const int nvec = a.conv_dim / V;
   const int64_t item = (int64_t)blockIdx.x * kConvThreads + threadIdx.x;
   const int64_t total = (int64_t)a.tab.tile[a.tab.n] * nvec;
@@ -55,9 +63,31 @@ conv1d_silu_kernel(const __grid_constant__ ConvArgs a) {
   const T* x = static_cast<const T*>(a.x);
   T* dst = static_cast<T*>(a.dst);
   T* cst = static_cast<T*>(a.conv_state);
+  const int t = threadIdx.x;
 
-  // taps and bias for this thread's channels (16-byte loads: V*K floats are
-  // contiguous and 16-byte aligned since V*4 bytes is)
+  // the H window rows before the tile (zeros for a fresh slot), then the tile's rows
+#pragma unroll
+  for (int i = 0; i < H; ++i) {
+    const int pos = q0 - H + i;
+    const T* src = pos >= 0 ? x + (int64_t)(row0 + pos) * a.conv_dim + c0
+                            : cst + slot_base + (int64_t)(H + pos) * a.conv_dim + c0;
+    const uint32_t d = (uint32_t)__cvta_generic_to_shared(&sm_rows[i][t]);
+    // a fresh slot's history is zeros: a zero-byte copy (source in the slot row, never read)
+    const bool real = pos >= 0 || !fresh;
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(d), "l"(real ? src : cst + slot_base + c0),
+                 "r"(real ? 16 : 0));
+  }
+#pragma unroll
+  for (int r = 0; r < kConvRows; ++r) {
+    if (r < nrows) {
+      const uint32_t d = (uint32_t)__cvta_generic_to_shared(&sm_rows[H + r][t]);
+      asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(d), "l"(x + (int64_t)(row0 + q0 + r) * a.conv_dim + c0));
+    }
+  }
+  asm volatile("cp.async.commit_group;\n" ::: "memory");
+
+  // taps and bias for this thread's channels, while the rows are in flight
+  // (16-byte loads: V*K floats are contiguous and 16-byte aligned since V*4 bytes is)
   float w[K][V], b[V];
   {
     const float4* wp = reinterpret_cast<const float4*>(a.weight + (int64_t)c0 * K);
@@ -75,49 +105,25 @@ conv1d_silu_kernel(const __grid_constant__ ConvArgs a) {
       b[4 * q] = f.x; b[4 * q + 1] = f.y; b[4 * q + 2] = f.z; b[4 * q + 3] = f.w;
     }
   }
+  asm volatile("cp.async.wait_group 0;\n" ::: "memory");  // this thread's own rows (it reads no other's)
 
-  // raw conv inputs u[q0 .. q0 + H + kConvRows - 1] (positions q0 - H ..): the
-  // H window rows before the tile, then the tile's rows; tap k of tile row r is
-  // rows[r + k]. Loads first, then the K-tap dot products.
-  uint4 rows[H + kConvRows];
-#pragma unroll
-  for (int i = 0; i < H; ++i) {
-    const int pos = q0 - H + i;
-    if (pos >= 0) {
-      rows[i] = *reinterpret_cast<const uint4*>(x + (int64_t)(row0 + pos) * a.conv_dim + c0);
-    } else if (fresh) {
-      rows[i] = make_uint4(0u, 0u, 0u, 0u);
-    } else {
-      rows[i] = *reinterpret_cast<const uint4*>(cst + slot_base + (int64_t)(H + pos) * a.conv_dim + c0);
-    }
-  }
-#pragma unroll
-  for (int r = 0; r < kConvRows; ++r)
-    if (r < nrows)
-      rows[H + r] = *reinterpret_cast<const uint4*>(x + (int64_t)(row0 + q0 + r) * a.conv_dim + c0);
-  // unpack each row once; tap k of tile row r is u[r + k]
-  float u[H + kConvRows][V];
-#pragma unroll
-  for (int i = 0; i < H; ++i) Vec16<T>::load(reinterpret_cast<const T*>(&rows[i]), u[i]);
+  // tile row r: silu(bias + sum_k w[:, k] u[r + k]), each tap unpacked from smem
 #pragma unroll
   for (int r = 0; r < kConvRows; ++r) {
     if (r < nrows) {
-      Vec16<T>::load(reinterpret_cast<const T*>(&rows[H + r]), u[H + r]);
-      float out[V];
+      float acc[V];
 #pragma unroll
-      for (int j = 0; j < V; ++j) {
-        float wk[K], uk[K];
+      for (int j = 0; j < V; ++j) acc[j] = b[j];
 #pragma unroll
-        for (int k = 0; k < K; ++k) {
-          wk[k] = w[k][j];
-          uk[k] = u[r + k][j];
-        }
-        float acc = b[j];
+      for (int k = 0; k < K; ++k) {
+        float u[V];
+        Vec16<T>::load(reinterpret_cast<const T*>(&sm_rows[r + k][t]), u);
 #pragma unroll
-        for (int k = 0; k < K; ++k) acc = fmaf(wk[k], uk[k], acc);
-        out[j] = silu_f(acc);
+        for (int j = 0; j < V; ++j) acc[j] = fmaf(w[k][j], u[j], acc[j]);
       }
-      Vec16<T>::store(dst + (int64_t)(row0 + q0 + r) * a.conv_dim + c0, out);
+#pragma unroll
+      for (int j = 0; j < V; ++j) acc[j] = silu_f(acc[j]);
+      Vec16<T>::store(dst + (int64_t)(row0 + q0 + r) * a.conv_dim + c0, acc);
     }
   }
 
@@ -145,6 +151,10 @@ static cudaError_t launch_conv_t(const ConvArgs& a, cudaStream_t st) {
   const int64_t total = (int64_t)a.tab.tile[a.tab.n] * nvec;
   if (total == 0) return cudaSuccess;
   const int64_t blocks = (total + kConvThreads - 1) / kConvThreads;
+  // four CTAs of 40-44 KB static shared memory per SM
+  cudaError_t e = cudaFuncSetAttribute(conv1d_silu_kernel<T, K>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                       (int)cudaSharedmemCarveoutMaxShared);
+  if (e != cudaSuccess) return e;
   conv1d_silu_kernel<T, K><<<(unsigned)blocks, kConvThreads, 0, st>>>(a);
   return cudaGetLastError();
 }
