@@ -19,12 +19,13 @@
 // Full pass: one CTA per (sequence segment, head), 20 warps in fixed roles
 // that hand work to each other through mbarriers (no CTA-wide barrier in the
 // chunk loop):
-//   warps 0-7   M(i) = CB o decay (+ D on the diagonal), bf16 hi + lo written
-//               over CB in TMEM (TMEM lane t = token row t)
-//   warps 8-15  per chunk i: X o w (bf16 hi + lo); the state through chunk
-//               i-1 (H = exp(total) H + dH, fp32 in registers, bf16 copy of
-//               H^T to smem; TMEM lane n = state row n); the output of chunk
-//               i-1, y = Y + exp(s_t) Yoff, stored from registers
+//   warps 0-7   X o w of chunk i (bf16 hi + lo), then M(i) = CB o decay (+ D
+//               on the diagonal), bf16 hi + lo written over CB in TMEM (TMEM
+//               lane t = token row t)
+//   warps 8-15  per chunk i: the state through chunk i-1 (H = exp(total) H +
+//               dH, fp32 in registers, bf16 copy of H^T to smem; TMEM lane n =
+//               state row n), beside the other group's X o w; the output of
+//               chunk i-1, y = Y + exp(s_t) Yoff, stored from registers
 //               (two warps per TMEM lane quarter in each group, so M and the
 //               state / output work run side by side on every sub-partition)
 //   warp 16     CB = C . B^T                M=128 N=128 K=128; before it, the
@@ -93,9 +94,9 @@ constexpr int kDtRing = 4;                              // dt buffers (chunk i i
 constexpr uint32_t kOffDt = kOffHT + TN * TP * 2;      // kDtRing buffers of {s2, dt', v}[TQ] floats
 constexpr uint32_t kDtBuf = 3 * TQ * 4;
 constexpr uint32_t kOffBar = kOffDt + kDtRing * kDtBuf;
-enum FullBar : int {  // + chunk % 2 (+ chunk % 4 for kEpiDone)
+enum FullBar : int {  // + chunk % 2 (+ chunk % 4 for kDtReady and kEpiDone)
   kFullCB = 0, kFullX = 2, kCBDone = 4, kYoDone = 6, kDHDone = 8, kYdDone = 10,
-  kHDone = 12, kXWReady = 14, kMReady = 16, kDtReady = 18, kEpiDone = 20, kNumFullBars = 24
+  kHDone = 12, kXWReady = 14, kMReady = 16, kDtReady = 18, kEpiDone = 22, kNumFullBars = 26
 };
 constexpr uint32_t kOffMisc = kOffBar + 8 * kNumFullBars;  // TMEM base, abort flag
 constexpr uint32_t kFullSmem = kOffMisc + 16 + 1024;        // + slack to align the base to 1024
@@ -165,13 +166,20 @@ __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
                : "=r"(done) : "r"(bar), "r"(parity), "r"(kSuspendNs) : "memory");
   return done != 0;
 }
-// (The waits are out of line: one copy of the polling loop instead of one per
-// call site keeps the kernels' hot code small in the instruction cache.)
+// (The polling loop is out of line: one copy instead of one per call site keeps
+// the kernels' hot code small in the instruction cache.)
+// Non-blocking test of the phase (no suspension: returns at once either way).
+__device__ __forceinline__ bool mbar_done(uint32_t bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile("{\n.reg .pred P;\nmbarrier.test_wait.parity.shared::cta.b64 P, [%1], %2;\nselp.u32 %0, 1, 0, P;\n}\n"
+               : "=r"(done) : "r"(bar), "r"(parity) : "memory");
+  return done != 0;
+}
 // Bounded wait for the completion of the barrier phase with this parity; after
 // a few rounds the thread sleeps between polls, so waiting warps leave the
 // issue slots to the working ones. Gives up when the CTA's abort flag is
 // raised, and raises it itself on a timeout.
-__device__ __noinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile uint32_t* abort_flag) {
+__device__ __noinline__ bool wait_bar_slow(uint32_t bar, uint32_t parity, volatile uint32_t* abort_flag) {
   for (uint32_t it = 0; it < kWaitLimit; ++it) {
     if (mbar_test(bar, parity)) return true;
     if (*abort_flag) return false;
@@ -180,9 +188,15 @@ __device__ __noinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile ui
   *abort_flag = 1u;
   return false;
 }
+// A phase that has already completed costs one non-blocking test: a suspending
+// try_wait takes hundreds of cycles even then, and most waits here find their
+// phase complete.
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile uint32_t* abort_flag) {
+  return mbar_done(bar, parity) || wait_bar_slow(bar, parity, abort_flag);
+}
 // The same, decided for the whole warp (every lane waits; all get the same
 // answer), for warps whose lanes then run .sync.aligned or __syncwarp code.
-__device__ __noinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile uint32_t* abort_flag) {
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile uint32_t* abort_flag) {
   return __all_sync(0xffffffffu, wait_bar(bar, parity, abort_flag));
 }
 // Bounded wait that ignores the abort flag (draining work already issued).
@@ -382,9 +396,11 @@ ssd_tc_full(const __grid_constant__ ScanArgs a, const __grid_constant__ CUtensor
       mbar_init(bar(kHDone + b), kMathWarps / 2);
       mbar_init(bar(kXWReady + b), kMathWarps / 2);
       mbar_init(bar(kMReady + b), kMathWarps / 2);
-      mbar_init(bar(kDtReady + b), 1);
     }
-    for (int b = 0; b < 4; ++b) mbar_init(bar(kEpiDone + b), kMathWarps / 2);
+    for (int b = 0; b < 4; ++b) {
+      mbar_init(bar(kDtReady + b), 1);
+      mbar_init(bar(kEpiDone + b), kMathWarps / 2);
+    }
     *s_abort = 0u;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -424,8 +440,41 @@ ssd_tc_full(const __grid_constant__ ScanArgs a, const __grid_constant__ CUtensor
       // the diagonal block exponentiates each pair.
       for (int i = 0; i < n; ++i) {
         if (*s_abort) break;
-        const bool ok = warp_wait(bar(kDtReady + (i & 1)), par(i), s_abort) &&
-                        warp_wait(bar(kCBDone + (i & 1)), par(i), s_abort);
+        // (b) X o w of chunk i (bf16 hi + lo), w_j = exp(s_end - s_j) dt'_j. Work items
+        // (row j, 16-column group g): lane quarter 0 takes groups 0 and 1, quarters 1
+        // and 2 one group each, quarter 3 (the heaviest share of M) none. Runs beside
+        // the other group's state update: both only need the previous dH.
+        bool xok = warp_wait(bar(kDtReady + (i & 3)), (uint32_t)((i >> 2) & 1), s_abort) &&
+                   warp_wait(bar(kFullX + (i & 1)), par(i), s_abort);
+        if (xok && i > 0) xok = warp_wait(bar(kDHDone + ((i - 1) & 1)), par(i - 1), s_abort);  // X o w buffer read
+        if (xok && qrt < 3) {
+          const float* D0 = dtbuf(i);
+          const unsigned char* xt = smem + (uint32_t)(i & 1) * kStage + kTileC + kTileB;
+#pragma unroll 1
+          for (int it = 0; it < (qrt == 0 ? 4 : 2); ++it) {
+            const int xr = half * 32 + lane + 64 * (it & 1);
+            const int g = qrt == 0 ? (it >> 1) : qrt + 1;
+            const float w = ex2(D0[TQ - 1] - D0[xr]) * D0[TQ + xr];
+#pragma unroll
+            for (int q = 0; q < 2; ++q) {
+              const uint32_t o = tile_off(xr, 16 * g + 8 * q, TQ);
+              const uint4 xv = *reinterpret_cast<const uint4*>(xt + o);
+              const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
+              uint32_t hi[4], lo[4];
+#pragma unroll
+              for (int e = 0; e < 4; ++e)
+                split2(__uint_as_float(xw[e] << 16) * w, __uint_as_float(xw[e] & 0xffff0000u) * w, hi[e], lo[e]);
+              *reinterpret_cast<uint4*>(smem + kOffXWhi + o) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+              *reinterpret_cast<uint4*>(smem + kOffXWlo + o) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+            }
+          }
+        }
+        fence_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(kXWReady + (i & 1)));
+
+        // (c) M(i)
+        const bool ok = xok && warp_wait(bar(kCBDone + (i & 1)), par(i), s_abort);
         if (ok) {
           tc_fence_after();
           const float* D0 = dtbuf(i);
@@ -526,9 +575,6 @@ ssd_tc_full(const __grid_constant__ ScanArgs a, const __grid_constant__ CUtensor
           *reinterpret_cast<uint4*>(smem + kOffHT + tile_off(row, pc0 + 8 * q, TN)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
         }
       };
-      // X o w work items: row xr, 16-column groups g0 and g0 + 2
-      const int xu = (warp - kMathWarps / 2) * 32 + lane;
-      const int xr = xu & 127, g0 = xu >> 7;
 
       bool live = true;
       for (int i = 0; i <= n; ++i) {
@@ -537,35 +583,11 @@ ssd_tc_full(const __grid_constant__ ScanArgs a, const __grid_constant__ CUtensor
           break;
         }
         if (i < n) {
-          // (b) X o w of chunk i (bf16 hi + lo), w_j = exp(s_end - s_j) dt'_j
-          bool ok = warp_wait(bar(kDtReady + (i & 1)), par(i), s_abort) && warp_wait(bar(kFullX + (i & 1)), par(i), s_abort);
-          if (ok && i > 0) ok = warp_wait(bar(kDHDone + ((i - 1) & 1)), par(i - 1), s_abort);  // X o w buffer read
-          if (ok) {
-            const float* D0 = dtbuf(i);
-            const float w = ex2(D0[TQ - 1] - D0[xr]) * D0[TQ + xr];
-            const unsigned char* xt = smem + (uint32_t)(i & 1) * kStage + kTileC + kTileB;
-#pragma unroll 1
-            for (int gi = 0; gi < 4; ++gi) {  // 8-column pieces of groups g0 and g0 + 2
-              {
-                const uint32_t o = tile_off(xr, 16 * (g0 + 2 * (gi >> 1)) + 8 * (gi & 1), TQ);
-                const uint4 xv = *reinterpret_cast<const uint4*>(xt + o);
-                const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
-                uint32_t hi[4], lo[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e)
-                  split2(__uint_as_float(xw[e] << 16) * w, __uint_as_float(xw[e] & 0xffff0000u) * w, hi[e], lo[e]);
-                *reinterpret_cast<uint4*>(smem + kOffXWhi + o) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-                *reinterpret_cast<uint4*>(smem + kOffXWlo + o) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-              }
-            }
-          }
-          fence_async_smem();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(bar(kXWReady + (i & 1)));
-
+          bool ok;
           // (a) state through chunk i-1 -> H^T for C . H^T(i); releases the dH accumulator
           if (i > 0) {
-            ok = warp_wait(bar(kDHDone + ((i - 1) & 1)), par(i - 1), s_abort) &&
+            ok = warp_wait(bar(kDtReady + ((i - 1) & 3)), (uint32_t)(((i - 1) >> 2) & 1), s_abort) &&
+                 warp_wait(bar(kDHDone + ((i - 1) & 1)), par(i - 1), s_abort) &&
                  warp_wait(bar(kYoDone + ((i - 1) & 1)), par(i - 1), s_abort);  // C . H^T(i-1) has read H^T
             if (ok) {
               tc_fence_after();
@@ -584,7 +606,9 @@ ssd_tc_full(const __grid_constant__ ScanArgs a, const __grid_constant__ CUtensor
           // (d) output of chunk j = i-1: y = M . X + exp(s_t) C . H^T, straight to HBM
           const int j = i - 1;
           bool ok = warp_wait(bar(kYdDone + (j & 1)), par(j), s_abort);
-          if (i == n) ok = ok && warp_wait(bar(kYoDone + (j & 1)), par(j), s_abort);
+          if (i == n)  // the state step of this iteration (which waits these) does not run
+            ok = ok && warp_wait(bar(kYoDone + (j & 1)), par(j), s_abort) &&
+                 warp_wait(bar(kDtReady + (j & 3)), (uint32_t)((j >> 2) & 1), s_abort);
           if (ok) {
             tc_fence_after();
             const float et = ex2(dtbuf(j)[row]);
@@ -671,7 +695,7 @@ ssd_tc_full(const __grid_constant__ ScanArgs a, const __grid_constant__ CUtensor
         *reinterpret_cast<float4*>(D0 + 2 * TQ + 4 * lane) =
             make_float4(ex2(Se - S[0]) * dp[0], ex2(Se - S[1]) * dp[1], ex2(Se - S[2]) * dp[2], ex2(Se - S[3]) * dp[3]);
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar(kDtReady + (i & 1)));
+        if (lane == 0) mbar_arrive(bar(kDtReady + (i & 3)));
       }
       if (!warp_wait(bar(kFullCB + (i & 1)), par(i), s_abort)) break;
       if (i >= 2 && !warp_wait(bar(kYdDone + (i & 1)), par(i - 2), s_abort)) break;  // M(i-2) consumed
