@@ -444,9 +444,11 @@ ssd_tc_full(const __grid_constant__ ScanArgs a, const __grid_constant__ CUtensor
         // (row j, 16-column group g): lane quarter 0 takes groups 0 and 1, quarters 1
         // and 2 one group each, quarter 3 (the heaviest share of M) none. Runs beside
         // the other group's state update: both only need the previous dH.
-        bool xok = warp_wait(bar(kDtReady + (i & 3)), (uint32_t)((i >> 2) & 1), s_abort) &&
-                   warp_wait(bar(kFullX + (i & 1)), par(i), s_abort);
-        if (xok && i > 0) xok = warp_wait(bar(kDHDone + ((i - 1) & 1)), par(i - 1), s_abort);  // X o w buffer read
+        bool xok = warp_wait(bar(kDtReady + (i & 3)), (uint32_t)((i >> 2) & 1), s_abort);
+        if (qrt < 3) {  // quarter 3 forms no X o w: M needs only its dt and CB
+          if (xok) xok = warp_wait(bar(kFullX + (i & 1)), par(i), s_abort);
+          if (xok && i > 0) xok = warp_wait(bar(kDHDone + ((i - 1) & 1)), par(i - 1), s_abort);  // X o w buffer read
+        }
         if (xok && qrt < 3) {
           const float* D0 = dtbuf(i);
           const unsigned char* xt = smem + (uint32_t)(i & 1) * kStage + kTileC + kTileB;
