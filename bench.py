@@ -18,6 +18,7 @@ workload.
 from __future__ import annotations
 
 import argparse
+import hashlib
 import json
 import os
 import statistics
@@ -326,10 +327,7 @@ def run_ours(args, rank, world, local_rank):
     kern["scan"]["frac_tensor_sustained"] = kern["scan"]["TFLOP/s"] / tf_sus
     dominant = max(("conv", "scan", "norm"), key=lambda n: kern[n]["ms"])
     dk = kern[dominant]
-    prof = ROOT / "profiles" / "traffic.json"
-    traffic = None
-    if prof.exists():
-        traffic = json.loads(prof.read_text()).get(dominant)
+    traffic = measured_traffic(dominant, T)
 
     # batched decode (256 sequences x 128 steps), timed separately
     dec_us, dec_n, dec_bytes, dec_steps = time_decode_batch(dev, reps=max(2, args.steps // 100), warm=1)
@@ -441,6 +439,27 @@ def run_reference(args):
                          "sample": f"prefill of the first {sample} of the {TOKENS} tokens per step"},
         "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
+
+
+KERNEL_SOURCES = {"conv": "conv1d.cu", "scan": "scan_tc.cu", "norm": "norm.cu"}
+
+
+def kernel_source_sha(name: str) -> str:
+    src = ROOT / "selective_scan_gb300" / "csrc" / KERNEL_SOURCES[name]
+    return hashlib.sha256(src.read_bytes()).hexdigest()
+
+
+def measured_traffic(name: str, tokens: int):
+    """DRAM bytes of one launch of `name` from the committed ncu capture, scaled
+    to `tokens` (traffic grows with the rows); None when the kernel's source has
+    changed since the counters were taken."""
+    prof = ROOT / "profiles" / "traffic.json"
+    if not prof.exists():
+        return None
+    rec = json.loads(prof.read_text())
+    if name not in rec or rec.get("_sha256", {}).get(name) != kernel_source_sha(name):
+        return None
+    return int(round(rec[name] * tokens / rec["_tokens"]))
 
 
 def main():
