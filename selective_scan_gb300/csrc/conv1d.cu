@@ -7,19 +7,24 @@
 // fresh) followed by the run's inputs; the slot then holds u's last kernel-1
 // rows.
 //
-// Layout and work split: every thread owns one 16-byte channel vector (8 bf16
-// or 4 fp32 channels) over a tile of kRows consecutive rows of ONE sequence.
-// Tiles never straddle sequences (the host numbers tiles per sequence). The
-// tile's rows and the kernel-1 rows before it are copied asynchronously into
-// the thread's own shared-memory slots, so four CTAs per SM keep enough loads
-// in flight to stream at HBM speed.
+// Layout and work split: a CTA covers 32 consecutive 16-byte channel vectors
+// (8 bf16 or 4 fp32 channels each) over kConvThreads / 32 consecutive tiles of
+// kConvRows rows; lane l of warp w owns channel vector l of tile w. Tiles never
+// straddle sequences (the host numbers tiles per sequence). A warp copies its
+// tile's rows asynchronously into its own shared-memory slots (a row of the
+// warp's 32 vectors is 512 contiguous bytes); the kernel-1 window rows before a
+// tile are the previous warp's last rows when that warp holds the previous tile
+// of the same sequence, else they are copied too (from the input, or from the
+// slot at a sequence start). The taps and bias of the CTA's channels are copied
+// once into shared memory beside the rows, so every input byte and weight byte
+// crosses from L2 once per CTA.
 // Only tile 0 of a sequence reads the slot (kRows >= kernel-1), and that same
 // thread writes the new history for its channels at the end: no other thread
 // touches those slot bytes, so no ordering between CTAs is needed. A
 // zero-length sequence still gets one (empty) tile for its slot update.
 //
-// Memory: each input row is read once by its tile plus kernel-1 window rows
-// read again by the next tile (L2 hits); each output row written once. The
+// Memory: each input row is read once (plus kernel-1 window rows at the first
+// tile of a CTA or of a sequence, L2 hits); each output row written once. The
 // kernel is HBM-bound: 2 * conv_dim * sizeof(act) bytes per row.
 //
 // Rounding: outputs are computed in fp32 (taps in order, fast exponential and
@@ -34,79 +39,96 @@
 
 namespace mamba2 {
 
+constexpr int kConvTilesPerCta = kConvThreads / 32;  // one tile per warp
+
 template <typename T, int K>
-__global__ void __launch_bounds__(kConvThreads, 4)
+__global__ void __launch_bounds__(kConvThreads, 3)
 conv1d_silu_kernel(const __grid_constant__ ConvArgs a) {
   constexpr int V = Vec16<T>::n;
   constexpr int H = K - 1;  // history rows
   constexpr int R = H + kConvRows;
+  constexpr int kWq = V * K / 4 + V / 4;  // float4s of taps and bias per channel vector
+  static_assert(H <= kConvRows, "the window rows must fit in one tile");
   // raw conv inputs of this thread, u[q0 - H .. q0 + kConvRows - 1], one 16-byte
-  // vector per row: [row][thread], so a warp's reads of one row are 512
-  // contiguous bytes. Copied asynchronously: the thread holds no registers for
-  // them while they are in flight (four CTAs per SM keep the loads deep).
+  // vector per row: [row][thread]; then the taps (V*K floats) and bias (V floats)
+  // of the CTA's 32 channel vectors, [float4 q][vector] (a warp's reads of one q
+  // are 512 contiguous bytes)
   __shared__ __align__(16) uint4 sm_rows[R][kConvThreads];
+  __shared__ __align__(16) float4 sm_w[kWq][32];
   const int nvec = a.conv_dim / V;
-  const int64_t item = (int64_t)blockIdx.x * kConvThreads + threadIdx.x;
-  const int64_t total = (int64_t)a.tab.tile[a.tab.n] * nvec;
-  if (item >= total) return;
-  const int tile = (int)(item / nvec);
-  const int cv = (int)(item - (int64_t)tile * nvec);
-  const int s = find_tile_seq(a.tab, tile);
+  const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
+  const int ntiles = a.tab.tile[a.tab.n];
+  const int tile = blockIdx.x * kConvTilesPerCta + warp;
+  const int cv = blockIdx.y * 32 + lane;
+  const bool active = tile < ntiles && cv < nvec;  // (no early return: the CTA synchronises below)
+  const int s = active ? find_tile_seq(a.tab, tile) : 0;
   const int local_tile = tile - a.tab.tile[s];
   const int row0 = a.tab.cu[s];
   const int T_len = a.tab.cu[s + 1] - row0;
   const int q0 = local_tile * kConvRows;
   const int nrows = min(kConvRows, T_len - q0);
-  const bool fresh = seq_fresh(a.tab, s);
-  const int64_t slot_base = (int64_t)seq_slot(a.tab, s) * H * a.conv_dim;
   const int c0 = cv * V;
   const T* x = static_cast<const T*>(a.x);
   T* dst = static_cast<T*>(a.dst);
   T* cst = static_cast<T*>(a.conv_state);
-  const int t = threadIdx.x;
+  // the window rows are the previous warp's last rows (its tile is this sequence's previous, whole tile)
+  const bool prev_rows = warp > 0 && local_tile > 0;
 
-  // the H window rows before the tile (zeros for a fresh slot), then the tile's rows
-#pragma unroll
-  for (int i = 0; i < H; ++i) {
-    const int pos = q0 - H + i;
-    const T* src = pos >= 0 ? x + (int64_t)(row0 + pos) * a.conv_dim + c0
-                            : cst + slot_base + (int64_t)(H + pos) * a.conv_dim + c0;
-    const uint32_t d = (uint32_t)__cvta_generic_to_shared(&sm_rows[i][t]);
-    // a fresh slot's history is zeros: a zero-byte copy (source in the slot row, never read)
-    const bool real = pos >= 0 || !fresh;
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(d), "l"(real ? src : cst + slot_base + c0),
-                 "r"(real ? 16 : 0));
-  }
-#pragma unroll
-  for (int r = 0; r < kConvRows; ++r) {
-    if (r < nrows) {
-      const uint32_t d = (uint32_t)__cvta_generic_to_shared(&sm_rows[H + r][t]);
-      asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(d), "l"(x + (int64_t)(row0 + q0 + r) * a.conv_dim + c0));
+  // taps and bias of the CTA's channel vectors (vectors past nvec are not copied)
+  for (int i = t; i < 32 * kWq; i += kConvThreads) {
+    const int v = i / kWq, q = i - v * kWq;
+    const int cvv = blockIdx.y * 32 + v;
+    if (cvv < nvec) {
+      const float* src = q < V * K / 4 ? a.weight + (int64_t)cvv * V * K + 4 * q : a.bias + (int64_t)cvv * V + 4 * (q - V * K / 4);
+      asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"((uint32_t)__cvta_generic_to_shared(&sm_w[q][v])), "l"(src));
     }
   }
-  asm volatile("cp.async.commit_group;\n" ::: "memory");
+  if (active) {
+    if (!prev_rows) {
+      const bool fresh = seq_fresh(a.tab, s);
+      const int64_t slot_base = (int64_t)seq_slot(a.tab, s) * H * a.conv_dim;
+      // the H window rows before the tile (zeros for a fresh slot)
+#pragma unroll
+      for (int i = 0; i < H; ++i) {
+        const int pos = q0 - H + i;
+        const T* src = pos >= 0 ? x + (int64_t)(row0 + pos) * a.conv_dim + c0
+                                : cst + slot_base + (int64_t)(H + pos) * a.conv_dim + c0;
+        const uint32_t d = (uint32_t)__cvta_generic_to_shared(&sm_rows[i][t]);
+        // a fresh slot's history is zeros: a zero-byte copy (source in the slot row, never read)
+        const bool real = pos >= 0 || !fresh;
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(d), "l"(real ? src : cst + slot_base + c0),
+                     "r"(real ? 16 : 0));
+      }
+    }
+#pragma unroll
+    for (int r = 0; r < kConvRows; ++r) {
+      if (r < nrows) {
+        const uint32_t d = (uint32_t)__cvta_generic_to_shared(&sm_rows[H + r][t]);
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(d), "l"(x + (int64_t)(row0 + q0 + r) * a.conv_dim + c0));
+      }
+    }
+  }
+  asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;\n" ::: "memory");
+  __syncthreads();  // the weights and the previous warp's rows are in shared memory
+  if (!active) return;
 
-  // taps and bias for this thread's channels, while the rows are in flight
-  // (16-byte loads: V*K floats are contiguous and 16-byte aligned since V*4 bytes is)
   float w[K][V], b[V];
-  {
-    const float4* wp = reinterpret_cast<const float4*>(a.weight + (int64_t)c0 * K);
 #pragma unroll
-    for (int q = 0; q < V * K / 4; ++q) {
-      const float4 f = __ldg(wp + q);
-      const float e[4] = {f.x, f.y, f.z, f.w};
+  for (int q = 0; q < V * K / 4; ++q) {
+    const float4 f = sm_w[q][lane];
+    const float e[4] = {f.x, f.y, f.z, f.w};
 #pragma unroll
-      for (int i = 0; i < 4; ++i) w[(4 * q + i) % K][(4 * q + i) / K] = e[i];
-    }
-    const float4* bp = reinterpret_cast<const float4*>(a.bias + c0);
-#pragma unroll
-    for (int q = 0; q < V / 4; ++q) {
-      const float4 f = __ldg(bp + q);
-      b[4 * q] = f.x; b[4 * q + 1] = f.y; b[4 * q + 2] = f.z; b[4 * q + 3] = f.w;
-    }
+    for (int i = 0; i < 4; ++i) w[(4 * q + i) % K][(4 * q + i) / K] = e[i];
   }
-  asm volatile("cp.async.wait_group 0;\n" ::: "memory");  // this thread's own rows (it reads no other's)
+#pragma unroll
+  for (int q = 0; q < V / 4; ++q) {
+    const float4 f = sm_w[V * K / 4 + q][lane];
+    b[4 * q] = f.x; b[4 * q + 1] = f.y; b[4 * q + 2] = f.z; b[4 * q + 3] = f.w;
+  }
 
+  // window row i < H of this tile: win[i * kConvThreads], the thread's own slot or
+  // the previous warp's row kConvRows - H + i (same row stride)
+  const uint4* win = prev_rows ? &sm_rows[kConvRows][t - 32] : &sm_rows[0][t];
   // tile row r: silu(bias + sum_k w[:, k] u[r + k]), each tap unpacked from smem
 #pragma unroll
   for (int r = 0; r < kConvRows; ++r) {
@@ -117,7 +139,8 @@ conv1d_silu_kernel(const __grid_constant__ ConvArgs a) {
 #pragma unroll
       for (int k = 0; k < K; ++k) {
         float u[V];
-        Vec16<T>::load(reinterpret_cast<const T*>(&sm_rows[r + k][t]), u);
+        const uint4* src = r + k < H ? win + (r + k) * kConvThreads : &sm_rows[r + k][t];
+        Vec16<T>::load(reinterpret_cast<const T*>(src), u);
 #pragma unroll
         for (int j = 0; j < V; ++j) acc[j] = fmaf(w[k][j], u[j], acc[j]);
       }
@@ -129,6 +152,8 @@ conv1d_silu_kernel(const __grid_constant__ ConvArgs a) {
 
   // slot update by tile 0: new history = u[T .. T + H - 1] (bit copies)
   if (local_tile == 0) {
+    const bool fresh = seq_fresh(a.tab, s);
+    const int64_t slot_base = (int64_t)seq_slot(a.tab, s) * H * a.conv_dim;
 #pragma unroll
     for (int j = 0; j < H; ++j) {
       const int upos = T_len + j;  // index into u
@@ -148,14 +173,15 @@ conv1d_silu_kernel(const __grid_constant__ ConvArgs a) {
 template <typename T, int K>
 static cudaError_t launch_conv_t(const ConvArgs& a, cudaStream_t st) {
   const int nvec = a.conv_dim / Vec16<T>::n;
-  const int64_t total = (int64_t)a.tab.tile[a.tab.n] * nvec;
-  if (total == 0) return cudaSuccess;
-  const int64_t blocks = (total + kConvThreads - 1) / kConvThreads;
-  // four CTAs of 40-44 KB static shared memory per SM
+  const int ntiles = a.tab.tile[a.tab.n];
+  if (ntiles == 0 || nvec == 0) return cudaSuccess;
+  const dim3 grid((unsigned)((ntiles + kConvTilesPerCta - 1) / kConvTilesPerCta), (unsigned)((nvec + 31) / 32));
+  if (grid.y > 65535u) return cudaErrorInvalidValue;
+  // three CTAs of up to 74 KB static shared memory per SM (14-row tiles)
   cudaError_t e = cudaFuncSetAttribute(conv1d_silu_kernel<T, K>, cudaFuncAttributePreferredSharedMemoryCarveout,
                                        (int)cudaSharedmemCarveoutMaxShared);
   if (e != cudaSuccess) return e;
-  conv1d_silu_kernel<T, K><<<(unsigned)blocks, kConvThreads, 0, st>>>(a);
+  conv1d_silu_kernel<T, K><<<grid, kConvThreads, 0, st>>>(a);
   return cudaGetLastError();
 }
 

@@ -25,7 +25,7 @@ struct SeqTable {
 
 // ---------------------------------------------------------------- conv ----
 constexpr int kConvThreads = 256;
-constexpr int kConvRows = 8;  // rows per work tile (>= kernel - 1)
+constexpr int kConvRows = 14;  // rows per work tile (>= kernel - 1)
 
 struct ConvArgs {
   const void* x;
