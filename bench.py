@@ -155,7 +155,10 @@ class Prefill:
         self.out = torch.empty_like(self.y)
         need = ss.ssd_scan_workspace_bytes(d, b.rows, b.cu_seqlens, b.slots, b.fresh)
         self.ws = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
-        self.scan_launches = 2 if need > 0 else 1
+        # tensor-core scan: the dt' pre-pass, the state pass when a run is cut into
+        # segments (the workspace then holds segment states beyond dt'), the full pass
+        segmented = need > b.rows * d.heads * 4 + 256
+        self.scan_launches = 3 if segmented else 2
         self.dec_x = wl.dec_xBC.to(dev)
         self.dec_z = wl.dec_z.to(dev)
         self.dec_dt = wl.dec_dt.to(dev)
@@ -275,6 +278,7 @@ def cpu_baseline(target_s=12.0):
 
 
 def run_ours(args, rank, world, local_rank):
+    import selective_scan_gb300 as ss
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
     hbm, tf_burst, tf_sus, peak_kind = peaks()
@@ -333,23 +337,21 @@ def run_ours(args, rank, world, local_rank):
     dec_us, dec_n, dec_bytes, dec_steps = time_decode_batch(dev, reps=max(2, args.steps // 100), warm=1)
     dec_gbs = dec_bytes / (dec_us * 1e-6) / 1e9
 
-    # end to end through the public API: pinned host inputs in, output back, every step
-    hx = torch.empty_like(pf.x, device="cpu").pin_memory()
-    hz = torch.empty_like(pf.z, device="cpu").pin_memory()
-    hdt = torch.empty_like(pf.dt, device="cpu").pin_memory()
-    hx.copy_(wl.xBC)
-    hz.copy_(wl.z)
-    hdt.copy_(wl.dt)
-    hout = torch.empty_like(pf.out, device="cpu").pin_memory()
-    dx, dz, ddt = torch.empty_like(pf.x), torch.empty_like(pf.z), torch.empty_like(pf.dt)
+    # end to end through the C ABI with HOST buffers: mamba2_prefill_host copies each
+    # piece's xBC, z and dt in from pinned host memory and its output back, on its own
+    # copy streams overlapping the compute, every step inside the timed region
+    hx = wl.xBC.pin_memory()
+    hz = wl.z.pin_memory()
+    hdt = wl.dt.pin_memory()
+    hout = torch.empty(tuple(pf.out.shape), dtype=pf.out.dtype).pin_memory()
+    cw, cb, A, dtb, Dv, nw = pf.pw
+    e2e_need = ss.prefill_host_workspace_bytes(pf.dims, ss.BF16, args.e2e_piece, batch=pf.batch)
+    e2e_ws = torch.empty(max(e2e_need, 256), dtype=torch.uint8, device=dev)
     e2e_steps = max(3, args.steps // 20)
 
     def e2e_step():
-        dx.copy_(hx, non_blocking=True)
-        dz.copy_(hz, non_blocking=True)
-        ddt.copy_(hdt, non_blocking=True)
-        pf.prefill(x=dx, z=dz, dt=ddt)
-        hout.copy_(pf.out, non_blocking=True)
+        ss.prefill_host(hout, hx, hz, hdt, cw, cb, A, dtb, Dv, nw, wl.params.norm_groups, wl.params.eps, pf.conv,
+                        pf.ssm, pf.dims, piece_rows=args.e2e_piece, workspace=e2e_ws, batch=pf.batch)
 
     e2e_step()
     torch.cuda.synchronize()
@@ -395,7 +397,8 @@ def run_ours(args, rank, world, local_rank):
                    "bytes_per_step": dec_bytes, "steps_timed": dec_steps},
         "e2e": {"value": world * T / (e2e_ms * 1e-3), "unit": "tokens/s",
                 "h2d_bytes_per_step": hx.numel() * 2 + hz.numel() * 2 + hdt.numel() * 2,
-                "d2h_bytes_per_step": hout.numel() * 2},
+                "d2h_bytes_per_step": hout.numel() * 2, "api": "mamba2_prefill_host",
+                "piece_rows": args.e2e_piece},
         "gpu_launches": args.steps * (1 + pf.scan_launches + 1 + DECODE_TAIL),
         "clocks": clk.summary(),
     }
@@ -470,6 +473,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--tokens", type=int, default=TOKENS, help="prefill length (profiling captures use less)")
+    ap.add_argument("--e2e-piece", type=int, default=8192, help="rows per piece of the streamed host prefill")
     args = ap.parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

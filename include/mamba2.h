@@ -7,15 +7,18 @@
  * CausalConv1D, SSMScan and GatedRMSNorm, plus one fused decode step that
  * chains the three for a single token per sequence (the per-token recurrence
  * over conv and SSM cache state that the page "Granite Mamba2 Inference
- * Optimization" names as the decode path). The stateful calls take a
+ * Optimization" names as the decode path), and a prefill that chains the
+ * three ops over activations in host memory, streamed in pieces so the
+ * host-device copies overlap the compute. The stateful calls take a
  * RecurrentBatch: per sequence a run of rows, a state slot and a fresh flag.
  *
  * Conventions shared by every entry point
  * ---------------------------------------
  *  - Device buffers are caller-owned device pointers, row-major and
- *    contiguous, 16-byte aligned. The library allocates no device memory and
- *    keeps no state between calls; only `dst`, the named slots of the state
- *    pools and a caller-provided workspace are written.
+ *    contiguous, 16-byte aligned (mamba2_prefill_host alone takes its
+ *    activations and output in host memory). The library allocates no device
+ *    memory and keeps no state between calls; only `dst`, the named slots of
+ *    the state pools and a caller-provided workspace are written.
  *  - Batch metadata (mamba2_recurrent_batch) is HOST memory. It is validated
  *    on the host and passed to the kernels by value in their launch
  *    parameters, so the host arrays may be reused as soon as the call returns.
@@ -231,6 +234,70 @@ mamba2_status mamba2_decode_step(void* dst, const void* xBC, const void* z,
                                  mamba2_dtype act,
                                  const mamba2_recurrent_batch* rb,
                                  void* stream);
+
+/*
+ * Bytes of device workspace mamba2_prefill_host needs for this batch, piece
+ * size and activation type on the current device; 0 for arguments it would
+ * reject. rb->cu_seqlens is required (the call's row count is its last entry).
+ */
+size_t mamba2_prefill_host_workspace_bytes(const mamba2_dims* dims, mamba2_dtype act,
+                                           const mamba2_recurrent_batch* rb,
+                                           int32_t piece_rows);
+
+/*
+ * Prefill from HOST memory, streamed: the three ops above, CausalConv1D ->
+ * SSMScan -> GatedRMSNorm (gllm PR #85, section "Ops"), on a RecurrentBatch
+ * whose activations and output live in host memory. The rows are cut into
+ * pieces of piece_rows rows, except that the last piece_rows or fewer rows
+ * are halved again and again while the remainder keeps at least 1024 rows
+ * (pieces of at least 512 rows), so that little compute and copying remains
+ * after the last input copy. For each piece, the call copies the
+ * piece's xBC, z and dt rows to the device on an internal stream. It runs the
+ * three ops on `stream` and copies the piece's output back on a second
+ * internal stream. Inputs and outputs are double-buffered in the workspace,
+ * so the copies of neighbouring pieces overlap the compute and each other.
+ * A run cut by a piece edge continues in the next piece from its slots, as
+ * two consecutive calls with fresh = 0 would; only its first part keeps the
+ * caller's fresh flag. So conv outputs and conv state are bit-identical to
+ * one call over the whole batch. y and the SSM state may differ in rounding
+ * where the chunked scan's chunk boundaries move.
+ *
+ *   out_host  [rows, heads*headdim] act   HOST, written
+ *   xBC_host  [rows, conv_dim] act        HOST
+ *   z_host    [rows, heads*headdim] act   HOST
+ *   dt_host   [rows, heads] act           HOST
+ *     (page-locked host memory lets the copies run asynchronously; pageable
+ *      memory works but serialises them)
+ *   conv_w [conv_dim, conv_kernel], conv_b [conv_dim], A_log / dt_bias / D
+ *   [heads], norm_w [heads*headdim]: device f32, as for the ops above
+ *   conv_state, ssm_state: the device pools, updated in place at rb->slots
+ *   rb         HOST batch; rb->cu_seqlens required; rows = cu_seqlens[num_seqs]
+ *   piece_rows rows per piece (>= 1)
+ *   workspace  device scratch of at least mamba2_prefill_host_workspace_bytes
+ *              bytes, 256-byte aligned; holds the piece buffers and the scan's
+ *              workspace (no initialisation needed)
+ *
+ * Asynchronous like the other calls: it returns once everything is enqueued
+ * and `stream` completes after the last output copy. Read out_host, and
+ * reuse or free the host inputs and the workspace, only after that. The two
+ * copy streams and their events are created by the call and released at its
+ * end (their release waits for the enqueued work), so no state is kept
+ * between calls. Errors: the checks of the three ops for the whole batch,
+ * then MAMBA2_ERR_WORKSPACE_TOO_SMALL, all before anything is enqueued;
+ * MAMBA2_ERR_CUDA if a copy, launch or stream/event creation fails.
+ */
+mamba2_status mamba2_prefill_host(void* out_host, const void* xBC_host,
+                                  const void* z_host, const void* dt_host,
+                                  const float* conv_w, const float* conv_b,
+                                  const float* A_log, const float* dt_bias,
+                                  const float* D, const float* norm_w,
+                                  int32_t norm_groups, float eps,
+                                  void* conv_state, float* ssm_state,
+                                  int32_t num_slots, const mamba2_dims* dims,
+                                  mamba2_dtype act,
+                                  const mamba2_recurrent_batch* rb,
+                                  int32_t piece_rows, void* workspace,
+                                  size_t workspace_bytes, void* stream);
 
 /*
  * Bytes of recurrent state one sequence holds in one layer: the fp32 SSM

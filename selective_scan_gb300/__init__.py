@@ -8,7 +8,8 @@ without the built library raises.
 
 Entry points (same names as the C ABI without the ``mamba2_`` prefix):
 ``causal_conv1d``, ``ssd_scan`` (+ ``ssd_scan_workspace_bytes``),
-``gated_rmsnorm``, ``decode_step``, ``state_bytes_per_layer``.
+``gated_rmsnorm``, ``decode_step``, ``prefill_host`` (+
+``prefill_host_workspace_bytes``), ``state_bytes_per_layer``.
 """
 from __future__ import annotations
 
@@ -71,7 +72,12 @@ def _lib():
         lib.mamba2_status_string.argtypes = [ctypes.c_int]
         lib.mamba2_status_string.restype = ctypes.c_char_p
         lib.mamba2_last_cuda_error.restype = ctypes.c_char_p
-        for name in ("mamba2_causal_conv1d", "mamba2_ssd_scan", "mamba2_gated_rmsnorm", "mamba2_decode_step"):
+        lib.mamba2_prefill_host_workspace_bytes.argtypes = [dims, ctypes.c_int, rb, i32]
+        lib.mamba2_prefill_host_workspace_bytes.restype = sz
+        lib.mamba2_prefill_host.argtypes = [p, p, p, p, p, p, p, p, p, p, i32, f32, p, p, i32, dims, ctypes.c_int,
+                                            rb, i32, p, sz, p]
+        for name in ("mamba2_causal_conv1d", "mamba2_ssd_scan", "mamba2_gated_rmsnorm", "mamba2_decode_step",
+                     "mamba2_prefill_host"):
             getattr(lib, name).restype = ctypes.c_int
         _LIB = lib
     return _LIB
@@ -224,6 +230,41 @@ def decode_step(dst, xBC, z, dt, conv_w, conv_b, A_log, dt_bias, D, norm_w, norm
                                    ctypes.byref(d), _dt(xBC), b.ref(), _stream(stream))
     if check:
         _check(st, "mamba2_decode_step")
+    return st
+
+
+def prefill_host_workspace_bytes(dims, act: int, piece_rows: int, cu_seqlens=None, slots=None, fresh=None,
+                                 batch=None) -> int:
+    """``mamba2_prefill_host_workspace_bytes`` for this batch and piece size."""
+    b = _batch(cu_seqlens, slots, fresh, batch)
+    d = _dims(dims)
+    return int(_lib().mamba2_prefill_host_workspace_bytes(ctypes.byref(d), int(act), b.ref(), int(piece_rows)))
+
+
+def prefill_host(out_host, xBC_host, z_host, dt_host, conv_w, conv_b, A_log, dt_bias, D, norm_w, norm_groups, eps,
+                 conv_state, ssm_state, dims, cu_seqlens=None, slots=None, fresh=None, piece_rows=8192,
+                 workspace=None, stream=None, check=True, batch=None) -> int:
+    """``mamba2_prefill_host``: conv -> scan -> gated norm from host tensors, streamed in pieces.
+
+    ``out_host``, ``xBC_host``, ``z_host``, ``dt_host`` are CPU tensors (pinned for
+    overlap); the weights and pools are device tensors. ``workspace`` is a device
+    tensor of at least ``prefill_host_workspace_bytes`` bytes (allocated here with
+    torch when None). Asynchronous: synchronise the stream before reading ``out_host``.
+    """
+    import torch
+    d = _dims(dims)
+    b = _batch(cu_seqlens, slots, fresh, batch)
+    act = _dt(xBC_host)
+    if workspace is None:
+        need = int(_lib().mamba2_prefill_host_workspace_bytes(ctypes.byref(d), act, b.ref(), int(piece_rows)))
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=ssm_state.device)
+    st = _lib().mamba2_prefill_host(_ptr(out_host), _ptr(xBC_host), _ptr(z_host), _ptr(dt_host), _ptr(conv_w),
+                                    _ptr(conv_b), _ptr(A_log), _ptr(dt_bias), _ptr(D), _ptr(norm_w), int(norm_groups),
+                                    float(eps), _ptr(conv_state), _ptr(ssm_state), ssm_state.shape[0], ctypes.byref(d),
+                                    act, b.ref(), int(piece_rows), _ptr(workspace),
+                                    workspace.numel() * workspace.element_size(), _stream(stream))
+    if check:
+        _check(st, "mamba2_prefill_host")
     return st
 
 

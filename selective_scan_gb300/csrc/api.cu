@@ -160,6 +160,102 @@ void fill_scan_tiles(SeqTable& t, const ScanPlan& p, int Q) {
   }
 }
 
+// ---- streamed prefill from host memory
+
+// One piece of a streamed prefill: rows [r0, r1) of the call and the runs that
+// fall in it, cut at the piece's edges. A run cut by an edge continues in the
+// next piece from its slots, so only its first part keeps the caller's fresh
+// flag. A zero-length run goes to the piece holding its start row (the last
+// piece when it starts at the call's end).
+// Pieces are piece_rows long, except that the last piece_rows or fewer rows
+// are halved again and again while the remainder keeps at least
+// 2 * kMinTailRows rows: once the last input copy has landed, only the last
+// small piece's compute and output copy remain.
+constexpr int32_t kMinTailRows = 512;
+struct Piece {
+  int32_t r0 = 0, r1 = 0;
+  std::vector<int32_t> cu, slots;
+  std::vector<uint8_t> fresh;
+  mamba2_recurrent_batch batch() const {
+    mamba2_recurrent_batch b;
+    b.num_seqs = (int32_t)slots.size();
+    b.cu_seqlens = cu.data();
+    b.slots = slots.data();
+    b.fresh = fresh.data();
+    return b;
+  }
+};
+
+std::vector<Piece> cut_pieces(const mamba2_recurrent_batch* rb, int32_t rows, int32_t piece_rows) {
+  std::vector<int32_t> cuts{0};
+  int32_t r = 0;
+  while (rows - r > piece_rows) cuts.push_back(r += piece_rows);
+  for (int32_t left = rows - r; left >= 2 * kMinTailRows; left -= left / 2) cuts.push_back(r += left / 2);
+  if (rows > 0) cuts.push_back(rows);
+  const size_t np = rows == 0 ? 1 : cuts.size() - 1;
+  std::vector<Piece> out(np);
+  const int32_t* cu = rb->cu_seqlens;
+  for (size_t k = 0; k < np; ++k) {
+    Piece& pc = out[k];
+    pc.r0 = cuts[k];
+    pc.r1 = rows == 0 ? 0 : cuts[k + 1];
+    pc.cu.push_back(0);
+    for (int i = 0; i < rb->num_seqs; ++i) {
+      const int32_t a = cu[i], b = cu[i + 1];
+      bool in;
+      if (a == b)
+        in = (a >= pc.r0 && a < pc.r1) || (a == rows && k == np - 1);
+      else
+        in = a < pc.r1 && b > pc.r0;
+      if (!in) continue;
+      const int32_t s0 = std::max(a, pc.r0), s1 = std::min(b, pc.r1);
+      pc.cu.push_back(s1 - pc.r0);
+      pc.slots.push_back(rb->slots[i]);
+      pc.fresh.push_back(rb->fresh[i] && s0 == a ? 1 : 0);
+    }
+  }
+  return out;
+}
+
+// Device workspace of a streamed prefill: two input and two output piece
+// buffers, the conv output and y of one piece, then the scan's workspace.
+struct PrefillLayout {
+  size_t x_in[2], z_in[2], dt_in[2], out[2], xbc, y, scan, scan_bytes, total;
+};
+
+size_t align256(size_t v) { return (v + 255) / 256 * 256; }
+
+PrefillLayout prefill_layout(const mamba2_dims* d, mamba2_dtype act, int32_t rows, int32_t piece_rows,
+                             const std::vector<Piece>& pieces) {
+  PrefillLayout L;
+  const size_t P = (size_t)std::max<int32_t>(1, std::min<int32_t>(piece_rows, std::max<int32_t>(rows, 1)));
+  const size_t a = act_size(act);
+  const size_t d_inner = (size_t)d->heads * d->headdim;
+  const size_t conv_dim = d_inner + 2 * (size_t)d->ngroups * d->d_state;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t o = off;
+    off = align256(off + bytes);
+    return o;
+  };
+  for (int b = 0; b < 2; ++b) {
+    L.x_in[b] = take(P * conv_dim * a);
+    L.z_in[b] = take(P * d_inner * a);
+    L.dt_in[b] = take(P * d->heads * a);
+    L.out[b] = take(P * d_inner * a);
+  }
+  L.xbc = take(P * conv_dim * a);
+  L.y = take(P * d_inner * a);
+  L.scan_bytes = 0;
+  for (const Piece& pc : pieces) {
+    const mamba2_recurrent_batch b = pc.batch();
+    if (b.num_seqs > 0) L.scan_bytes = std::max(L.scan_bytes, plan_scan(d, act, &b).ws_bytes);
+  }
+  L.scan = take(L.scan_bytes);
+  L.total = off;
+  return L;
+}
+
 }  // namespace
 }  // namespace mamba2
 
@@ -352,6 +448,130 @@ mamba2_status mamba2_decode_step(void* dst, const void* xBC, const void* z, cons
   fill_table(a.tab, rb);
   for (int i = 0; i <= n; ++i) a.tab.tile[i] = i;
   cudaError_t e = launch_decode(a, act, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? MAMBA2_OK : cuda_fail(e);
+}
+
+size_t mamba2_prefill_host_workspace_bytes(const mamba2_dims* dims, mamba2_dtype act,
+                                           const mamba2_recurrent_batch* rb, int32_t piece_rows) {
+  if (!act_ok(act) || !dims_ok(dims) || piece_rows < 1 || !rb || !rb->cu_seqlens || rb->num_seqs < 0 ||
+      rb->num_seqs > MAMBA2_MAX_SEQS || !rb->slots || !rb->fresh)
+    return 0;
+  const int n = rb->num_seqs;
+  if (rb->cu_seqlens[0] != 0) return 0;
+  for (int i = 0; i < n; ++i)
+    if (rb->cu_seqlens[i + 1] < rb->cu_seqlens[i]) return 0;
+  const int32_t rows = rb->cu_seqlens[n];
+  return prefill_layout(dims, act, rows, piece_rows, cut_pieces(rb, rows, piece_rows)).total;
+}
+
+mamba2_status mamba2_prefill_host(void* out_host, const void* xBC_host, const void* z_host, const void* dt_host,
+                                  const float* conv_w, const float* conv_b, const float* A_log,
+                                  const float* dt_bias, const float* D, const float* norm_w, int32_t norm_groups,
+                                  float eps, void* conv_state, float* ssm_state, int32_t num_slots,
+                                  const mamba2_dims* dims, mamba2_dtype act, const mamba2_recurrent_batch* rb,
+                                  int32_t piece_rows, void* workspace, size_t workspace_bytes, void* stream) {
+  // ---- every check before anything is enqueued
+  if (!act_ok(act) || !dims_ok(dims) || piece_rows < 1 || norm_groups <= 0 || !(eps >= 0.0f))
+    return MAMBA2_ERR_INVALID_ARGUMENT;
+  const int32_t d_inner = dims->heads * dims->headdim;
+  const int32_t conv_dim = d_inner + 2 * dims->ngroups * dims->d_state;
+  if (d_inner % norm_groups != 0) return MAMBA2_ERR_INVALID_ARGUMENT;
+  if (((size_t)(d_inner / norm_groups) * act_size(act)) % 16 != 0) return MAMBA2_ERR_NOT_IMPLEMENTED;
+  if (((size_t)conv_dim * act_size(act)) % 16 != 0) return MAMBA2_ERR_NOT_IMPLEMENTED;
+  if (!scan_chunked_supported(act, dims->headdim, dims->d_state) &&
+      (dims->headdim > kSerialMaxP || dims->d_state > kSerialMaxN))
+    return MAMBA2_ERR_NOT_IMPLEMENTED;
+  if (!rb || !rb->cu_seqlens) return MAMBA2_ERR_INVALID_ARGUMENT;
+  if (rb->num_seqs < 0 || rb->num_seqs > MAMBA2_MAX_SEQS) return MAMBA2_ERR_INVALID_ARGUMENT;
+  const int32_t rows = rb->num_seqs > 0 ? rb->cu_seqlens[rb->num_seqs] : 0;
+  if (rb->num_seqs > 0) {
+    if (!conv_w || !conv_b || !A_log || !dt_bias || !D || !norm_w || !ssm_state ||
+        (dims->conv_kernel > 1 && !conv_state))
+      return MAMBA2_ERR_INVALID_ARGUMENT;
+    if (!aligned16(conv_w) || !aligned16(conv_b) || !aligned16(norm_w) || !aligned16(ssm_state) ||
+        (dims->conv_kernel > 1 && !aligned16(conv_state)))
+      return MAMBA2_ERR_INVALID_ARGUMENT;
+  }
+  if (rows > 0 && (!out_host || !xBC_host || !z_host || !dt_host)) return MAMBA2_ERR_INVALID_ARGUMENT;
+  mamba2_status st = validate_batch(rb, num_slots, rows, true);
+  if (st != MAMBA2_OK) return st;
+  if (rb->num_seqs == 0) return MAMBA2_OK;
+  const std::vector<Piece> pieces = cut_pieces(rb, rows, piece_rows);
+  const PrefillLayout L = prefill_layout(dims, act, rows, piece_rows, pieces);
+  if (!workspace || workspace_bytes < L.total) return MAMBA2_ERR_WORKSPACE_TOO_SMALL;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return MAMBA2_ERR_INVALID_ARGUMENT;
+
+  // ---- two copy streams and their events, made for this call and released at its end
+  // (destruction waits for the work already enqueued on them)
+  cudaStream_t cs = static_cast<cudaStream_t>(stream), s_in = nullptr, s_out = nullptr;
+  cudaEvent_t ev[9] = {};  // start, in_ready[2], in_free[2], out_ready[2], out_free[2]
+  auto release = [&]() {
+    for (cudaEvent_t& e : ev)
+      if (e) cudaEventDestroy(e);
+    if (s_in) cudaStreamDestroy(s_in);
+    if (s_out) cudaStreamDestroy(s_out);
+  };
+  cudaError_t e = cudaStreamCreateWithFlags(&s_in, cudaStreamNonBlocking);
+  if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&s_out, cudaStreamNonBlocking);
+  for (int i = 0; i < 9 && e == cudaSuccess; ++i) e = cudaEventCreateWithFlags(&ev[i], cudaEventDisableTiming);
+  if (e != cudaSuccess) {
+    release();
+    return cuda_fail(e);
+  }
+  cudaEvent_t ev_start = ev[0], *in_ready = ev + 1, *in_free = ev + 3, *out_ready = ev + 5, *out_free = ev + 7;
+
+  char* ws = static_cast<char*>(workspace);
+  const size_t a = act_size(act);
+  // work already on the caller's stream (pools, weights) comes first
+  e = cudaEventRecord(ev_start, cs);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(s_in, ev_start, 0);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(s_out, ev_start, 0);
+  for (size_t k = 0; k < pieces.size() && e == cudaSuccess; ++k) {
+    const Piece& pc = pieces[k];
+    const int b = (int)(k & 1);
+    const size_t pr = (size_t)(pc.r1 - pc.r0);
+    // inputs of piece k into buffer b once piece k-2 has consumed it
+    if (k >= 2) e = cudaStreamWaitEvent(s_in, in_free[b], 0);
+    if (e == cudaSuccess && pr > 0)
+      e = cudaMemcpyAsync(ws + L.x_in[b], static_cast<const char*>(xBC_host) + (size_t)pc.r0 * conv_dim * a,
+                          pr * conv_dim * a, cudaMemcpyHostToDevice, s_in);
+    if (e == cudaSuccess && pr > 0)
+      e = cudaMemcpyAsync(ws + L.z_in[b], static_cast<const char*>(z_host) + (size_t)pc.r0 * d_inner * a,
+                          pr * d_inner * a, cudaMemcpyHostToDevice, s_in);
+    if (e == cudaSuccess && pr > 0)
+      e = cudaMemcpyAsync(ws + L.dt_in[b], static_cast<const char*>(dt_host) + (size_t)pc.r0 * dims->heads * a,
+                          pr * dims->heads * a, cudaMemcpyHostToDevice, s_in);
+    if (e == cudaSuccess) e = cudaEventRecord(in_ready[b], s_in);
+    // conv -> scan -> norm on the caller's stream, into output buffer b once piece k-2's copy-out is done
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(cs, in_ready[b], 0);
+    if (e == cudaSuccess && k >= 2) e = cudaStreamWaitEvent(cs, out_free[b], 0);
+    if (e != cudaSuccess) break;
+    const mamba2_recurrent_batch pb = pc.batch();
+    st = mamba2_causal_conv1d(ws + L.xbc, ws + L.x_in[b], conv_w, conv_b, conv_state, num_slots, (int32_t)pr,
+                              conv_dim, dims->conv_kernel, act, &pb, cs);
+    if (st == MAMBA2_OK)
+      st = mamba2_ssd_scan(ws + L.y, ws + L.xbc, ws + L.dt_in[b], A_log, dt_bias, D, ssm_state, num_slots,
+                           (int32_t)pr, dims, act, &pb, L.scan_bytes ? ws + L.scan : nullptr, L.scan_bytes, cs);
+    if (st == MAMBA2_OK)
+      st = mamba2_gated_rmsnorm(ws + L.out[b], ws + L.y, ws + L.z_in[b], norm_w, (int32_t)pr, d_inner,
+                                norm_groups, eps, act, cs);
+    if (st != MAMBA2_OK) {
+      release();
+      return st;
+    }
+    e = cudaEventRecord(in_free[b], cs);
+    if (e == cudaSuccess) e = cudaEventRecord(out_ready[b], cs);
+    // output of piece k back to the host
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(s_out, out_ready[b], 0);
+    if (e == cudaSuccess && pr > 0)
+      e = cudaMemcpyAsync(static_cast<char*>(out_host) + (size_t)pc.r0 * d_inner * a, ws + L.out[b],
+                          pr * d_inner * a, cudaMemcpyDeviceToHost, s_out);
+    if (e == cudaSuccess) e = cudaEventRecord(out_free[b], s_out);
+  }
+  // the caller's stream finishes after the last copy-out
+  if (e == cudaSuccess) e = cudaEventRecord(ev_start, s_out);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(cs, ev_start, 0);
+  release();
   return e == cudaSuccess ? MAMBA2_OK : cuda_fail(e);
 }
 

@@ -115,3 +115,41 @@ def test_argument_checks(product_lib):
     # norm: groups must divide dim
     assert lib.mamba2_gated_rmsnorm(FAKE[0], FAKE[1], FAKE[2], FAKE[3], 2, 64, 3, 1e-5, ss.BF16,
                                     None) == ss.ERR_INVALID_ARGUMENT
+
+
+def _prefill_host(lib, cu, slots, piece_rows=64, ws=None, ws_bytes=1 << 30, num_slots=4, fresh=None):
+    d = ss.Dims(4, 16, 16, 2, 4)
+    b = ss._Batch(cu, slots, fresh if fresh is not None else [0] * len(slots))
+    return lib.mamba2_prefill_host(*FAKE[:10], 2, 1e-5, FAKE[10], FAKE[11], num_slots, ctypes.byref(d), ss.BF16,
+                                   b.ref(), piece_rows, FAKE[12] if ws is None else ws, ws_bytes, None)
+
+
+def test_prefill_host_rejections(product_lib):
+    """The streamed host prefill applies the ops' batch checks to the whole batch,
+    then its own (piece size, workspace), all before anything is enqueued."""
+    lib = product_lib
+    assert _prefill_host(lib, [0, 3, 7], [0, 4]) == ss.ERR_SLOT_OUT_OF_RANGE
+    assert _prefill_host(lib, [0, 3, 7], [2, 2]) == ss.ERR_SLOT_SHARED
+    assert _prefill_host(lib, [0, 5, 4], [0, 1]) == ss.ERR_RUNS_DONT_COVER_ROWS
+    assert _prefill_host(lib, [2, 3, 7], [0, 1]) == ss.ERR_RUNS_DONT_COVER_ROWS
+    assert _prefill_host(lib, [0, 3, 7], [0, 1], piece_rows=0) == ss.ERR_INVALID_ARGUMENT
+    d = ss.Dims(4, 16, 16, 2, 4)
+    b = ss._Batch([0, 3, 7], [0, 1], [1, 0])
+    need = lib.mamba2_prefill_host_workspace_bytes(ctypes.byref(d), ss.BF16, b.ref(), 64)
+    assert need > 0
+    assert _prefill_host(lib, [0, 3, 7], [0, 1], ws_bytes=need - 1) == ss.ERR_WORKSPACE_TOO_SMALL
+    assert _prefill_host(lib, [0, 3, 7], [0, 1], ws=FAKE[12] + 16, ws_bytes=need) == ss.ERR_INVALID_ARGUMENT
+    assert lib.mamba2_prefill_host_workspace_bytes(ctypes.byref(d), ss.BF16, b.ref(), 0) == 0
+
+
+def test_prefill_host_workspace_grows_with_piece(product_lib):
+    """Piece buffers scale with the piece size (capped at the call's rows)."""
+    lib = product_lib
+    d = ss.Dims(24, 64, 128, 1, 4)
+    b = ss._Batch([0, 5000], [0], [1])
+    sizes = [lib.mamba2_prefill_host_workspace_bytes(ctypes.byref(d), ss.BF16, b.ref(), p)
+             for p in (256, 1024, 5000, 100000)]
+    assert sizes[0] < sizes[1] < sizes[2] == sizes[3]
+    conv_dim, d_inner = 24 * 64 + 2 * 128, 24 * 64
+    per_row = 2 * (conv_dim + 2 * d_inner + 24) * 2 + (conv_dim + d_inner) * 2  # double-buffered in/out, xbc, y
+    assert sizes[2] >= 5000 * per_row

@@ -348,3 +348,96 @@ def test_long_prefill_65536_split_and_decode():
     cont = W.Workload("tail", d, wl.act, p, W.Batch([0, 1], [0], [0]), wl.xBC[:0], wl.z[:0], wl.dt[:0],
                       conv.cpu(), ssm.cpu(), wl.dec_xBC, wl.dec_z, wl.dec_dt)
     _decode_parity(cont, wl.dec_xBC.shape[0], dev)
+
+
+def _host_pieces(cu, slots, fresh, piece_rows, min_tail=512):
+    """The piece rule of mamba2_prefill_host, restated: pieces of piece_rows rows,
+    the last piece_rows or fewer rows halved while the remainder keeps at least
+    2 * min_tail rows; a run cut at a piece edge continues in the next piece
+    (fresh only in its first part); a zero-length run goes to the piece holding
+    its start row."""
+    rows = cu[-1]
+    cuts, r = [0], 0
+    while rows - r > piece_rows:
+        r += piece_rows
+        cuts.append(r)
+    left = rows - r
+    while left >= 2 * min_tail:
+        r += left // 2
+        cuts.append(r)
+        left -= left // 2
+    if rows > 0:
+        cuts.append(rows)
+    n_pieces = 1 if rows == 0 else len(cuts) - 1
+    out = []
+    for k in range(n_pieces):
+        r0, r1 = cuts[k], (cuts[k + 1] if rows > 0 else 0)
+        pc, ps, pf = [0], [], []
+        for i in range(len(slots)):
+            a, b = cu[i], cu[i + 1]
+            inside = (r0 <= a < r1 or (a == rows and k == n_pieces - 1)) if a == b else (a < r1 and b > r0)
+            if inside:
+                pc.append(min(b, r1) - r0)
+                ps.append(slots[i])
+                pf.append(1 if fresh[i] and max(a, r0) == a else 0)
+        out.append((r0, r1, pc, ps, pf))
+    return out
+
+
+HOST_CASES = [
+    # pieces of 200 rows cutting runs mid-way, zero-length runs at piece starts; oracle-checked
+    ("small", [1, 63, 0, 300, 65, 0, 517, 130, 0], [1, 0, 1, 0, 1, 0, 0, 1, 1], 200, True),
+    # 5 900 rows in pieces of 2 048: the last 1 804 rows are halved into 902 + 902
+    ("tail", [3000, 1, 0, 2899], [1, 0, 1, 0], 2048, False),
+    # 6 000 rows in pieces of 4 096: the last 1 904 rows are halved into 952 + 952
+    ("tail-halved", [700, 5300], [0, 1], 4096, False),
+]
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("name,lengths,fresh,P,with_oracle", HOST_CASES, ids=[c[0] for c in HOST_CASES])
+def test_prefill_host_streamed(name, lengths, fresh, P, with_oracle):
+    """mamba2_prefill_host from pinned host memory: bit-identical to the device ops
+    called once per piece (so the copies, buffers and ordering lose nothing), and,
+    on the small case, against the oracle over the whole batch: conv state
+    bit-exact, the chained output and the SSM state by relative L2."""
+    dev = torch.device("cuda:0")
+    wl = W.make_prefill("host-" + name, 41, W.DIMS_130M, lengths, torch.bfloat16, 12, fresh)
+    p, b, d = wl.params, wl.batch, wl.dims
+    w = [t.to(dev) for t in (p.conv_w, p.conv_b, p.A_log, p.dt_bias, p.D, p.norm_w)]
+    hx, hz, hdt = wl.xBC.pin_memory(), wl.z.pin_memory(), wl.dt.pin_memory()
+    hout = torch.full((b.rows, d.d_inner), float("nan"), dtype=torch.bfloat16).pin_memory()
+    conv_h, ssm_h = wl.conv_state.to(dev), wl.ssm_state.to(dev)
+    ss.prefill_host(hout, hx, hz, hdt, *w[:5], w[5], p.norm_groups, p.eps, conv_h, ssm_h, d, b.cu_seqlens,
+                    b.slots, b.fresh, piece_rows=P)
+    torch.cuda.synchronize()
+
+    conv_r, ssm_r = wl.conv_state.to(dev), wl.ssm_state.to(dev)
+    out_r = torch.empty((b.rows, d.d_inner), dtype=torch.bfloat16, device=dev)
+    pieces = _host_pieces(b.cu_seqlens, b.slots, b.fresh, P)
+    assert len(pieces) > 2
+    for r0, r1, pc, ps, pf in pieces:
+        x = wl.xBC[r0:r1].to(dev)
+        xbc = torch.empty_like(x)
+        ss.causal_conv1d(xbc, x, w[0], w[1], conv_r, pc, ps, pf)
+        y = torch.empty((r1 - r0, d.d_inner), dtype=torch.bfloat16, device=dev)
+        ss.ssd_scan(y, xbc, wl.dt[r0:r1].to(dev), w[2], w[3], w[4], ssm_r, d, pc, ps, pf)
+        ss.gated_rmsnorm(out_r[r0:r1], y, wl.z[r0:r1].to(dev), w[5], p.norm_groups, p.eps)
+    torch.cuda.synchronize()
+    assert_bits_equal(hout, out_r.cpu(), "streamed output vs per-piece device calls")
+    assert_bits_equal(conv_h.cpu(), conv_r.cpu(), "conv pool")
+    assert_bits_equal(ssm_h.cpu(), ssm_r.cpu(), "ssm pool")
+    if name == "tail-halved":
+        assert [r1 - r0 for r0, r1, *_ in pieces] == [4096, 952, 952]
+    if not with_oracle:
+        return
+
+    conv_o, ssm_o = wl.conv_state.clone(), wl.ssm_state.clone()
+    xbc_o, _ = oracle.causal_conv1d(wl.xBC, p.conv_w, p.conv_b, conv_o, b.cu_seqlens, b.slots, b.fresh)
+    y_o, _ = oracle.ssd_scan(xbc_o, wl.dt, p.A_log, p.dt_bias, p.D, ssm_o, d.tuple4(), b.cu_seqlens, b.slots,
+                             b.fresh)
+    _, out64 = oracle.gated_rmsnorm(y_o, wl.z, p.norm_w, p.norm_groups, p.eps)
+    assert_bits_equal(conv_h.cpu(), conv_o, "conv pool vs oracle")
+    assert rel_l2(hout.double(), out64) <= 1e-2
+    idx = torch.tensor(b.slots)
+    assert rel_l2(ssm_h.cpu()[idx], ssm_o[idx]) <= 1e-3
