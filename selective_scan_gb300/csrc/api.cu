@@ -85,6 +85,7 @@ bool dims_ok(const mamba2_dims* d) {
 struct ScanPlan {
   bool chunked = false;
   int seg_chunks = 1;
+  int state_pieces = 1;  // tcgen05 path: state-pass entries per segment
   int total_segs = 0;
   bool segmented = false;
   size_t ws_state_floats = 0;
@@ -103,10 +104,14 @@ ScanPlan plan_scan(const mamba2_dims* d, mamba2_dtype act, const mamba2_recurren
     return p;
   }
   const int Q = scan_chunk_tokens(d->headdim, d->d_state);
+  const bool tc = scan_uses_tc(act, d->headdim, d->d_state);
+  constexpr int kMaxStatePieces = 8;
   // Chunks per segment: both passes run one CTA per SM, so pick the segment
   // length that minimises whole waves x chunks per CTA, counting a state-pass
   // chunk (one product, no output) at about a third of a full-pass chunk and
-  // about two chunks of fill and drain per CTA.
+  // about two chunks of fill and drain per CTA. On the tcgen05 path the state
+  // pass may cut each segment into several pieces (one entry each, folded in
+  // order by the full pass), so that its CTAs fill the SMs the segments leave.
   std::vector<int64_t> ch(n);
   for (int i = 0; i < n; ++i) ch[i] = (rb->cu_seqlens[i + 1] - rb->cu_seqlens[i] + Q - 1) / Q;
   std::sort(ch.begin(), ch.end(), std::greater<int64_t>());
@@ -118,11 +123,24 @@ ScanPlan plan_scan(const mamba2_dims* d, mamba2_dtype act, const mamba2_recurren
     int64_t extra = 0;  // segments beyond one per sequence = state-pass CTAs per head
     for (int i = 0; i < n && ch[i] > sc; ++i) extra += (ch[i] + sc - 1) / sc - 1;
     const int64_t full_waves = (d->heads * (n + extra) + nsm - 1) / nsm;
-    const int64_t state_waves = (d->heads * extra + nsm - 1) / nsm;
-    const double cost = (double)full_waves * (double)(std::min(sc, max_ch) + 2) + (double)state_waves * (0.35 * sc + 1.0);
+    double state_cost = 0.0;
+    int pieces = 1;
+    if (extra > 0) {
+      state_cost = 1e300;
+      for (int P = 1; P <= (tc ? std::min<int64_t>(kMaxStatePieces, sc) : 1); ++P) {  // no empty piece
+        const int64_t state_waves = (d->heads * extra * P + nsm - 1) / nsm;
+        const double c = (double)state_waves * (0.35 * (double)((sc + P - 1) / P) + 1.0);
+        if (c < state_cost - 1e-9) {
+          state_cost = c;
+          pieces = P;
+        }
+      }
+    }
+    const double cost = (double)full_waves * (double)(std::min(sc, max_ch) + 2) + state_cost;
     if (cost < best - 1e-9) {
       best = cost;
       p.seg_chunks = (int)sc;
+      p.state_pieces = pieces;
     }
   }
   p.total_segs = 0;
@@ -134,10 +152,12 @@ ScanPlan plan_scan(const mamba2_dims* d, mamba2_dtype act, const mamba2_recurren
     p.total_segs += segs;
   }
   size_t bytes = 0;
+  if (!p.segmented) p.state_pieces = 1;
   if (p.segmented) {
-    p.ws_state_floats = (size_t)p.total_segs * d->heads * d->headdim * d->d_state;
+    const size_t entries = (size_t)p.total_segs * p.state_pieces;
+    p.ws_state_floats = entries * d->heads * d->headdim * d->d_state;
     p.off_decay = (p.ws_state_floats * 4 + 255) / 256 * 256;
-    bytes = p.off_decay + (size_t)p.total_segs * d->heads * 4;
+    bytes = p.off_decay + entries * d->heads * 4;
   }
   p.has_dtp = scan_uses_tc(act, d->headdim, d->d_state);
   if (p.has_dtp) {
@@ -371,6 +391,7 @@ mamba2_status mamba2_ssd_scan(void* dst, const void* xbc, const void* dt, const 
   a.ngroups = dims->ngroups;
   a.conv_dim = dims->heads * dims->headdim + 2 * dims->ngroups * dims->d_state;
   a.seg_chunks = plan.seg_chunks;
+  a.state_pieces = plan.state_pieces;
   if (plan.segmented) {
     a.ws_state = static_cast<float*>(workspace);
     a.ws_decay = reinterpret_cast<float*>(static_cast<char*>(workspace) + plan.off_decay);

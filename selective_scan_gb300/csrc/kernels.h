@@ -49,11 +49,12 @@ struct ScanArgs {
   const float* dt_bias;
   const float* D;
   float* ssm_state;
-  float* ws_state;  // [segments, heads, P, N] (null when unsegmented)
-  float* ws_decay;  // [segments, heads]
+  float* ws_state;  // [segments * state_pieces, heads, P, N] (null when unsegmented)
+  float* ws_decay;  // [segments * state_pieces, heads]
   float* dtp;       // [heads, rows] dt' = softplus(dt + dt_bias) (tcgen05 path; null otherwise)
   int32_t heads, headdim, d_state, ngroups, conv_dim;
   int32_t seg_chunks;  // chunks per segment (tile = segment)
+  int32_t state_pieces;  // tcgen05 state pass: entries per segment, each over an equal share of its chunks
   SeqTable tab;
 };
 // True when the chunked tensor-core kernels cover this shape: tcgen05 for

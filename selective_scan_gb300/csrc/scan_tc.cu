@@ -305,9 +305,8 @@ struct Cta {
   int x_col, b_col, c_col;
   float A2, Dh;  // decay rate in log2 units, skip weight
 };
-__device__ __forceinline__ Cta cta_info(const ScanArgs& a) {
+__device__ __forceinline__ Cta cta_info(const ScanArgs& a, int seg) {
   Cta c;
-  const int seg = blockIdx.x;
   c.h = blockIdx.y;
   c.sq = find_tile_seq(a.tab, seg);
   c.seg0 = a.tab.tile[c.sq];
@@ -374,7 +373,7 @@ ssd_tc_full(const __grid_constant__ ScanArgs a, const __grid_constant__ CUtensor
   auto par = [](int i) { return (uint32_t)((i >> 1) & 1); };  // phase parity of chunk i on a [2] barrier
   auto stage = [&](int i) { return sbase + (uint32_t)(i & 1) * kStage; };
 
-  const Cta ci = cta_info(a);
+  const Cta ci = cta_info(a, blockIdx.x);
   const int n = ci.n;
   const int H = a.heads;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -544,17 +543,19 @@ ssd_tc_full(const __grid_constant__ ScanArgs a, const __grid_constant__ CUtensor
 #pragma unroll
         for (int i = 0; i < 32; ++i) hst[i] = src ? src[(int64_t)(pc0 + i) * TN + row] : 0.0f;
       };
+      const int P = a.state_pieces > 0 ? a.state_pieces : 1;
       if (ci.k == 0) {
         // the first segment starts from the slot (from the state pass's copy when the
         // last segment will overwrite the slot in this same launch)
-        load_state(ci.fresh ? nullptr : (ci.nseg > 1 ? ws_entry(ci.seg0 + ci.nseg - 1) : slot_ptr));
+        load_state(ci.fresh ? nullptr : (ci.nseg > 1 ? ws_entry((ci.seg0 + ci.nseg - 1) * P) : slot_ptr));
       } else {
-        load_state(ws_entry(ci.seg0));
-        for (int j = 1; j < ci.k; ++j) {
-          const float d = __expf(a.ws_decay[(int64_t)(ci.seg0 + j) * H + ci.h]);
-          const float* e = ws_entry(ci.seg0 + j);
+        // the entries of every piece of the earlier segments, in order
+        load_state(ws_entry(ci.seg0 * P));
+        for (int e = ci.seg0 * P + 1; e < (ci.seg0 + ci.k) * P; ++e) {
+          const float d = __expf(a.ws_decay[(int64_t)e * H + ci.h]);
+          const float* src = ws_entry(e);
 #pragma unroll
-          for (int i = 0; i < 32; ++i) hst[i] = fmaf(d, hst[i], e[(int64_t)(pc0 + i) * TN + row]);
+          for (int i = 0; i < 32; ++i) hst[i] = fmaf(d, hst[i], src[(int64_t)(pc0 + i) * TN + row]);
         }
       }
       auto state_update = [&](int j) {  // H = exp(total_j) H + dH(j), dH = hi part + lo part
@@ -831,8 +832,28 @@ ssd_tc_full(const __grid_constant__ ScanArgs a, const __grid_constant__ CUtensor
 //   warp 18     dt' and the token weights, up to four chunks ahead
 __global__ void __launch_bounds__(kStateThreads, 1)
 ssd_tc_state(const __grid_constant__ ScanArgs a, const __grid_constant__ CUtensorMap tm, const int use_tma) {
-  const Cta ci = cta_info(a);
+  // CTA b: piece q = b % P of segment b / P, an equal share of the segment's
+  // chunks; its entry (index b) is the piece's end state from zero (the first
+  // piece of a sequence's first segment from the slot) and total log-decay
+  const int P = a.state_pieces > 0 ? a.state_pieces : 1;
+  const int entry = blockIdx.x, q = entry % P;
+  Cta ci = cta_info(a, entry / P);
   if (ci.k == ci.nseg - 1) return;  // the last segment has no entry (the full pass ends it)
+  {
+    // balanced shares: sizes differ by at most one chunk, none empty while P <= chunks
+    const int nk = ci.c_end - ci.c_begin;
+    const int pb = ci.c_begin + (int)((int64_t)q * nk / P), pe = ci.c_begin + (int)((int64_t)(q + 1) * nk / P);
+    ci.c_begin = pb;
+    ci.c_end = pe;
+    ci.n = pe - pb;
+  }
+  const int H = a.heads;
+  if (ci.n == 0) {  // an empty piece (only when a segment has fewer than P chunks): zero state, zero decay
+    float* dst = a.ws_state + ((int64_t)entry * H + ci.h) * TP * TN;
+    for (int i = threadIdx.x; i < TP * TN; i += blockDim.x) dst[i] = 0.0f;
+    if (threadIdx.x == 0) a.ws_decay[(int64_t)entry * H + ci.h] = 0.0f;
+    return;
+  }
   extern __shared__ unsigned char smem_raw[];
   const uint32_t raw_base = su32(smem_raw);
   unsigned char* smem = smem_raw + (((raw_base + 1023u) & ~1023u) - raw_base);
@@ -846,8 +867,7 @@ ssd_tc_state(const __grid_constant__ ScanArgs a, const __grid_constant__ CUtenso
   auto p3 = [](int i) { return (uint32_t)((i / kStStages) & 1); };  // phase parity on a [3] barrier
   auto p4 = [](int i) { return (uint32_t)((i >> 2) & 1); };         // phase parity on a [4] barrier
 
-  const int n = ci.n;  // >= 1 for every segment but the last
-  const int H = a.heads;
+  const int n = ci.n;  // >= 1 here
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
   if (warp == 0) {
@@ -921,13 +941,14 @@ ssd_tc_state(const __grid_constant__ ScanArgs a, const __grid_constant__ CUtenso
       float dhi[16], dlo[16];
       tmem_ld16x2(tmem + lane_off + 16 * cg, tmem + lane_off + 64 + 16 * cg, dhi, dlo);
       const float Rt = *s_R;  // written before the weights of the last chunk were published
-      float* dst = ws_entry(blockIdx.x);
-      if (ci.k == 0 && !ci.fresh) {
-        // the first segment starts from the slot's state: add its decayed share, and
+      float* dst = ws_entry(entry);
+      if (ci.k == 0 && q == 0 && !ci.fresh) {
+        // the first piece starts from the slot's state: add its decayed share, and
         // leave a copy of it for the full pass (whose last segment overwrites the slot)
+        // in the first entry of the last segment, which has no entries of its own
         const float d = ex2(Rt);
         const float* slot_ptr = a.ssm_state + (int64_t)seq_slot(a.tab, ci.sq) * H * TP * TN + head_off;
-        float* copy = ws_entry(ci.seg0 + ci.nseg - 1);
+        float* copy = ws_entry((ci.seg0 + ci.nseg - 1) * P);
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
           const float h0 = slot_ptr[(int64_t)(16 * cg + i) * TN + row];
@@ -938,7 +959,7 @@ ssd_tc_state(const __grid_constant__ ScanArgs a, const __grid_constant__ CUtenso
 #pragma unroll
         for (int i = 0; i < 16; ++i) dst[(int64_t)(16 * cg + i) * TN + row] = dhi[i] + dlo[i];
       }
-      if (tid == 0) a.ws_decay[(int64_t)blockIdx.x * H + ci.h] = Rt * 0.6931471805599453f;
+      if (tid == 0) a.ws_decay[(int64_t)entry * H + ci.h] = Rt * 0.6931471805599453f;
     }
   } else if (warp == kMathWarps) {
     // =================== B and X tile loads
@@ -1075,7 +1096,8 @@ cudaError_t launch_scan_tc(const ScanArgs& a, cudaStream_t st) {
   if (segmented) {
     cudaError_t e = cudaFuncSetAttribute(ssd_tc_state, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kStateSmem);
     if (e != cudaSuccess) return e;
-    ssd_tc_state<<<grid, kStateThreads, kStateSmem, st>>>(a, tm, use_tma);
+    const dim3 sgrid((unsigned)(segs * (a.state_pieces > 0 ? a.state_pieces : 1)), (unsigned)a.heads);
+    ssd_tc_state<<<sgrid, kStateThreads, kStateSmem, st>>>(a, tm, use_tma);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
