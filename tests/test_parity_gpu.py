@@ -441,3 +441,34 @@ def test_prefill_host_streamed(name, lengths, fresh, P, with_oracle):
     assert rel_l2(hout.double(), out64) <= 1e-2
     idx = torch.tensor(b.slots)
     assert rel_l2(ssm_h.cpu()[idx], ssm_o[idx]) <= 1e-3
+
+
+NORM_SHAPES = [
+    # rows, dim, groups, act: an odd row count (the last CTA holds one row), several groups,
+    # groups wider than the vectors a thread keeps in registers, and a group too wide for
+    # its weights to be staged in shared memory
+    (7, 3072, 1, torch.bfloat16),
+    (33, 1536, 4, torch.bfloat16),
+    (5, 8192, 1, torch.bfloat16),
+    (3, 16384, 1, torch.bfloat16),
+    (9, 2048, 2, torch.float32),
+]
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("rows,dim,groups,act", NORM_SHAPES,
+                         ids=[f"{r}x{d}g{g}{'bf16' if a == torch.bfloat16 else 'f32'}" for r, d, g, a in NORM_SHAPES])
+def test_gated_rmsnorm_shapes(rows, dim, groups, act):
+    """GatedRMSNorm alone on seeded N(0,1) inputs and weights N(1, 0.1^2) against the
+    oracle, element by element, across the kernel's row pairing and its three weight
+    and width paths."""
+    dev = torch.device("cuda:0")
+    g = torch.Generator().manual_seed(rows * 1000 + dim + groups)
+    x = torch.randn((rows, dim), generator=g).to(act)
+    z = torch.randn((rows, dim), generator=g).to(act)
+    w = 1.0 + 0.1 * torch.randn(dim, generator=g)
+    out = torch.empty((rows, dim), dtype=act, device=dev)
+    ss.gated_rmsnorm(out, x.to(dev), z.to(dev), w.to(dev), groups, 1e-5)
+    torch.cuda.synchronize()
+    _, out64 = oracle.gated_rmsnorm(x, z, w, groups, 1e-5)
+    check_act(out.cpu(), out64, f"norm {rows}x{dim} groups {groups}")
