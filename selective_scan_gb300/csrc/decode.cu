@@ -10,7 +10,8 @@
 // recurrent inference" (section "Summary") runs it as indexed recurrent decode
 // over a state pool.
 //
-// Work split: a thread-block cluster per sequence; CTA r of the cluster owns
+// Work split: a thread-block cluster per sequence (16 CTAs for batches small
+// enough that all such clusters fit on the SMs at once, else 8); CTA r of the cluster owns
 // heads [r*hpc, (r+1)*hpc). Each CTA
 //   1. computes the conv for its heads' x channels and for all B/C channels
 //      (B/C recomputed per CTA: 2*G*N channels, tiny), writes the new conv
@@ -362,6 +363,10 @@ static cudaError_t launch_decode_t(const DecodeArgs& a, cudaStream_t st) {
   const size_t smem = sizeof(float) * (3 * (size_t)a.heads_per_cta * a.headdim + 2 * (size_t)a.ngroups * a.d_state +
                                        3 * (size_t)a.heads_per_cta + kDecodeMaxNormGroups + kDecodeWarps);
   auto kern = decode_step_kernel<T, K>;
+  if (a.cluster > kDecodePortableCluster) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e != cudaSuccess) return e;
+  }
   if (smem > 48 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
