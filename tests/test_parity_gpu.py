@@ -391,6 +391,9 @@ HOST_CASES = [
     ("tail", [3000, 1, 0, 2899], [1, 0, 1, 0], 2048, False),
     # 6 000 rows in pieces of 4 096: the last 1 904 rows are halved into 952 + 952
     ("tail-halved", [700, 5300], [0, 1], 4096, False),
+    # fp32 activations at the tiny shape (4 heads x 16, d_state 16, 2 groups): the other
+    # scan kernel through the same pieces; oracle-checked
+    ("tiny-f32", [5, 130, 0, 64, 301], [1, 0, 1, 1, 0], 100, True),
 ]
 
 
@@ -402,25 +405,28 @@ def test_prefill_host_streamed(name, lengths, fresh, P, with_oracle):
     on the small case, against the oracle over the whole batch: conv state
     bit-exact, the chained output and the SSM state by relative L2."""
     dev = torch.device("cuda:0")
-    wl = W.make_prefill("host-" + name, 41, W.DIMS_130M, lengths, torch.bfloat16, 12, fresh)
+    tiny = name.startswith("tiny")
+    wl = W.make_prefill("host-" + name, 41, W.DIMS_TINY if tiny else W.DIMS_130M, lengths,
+                        torch.float32 if tiny else torch.bfloat16, 12, fresh, **({"norm_groups": 2} if tiny else {}))
     p, b, d = wl.params, wl.batch, wl.dims
+    act = wl.act
     w = [t.to(dev) for t in (p.conv_w, p.conv_b, p.A_log, p.dt_bias, p.D, p.norm_w)]
     hx, hz, hdt = wl.xBC.pin_memory(), wl.z.pin_memory(), wl.dt.pin_memory()
-    hout = torch.full((b.rows, d.d_inner), float("nan"), dtype=torch.bfloat16).pin_memory()
+    hout = torch.full((b.rows, d.d_inner), float("nan"), dtype=act).pin_memory()
     conv_h, ssm_h = wl.conv_state.to(dev), wl.ssm_state.to(dev)
     ss.prefill_host(hout, hx, hz, hdt, *w[:5], w[5], p.norm_groups, p.eps, conv_h, ssm_h, d, b.cu_seqlens,
                     b.slots, b.fresh, piece_rows=P)
     torch.cuda.synchronize()
 
     conv_r, ssm_r = wl.conv_state.to(dev), wl.ssm_state.to(dev)
-    out_r = torch.empty((b.rows, d.d_inner), dtype=torch.bfloat16, device=dev)
+    out_r = torch.empty((b.rows, d.d_inner), dtype=act, device=dev)
     pieces = _host_pieces(b.cu_seqlens, b.slots, b.fresh, P)
     assert len(pieces) > 2
     for r0, r1, pc, ps, pf in pieces:
         x = wl.xBC[r0:r1].to(dev)
         xbc = torch.empty_like(x)
         ss.causal_conv1d(xbc, x, w[0], w[1], conv_r, pc, ps, pf)
-        y = torch.empty((r1 - r0, d.d_inner), dtype=torch.bfloat16, device=dev)
+        y = torch.empty((r1 - r0, d.d_inner), dtype=act, device=dev)
         ss.ssd_scan(y, xbc, wl.dt[r0:r1].to(dev), w[2], w[3], w[4], ssm_r, d, pc, ps, pf)
         ss.gated_rmsnorm(out_r[r0:r1], y, wl.z[r0:r1].to(dev), w[5], p.norm_groups, p.eps)
     torch.cuda.synchronize()
