@@ -478,3 +478,33 @@ def test_gated_rmsnorm_shapes(rows, dim, groups, act):
     torch.cuda.synchronize()
     _, out64 = oracle.gated_rmsnorm(x, z, w, groups, 1e-5)
     check_act(out.cpu(), out64, f"norm {rows}x{dim} groups {groups}")
+
+
+@pytest.mark.gpu
+def test_prefill_host_all_runs_empty():
+    """A streamed host prefill whose runs are all empty (no rows at all): fresh slots
+    end with zero conv history and zero state, resumed slots and the others are left
+    untouched, and the output buffer is not written."""
+    dev = torch.device("cuda:0")
+    wl = W.make_prefill("host-empty", 43, W.DIMS_130M, [0, 0, 0], torch.bfloat16, 6, [1, 0, 1])
+    p, b, d = wl.params, wl.batch, wl.dims
+    w = [t.to(dev) for t in (p.conv_w, p.conv_b, p.A_log, p.dt_bias, p.D, p.norm_w)]
+    conv0, ssm0 = wl.conv_state.clone(), wl.ssm_state.clone()
+    conv_h, ssm_h = conv0.to(dev), ssm0.to(dev)
+    empty = torch.empty((0, d.conv_dim), dtype=torch.bfloat16).pin_memory()
+    hz = torch.empty((0, d.d_inner), dtype=torch.bfloat16).pin_memory()
+    hdt = torch.empty((0, d.heads), dtype=torch.bfloat16).pin_memory()
+    hout = torch.empty((0, d.d_inner), dtype=torch.bfloat16).pin_memory()
+    ss.prefill_host(hout, empty, hz, hdt, *w[:5], w[5], p.norm_groups, p.eps, conv_h, ssm_h, d, b.cu_seqlens,
+                    b.slots, b.fresh, piece_rows=256)
+    torch.cuda.synchronize()
+    conv_g, ssm_g = conv_h.cpu(), ssm_h.cpu()
+    for i, s in enumerate(b.slots):
+        if b.fresh[i]:
+            assert not conv_g[s].float().abs().any() and not ssm_g[s].abs().any(), f"fresh slot {s} not zeroed"
+        else:
+            assert_bits_equal(conv_g[s], conv0[s], f"resumed slot {s} conv")
+            assert_bits_equal(ssm_g[s], ssm0[s], f"resumed slot {s} ssm")
+    others = [s for s in range(conv0.shape[0]) if s not in set(b.slots)]
+    assert_bits_equal(conv_g[others], conv0[others], "other conv slots")
+    assert_bits_equal(ssm_g[others], ssm0[others], "other ssm slots")
