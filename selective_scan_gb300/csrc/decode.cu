@@ -53,8 +53,17 @@ __device__ __forceinline__ float ld_dsmem_f32(const float* local, uint32_t rank)
   return v;
 }
 
-template <typename T, int K>
-__global__ void __launch_bounds__(kDecodeThreads, 2)
+constexpr int kRingRows = 8;  // d_state = 128: state rows per ring stage (one float4 per lane per row)
+// float offset of the state ring in the dynamic shared memory (16-byte aligned) and its bytes
+__host__ __device__ constexpr int ring_offset(int hpc, int P, int G, int N) {
+  return (3 * hpc * P + 2 * G * N + 3 * hpc + kDecodeMaxNormGroups + kDecodeWarps + 3) & ~3;
+}
+constexpr int kRingBytes = kDecodeWarps * 2 * kRingRows * 32 * 16;
+
+// kRing: d_state = 128, the state streamed through a per-warp ring in shared memory
+// (no state rows held in registers, three CTAs per SM); otherwise rows in registers.
+template <typename T, int K, bool kRing>
+__global__ void __launch_bounds__(kDecodeThreads, kRing ? 3 : 2)
 decode_step_kernel(const __grid_constant__ DecodeArgs a) {
   constexpr int V = Vec16<T>::n;
   constexpr int HIST = K - 1;
@@ -108,7 +117,32 @@ decode_step_kernel(const __grid_constant__ DecodeArgs a) {
       if (!fresh && r < rows && q < nq) hv[u] = __ldcs(st + (int64_t)r * nq + q);
     }
   };
-  load_rows(base0, 0);
+  // kRing: warp w streams its rows [128 j + 16 w, +16) as two 8-row stages each
+  // (stage k: j = k / 2, half k % 2) through two ring slots filled by cp.async;
+  // stages 0 and 1 are issued now, stage k + 2 once stage k is done
+  float4* ring = reinterpret_cast<float4*>(dsm + ring_offset(a.heads_per_cta, P, G, N));
+  auto stage_base = [&](int k) { return (k >> 1) * (kDecodeWarps * 16) + warp * 16 + (k & 1) * kRingRows; };
+  auto issue = [&](int k) {
+    asm volatile("" ::: "memory");  // the slot's earlier shared-memory reads stay before its refill
+    const int base = stage_base(k);
+    if (base < rows) {
+      float4* slot = ring + (warp * 2 + (k & 1)) * kRingRows * 32 + lane;
+#pragma unroll
+      for (int u = 0; u < kRingRows; ++u) {
+        const int r = base + u;
+        const bool real = !fresh && r < rows;  // a fresh state is zeros: a zero-byte copy (source never read)
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(smem_addr(slot + u * 32)),
+                     "l"(real ? st + (int64_t)r * 32 + lane : st), "r"(real ? 16 : 0));
+      }
+    }
+    asm volatile("cp.async.commit_group;\n" ::: "memory");
+  };
+  if constexpr (kRing) {
+    issue(0);
+    issue(1);
+  } else {
+    load_rows(base0, 0);
+  }
 
   // ---- 1. conv for own x channels and all B/C channels -------------------
   const int nxv = rows / V;
@@ -200,7 +234,55 @@ decode_step_kernel(const __grid_constant__ DecodeArgs a) {
   __syncthreads();
 
   // ---- 2. state stream: h = h*decay + dt'*x*B; y = h.C + D*x -------------
-  if (lpr == 32 && qpl == 1) {
+  if constexpr (kRing) {
+    const int hpg = H / G;
+    for (int k = 0; stage_base(k) < rows; ++k) {
+      asm volatile("cp.async.wait_group 1;\n" ::: "memory");  // stage k has landed (k + 1 may be in flight)
+      const int base = stage_base(k);
+      const int hl = base / P;  // a stage lies in one head (P % 8 == 0)
+      const int g = (h0 + hl) / hpg;
+      const float dtp = hdt[hl], dec = hdec[hl];
+      const float4 b4 = *reinterpret_cast<const float4*>(bc + g * N + 4 * lane);
+      const float4 c4 = *reinterpret_cast<const float4*>(bc + G * N + g * N + 4 * lane);
+      const float4* slot = ring + (warp * 2 + (k & 1)) * kRingRows * 32 + lane;
+      float acc[kRingRows];
+#pragma unroll
+      for (int u = 0; u < kRingRows; ++u) {
+        const int r = base + u;
+        acc[u] = 0.0f;
+        if (r < rows) {
+          const float xd = dtp * xs[r];
+          float4 h = slot[u * 32];
+          h.x = fmaf(h.x, dec, xd * b4.x);
+          h.y = fmaf(h.y, dec, xd * b4.y);
+          h.z = fmaf(h.z, dec, xd * b4.z);
+          h.w = fmaf(h.w, dec, xd * b4.w);
+          __stcs(st + (int64_t)r * nq + lane, h);
+          float t = h.x * c4.x;
+          t = fmaf(h.y, c4.y, t);
+          t = fmaf(h.z, c4.z, t);
+          acc[u] = fmaf(h.w, c4.w, t);
+        }
+      }
+      // the 8 row sums across the warp by recursive halving, then the last two lane bits
+#pragma unroll
+      for (int d = 16, m = kRingRows; d >= 4; d >>= 1, m >>= 1) {
+        const bool upper = (lane & d) != 0;
+#pragma unroll
+        for (int i = 0; i < m / 2; ++i) {
+          const float send = upper ? acc[i] : acc[i + m / 2];
+          const float keep = upper ? acc[i + m / 2] : acc[i];
+          acc[i] = keep + __shfl_xor_sync(0xffffffffu, send, d);
+        }
+      }
+      acc[0] += __shfl_xor_sync(0xffffffffu, acc[0], 2);
+      acc[0] += __shfl_xor_sync(0xffffffffu, acc[0], 1);
+      const int rl = ((lane >> 4) & 1) * 4 + ((lane >> 3) & 1) * 2 + ((lane >> 2) & 1);
+      if ((lane & 3) == 0 && base + rl < rows) ys[base + rl] = acc[0];
+      issue(k + 2);
+    }
+    asm volatile("cp.async.wait_group 0;\n" ::: "memory");
+  } else if (lpr == 32 && qpl == 1) {
     // d_state = 128: one float4 per lane per row, rows of a 16-row batch all
     // in one head (P % 16 == 0), so B and C are loaded once per batch; the 16
     // row sums are reduced across the warp by recursive halving (16 shuffles
@@ -358,11 +440,12 @@ bool decode_supported(mamba2_dtype act, const mamba2_dims& d, int norm_groups) {
   return true;
 }
 
-template <typename T, int K>
-static cudaError_t launch_decode_t(const DecodeArgs& a, cudaStream_t st) {
-  const size_t smem = sizeof(float) * (3 * (size_t)a.heads_per_cta * a.headdim + 2 * (size_t)a.ngroups * a.d_state +
-                                       3 * (size_t)a.heads_per_cta + kDecodeMaxNormGroups + kDecodeWarps);
-  auto kern = decode_step_kernel<T, K>;
+template <typename T, int K, bool kRing>
+static cudaError_t launch_decode_tk(const DecodeArgs& a, cudaStream_t st) {
+  size_t smem = sizeof(float) * (3 * (size_t)a.heads_per_cta * a.headdim + 2 * (size_t)a.ngroups * a.d_state +
+                                 3 * (size_t)a.heads_per_cta + kDecodeMaxNormGroups + kDecodeWarps);
+  if (kRing) smem = sizeof(float) * (size_t)ring_offset(a.heads_per_cta, a.headdim, a.ngroups, a.d_state) + kRingBytes;
+  auto kern = decode_step_kernel<T, K, kRing>;
   if (a.cluster > kDecodePortableCluster) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     if (e != cudaSuccess) return e;
@@ -384,6 +467,12 @@ static cudaError_t launch_decode_t(const DecodeArgs& a, cudaStream_t st) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, kern, a);
+}
+
+template <typename T, int K>
+static cudaError_t launch_decode_t(const DecodeArgs& a, cudaStream_t st) {
+  if (a.d_state == 128 && a.headdim % kRingRows == 0) return launch_decode_tk<T, K, true>(a, st);
+  return launch_decode_tk<T, K, false>(a, st);
 }
 
 cudaError_t launch_decode(const DecodeArgs& a, mamba2_dtype act, cudaStream_t st) {
