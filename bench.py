@@ -277,6 +277,22 @@ def cpu_baseline(target_s=12.0):
                       f"48 heads), {t:.1f} s"}
 
 
+def max_over_ranks(values, world, device):
+    """Each rank's timings replaced by their maximum over the ranks (the job ends with
+    its slowest replica); the identity on one rank."""
+    if world <= 1:
+        return list(values)
+    t = torch.tensor(list(values), dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return t.tolist()
+
+
+def job_throughput(world, tokens_per_rank, ms):
+    """Whole-job tokens/s: `world` replicas, each processing tokens_per_rank tokens, the
+    slowest in `ms` milliseconds (weak scaling: the work per GPU is fixed)."""
+    return world * tokens_per_rank / (ms * 1e-3)
+
+
 def run_ours(args, rank, world, local_rank):
     import selective_scan_gb300 as ss
     dev = torch.device("cuda", local_rank)
@@ -313,10 +329,7 @@ def run_ours(args, rank, world, local_rank):
     t_norm = sum(e[2].elapsed_time(e[3]) for e in evs) / args.steps
     t_tail = sum(e[3].elapsed_time(e[4]) for e in evs) / args.steps
     t_prefill = t_conv + t_scan + t_norm
-    if world > 1:
-        tt = torch.tensor([total_ms, t_prefill], device=dev)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        total_ms, t_prefill = tt.tolist()
+    total_ms, t_prefill = max_over_ranks([total_ms, t_prefill], world, dev)
 
     T = args.tokens
     gb = lambda nbytes, ms: nbytes / (ms * 1e-3) / 1e9  # noqa: E731
@@ -362,14 +375,11 @@ def run_ours(args, rank, world, local_rank):
     a1.record()
     torch.cuda.synchronize()
     e2e_ms = a0.elapsed_time(a1) / e2e_steps
-    if world > 1:
-        tt = torch.tensor([e2e_ms], device=dev)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        e2e_ms = tt.item()
+    (e2e_ms,) = max_over_ranks([e2e_ms], world, dev)
 
     line = {
         "metric": METRIC,
-        "value": world * T / (t_prefill * 1e-3),
+        "value": job_throughput(world, T, t_prefill),
         "unit": "tokens/s",
         "n_gpus": world,
         "steps": args.steps,
@@ -395,7 +405,7 @@ def run_ours(args, rank, world, local_rank):
                    "us_per_step": dec_us, "tokens_per_s": dec_n / (dec_us * 1e-6), "GB/s": dec_gbs,
                    "roofline_frac": dec_gbs / hbm, "roofline_frac_8TBs": dec_gbs / 8000.0,
                    "bytes_per_step": dec_bytes, "steps_timed": dec_steps},
-        "e2e": {"value": world * T / (e2e_ms * 1e-3), "unit": "tokens/s",
+        "e2e": {"value": job_throughput(world, T, e2e_ms), "unit": "tokens/s",
                 "h2d_bytes_per_step": hx.numel() * 2 + hz.numel() * 2 + hdt.numel() * 2,
                 "d2h_bytes_per_step": hout.numel() * 2, "api": "mamba2_prefill_host",
                 "piece_rows": args.e2e_piece},
