@@ -277,6 +277,11 @@ def cpu_baseline(target_s=12.0):
                       f"48 heads), {t:.1f} s"}
 
 
+def output_digest(t) -> str:
+    """SHA-256 of a tensor's bytes (device tensors are copied to the host first)."""
+    return hashlib.sha256(t.detach().contiguous().cpu().view(torch.uint8).numpy().tobytes()).hexdigest()
+
+
 def max_over_ranks(values, world, device):
     """Each rank's timings replaced by their maximum over the ranks (the job ends with
     its slowest replica); the identity on one rank."""
@@ -310,6 +315,9 @@ def run_ours(args, rank, world, local_rank):
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
+    # every prefill step is fresh and every kernel reduces in a fixed order, so each
+    # step's output is bit-identical: the warm-up digest must survive the timed loop
+    digest_warm = output_digest(pf.out)
     if world > 1:
         torch.distributed.barrier()
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
@@ -330,6 +338,9 @@ def run_ours(args, rank, world, local_rank):
     t_tail = sum(e[3].elapsed_time(e[4]) for e in evs) / args.steps
     t_prefill = t_conv + t_scan + t_norm
     total_ms, t_prefill = max_over_ranks([total_ms, t_prefill], world, dev)
+    digest_timed = output_digest(pf.out)
+    if digest_timed != digest_warm:
+        raise SystemExit("prefill output of the timed steps differs from the warm-up output")
 
     T = args.tokens
     gb = lambda nbytes, ms: nbytes / (ms * 1e-3) / 1e9  # noqa: E731
@@ -368,6 +379,7 @@ def run_ours(args, rank, world, local_rank):
 
     e2e_step()
     torch.cuda.synchronize()
+    e2e_digest_first = output_digest(hout)
     a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     a0.record()
     for _ in range(e2e_steps):
@@ -375,6 +387,8 @@ def run_ours(args, rank, world, local_rank):
     a1.record()
     torch.cuda.synchronize()
     e2e_ms = a0.elapsed_time(a1) / e2e_steps
+    if output_digest(hout) != e2e_digest_first:
+        raise SystemExit("streamed host prefill output changed between calls")
     (e2e_ms,) = max_over_ranks([e2e_ms], world, dev)
 
     line = {
@@ -410,6 +424,8 @@ def run_ours(args, rank, world, local_rank):
                 "d2h_bytes_per_step": hout.numel() * 2, "api": "mamba2_prefill_host",
                 "piece_rows": args.e2e_piece},
         "gpu_launches": args.steps * (1 + pf.scan_launches + 1 + DECODE_TAIL),
+        "output_digest": {"prefill_sha256": digest_timed, "stable_over_timed_steps": True,
+                          "e2e_sha256": e2e_digest_first, "stable_over_e2e_steps": True},
         "clocks": clk.summary(),
     }
     if rank == 0 and not args.no_cpu_baseline:
