@@ -72,7 +72,7 @@ constexpr int TN = 128;  // d_state
 constexpr int kMathWarps = 16;
 constexpr int kMathThreads = 32 * kMathWarps;
 constexpr int kFullThreads = kMathThreads + 4 * 32;   // + CB (and dt), Yoff, dH, Y issuers
-constexpr int kStateThreads = kMathThreads + 3 * 32;  // + loader, dH issuer, weight producer
+constexpr int kStateThreads = kMathThreads + 4 * 32;  // + X loader, B loader, dH issuer, weight producer
 constexpr uint32_t kWaitLimit = 1u << 22;  // try_wait rounds before giving up (about a second at the backoff)
 constexpr uint32_t kSuspendNs = 1000;      // a waiting thread sleeps up to this long per try_wait round
 
@@ -102,15 +102,19 @@ constexpr uint32_t kOffMisc = kOffBar + 8 * kNumFullBars;  // TMEM base, abort f
 constexpr uint32_t kFullSmem = kOffMisc + 16 + 1024;        // + slack to align the base to 1024
 static_assert(kFullSmem <= 232448, "full-pass shared memory plan exceeds 227 KB");
 
-// ---- state pass: shared memory (3 stages of B, X), TMEM D = [hi part | lo part] in [0,128)
-constexpr int kStStages = 3;
-constexpr uint32_t kStStage = kTileB + kTileX;
-constexpr uint32_t kStOffXW = kStStages * kStStage;   // [2][hi, lo] X o w tiles
-constexpr uint32_t kStOffW = kStOffXW + 4 * kTileX;   // [4][TQ] token weights (chunk i in i % 4)
-constexpr uint32_t kStOffR = kStOffW + 4 * TQ * 4;    // total log2 decay of the segment
+// ---- state pass: shared memory (4 stages of X, 3 of B), TMEM D = [hi part | lo part] in [0,128).
+// An X stage is free once X o w has read it, a B stage once the dH product has,
+// so the X loads (from HBM) run a chunk further ahead than the B loads (L2).
+constexpr int kStNX = 4;                               // X stages (chunk i in i % 4)
+constexpr int kStNB = 3;                               // B stages (chunk i in i % 3)
+constexpr int kStNW = 2;                               // token-weight buffers (chunk i in i % 2)
+constexpr uint32_t kStOffB = kStNX * kTileX;
+constexpr uint32_t kStOffXW = kStOffB + kStNB * kTileB;  // [2][hi, lo] X o w tiles
+constexpr uint32_t kStOffW = kStOffXW + 4 * kTileX;      // [kStNW][TQ] token weights
+constexpr uint32_t kStOffR = kStOffW + kStNW * TQ * 4;   // total log2 decay of the segment
 constexpr uint32_t kStOffBar = kStOffR + 16;
-enum StateBar : int {  // + chunk % 3 (stages) or chunk % 4 (weights)
-  kStFull = 0, kStDHDone = 3, kStXWReady = 6, kStWReady = 10, kNumStateBars = 14
+enum StateBar : int {  // + chunk % 4 (X stages, X o w ready), % 3 (B stages, dH done) or % 2 (weights)
+  kStFullX = 0, kStFullB = 4, kStDHDone = 7, kStXWReady = 10, kStWReady = 14, kNumStateBars = 16
 };
 constexpr uint32_t kStOffMisc = kStOffBar + 8 * kNumStateBars;
 constexpr uint32_t kStateSmem = kStOffMisc + 16 + 1024;
@@ -827,9 +831,10 @@ ssd_tc_full(const __grid_constant__ ScanArgs a, const __grid_constant__ CUtensor
 // w_j = 2^(R + S_end - S_j) dt'_j (S the chunk's cumulative log2 decay), so
 // B^T . (X o w) of every chunk accumulates into the same TMEM columns.
 //   warps 0-15  X o w (bf16 hi + lo); at the end, the segment's state
-//   warp 16     B and X tile loads (three stages)
-//   warp 17     dH^T += B^T . [X o w hi | lo]  (M=128 N=128 K=128 per chunk)
-//   warp 18     dt' and the token weights, up to four chunks ahead
+//   warp 16     X tile loads (four stages)
+//   warp 17     B tile loads (three stages)
+//   warp 18     dH^T += B^T . [X o w hi | lo]  (M=128 N=128 K=128 per chunk)
+//   warp 19     dt' and the token weights, up to two chunks ahead
 __global__ void __launch_bounds__(kStateThreads, 1)
 ssd_tc_state(const __grid_constant__ ScanArgs a, const __grid_constant__ CUtensorMap tm, const int use_tma) {
   // CTA b: piece q = b % P of segment b / P, an equal share of the segment's
@@ -863,9 +868,11 @@ ssd_tc_state(const __grid_constant__ ScanArgs a, const __grid_constant__ CUtenso
   float* s_w = reinterpret_cast<float*>(smem + kStOffW);
   float* s_R = reinterpret_cast<float*>(smem + kStOffR);
   auto bar = [&](int id) { return sbase + kStOffBar + 8u * (uint32_t)id; };
-  auto stg = [&](int i) { return sbase + (uint32_t)(i % kStStages) * kStStage; };
-  auto p3 = [](int i) { return (uint32_t)((i / kStStages) & 1); };  // phase parity on a [3] barrier
-  auto p4 = [](int i) { return (uint32_t)((i >> 2) & 1); };         // phase parity on a [4] barrier
+  auto stg_x = [&](int i) { return sbase + (uint32_t)(i % kStNX) * kTileX; };
+  auto stg_b = [&](int i) { return sbase + kStOffB + (uint32_t)(i % kStNB) * kTileB; };
+  auto p3 = [](int i) { return (uint32_t)((i / 3) & 1); };   // phase parity on a [3] barrier
+  auto p4 = [](int i) { return (uint32_t)((i >> 2) & 1); };  // phase parity on a [4] barrier
+  auto p2 = [](int i) { return (uint32_t)((i >> 1) & 1); };  // phase parity on a [2] barrier
 
   const int n = ci.n;  // >= 1 here
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -875,14 +882,15 @@ ssd_tc_state(const __grid_constant__ ScanArgs a, const __grid_constant__ CUtenso
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
   }
   if (tid == kMathThreads) {
-    for (int s = 0; s < kStStages; ++s) {
-      mbar_init(bar(kStFull + s), 2);    // B tile, X tile
+    for (int s = 0; s < kStNB; ++s) {
+      mbar_init(bar(kStFullB + s), 1);
       mbar_init(bar(kStDHDone + s), 1);
     }
-    for (int b = 0; b < 4; ++b) {
+    for (int b = 0; b < kStNX; ++b) {
+      mbar_init(bar(kStFullX + b), 1);
       mbar_init(bar(kStXWReady + b), kMathWarps);
-      mbar_init(bar(kStWReady + b), 1);
     }
+    for (int b = 0; b < kStNW; ++b) mbar_init(bar(kStWReady + b), 1);
     *s_abort = 0u;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -910,15 +918,15 @@ ssd_tc_state(const __grid_constant__ ScanArgs a, const __grid_constant__ CUtenso
     auto ws_entry = [&](int segidx) -> float* { return a.ws_state + (int64_t)segidx * H * TP * TN + head_off; };
     bool live = true;
     for (int i = 0; i < n; ++i) {
-      bool ok = warp_wait(bar(kStFull + i % kStStages), p3(i), s_abort) &&
-                warp_wait(bar(kStWReady + (i & 3)), p4(i), s_abort);
-      if (ok && i >= 2) ok = warp_wait(bar(kStDHDone + (i - 2) % kStStages), p3(i - 2), s_abort);  // X o w buffer read
+      bool ok = warp_wait(bar(kStFullX + (i & 3)), p4(i), s_abort) &&
+                warp_wait(bar(kStWReady + (i & 1)), p2(i), s_abort);
+      if (ok && i >= 2) ok = warp_wait(bar(kStDHDone + (i - 2) % kStNB), p3(i - 2), s_abort);  // X o w buffer read
       if (!ok) {
         live = false;
         break;
       }
-      const float w = s_w[(i & 3) * TQ + row];
-      const unsigned char* xt = smem + (uint32_t)(i % kStStages) * kStStage + kTileB;
+      const float w = s_w[(i & 1) * TQ + row];
+      const unsigned char* xt = smem + (uint32_t)(i % kStNX) * kTileX;
       unsigned char* xw = smem + kStOffXW + (uint32_t)(i & 1) * 2 * kTileX;
 #pragma unroll
       for (int q = 0; q < 2; ++q) {
@@ -936,7 +944,7 @@ ssd_tc_state(const __grid_constant__ ScanArgs a, const __grid_constant__ CUtenso
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(kStXWReady + (i & 3)));
     }
-    if (live && warp_wait(bar(kStDHDone + (n - 1) % kStStages), p3(n - 1), s_abort)) {
+    if (live && warp_wait(bar(kStDHDone + (n - 1) % kStNB), p3(n - 1), s_abort)) {
       tc_fence_after();
       float dhi[16], dlo[16];
       tmem_ld16x2(tmem + lane_off + 16 * cg, tmem + lane_off + 64 + 16 * cg, dhi, dlo);
@@ -962,40 +970,48 @@ ssd_tc_state(const __grid_constant__ ScanArgs a, const __grid_constant__ CUtenso
       if (tid == 0) a.ws_decay[(int64_t)entry * H + ci.h] = Rt * 0.6931471805599453f;
     }
   } else if (warp == kMathWarps) {
-    // =================== B and X tile loads
+    // =================== X tile loads: stage i % 4 is free once X o w of chunk i - 4 is done
     int loaded = 0;
     for (int i = 0; i < n; ++i) {
-      if (i >= kStStages && !warp_wait(bar(kStDHDone + i % kStStages), p3(i - kStStages), s_abort)) break;
-      const ChunkSrc s = chunk_src(i);
-      load_tile(stg(i), s, &tm, use_tma != 0, ci.b_col, TN, bar(kStFull + i % kStStages), lane);
-      load_tile(stg(i) + kTileB, s, &tm, use_tma != 0, ci.x_col, TP, bar(kStFull + i % kStStages), lane);
+      if (i >= kStNX && !warp_wait(bar(kStXWReady + (i & 3)), p4(i - kStNX), s_abort)) break;
+      load_tile(stg_x(i), chunk_src(i), &tm, use_tma != 0, ci.x_col, TP, bar(kStFullX + (i & 3)), lane);
       loaded = i + 1;
     }
     if (lane == 0 && *s_abort)
-      for (int i = max(0, loaded - kStStages); i < loaded; ++i) drain_bar(bar(kStFull + i % kStStages), p3(i));
+      for (int i = max(0, loaded - kStNX); i < loaded; ++i) drain_bar(bar(kStFullX + (i & 3)), p4(i));
   } else if (warp == kMathWarps + 1) {
+    // =================== B tile loads: stage i % 3 is free once the dH product of chunk i - 3 is done
+    int loaded = 0;
+    for (int i = 0; i < n; ++i) {
+      if (i >= kStNB && !warp_wait(bar(kStDHDone + i % kStNB), p3(i - kStNB), s_abort)) break;
+      load_tile(stg_b(i), chunk_src(i), &tm, use_tma != 0, ci.b_col, TN, bar(kStFullB + i % kStNB), lane);
+      loaded = i + 1;
+    }
+    if (lane == 0 && *s_abort)
+      for (int i = max(0, loaded - kStNB); i < loaded; ++i) drain_bar(bar(kStFullB + i % kStNB), p3(i));
+  } else if (warp == kMathWarps + 2) {
     // =================== dH^T += B^T . [X o w hi | X o w lo] (one N=128 product per chunk)
     if (lane == 0) {
       int last = -1;
       for (int i = 0; i < n; ++i) {
-        if (!wait_bar(bar(kStFull + i % kStStages), p3(i), s_abort)) break;
+        if (!wait_bar(bar(kStFullB + i % kStNB), p3(i), s_abort)) break;
         if (!wait_bar(bar(kStXWReady + (i & 3)), p4(i), s_abort)) break;
         tc_fence_after();
-        const uint64_t bt0 = sdesc(stg(i), TQ * 128, 1024);
+        const uint64_t bt0 = sdesc(stg_b(i), TQ * 128, 1024);
         const uint64_t xw0 = sdesc(sbase + kStOffXW + (uint32_t)(i & 1) * 2 * kTileX, kTileX, 1024);  // hi | lo blocks
 #pragma unroll
         for (int s2 = 0; s2 < TQ / 16; ++s2) {
           const uint32_t jk = (s2 * 2048) >> 4;
           mma_ss(tmem, bt0 + jk, xw0 + jk, idesc128(128, 1, 1), (i > 0 || s2 > 0) ? 1u : 0u);
         }
-        mma_commit(bar(kStDHDone + i % kStStages));
+        mma_commit(bar(kStDHDone + i % kStNB));
         last = i;
       }
-      if (last >= 0) drain_bar(bar(kStDHDone + last % kStStages), p3(last));
+      if (last >= 0) drain_bar(bar(kStDHDone + last % kStNB), p3(last));
     }
   } else {
-    // =================== dt' and token weights of chunk i into ring slot i % 4
-    // (lane l: tokens 4l .. 4l+3); slot i % 4 last served chunk i-4
+    // =================== dt' and token weights of chunk i into buffer i % 2
+    // (lane l: tokens 4l .. 4l+3); buffer i % 2 last served chunk i-2
     // dt' of chunks i .. i+3, loaded four chunks ahead
     const int64_t rows_all = a.tab.cu[a.tab.n];
     auto load_dtp = [&](int i) {
@@ -1012,7 +1028,7 @@ ssd_tc_state(const __grid_constant__ ScanArgs a, const __grid_constant__ CUtenso
     float R = 0.f;  // log2 decay from the end of the chunks already read to the segment end
     DtQuad r0 = load_dtp(0), r1 = load_dtp(1), r2 = load_dtp(2), r3 = load_dtp(3);
     for (int i = 0; i < n; ++i) {
-      if (i >= 4 && !warp_wait(bar(kStXWReady + (i & 3)), p4(i - 4), s_abort)) break;
+      if (i >= kStNW && !warp_wait(bar(kStXWReady + ((i - kStNW) & 3)), p4(i - kStNW), s_abort)) break;
       float dp[4], S[4], run = 0.f;
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
@@ -1027,12 +1043,12 @@ ssd_tc_state(const __grid_constant__ ScanArgs a, const __grid_constant__ CUtenso
       const float incl = warp_incl_sum(run, lane);
       const float tot = __shfl_sync(0xffffffffu, incl, 31);
       const float base = R + (tot - (incl - run));  // R + S_end - (S before this lane's tokens)
-      *reinterpret_cast<float4*>(s_w + (i & 3) * TQ + 4 * lane) =
+      *reinterpret_cast<float4*>(s_w + (i & 1) * TQ + 4 * lane) =
           make_float4(ex2(base - S[0]) * dp[0], ex2(base - S[1]) * dp[1], ex2(base - S[2]) * dp[2], ex2(base - S[3]) * dp[3]);
       R += tot;
       if (i == n - 1 && lane == 0) *s_R = R;
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(kStWReady + (i & 3)));
+      if (lane == 0) mbar_arrive(bar(kStWReady + (i & 1)));
     }
   }
 
