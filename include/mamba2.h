@@ -11,6 +11,8 @@
  * three ops over activations in host memory, streamed in pieces so the
  * host-device copies overlap the compute. The stateful calls take a
  * RecurrentBatch: per sequence a run of rows, a state slot and a fresh flag.
+ * mamba2_decode_step_device takes the decode batch from device memory
+ * instead, for CUDA-graph replay.
  *
  * Conventions shared by every entry point
  * ---------------------------------------
@@ -22,6 +24,8 @@
  *  - Batch metadata (mamba2_recurrent_batch) is HOST memory. It is validated
  *    on the host and passed to the kernels by value in their launch
  *    parameters, so the host arrays may be reused as soon as the call returns.
+ *    (mamba2_decode_step_device alone reads its batch from device memory and
+ *    checks it on the device, as its comment describes.)
  *  - `stream` is a cudaStream_t (NULL = the legacy default stream). Calls are
  *    asynchronous and ordered on that stream; the current CUDA device must be
  *    the one owning the buffers.
@@ -31,7 +35,9 @@
  *  - Errors: every check runs on the host before anything is enqueued, so a
  *    non-OK status means no buffer was touched. Checks run in this order:
  *    arguments, slot range, shared slots, run coverage. MAMBA2_ERR_CUDA
- *    reports a failed launch (nothing else can fail after validation).
+ *    reports a failed launch (nothing else can fail after validation). The
+ *    device batch of mamba2_decode_step_device is checked on the device,
+ *    with the same rules in the same order.
  *  - A fresh sequence starts from zero state and never reads its slot; its
  *    slot is written with the sequence's end state.
  */
@@ -234,6 +240,52 @@ mamba2_status mamba2_decode_step(void* dst, const void* xBC, const void* z,
                                  mamba2_dtype act,
                                  const mamba2_recurrent_batch* rb,
                                  void* stream);
+
+/*
+ * mamba2_decode_step with the batch in DEVICE memory, so that one captured
+ * CUDA graph serves every step: the caller rewrites the slot, fresh and count
+ * arrays between replays (InfiniLM PR #575, "Summary": indexed recurrent
+ * Decode replayed through Decode graphs; "Benchmark / Performance Impact":
+ * graphs cut the per-token latency at batch one).
+ *
+ *   slots_dev    [capacity] int32, device: slot of sequence s
+ *   fresh_dev    [capacity] uint8, device: nonzero = fresh
+ *   num_seqs_dev int32, device: n, the sequences of this step (0 <= n <= capacity)
+ *   capacity     host, 1 <= capacity <= MAMBA2_MAX_SEQS: the grid is sized
+ *                for it; sequence s < n uses row s of dst, xBC, z and dt
+ *   status_dev   int32, device: receives this step's mamba2_status
+ *
+ * The other arguments, layouts and arithmetic are those of mamba2_decode_step
+ * (bit-identical results when capacity equals that call's num_seqs; the
+ * capacity sets the CTAs per sequence, and with it the order of the norm's
+ * partial sums). Two kernels run on the
+ * stream. The first checks the batch on the device, in the host check's
+ * order and with its rules (gllm PR #85, "Ops": reject a slot out of range or
+ * a slot shared by two sequences): n outside [0, capacity] gives
+ * MAMBA2_ERR_INVALID_ARGUMENT, then MAMBA2_ERR_SLOT_OUT_OF_RANGE, then
+ * MAMBA2_ERR_SLOT_SHARED, else MAMBA2_OK, written to *status_dev. The
+ * second is the fused step; it touches nothing (no output row, no pool
+ * entry) unless that status is MAMBA2_OK, and rows >= n of dst are never
+ * written. So a rejected step leaves every buffer but *status_dev
+ * bit-identical; read *status_dev once the stream has passed the call.
+ * The return value covers only the host checks (null or misaligned pointers,
+ * capacity, shape support: nothing enqueued) and launch failures
+ * (MAMBA2_ERR_CUDA). No host synchronisation, allocation or copy: the call
+ * can be captured into a CUDA graph.
+ */
+mamba2_status mamba2_decode_step_device(void* dst, const void* xBC, const void* z,
+                                        const void* dt, const float* conv_w,
+                                        const float* conv_b, const float* A_log,
+                                        const float* dt_bias, const float* D,
+                                        const float* norm_w, int32_t norm_groups,
+                                        float eps, void* conv_state,
+                                        float* ssm_state, int32_t num_slots,
+                                        const mamba2_dims* dims, mamba2_dtype act,
+                                        const int32_t* slots_dev,
+                                        const uint8_t* fresh_dev,
+                                        const int32_t* num_seqs_dev,
+                                        int32_t capacity, int32_t* status_dev,
+                                        void* stream);
 
 /*
  * Bytes of device workspace mamba2_prefill_host needs for this batch, piece

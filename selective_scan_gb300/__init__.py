@@ -67,6 +67,8 @@ def _lib():
         lib.mamba2_gated_rmsnorm.argtypes = [p, p, p, p, i32, i32, i32, f32, ctypes.c_int, p]
         lib.mamba2_decode_step.argtypes = [p, p, p, p, p, p, p, p, p, p, i32, f32, p, p, i32, dims,
                                            ctypes.c_int, rb, p]
+        lib.mamba2_decode_step_device.argtypes = [p, p, p, p, p, p, p, p, p, p, i32, f32, p, p, i32, dims,
+                                                  ctypes.c_int, p, p, p, i32, p, p]
         lib.mamba2_state_bytes_per_layer.argtypes = [dims, ctypes.c_int]
         lib.mamba2_state_bytes_per_layer.restype = ctypes.c_int64
         lib.mamba2_status_string.argtypes = [ctypes.c_int]
@@ -77,7 +79,7 @@ def _lib():
         lib.mamba2_prefill_host.argtypes = [p, p, p, p, p, p, p, p, p, p, i32, f32, p, p, i32, dims, ctypes.c_int,
                                             rb, i32, p, sz, p]
         for name in ("mamba2_causal_conv1d", "mamba2_ssd_scan", "mamba2_gated_rmsnorm", "mamba2_decode_step",
-                     "mamba2_prefill_host"):
+                     "mamba2_decode_step_device", "mamba2_prefill_host"):
             getattr(lib, name).restype = ctypes.c_int
         _LIB = lib
     return _LIB
@@ -230,6 +232,28 @@ def decode_step(dst, xBC, z, dt, conv_w, conv_b, A_log, dt_bias, D, norm_w, norm
                                    ctypes.byref(d), _dt(xBC), b.ref(), _stream(stream))
     if check:
         _check(st, "mamba2_decode_step")
+    return st
+
+
+def decode_step_device(dst, xBC, z, dt, conv_w, conv_b, A_log, dt_bias, D, norm_w, norm_groups, eps,
+                       conv_state, ssm_state, dims, slots_dev, fresh_dev, num_seqs_dev, status_dev,
+                       stream=None, check=True) -> int:
+    """``mamba2_decode_step_device``: the fused decode step with its batch in device memory.
+
+    ``slots_dev`` (int32), ``fresh_dev`` (uint8) are device tensors of the capacity
+    (their length); ``num_seqs_dev`` and ``status_dev`` are one-element int32 device
+    tensors. The batch is checked on the device: ``status_dev`` holds the outcome once
+    the stream has passed the call. The return value covers the host checks only.
+    """
+    d = _dims(dims)
+    st = _lib().mamba2_decode_step_device(_ptr(dst), _ptr(xBC), _ptr(z), _ptr(dt), _ptr(conv_w), _ptr(conv_b),
+                                          _ptr(A_log), _ptr(dt_bias), _ptr(D), _ptr(norm_w), int(norm_groups),
+                                          float(eps), _ptr(conv_state), _ptr(ssm_state), ssm_state.shape[0],
+                                          ctypes.byref(d), _dt(xBC), _ptr(slots_dev), _ptr(fresh_dev),
+                                          _ptr(num_seqs_dev), int(slots_dev.shape[0]), _ptr(status_dev),
+                                          _stream(stream))
+    if check:
+        _check(st, "mamba2_decode_step_device")
     return st
 
 

@@ -476,6 +476,66 @@ mamba2_status mamba2_decode_step(void* dst, const void* xBC, const void* z, cons
   return e == cudaSuccess ? MAMBA2_OK : cuda_fail(e);
 }
 
+mamba2_status mamba2_decode_step_device(void* dst, const void* xBC, const void* z, const void* dt,
+                                        const float* conv_w, const float* conv_b, const float* A_log,
+                                        const float* dt_bias, const float* D, const float* norm_w,
+                                        int32_t norm_groups, float eps, void* conv_state, float* ssm_state,
+                                        int32_t num_slots, const mamba2_dims* dims, mamba2_dtype act,
+                                        const int32_t* slots_dev, const uint8_t* fresh_dev,
+                                        const int32_t* num_seqs_dev, int32_t capacity, int32_t* status_dev,
+                                        void* stream) {
+  if (!act_ok(act) || !dims_ok(dims) || !(eps >= 0.0f) || norm_groups <= 0) return MAMBA2_ERR_INVALID_ARGUMENT;
+  if (!decode_supported(act, *dims, norm_groups)) return MAMBA2_ERR_NOT_IMPLEMENTED;
+  if (capacity < 1 || capacity > MAMBA2_MAX_SEQS || num_slots < 0) return MAMBA2_ERR_INVALID_ARGUMENT;
+  const void* ptrs[] = {dst, xBC, z, dt, conv_w, conv_b, A_log, dt_bias, D, norm_w, ssm_state,
+                        slots_dev, fresh_dev, num_seqs_dev, status_dev};
+  for (const void* p : ptrs)
+    if (!p) return MAMBA2_ERR_INVALID_ARGUMENT;
+  if (dims->conv_kernel > 1 && !conv_state) return MAMBA2_ERR_INVALID_ARGUMENT;
+  if (!aligned16(dst) || !aligned16(xBC) || !aligned16(z) || !aligned16(ssm_state) ||
+      (dims->conv_kernel > 1 && !aligned16(conv_state)) || !aligned16(norm_w))
+    return MAMBA2_ERR_INVALID_ARGUMENT;
+  const auto aligned4 = [](const void* q) { return (reinterpret_cast<uintptr_t>(q) & 3u) == 0; };
+  if (!aligned4(slots_dev) || !aligned4(num_seqs_dev) || !aligned4(status_dev)) return MAMBA2_ERR_INVALID_ARGUMENT;
+
+  DecodeArgs a;
+  std::memset(&a, 0, sizeof a);
+  a.dst = dst;
+  a.xBC = xBC;
+  a.z = z;
+  a.dt = dt;
+  a.conv_w = conv_w;
+  a.conv_b = conv_b;
+  a.A_log = A_log;
+  a.dt_bias = dt_bias;
+  a.D = D;
+  a.norm_w = norm_w;
+  a.conv_state = conv_state;
+  a.ssm_state = ssm_state;
+  a.heads = dims->heads;
+  a.headdim = dims->headdim;
+  a.d_state = dims->d_state;
+  a.ngroups = dims->ngroups;
+  a.conv_kernel = dims->conv_kernel;
+  a.norm_groups = norm_groups;
+  a.eps = eps;
+  // the grid is sized for the capacity (clusters past the device count leave at once)
+  const int cl_max =
+      (int64_t)capacity * kDecodeMaxCluster <= device_sm_count() ? kDecodeMaxCluster : kDecodePortableCluster;
+  const int cl = std::min(cl_max, dims->heads);
+  a.heads_per_cta = (dims->heads + cl - 1) / cl;
+  a.cluster = (dims->heads + a.heads_per_cta - 1) / a.heads_per_cta;
+  a.tab.n = capacity;
+  a.dev_slots = slots_dev;
+  a.dev_fresh = fresh_dev;
+  a.dev_n = num_seqs_dev;
+  a.dev_status = status_dev;
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = launch_check_device_batch(slots_dev, num_seqs_dev, capacity, num_slots, status_dev, st);
+  if (e == cudaSuccess) e = launch_decode(a, act, st);
+  return e == cudaSuccess ? MAMBA2_OK : cuda_fail(e);
+}
+
 size_t mamba2_prefill_host_workspace_bytes(const mamba2_dims* dims, mamba2_dtype act,
                                            const mamba2_recurrent_batch* rb, int32_t piece_rows) {
   if (!act_ok(act) || !dims_ok(dims) || piece_rows < 1 || !rb || !rb->cu_seqlens || rb->num_seqs < 0 ||

@@ -78,8 +78,12 @@ decode_step_kernel(const __grid_constant__ DecodeArgs a) {
   const int h1 = min(H, h0 + a.heads_per_cta);
   const int nh = max(0, h1 - h0);
   const int rows = nh * P;  // state rows owned by this CTA
-  const bool fresh = seq_fresh(a.tab, s);
-  const int64_t slot = seq_slot(a.tab, s);
+  const bool dev = a.dev_slots != nullptr;
+  // a device batch: every CTA of a cluster reads the same status word and count (written
+  // by the batch check before this launch), so a cluster leaves whole, before any barrier
+  if (dev && (__ldg(a.dev_status) != 0 || s >= __ldg(a.dev_n))) return;
+  const bool fresh = dev ? __ldg(a.dev_fresh + s) != 0 : seq_fresh(a.tab, s);
+  const int64_t slot = dev ? (int64_t)__ldg(a.dev_slots + s) : (int64_t)seq_slot(a.tab, s);
 
   float* xs = dsm;                           // [heads_per_cta * P] conv output x
   float* ys = xs + a.heads_per_cta * P;      // [heads_per_cta * P] y, then g
@@ -440,6 +444,50 @@ bool decode_supported(mamba2_dtype act, const mamba2_dims& d, int norm_groups) {
   return true;
 }
 
+// The batch check of a device batch, in the host check's order: the count, then every
+// slot's range, then slots named twice (a bitmap in shared memory when the pool has at
+// most kCheckBitmapWords * 32 slots, else pairwise). One CTA; writes only *status.
+constexpr int kCheckThreads = 1024;
+constexpr int kCheckBitmapWords = 8192;  // 32 KB
+__global__ void __launch_bounds__(kCheckThreads) check_device_batch_kernel(const int32_t* __restrict__ slots,
+                                                                          const int32_t* __restrict__ n_ptr,
+                                                                          int32_t capacity, int32_t num_slots,
+                                                                          int32_t* __restrict__ status) {
+  extern __shared__ uint32_t seen[];
+  const int n = *n_ptr;
+  if (n < 0 || n > capacity) {  // the same n in every thread: the CTA leaves together
+    if (threadIdx.x == 0) *status = MAMBA2_ERR_INVALID_ARGUMENT;
+    return;
+  }
+  int bad = 0;
+  for (int i = threadIdx.x; i < n; i += blockDim.x) {
+    const int32_t sl = slots[i];
+    bad |= (sl < 0 || sl >= num_slots) ? 1 : 0;
+  }
+  if (__syncthreads_or(bad)) {
+    if (threadIdx.x == 0) *status = MAMBA2_ERR_SLOT_OUT_OF_RANGE;
+    return;
+  }
+  int dup = 0;
+  const int words = (num_slots + 31) / 32;
+  if (words <= kCheckBitmapWords) {
+    for (int w = threadIdx.x; w < words; w += blockDim.x) seen[w] = 0u;
+    __syncthreads();
+    for (int i = threadIdx.x; i < n; i += blockDim.x) {
+      const int32_t sl = slots[i];  // in range here
+      const uint32_t bit = 1u << (sl & 31);
+      dup |= (atomicOr(&seen[sl >> 5], bit) & bit) ? 1 : 0;
+    }
+  } else {
+    for (int i = threadIdx.x; i < n; i += blockDim.x) {
+      const int32_t sl = slots[i];
+      for (int j = 0; j < i; ++j) dup |= (slots[j] == sl) ? 1 : 0;
+    }
+  }
+  dup = __syncthreads_or(dup);
+  if (threadIdx.x == 0) *status = dup ? MAMBA2_ERR_SLOT_SHARED : MAMBA2_OK;
+}
+
 template <typename T, int K, bool kRing>
 static cudaError_t launch_decode_tk(const DecodeArgs& a, cudaStream_t st) {
   size_t smem = sizeof(float) * (3 * (size_t)a.heads_per_cta * a.headdim + 2 * (size_t)a.ngroups * a.d_state +
@@ -473,6 +521,14 @@ template <typename T, int K>
 static cudaError_t launch_decode_t(const DecodeArgs& a, cudaStream_t st) {
   if (a.d_state == 128 && a.headdim % kRingRows == 0) return launch_decode_tk<T, K, true>(a, st);
   return launch_decode_tk<T, K, false>(a, st);
+}
+
+cudaError_t launch_check_device_batch(const int32_t* slots, const int32_t* n, int32_t capacity, int32_t num_slots,
+                                      int32_t* status, cudaStream_t st) {
+  const int words = (num_slots + 31) / 32;
+  const size_t smem = words <= kCheckBitmapWords ? sizeof(uint32_t) * (size_t)(words > 0 ? words : 1) : 0;
+  check_device_batch_kernel<<<1, kCheckThreads, smem, st>>>(slots, n, capacity, num_slots, status);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_decode(const DecodeArgs& a, mamba2_dtype act, cudaStream_t st) {

@@ -113,9 +113,19 @@ struct DecodeArgs {
   float eps;
   int32_t cluster;         // CTAs per sequence
   int32_t heads_per_cta;
-  SeqTable tab;
+  SeqTable tab;            // host batch: tab.n sequences; device batch: tab.n = capacity, rest unused
+  // Device batch (all null for a host batch): sequence s < *dev_n has slot dev_slots[s]
+  // and is fresh when dev_fresh[s] != 0; no CTA touches anything while *dev_status != 0.
+  const int32_t* dev_slots;
+  const uint8_t* dev_fresh;
+  const int32_t* dev_n;
+  const int32_t* dev_status;
 };
 bool decode_supported(mamba2_dtype act, const mamba2_dims& d, int norm_groups);
 cudaError_t launch_decode(const DecodeArgs& a, mamba2_dtype act, cudaStream_t st);
+// Checks a device batch (count in [0, capacity], slots in range, no slot twice) and
+// writes its mamba2_status to *status.
+cudaError_t launch_check_device_batch(const int32_t* slots, const int32_t* n, int32_t capacity, int32_t num_slots,
+                                      int32_t* status, cudaStream_t st);
 
 }  // namespace mamba2

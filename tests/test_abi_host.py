@@ -153,3 +153,26 @@ def test_prefill_host_workspace_grows_with_piece(product_lib):
     conv_dim, d_inner = 24 * 64 + 2 * 128, 24 * 64
     per_row = 2 * (conv_dim + 2 * d_inner + 24) * 2 + (conv_dim + d_inner) * 2  # double-buffered in/out, xbc, y
     assert sizes[2] >= 5000 * per_row
+
+
+def test_decode_device_batch_host_rejections(product_lib):
+    """mamba2_decode_step_device: the host-side checks (nothing enqueued) reject a
+    capacity outside [1, MAMBA2_MAX_SEQS], null or misaligned batch pointers and bad
+    scalars; the batch itself is checked on the device (GPU tests)."""
+    lib = product_lib
+    d = ss.Dims(4, 16, 16, 2, 4)
+
+    def call(capacity=4, slots=FAKE[12], fresh=FAKE[13], n=FAKE[14], status=FAKE[15], groups=2, eps=1e-5,
+             num_slots=8, dst=FAKE[0]):
+        return lib.mamba2_decode_step_device(dst, *FAKE[1:10], groups, eps, FAKE[10], FAKE[11], num_slots,
+                                             ctypes.byref(d), ss.BF16, slots, fresh, n, capacity, status, None)
+
+    assert call(capacity=0) == ss.ERR_INVALID_ARGUMENT
+    assert call(capacity=ss.MAX_SEQS + 1) == ss.ERR_INVALID_ARGUMENT
+    for kw in ({"slots": None}, {"fresh": None}, {"n": None}, {"status": None}, {"dst": None}):
+        assert call(**kw) == ss.ERR_INVALID_ARGUMENT, kw
+    for kw in ({"slots": FAKE[12] + 2}, {"n": FAKE[14] + 1}, {"status": FAKE[15] + 2}, {"dst": FAKE[0] + 4}):
+        assert call(**kw) == ss.ERR_INVALID_ARGUMENT, kw
+    assert call(groups=0) == ss.ERR_INVALID_ARGUMENT
+    assert call(eps=-1.0) == ss.ERR_INVALID_ARGUMENT
+    assert call(num_slots=-1) == ss.ERR_INVALID_ARGUMENT
