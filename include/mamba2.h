@@ -361,6 +361,54 @@ mamba2_status mamba2_prefill_host(void* out_host, const void* xBC_host,
 int64_t mamba2_state_bytes_per_layer(const mamba2_dims* dims,
                                      mamba2_dtype conv_state_dtype);
 
+/*
+ * Padded batches (page "Granite Mamba2 Inference Optimization": the layer's
+ * forward takes an attention mask and must serve variable-length padded
+ * batches). A padded batch is [batch, seqlen, ...] with mask[b, t] != 0 where
+ * position t of row b is a token. Padding positions are not tokens of any
+ * sequence, and each row's tokens must form one contiguous span (left or
+ * right padding; an all-padding row is an empty sequence).
+ *
+ * mamba2_padded_spans (host only, no CUDA call): from mask [batch, seqlen]
+ * uint8 (host), writes cu_seqlens [batch + 1] (row b's span length, prefix
+ * sums from 0: the RecurrentBatch of the packed rows) and first [batch] (the
+ * span's first position; 0 for an empty row). MAMBA2_ERR_INVALID_ARGUMENT for
+ * a row whose tokens are not one span, batch outside [0, MAMBA2_MAX_SEQS],
+ * seqlen < 0, or null pointers (mask may be NULL when batch*seqlen is 0).
+ */
+mamba2_status mamba2_padded_spans(const uint8_t* mask, int32_t batch,
+                                  int32_t seqlen, int32_t* cu_seqlens,
+                                  int32_t* first);
+
+/*
+ * Gathers the tokens of a padded batch into packed rows: packed row
+ * cu_seqlens[b] + k = padded row (b, first[b] + k), width_bytes each.
+ *   dst [cu_seqlens[batch], width] device; src [batch, seqlen, width] device
+ *   cu_seqlens [batch + 1], first [batch]: host, as mamba2_padded_spans gives
+ *   them (any spans inside the rows are accepted)
+ * width_bytes > 0. The copy moves 16-, 4-, 2- or 1-byte units, the widest
+ * that divides both addresses and the width (any alignment works; 16-byte
+ * aligned rows are fastest).
+ * MAMBA2_ERR_INVALID_ARGUMENT for a span outside its row, cu_seqlens not
+ * starting at 0 or decreasing, or a bad width or null pointer (nothing
+ * enqueued).
+ */
+mamba2_status mamba2_pack_rows(void* dst, const void* src, int32_t batch,
+                               int32_t seqlen, int32_t width_bytes,
+                               const int32_t* cu_seqlens, const int32_t* first,
+                               void* stream);
+
+/*
+ * The inverse scatter: padded row (b, t) of dst gets packed row
+ * cu_seqlens[b] + t - first[b] inside row b's span and zero bytes outside it.
+ *   dst [batch, seqlen, width] device; src [cu_seqlens[batch], width] device.
+ * Same checks as mamba2_pack_rows.
+ */
+mamba2_status mamba2_unpack_rows(void* dst, const void* src, int32_t batch,
+                                 int32_t seqlen, int32_t width_bytes,
+                                 const int32_t* cu_seqlens, const int32_t* first,
+                                 void* stream);
+
 /* Static description of a status code. */
 const char* mamba2_status_string(mamba2_status status);
 

@@ -8,8 +8,10 @@ arithmetic).
 The C source follows gllm PR #85 "feat(backend): Mamba2 ops, with CPU
 reference implementations", sections "Ops" and "CPU reference": each op is the
 token-at-a-time definition in double with the SSM state rounded to fp32 after
-every token. This module only marshals torch CPU tensors into the C library
-(built on demand with gcc) and turns status codes into exceptions.
+every token. This module marshals torch CPU tensors into the C library
+(built on demand with gcc) and turns status codes into exceptions; the
+padded-batch index maps at its end (spans, gather, scatter) are written out in
+plain Python.
 """
 from __future__ import annotations
 
@@ -206,3 +208,43 @@ def decode_step(xBC, z, dt, conv_w, conv_b, A_log, dt_bias, D, norm_w, norm_grou
 def state_bytes_per_layer(heads, headdim, d_state, ngroups, conv_kernel, conv_act=BF16) -> int:
     return int(_load().mamba2_ref_state_bytes_per_layer(heads, headdim, d_state, ngroups,
                                                         conv_kernel, conv_act))
+
+
+# --------------------------------------------------------------------------
+# Padded batches (page "Granite Mamba2 Inference Optimization": the layer's
+# forward takes an attention mask and serves variable-length padded batches).
+# Reading: a padding position is not a token of any sequence, and a row's
+# tokens are one contiguous span. Plain index work, written out in Python.
+# --------------------------------------------------------------------------
+
+def padded_spans(mask):
+    """(status, cu_seqlens, first) of a [batch, seqlen] mask: row b's tokens are the
+    positions with mask != 0, which must be one run [first, first + len); an empty
+    row has first 0. A row with two runs gives ERR_INVALID_ARGUMENT."""
+    cu, first = [0], []
+    for row in mask.tolist():
+        pos = [t for t, m in enumerate(row) if m != 0]
+        if pos and pos != list(range(pos[0], pos[0] + len(pos))):
+            return ERR_INVALID_ARGUMENT, None, None
+        first.append(pos[0] if pos else 0)
+        cu.append(cu[-1] + len(pos))
+    return OK, cu, first
+
+
+def pack_rows(src, cu_seqlens, first):
+    """Packed [cu[-1], ...] rows: row cu[b] + k is padded row (b, first[b] + k)."""
+    out = []
+    for b in range(len(first)):
+        for k in range(cu_seqlens[b + 1] - cu_seqlens[b]):
+            out.append(src[b, first[b] + k])
+    return torch.stack(out) if out else src.new_zeros((0,) + tuple(src.shape[2:]))
+
+
+def unpack_rows(src, cu_seqlens, first, seqlen):
+    """Padded [batch, seqlen, ...]: each sequence's packed rows at its span, zeros elsewhere."""
+    batch = len(first)
+    out = src.new_zeros((batch, seqlen) + tuple(src.shape[1:]))
+    for b in range(batch):
+        for k in range(cu_seqlens[b + 1] - cu_seqlens[b]):
+            out[b, first[b] + k] = src[cu_seqlens[b] + k]
+    return out

@@ -8,8 +8,10 @@ without the built library raises.
 
 Entry points (same names as the C ABI without the ``mamba2_`` prefix):
 ``causal_conv1d``, ``ssd_scan`` (+ ``ssd_scan_workspace_bytes``),
-``gated_rmsnorm``, ``decode_step``, ``prefill_host`` (+
-``prefill_host_workspace_bytes``), ``state_bytes_per_layer``.
+``gated_rmsnorm``, ``decode_step``, ``decode_step_device``, ``prefill_host`` (+
+``prefill_host_workspace_bytes``), ``padded_spans``, ``pack_rows``, ``unpack_rows``,
+``state_bytes_per_layer``. ``selective_scan_gb300.padded`` holds the padded-batch
+layer view built on them (attention mask in, HF-style cache out).
 """
 from __future__ import annotations
 
@@ -69,6 +71,9 @@ def _lib():
                                            ctypes.c_int, rb, p]
         lib.mamba2_decode_step_device.argtypes = [p, p, p, p, p, p, p, p, p, p, i32, f32, p, p, i32, dims,
                                                   ctypes.c_int, p, p, p, i32, p, p]
+        lib.mamba2_padded_spans.argtypes = [p, i32, i32, p, p]
+        lib.mamba2_pack_rows.argtypes = [p, p, i32, i32, i32, p, p, p]
+        lib.mamba2_unpack_rows.argtypes = [p, p, i32, i32, i32, p, p, p]
         lib.mamba2_state_bytes_per_layer.argtypes = [dims, ctypes.c_int]
         lib.mamba2_state_bytes_per_layer.restype = ctypes.c_int64
         lib.mamba2_status_string.argtypes = [ctypes.c_int]
@@ -79,7 +84,8 @@ def _lib():
         lib.mamba2_prefill_host.argtypes = [p, p, p, p, p, p, p, p, p, p, i32, f32, p, p, i32, dims, ctypes.c_int,
                                             rb, i32, p, sz, p]
         for name in ("mamba2_causal_conv1d", "mamba2_ssd_scan", "mamba2_gated_rmsnorm", "mamba2_decode_step",
-                     "mamba2_decode_step_device", "mamba2_prefill_host"):
+                     "mamba2_decode_step_device", "mamba2_prefill_host", "mamba2_padded_spans", "mamba2_pack_rows",
+                     "mamba2_unpack_rows"):
             getattr(lib, name).restype = ctypes.c_int
         _LIB = lib
     return _LIB
@@ -255,6 +261,42 @@ def decode_step_device(dst, xBC, z, dt, conv_w, conv_b, A_log, dt_bias, D, norm_
     if check:
         _check(st, "mamba2_decode_step_device")
     return st
+
+
+def padded_spans(mask):
+    """``mamba2_padded_spans``: (cu_seqlens, first) lists of a [batch, seqlen] host mask
+    (nonzero = token); raises Mamba2Error when a row's tokens are not one span."""
+    import torch
+    m = mask.to(torch.uint8).contiguous()
+    batch, seqlen = int(m.shape[0]), int(m.shape[1])
+    cu = (ctypes.c_int32 * (batch + 1))()
+    first = (ctypes.c_int32 * max(batch, 1))()
+    st = _lib().mamba2_padded_spans(m.data_ptr() if m.numel() else None, batch, seqlen, cu, first)
+    _check(st, "mamba2_padded_spans")
+    return list(cu), list(first)[:batch]
+
+
+def _pack(fn, name, dst, src, batch, seqlen, width_bytes, cu_seqlens, first, stream, check):
+    cu = (ctypes.c_int32 * (len(cu_seqlens)))(*[int(v) for v in cu_seqlens])
+    fi = (ctypes.c_int32 * max(len(first), 1))(*[int(v) for v in first])
+    st = fn(_ptr(dst), _ptr(src), int(batch), int(seqlen), int(width_bytes), cu, fi, _stream(stream))
+    if check:
+        _check(st, name)
+    return st
+
+
+def pack_rows(dst, src, cu_seqlens, first, stream=None, check=True) -> int:
+    """``mamba2_pack_rows``: padded ``src`` [batch, seqlen, ...] -> packed ``dst`` [rows, ...]."""
+    width = src[0, 0].numel() * src.element_size() if src.numel() else dst.shape[-1] * dst.element_size()
+    return _pack(_lib().mamba2_pack_rows, "mamba2_pack_rows", dst, src, src.shape[0], src.shape[1], width,
+                 cu_seqlens, first, stream, check)
+
+
+def unpack_rows(dst, src, cu_seqlens, first, stream=None, check=True) -> int:
+    """``mamba2_unpack_rows``: packed ``src`` [rows, ...] -> padded ``dst`` [batch, seqlen, ...], zeros at padding."""
+    width = dst[0, 0].numel() * dst.element_size() if dst.numel() else src.shape[-1] * src.element_size()
+    return _pack(_lib().mamba2_unpack_rows, "mamba2_unpack_rows", dst, src, dst.shape[0], dst.shape[1], width,
+                 cu_seqlens, first, stream, check)
 
 
 def prefill_host_workspace_bytes(dims, act: int, piece_rows: int, cu_seqlens=None, slots=None, fresh=None,

@@ -536,6 +536,65 @@ mamba2_status mamba2_decode_step_device(void* dst, const void* xBC, const void* 
   return e == cudaSuccess ? MAMBA2_OK : cuda_fail(e);
 }
 
+mamba2_status mamba2_padded_spans(const uint8_t* mask, int32_t batch, int32_t seqlen, int32_t* cu_seqlens,
+                                  int32_t* first) {
+  if (batch < 0 || batch > MAMBA2_MAX_SEQS || seqlen < 0 || !cu_seqlens || !first) return MAMBA2_ERR_INVALID_ARGUMENT;
+  if (batch > 0 && seqlen > 0 && !mask) return MAMBA2_ERR_INVALID_ARGUMENT;
+  int64_t rows = 0;
+  cu_seqlens[0] = 0;
+  for (int b = 0; b < batch; ++b) {
+    const uint8_t* m = mask ? mask + (int64_t)b * seqlen : nullptr;
+    int f = 0;
+    while (f < seqlen && m[f] == 0) ++f;
+    int e = f;
+    while (e < seqlen && m[e] != 0) ++e;
+    for (int t = e; t < seqlen; ++t)
+      if (m[t] != 0) return MAMBA2_ERR_INVALID_ARGUMENT;  // a hole: two spans in one row
+    first[b] = e > f ? f : 0;
+    rows += e - f;
+    if (rows > INT32_MAX) return MAMBA2_ERR_INVALID_ARGUMENT;
+    cu_seqlens[b + 1] = (int32_t)rows;
+  }
+  return MAMBA2_OK;
+}
+
+namespace {
+mamba2_status pack_common(void* dst, const void* src, int32_t batch, int32_t seqlen, int32_t width_bytes,
+                          const int32_t* cu_seqlens, const int32_t* first, bool unpack, void* stream) {
+  if (batch < 0 || batch > MAMBA2_MAX_SEQS || seqlen < 0 || width_bytes <= 0 || !cu_seqlens || (batch > 0 && !first))
+    return MAMBA2_ERR_INVALID_ARGUMENT;
+  if (cu_seqlens[0] != 0) return MAMBA2_ERR_INVALID_ARGUMENT;
+  for (int b = 0; b < batch; ++b) {
+    const int64_t len = (int64_t)cu_seqlens[b + 1] - cu_seqlens[b];
+    if (len < 0 || first[b] < 0 || first[b] + len > seqlen) return MAMBA2_ERR_INVALID_ARGUMENT;
+  }
+  const int64_t moved = unpack ? (int64_t)batch * seqlen : (int64_t)cu_seqlens[batch];
+  if (moved > 0 && (!dst || !src)) return MAMBA2_ERR_INVALID_ARGUMENT;
+  if (moved == 0) return MAMBA2_OK;
+  PackArgs a;
+  std::memset(&a, 0, sizeof a);
+  a.src = src;
+  a.dst = dst;
+  a.batch = batch;
+  a.seqlen = seqlen;
+  a.width = width_bytes;
+  for (int b = 0; b <= batch; ++b) a.cu[b] = cu_seqlens[b];
+  for (int b = 0; b < batch; ++b) a.first[b] = first[b];
+  const cudaError_t e = launch_pack_rows(a, unpack, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? MAMBA2_OK : cuda_fail(e);
+}
+}  // namespace
+
+mamba2_status mamba2_pack_rows(void* dst, const void* src, int32_t batch, int32_t seqlen, int32_t width_bytes,
+                               const int32_t* cu_seqlens, const int32_t* first, void* stream) {
+  return pack_common(dst, src, batch, seqlen, width_bytes, cu_seqlens, first, false, stream);
+}
+
+mamba2_status mamba2_unpack_rows(void* dst, const void* src, int32_t batch, int32_t seqlen, int32_t width_bytes,
+                                 const int32_t* cu_seqlens, const int32_t* first, void* stream) {
+  return pack_common(dst, src, batch, seqlen, width_bytes, cu_seqlens, first, true, stream);
+}
+
 size_t mamba2_prefill_host_workspace_bytes(const mamba2_dims* dims, mamba2_dtype act,
                                            const mamba2_recurrent_batch* rb, int32_t piece_rows) {
   if (!act_ok(act) || !dims_ok(dims) || piece_rows < 1 || !rb || !rb->cu_seqlens || rb->num_seqs < 0 ||

@@ -122,6 +122,21 @@ struct DecodeArgs {
   const int32_t* dev_status;
 };
 bool decode_supported(mamba2_dtype act, const mamba2_dims& d, int norm_groups);
+
+// ------------------------------------------------------------ pack ----
+constexpr int kPackThreads = 256;
+// Padded [batch, seqlen, width] <-> packed [cu[batch], width]: sequence b's tokens sit
+// at padded positions [first[b], first[b] + cu[b+1] - cu[b]) of row b.
+struct PackArgs {
+  const void* src;
+  void* dst;
+  int32_t batch, seqlen, width;  // width in bytes
+  int32_t cu[MAMBA2_MAX_SEQS + 1];
+  int32_t first[MAMBA2_MAX_SEQS];
+};
+cudaError_t launch_pack_rows(const PackArgs& a, bool unpack, cudaStream_t st);
+// The widest copy unit (16, 4, 2 or 1 bytes) dividing both addresses and the width.
+int pack_unit_bytes(const void* dst, const void* src, int width);
 cudaError_t launch_decode(const DecodeArgs& a, mamba2_dtype act, cudaStream_t st);
 // Checks a device batch (count in [0, capacity], slots in range, no slot twice) and
 // writes its mamba2_status to *status.

@@ -171,6 +171,30 @@ def make_prefill(name, seed, dims: Dims, lengths, act, num_slots, fresh, slots=N
     return Workload(name, dims, act, params, batch, xBC, z, dt, conv, ssm)
 
 
+def padded_batch(seed: int, lengths, seqlen: int, sides, dims: Dims, act, num_slots: int = 0,
+                 norm_groups: int = 1):
+    """A padded batch [batch, seqlen, ...] (standard distributions at every position,
+    padding included, so the padding's values are arbitrary) with its attention mask:
+    row b holds lengths[b] tokens, at the end of the row when sides[b] == "left"
+    (left padding) and at its start when "right". Returns (xBC, z, dt, mask, params,
+    conv pool, ssm pool, slots); the pools hold the NaN sentinel."""
+    g = torch.Generator("cpu").manual_seed(seed)
+    batch = len(lengths)
+    xBC, z, dt = draw_tokens(g, batch * seqlen, dims, act)
+    params = draw_params(g, dims, norm_groups)
+    mask = torch.zeros((batch, seqlen), dtype=torch.uint8)
+    for b, (L, side) in enumerate(zip(lengths, sides)):
+        if side == "left":
+            mask[b, seqlen - L:] = 1
+        else:
+            mask[b, :L] = 1
+    num_slots = max(num_slots, batch)
+    slots = torch.randperm(num_slots, generator=g)[:batch].tolist()
+    conv, ssm = empty_pools(num_slots, dims, act)
+    return (xBC.view(batch, seqlen, -1), z.view(batch, seqlen, -1), dt.view(batch, seqlen, -1), mask, params,
+            conv, ssm, slots)
+
+
 # --------------------------------------------------------------------------
 # the five named workloads
 # --------------------------------------------------------------------------
