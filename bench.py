@@ -298,6 +298,40 @@ def job_throughput(world, tokens_per_rank, ms):
     return world * tokens_per_rank / (ms * 1e-3)
 
 
+def time_projections(dev, T, d, reps, tf_peak):
+    """The layer's projections around the path at T tokens, timed alone (CUDA events on
+    the current stream, inputs larger than L2): in_proj [T, d_model] -> z | xBC | dt and
+    out_proj [T, d_inner] -> [T, d_model], d_model = d_inner / 2 (the expand factor 2 of
+    Mamba2 layers); random-init bf16 weights."""
+    import selective_scan_gb300 as ss
+    d_model = d.d_inner // 2
+    g = torch.Generator("cpu").manual_seed(9)
+    w_in, w_out = (t.to(dev) for t in W.draw_proj(g, d, d_model))
+    hidden = torch.randn((T, d_model), generator=g).to(torch.bfloat16).to(dev)
+    gin = torch.randn((T, d.d_inner), generator=g).to(torch.bfloat16).to(dev)
+    z = torch.empty((T, d.d_inner), dtype=torch.bfloat16, device=dev)
+    x = torch.empty((T, d.conv_dim), dtype=torch.bfloat16, device=dev)
+    dt = torch.empty((T, d.heads), dtype=torch.bfloat16, device=dev)
+    out = torch.empty((T, d_model), dtype=torch.bfloat16, device=dev)
+    calls = {"in_proj": (lambda: ss.in_proj(z, x, dt, hidden, w_in, d), 2.0 * T * d_model * w_in.shape[0]),
+             "out_proj": (lambda: ss.out_proj(out, gin, w_out), 2.0 * T * d.d_inner * d_model)}
+    res = {"d_model": d_model, "peak_tflops": tf_peak, "peak_kind": "bf16 burst (kernel timed alone)"}
+    for name, (fn, flops) in calls.items():
+        for _ in range(3):
+            fn()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record()
+        for _ in range(reps):
+            fn()
+        e1.record()
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / reps
+        tf = flops / (ms * 1e-3) / 1e12
+        res[name] = {"ms": ms, "flops": flops, "TFLOP/s": tf, "frac_tensor": tf / tf_peak}
+    return res
+
+
 def run_ours(args, rank, world, local_rank):
     import selective_scan_gb300 as ss
     dev = torch.device("cuda", local_rank)
@@ -361,6 +395,11 @@ def run_ours(args, rank, world, local_rank):
     dec_us, dec_n, dec_bytes, dec_steps = time_decode_batch(dev, reps=max(2, args.steps // 100), warm=1)
     dec_gbs = dec_bytes / (dec_us * 1e-6) / 1e9
 
+    # the layer's projections around the path (tcgen05 GEMMs), timed alone
+    proj = time_projections(dev, T, d, reps=max(3, args.steps // 20), tf_peak=tf_burst)
+    proj["layer_prefill_ms"] = proj["in_proj"]["ms"] + t_prefill + proj["out_proj"]["ms"]
+    proj["layer_tokens_per_s"] = T / (proj["layer_prefill_ms"] * 1e-3)
+
     # end to end through the C ABI with HOST buffers: mamba2_prefill_host copies each
     # piece's xBC, z and dt in from pinned host memory and its output back, on its own
     # copy streams overlapping the compute, every step inside the timed region
@@ -419,6 +458,7 @@ def run_ours(args, rank, world, local_rank):
                    "us_per_step": dec_us, "tokens_per_s": dec_n / (dec_us * 1e-6), "GB/s": dec_gbs,
                    "roofline_frac": dec_gbs / hbm, "roofline_frac_8TBs": dec_gbs / 8000.0,
                    "bytes_per_step": dec_bytes, "steps_timed": dec_steps},
+        "layer": proj,
         "e2e": {"value": job_throughput(world, T, e2e_ms), "unit": "tokens/s",
                 "h2d_bytes_per_step": hx.numel() * 2 + hz.numel() * 2 + hdt.numel() * 2,
                 "d2h_bytes_per_step": hout.numel() * 2, "api": "mamba2_prefill_host",

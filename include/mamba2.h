@@ -362,6 +362,36 @@ int64_t mamba2_state_bytes_per_layer(const mamba2_dims* dims,
                                      mamba2_dtype conv_state_dtype);
 
 /*
+ * The projections around the recurrent path (the Mamba2 layer of the page
+ * "Granite Mamba2 Inference Optimization"; gllm PR #85, "Ops": the model
+ * splits in_proj into z, xBC and dt at load, so no split op is needed).
+ * tcgen05 GEMMs, bf16 operands, fp32 accumulation, each output rounded once
+ * to bf16.
+ *
+ * mamba2_in_proj: with W = w_in [d_in_proj, d_model] (row-major, the layer's
+ * weight as stored: output features x input features) and
+ * d_in_proj = d_inner + conv_dim + heads, the product hidden . W^T is written
+ * split by columns: [0, d_inner) to z [rows, d_inner], the next conv_dim
+ * columns to xBC [rows, conv_dim], the last heads to dt [rows, heads].
+ *   hidden [rows, d_model] bf16, all pointers device, 16-byte aligned.
+ * bf16 only; d_model, d_inner, conv_dim and heads multiples of 8 (else
+ * MAMBA2_ERR_NOT_IMPLEMENTED).
+ */
+mamba2_status mamba2_in_proj(void* z, void* xBC, void* dt, const void* hidden,
+                             const void* w_in, int32_t rows, int32_t d_model,
+                             const mamba2_dims* dims, mamba2_dtype act,
+                             void* stream);
+
+/*
+ * mamba2_out_proj: out [rows, d_model] = x [rows, d_inner] . w_out^T, with
+ * w_out [d_model, d_inner] row-major. bf16 only; d_inner and d_model
+ * multiples of 8.
+ */
+mamba2_status mamba2_out_proj(void* out, const void* x, const void* w_out,
+                              int32_t rows, int32_t d_inner, int32_t d_model,
+                              mamba2_dtype act, void* stream);
+
+/*
  * Padded batches (page "Granite Mamba2 Inference Optimization": the layer's
  * forward takes an attention mask and must serve variable-length padded
  * batches). A padded batch is [batch, seqlen, ...] with mask[b, t] != 0 where
@@ -416,8 +446,8 @@ const char* mamba2_status_string(mamba2_status status);
 const char* mamba2_last_cuda_error(void);
 
 /*
- * Failure detection: how many tensor-core scan CTAs on the current device gave
- * up waiting for their MMA completion barrier (each wait is bounded; a CTA
+ * Failure detection: how many tensor-core CTAs (scan and projection GEMMs) on
+ * the current device gave up waiting on an mbarrier (each wait is bounded; a CTA
  * that gives up writes nothing further, frees its tensor memory and exits).
  * Always 0 on a healthy GPU. Synchronous (reads a device counter);
  * 0xffffffff if the read fails.

@@ -248,3 +248,23 @@ def unpack_rows(src, cu_seqlens, first, seqlen):
         for k in range(cu_seqlens[b + 1] - cu_seqlens[b]):
             out[b, first[b] + k] = src[cu_seqlens[b] + k]
     return out
+
+
+# --------------------------------------------------------------------------
+# The projections around the path (gllm PR #85, "Ops": the model splits in_proj
+# into z, xBC and dt). A library matmul in double, then the column split.
+# --------------------------------------------------------------------------
+
+def in_proj(hidden, w_in, dims):
+    """(z, xBC, dt) in double: hidden [rows, d_model] . w_in^T, w_in [d_in_proj, d_model]
+    (output features x input features), columns split d_inner | conv_dim | heads."""
+    H, P, N, G = dims
+    d_inner, conv_dim = H * P, H * P + 2 * G * N
+    assert w_in.shape[0] == d_inner + conv_dim + H
+    y = hidden.double() @ w_in.double().t()
+    return y[:, :d_inner], y[:, d_inner:d_inner + conv_dim], y[:, d_inner + conv_dim:]
+
+
+def out_proj(x, w_out):
+    """x [rows, d_inner] . w_out^T in double, w_out [d_model, d_inner]."""
+    return x.double() @ w_out.double().t()

@@ -10,7 +10,7 @@ Entry points (same names as the C ABI without the ``mamba2_`` prefix):
 ``causal_conv1d``, ``ssd_scan`` (+ ``ssd_scan_workspace_bytes``),
 ``gated_rmsnorm``, ``decode_step``, ``decode_step_device``, ``prefill_host`` (+
 ``prefill_host_workspace_bytes``), ``padded_spans``, ``pack_rows``, ``unpack_rows``,
-``state_bytes_per_layer``. ``selective_scan_gb300.padded`` holds the padded-batch
+``in_proj``, ``out_proj``, ``state_bytes_per_layer``. ``selective_scan_gb300.padded`` holds the padded-batch
 layer view built on them (attention mask in, HF-style cache out).
 """
 from __future__ import annotations
@@ -71,6 +71,8 @@ def _lib():
                                            ctypes.c_int, rb, p]
         lib.mamba2_decode_step_device.argtypes = [p, p, p, p, p, p, p, p, p, p, i32, f32, p, p, i32, dims,
                                                   ctypes.c_int, p, p, p, i32, p, p]
+        lib.mamba2_in_proj.argtypes = [p, p, p, p, p, i32, i32, dims, ctypes.c_int, p]
+        lib.mamba2_out_proj.argtypes = [p, p, p, i32, i32, i32, ctypes.c_int, p]
         lib.mamba2_padded_spans.argtypes = [p, i32, i32, p, p]
         lib.mamba2_pack_rows.argtypes = [p, p, i32, i32, i32, p, p, p]
         lib.mamba2_unpack_rows.argtypes = [p, p, i32, i32, i32, p, p, p]
@@ -85,7 +87,7 @@ def _lib():
                                             rb, i32, p, sz, p]
         for name in ("mamba2_causal_conv1d", "mamba2_ssd_scan", "mamba2_gated_rmsnorm", "mamba2_decode_step",
                      "mamba2_decode_step_device", "mamba2_prefill_host", "mamba2_padded_spans", "mamba2_pack_rows",
-                     "mamba2_unpack_rows"):
+                     "mamba2_unpack_rows", "mamba2_in_proj", "mamba2_out_proj"):
             getattr(lib, name).restype = ctypes.c_int
         _LIB = lib
     return _LIB
@@ -260,6 +262,25 @@ def decode_step_device(dst, xBC, z, dt, conv_w, conv_b, A_log, dt_bias, D, norm_
                                           _stream(stream))
     if check:
         _check(st, "mamba2_decode_step_device")
+    return st
+
+
+def in_proj(z, xBC, dt, hidden, w_in, dims, stream=None, check=True) -> int:
+    """``mamba2_in_proj``: hidden . w_in^T split into z, xBC, dt (tcgen05 GEMM, bf16)."""
+    d = _dims(dims)
+    st = _lib().mamba2_in_proj(_ptr(z), _ptr(xBC), _ptr(dt), _ptr(hidden), _ptr(w_in), hidden.shape[0],
+                               hidden.shape[1], ctypes.byref(d), _dt(hidden), _stream(stream))
+    if check:
+        _check(st, "mamba2_in_proj")
+    return st
+
+
+def out_proj(out, x, w_out, stream=None, check=True) -> int:
+    """``mamba2_out_proj``: out = x . w_out^T (tcgen05 GEMM, bf16)."""
+    st = _lib().mamba2_out_proj(_ptr(out), _ptr(x), _ptr(w_out), x.shape[0], x.shape[1], w_out.shape[0], _dt(x),
+                                _stream(stream))
+    if check:
+        _check(st, "mamba2_out_proj")
     return st
 
 

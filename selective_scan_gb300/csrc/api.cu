@@ -299,7 +299,10 @@ const char* mamba2_status_string(mamba2_status s) {
 
 const char* mamba2_last_cuda_error(void) { return g_cuda_error; }
 
-unsigned int mamba2_device_timeouts(void) { return read_device_timeouts(); }
+unsigned int mamba2_device_timeouts(void) {
+  const unsigned int a = read_device_timeouts(), b = read_gemm_timeouts();
+  return (a == 0xffffffffu || b == 0xffffffffu) ? 0xffffffffu : a + b;
+}
 
 int64_t mamba2_state_bytes_per_layer(const mamba2_dims* d, mamba2_dtype conv_dtype) {
   if (!dims_ok(d) || !act_ok(conv_dtype)) return -1;
@@ -533,6 +536,57 @@ mamba2_status mamba2_decode_step_device(void* dst, const void* xBC, const void* 
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t e = launch_check_device_batch(slots_dev, num_seqs_dev, capacity, num_slots, status_dev, st);
   if (e == cudaSuccess) e = launch_decode(a, act, st);
+  return e == cudaSuccess ? MAMBA2_OK : cuda_fail(e);
+}
+
+mamba2_status mamba2_in_proj(void* z, void* xBC, void* dt, const void* hidden, const void* w_in, int32_t rows,
+                             int32_t d_model, const mamba2_dims* dims, mamba2_dtype act, void* stream) {
+  if (!act_ok(act) || !dims_ok(dims) || rows < 0 || d_model <= 0) return MAMBA2_ERR_INVALID_ARGUMENT;
+  const int32_t d_inner = dims->heads * dims->headdim;
+  const int32_t conv_dim = d_inner + 2 * dims->ngroups * dims->d_state;
+  if (act != MAMBA2_BF16 || d_model % 8 != 0 || d_inner % 8 != 0 || conv_dim % 8 != 0 || dims->heads % 8 != 0)
+    return MAMBA2_ERR_NOT_IMPLEMENTED;
+  if (rows == 0) return MAMBA2_OK;
+  const void* ptrs[] = {z, xBC, dt, hidden, w_in};
+  for (const void* q : ptrs)
+    if (!q || !aligned16(q)) return MAMBA2_ERR_INVALID_ARGUMENT;
+  GemmArgs g;
+  std::memset(&g, 0, sizeof g);
+  g.M = rows;
+  g.N = d_inner + conv_dim + dims->heads;
+  g.K = d_model;
+  g.nseg = 3;
+  g.seg_end[0] = d_inner;
+  g.seg_end[1] = d_inner + conv_dim;
+  g.seg_end[2] = g.N;
+  g.dst[0] = z;
+  g.dst[1] = xBC;
+  g.dst[2] = dt;
+  g.ld[0] = d_inner;
+  g.ld[1] = conv_dim;
+  g.ld[2] = dims->heads;
+  const cudaError_t e = launch_gemm_tc(g, hidden, w_in, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? MAMBA2_OK : cuda_fail(e);
+}
+
+mamba2_status mamba2_out_proj(void* out, const void* x, const void* w_out, int32_t rows, int32_t d_inner,
+                              int32_t d_model, mamba2_dtype act, void* stream) {
+  if (!act_ok(act) || rows < 0 || d_inner <= 0 || d_model <= 0) return MAMBA2_ERR_INVALID_ARGUMENT;
+  if (act != MAMBA2_BF16 || d_inner % 8 != 0 || d_model % 8 != 0) return MAMBA2_ERR_NOT_IMPLEMENTED;
+  if (rows == 0) return MAMBA2_OK;
+  const void* ptrs[] = {out, x, w_out};
+  for (const void* q : ptrs)
+    if (!q || !aligned16(q)) return MAMBA2_ERR_INVALID_ARGUMENT;
+  GemmArgs g;
+  std::memset(&g, 0, sizeof g);
+  g.M = rows;
+  g.N = d_model;
+  g.K = d_inner;
+  g.nseg = 1;
+  g.seg_end[0] = d_model;
+  g.dst[0] = out;
+  g.ld[0] = d_model;
+  const cudaError_t e = launch_gemm_tc(g, x, w_out, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? MAMBA2_OK : cuda_fail(e);
 }
 

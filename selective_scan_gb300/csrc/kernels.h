@@ -123,6 +123,20 @@ struct DecodeArgs {
 };
 bool decode_supported(mamba2_dtype act, const mamba2_dims& d, int norm_groups);
 
+// ------------------------------------------------------------ GEMM ----
+// dst = A[M, K] . B[N, K]^T (bf16, K contiguous in both), bf16 out. Output columns
+// [seg_end[i-1], seg_end[i]) go to dst[i] (row stride ld[i], column 0 = seg_end[i-1]);
+// every segment boundary is a multiple of 8 columns and every dst row 16-byte aligned.
+struct GemmArgs {
+  int32_t M, N, K;
+  int32_t nseg;
+  int32_t seg_end[3];
+  void* dst[3];
+  int64_t ld[3];
+};
+cudaError_t launch_gemm_tc(const GemmArgs& g, const void* A, const void* B, cudaStream_t st);
+unsigned int read_gemm_timeouts();
+
 // ------------------------------------------------------------ pack ----
 constexpr int kPackThreads = 256;
 // Padded [batch, seqlen, width] <-> packed [cu[batch], width]: sequence b's tokens sit

@@ -66,6 +66,8 @@ __device__ unsigned int g_tc_timeouts = 0;
 
 namespace {
 
+#include "tc.cuh"
+
 constexpr int TQ = 128;  // tokens per chunk
 constexpr int TP = 64;   // headdim
 constexpr int TN = 128;  // d_state
@@ -73,8 +75,6 @@ constexpr int kMathWarps = 16;
 constexpr int kMathThreads = 32 * kMathWarps;
 constexpr int kFullThreads = kMathThreads + 4 * 32;   // + CB (and dt), Yoff, dH, Y issuers
 constexpr int kStateThreads = kMathThreads + 4 * 32;  // + X loader, B loader, dH issuer, weight producer
-constexpr uint32_t kWaitLimit = 1u << 22;  // try_wait rounds before giving up (about a second at the backoff)
-constexpr uint32_t kSuspendNs = 1000;      // a waiting thread sleeps up to this long per try_wait round
 
 // ---- full pass: TMEM columns (128 lanes each)
 constexpr uint32_t kColCB = 0;     // [0,256): CB of chunk parity b at 128 b; M hi | M lo replace it
@@ -120,7 +120,6 @@ constexpr uint32_t kStOffMisc = kStOffBar + 8 * kNumStateBars;
 constexpr uint32_t kStateSmem = kStOffMisc + 16 + 1024;
 static_assert(kStateSmem <= 232448, "state-pass shared memory plan exceeds 227 KB");
 
-__device__ __forceinline__ uint32_t su32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
 
 // byte offset of element (r, c) in a [R][cols] bf16 tile, 128-byte swizzle,
 // 64-column blocks of R rows each (the layout a TMA box of 64 x R lands in)
@@ -128,116 +127,8 @@ __device__ __forceinline__ uint32_t tile_off(int r, int c, int R) {
   return (uint32_t)((c >> 6) * R * 128 + r * 128 + ((((c & 63) >> 3) ^ (r & 7)) << 4) + (c & 7) * 2);
 }
 
-__device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
-  return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
-         ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
-}
 
-// kind::f16 instruction descriptor: D f32, A/B bf16, M = 128
-__host__ __device__ constexpr uint32_t idesc128(int N, int a_mn, int b_mn) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)a_mn << 15) | ((uint32_t)b_mn << 16) |
-         ((uint32_t)(N >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
-}
 
-__device__ __forceinline__ void mma_ss(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
-  asm volatile("{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\ntcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n"
-               :: "r"(d), "l"(a), "l"(b), "r"(idesc), "r"(acc));
-}
-__device__ __forceinline__ void mma_ts(uint32_t d, uint32_t a_tmem, uint64_t b, uint32_t idesc, uint32_t acc) {
-  asm volatile("{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\ntcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n"
-               :: "r"(d), "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc));
-}
-__device__ __forceinline__ void mma_commit(uint32_t mbar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" :: "r"(mbar) : "memory");
-}
-__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
-
-// ---- mbarriers
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" :: "r"(bar), "r"(count) : "memory");
-}
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" :: "r"(bar) : "memory");
-}
-__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" :: "r"(bar), "r"(bytes) : "memory");
-}
-__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
-  uint32_t done;
-  asm volatile("{\n.reg .pred P;\nmbarrier.try_wait.parity.shared::cta.b64 P, [%1], %2, %3;\nselp.u32 %0, 1, 0, P;\n}\n"
-               : "=r"(done) : "r"(bar), "r"(parity), "r"(kSuspendNs) : "memory");
-  return done != 0;
-}
-// (The polling loop is out of line: one copy instead of one per call site keeps
-// the kernels' hot code small in the instruction cache.)
-// Non-blocking test of the phase (no suspension: returns at once either way).
-__device__ __forceinline__ bool mbar_done(uint32_t bar, uint32_t parity) {
-  uint32_t done;
-  asm volatile("{\n.reg .pred P;\nmbarrier.test_wait.parity.shared::cta.b64 P, [%1], %2;\nselp.u32 %0, 1, 0, P;\n}\n"
-               : "=r"(done) : "r"(bar), "r"(parity) : "memory");
-  return done != 0;
-}
-// Bounded wait for the completion of the barrier phase with this parity; after
-// a few rounds the thread sleeps between polls, so waiting warps leave the
-// issue slots to the working ones. Gives up when the CTA's abort flag is
-// raised, and raises it itself on a timeout.
-__device__ __noinline__ bool wait_bar_slow(uint32_t bar, uint32_t parity, volatile uint32_t* abort_flag) {
-  for (uint32_t it = 0; it < kWaitLimit; ++it) {
-    if (mbar_test(bar, parity)) return true;
-    if (*abort_flag) return false;
-    if (it >= 2) __nanosleep(it < 32 ? 32 : 128);  // back off: a polling warp takes issue slots
-  }
-  *abort_flag = 1u;
-  return false;
-}
-// A phase that has already completed costs one non-blocking test: a suspending
-// try_wait takes hundreds of cycles even then, and most waits here find their
-// phase complete.
-__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile uint32_t* abort_flag) {
-  return mbar_done(bar, parity) || wait_bar_slow(bar, parity, abort_flag);
-}
-// The same, decided for the whole warp (every lane waits; all get the same
-// answer), for warps whose lanes then run .sync.aligned or __syncwarp code.
-__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile uint32_t* abort_flag) {
-  return __all_sync(0xffffffffu, wait_bar(bar, parity, abort_flag));
-}
-// Bounded wait that ignores the abort flag (draining work already issued).
-__device__ __forceinline__ void drain_bar(uint32_t bar, uint32_t parity) {
-  for (uint32_t it = 0; it < kWaitLimit; ++it)
-    if (mbar_test(bar, parity)) return;
-}
-// ---- TMEM loads / stores (32 lanes x 32 bit)
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
-  uint32_t r[16];
-  asm volatile("tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-                 "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-               : "r"(taddr));
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
-}
-// two 16-column loads, one wait
-__device__ __forceinline__ void tmem_ld16x2(uint32_t ta, uint32_t tb, float (&va)[16], float (&vb)[16]) {
-  uint32_t r[32];
-  asm volatile("tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-                 "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-               : "r"(ta));
-  asm volatile("tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
-               : "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]),
-                 "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]),
-                 "=r"(r[30]), "=r"(r[31])
-               : "r"(tb));
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-  for (int i = 0; i < 16; ++i) {
-    va[i] = __uint_as_float(r[i]);
-    vb[i] = __uint_as_float(r[16 + i]);
-  }
-}
 
 // 2^x with the hardware approximation (flushes subnormal results to zero)
 __device__ __forceinline__ float ex2(float x) {
@@ -257,14 +148,6 @@ __device__ __forceinline__ void split2(float a, float b, uint32_t& hi, uint32_t&
 }
 
 // ---- tile loads
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool valid) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src), "r"(valid ? 16 : 0));
-}
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* tm, int x, int y, uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
-      :: "r"(dst), "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(bar) : "memory");
-}
 
 // Where one chunk's tiles come from: xbc rows [rb, rb + len), 1 <= len <= TQ.
 struct ChunkSrc {

@@ -171,6 +171,15 @@ def make_prefill(name, seed, dims: Dims, lengths, act, num_slots, fresh, slots=N
     return Workload(name, dims, act, params, batch, xBC, z, dt, conv, ssm)
 
 
+def draw_proj(g, dims: Dims, d_model: int, act=torch.bfloat16):
+    """Random-init projection weights of the layer: w_in [d_inner + conv_dim + heads, d_model]
+    ~ N(0, 1/d_model), w_out [d_model, d_inner] ~ N(0, 1/d_inner) (unit-variance outputs)."""
+    d_in_proj = dims.d_inner + dims.conv_dim + dims.heads
+    w_in = _normal(g, (d_in_proj, d_model), std=d_model ** -0.5, dtype=act)
+    w_out = _normal(g, (d_model, dims.d_inner), std=dims.d_inner ** -0.5, dtype=act)
+    return w_in, w_out
+
+
 def padded_batch(seed: int, lengths, seqlen: int, sides, dims: Dims, act, num_slots: int = 0,
                  norm_groups: int = 1):
     """A padded batch [batch, seqlen, ...] (standard distributions at every position,
