@@ -420,6 +420,21 @@ mamba2_status mamba2_gated_rmsnorm(void* dst, const void* x, const void* z, cons
   return e == cudaSuccess ? MAMBA2_OK : cuda_fail(e);
 }
 
+namespace {
+// CTAs per sequence of a decode step over n sequences. A small batch spreads each
+// sequence over 16 SMs (one sequence at 48 heads: 10.0 instead of 12.4 us a step with
+// 8). Once 16-CTA clusters would not all fit at once, each CTA takes up to 8 heads:
+// 256 sequences at 48 heads take 136 us a step in clusters of 6 against 147 with 8,
+// 143 with 7, 140 with 5 or 3 and 160 with 4 (one GB300).
+void decode_cluster(int64_t n, int heads, DecodeArgs& a) {
+  const int cl = n * kDecodeMaxCluster <= device_sm_count()
+                     ? std::min(kDecodeMaxCluster, heads)
+                     : std::min(kDecodePortableCluster, (heads + kDecodeHeadsPerCta - 1) / kDecodeHeadsPerCta);
+  a.heads_per_cta = (heads + cl - 1) / cl;
+  a.cluster = (heads + a.heads_per_cta - 1) / a.heads_per_cta;
+}
+}  // namespace
+
 mamba2_status mamba2_decode_step(void* dst, const void* xBC, const void* z, const void* dt, const float* conv_w,
                                  const float* conv_b, const float* A_log, const float* dt_bias, const float* D,
                                  const float* norm_w, int32_t norm_groups, float eps, void* conv_state,
@@ -466,13 +481,7 @@ mamba2_status mamba2_decode_step(void* dst, const void* xBC, const void* z, cons
   a.conv_kernel = dims->conv_kernel;
   a.norm_groups = norm_groups;
   a.eps = eps;
-  // a small batch spreads each sequence over 16 SMs (batch 1: 10.0 instead of 12.4 us a
-  // step at 48 heads); once 16-CTA clusters would not all fit at once, 8 per sequence
-  // stream the state faster (256 sequences: 160 against 257 us)
-  const int cl_max = (int64_t)n * kDecodeMaxCluster <= device_sm_count() ? kDecodeMaxCluster : kDecodePortableCluster;
-  const int cl = std::min(cl_max, dims->heads);
-  a.heads_per_cta = (dims->heads + cl - 1) / cl;
-  a.cluster = (dims->heads + a.heads_per_cta - 1) / a.heads_per_cta;
+  decode_cluster(n, dims->heads, a);
   fill_table(a.tab, rb);
   for (int i = 0; i <= n; ++i) a.tab.tile[i] = i;
   cudaError_t e = launch_decode(a, act, static_cast<cudaStream_t>(stream));
@@ -523,11 +532,7 @@ mamba2_status mamba2_decode_step_device(void* dst, const void* xBC, const void* 
   a.norm_groups = norm_groups;
   a.eps = eps;
   // the grid is sized for the capacity (clusters past the device count leave at once)
-  const int cl_max =
-      (int64_t)capacity * kDecodeMaxCluster <= device_sm_count() ? kDecodeMaxCluster : kDecodePortableCluster;
-  const int cl = std::min(cl_max, dims->heads);
-  a.heads_per_cta = (dims->heads + cl - 1) / cl;
-  a.cluster = (dims->heads + a.heads_per_cta - 1) / a.heads_per_cta;
+  decode_cluster(capacity, dims->heads, a);
   a.tab.n = capacity;
   a.dev_slots = slots_dev;
   a.dev_fresh = fresh_dev;

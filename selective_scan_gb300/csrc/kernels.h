@@ -92,7 +92,8 @@ cudaError_t launch_gated_rmsnorm(const NormArgs& a, mamba2_dtype act, cudaStream
 // -------------------------------------------------------------- decode ----
 constexpr int kDecodeThreads = 256;
 constexpr int kDecodeMaxCluster = 16;  // CTAs per sequence when the batch leaves SMs idle (non-portable size)
-constexpr int kDecodePortableCluster = 8;  // CTAs per sequence otherwise
+constexpr int kDecodePortableCluster = 8;  // at most this many CTAs per sequence otherwise,
+constexpr int kDecodeHeadsPerCta = 8;      // each taking up to this many heads
 constexpr int kDecodeMaxNormGroups = 64;
 
 struct DecodeArgs {
