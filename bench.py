@@ -251,6 +251,45 @@ def time_decode_batch(dev, reps, warm):
     return us, b.num_seqs, decode_bytes_per_seq(d) * b.num_seqs, reps * steps
 
 
+def time_decode_device_batch(dev, reps):
+    """The same 256 x 128 decode through mamba2_decode_step_device: the batch (slots,
+    fresh flags, count) in device memory and checked on the device every step, 128
+    steps captured in one CUDA graph; returns us/step."""
+    import selective_scan_gb300 as ss
+    wl = W.decode_batch()
+    p, d, b = wl.params, wl.dims, wl.batch
+    pw = [t.to(dev) for t in (p.conv_w, p.conv_b, p.A_log, p.dt_bias, p.D, p.norm_w)]
+    conv, ssm = wl.conv_state.to(dev), wl.ssm_state.to(dev)
+    xs, zs, dts = wl.dec_xBC.to(dev), wl.dec_z.to(dev), wl.dec_dt.to(dev)
+    out = torch.empty((b.num_seqs, d.d_inner), dtype=wl.act, device=dev)
+    slots = torch.tensor(b.slots, dtype=torch.int32, device=dev)
+    fresh = torch.tensor(b.fresh, dtype=torch.uint8, device=dev)
+    n = torch.full((1,), b.num_seqs, dtype=torch.int32, device=dev)
+    status = torch.full((1,), -1, dtype=torch.int32, device=dev)
+    steps = xs.shape[0]
+
+    def run_eager():
+        for t in range(steps):
+            ss.decode_step_device(out, xs[t], zs[t], dts[t], *pw, p.norm_groups, p.eps, conv, ssm, d, slots, fresh,
+                                  n, status)
+
+    run_eager()
+    torch.cuda.synchronize()
+    if int(status.item()) != ss.OK:
+        raise SystemExit(f"device-batch decode rejected its batch: status {int(status.item())}")
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        run_eager()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        graph.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) * 1e3 / (reps * steps)
+
+
 def cpu_baseline(target_s=12.0):
     """The oracle, as it stands, on a bounded prefix of the same workload."""
     import oracle
@@ -394,6 +433,7 @@ def run_ours(args, rank, world, local_rank):
     # batched decode (256 sequences x 128 steps), timed separately
     dec_us, dec_n, dec_bytes, dec_steps = time_decode_batch(dev, reps=max(2, args.steps // 100), warm=1)
     dec_gbs = dec_bytes / (dec_us * 1e-6) / 1e9
+    dec_dev_us = time_decode_device_batch(dev, reps=max(2, args.steps // 100))
 
     # the layer's projections around the path (tcgen05 GEMMs), timed alone
     proj = time_projections(dev, T, d, reps=max(3, args.steps // 20), tf_peak=tf_burst)
@@ -457,7 +497,10 @@ def run_ours(args, rank, world, local_rank):
                    "launch": "CUDA graph of the 128 steps",
                    "us_per_step": dec_us, "tokens_per_s": dec_n / (dec_us * 1e-6), "GB/s": dec_gbs,
                    "roofline_frac": dec_gbs / hbm, "roofline_frac_8TBs": dec_gbs / 8000.0,
-                   "bytes_per_step": dec_bytes, "steps_timed": dec_steps},
+                   "bytes_per_step": dec_bytes, "steps_timed": dec_steps,
+                   "device_batch_us_per_step": dec_dev_us,
+                   "device_batch": "mamba2_decode_step_device: batch in device memory, checked on the device "
+                                   "every step (one more kernel), 128 steps in one CUDA graph"},
         "layer": proj,
         "e2e": {"value": job_throughput(world, T, e2e_ms), "unit": "tokens/s",
                 "h2d_bytes_per_step": hx.numel() * 2 + hz.numel() * 2 + hdt.numel() * 2,
