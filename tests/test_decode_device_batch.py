@@ -93,7 +93,7 @@ def _same_step(L, n):
 
 def test_device_batch_matches_host_batch():
     dev = device()
-    # capacity = n: the same CTAs per sequence as the host call (8 at 40 sequences)
+    # capacity = n: the same CTAs per sequence as the host call (6 at 40 sequences)
     L = _Layer(dev, seed=31, num_slots=96, capacity=40)
     for _ in range(3):
         _same_step(L, 40)
@@ -170,7 +170,7 @@ def test_device_batch_graph_replay():
     with torch.cuda.graph(graph):
         L.device_step()
     conv_h, ssm_h = L.conv.clone(), L.ssm.clone()
-    for step, n in enumerate((24, 17, 10, 24, 13)):  # >= 10: 8 CTAs per sequence on both paths
+    for step, n in enumerate((24, 17, 10, 24, 13)):  # >= 10 sequences: one cluster shape on both paths
         slots, fresh = L.draw_step(n)
         if step == 3:  # a rejected replay in the middle leaves everything as it was
             L.set_batch(slots[:2] + [slots[0]], [0, 0, 0], 3)
