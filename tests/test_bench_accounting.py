@@ -1,0 +1,46 @@
+"""The algorithmic byte and FLOP counts bench.py divides by its timings (the
+roofline numerators), against the same counts worked out by hand from the ops'
+interface tensors (gllm PR #85 "feat(backend): Mamba2 ops, with CPU reference
+implementations", "Ops": what each op reads and writes).
+
+Per token of a bf16 prefill: the conv reads and writes conv_dim channels; the scan
+reads xbc (conv_dim) and dt (heads) and writes y (d_inner); the norm reads y and z
+and writes the output (d_inner each). Per sequence of a decode step: the fp32 SSM
+state and the kernel-1 rows of conv history are read and written once; the token's
+xBC, z and dt are read and the output written.
+"""
+import bench
+import workloads as W
+
+
+def test_prefill_bytes_per_token():
+    # 48 heads x 64, d_state 128, 1 group: conv_dim 3328, d_inner 3072
+    d = W.DIMS_48H
+    assert bench.conv_bytes(1, d) == 2 * 3328 * 2 == 13_312
+    assert bench.scan_bytes(1, d, state_rw=0) == (3328 + 48 + 3072) * 2 == 12_896
+    assert bench.norm_bytes(1, d) == 3 * 3072 * 2 == 18_432
+    assert 13_312 + 12_896 + 18_432 == 44_640
+    # the 130m shape (24 heads): conv_dim 1792, d_inner 1536
+    d = W.DIMS_130M
+    per_tok = bench.conv_bytes(1, d) + bench.scan_bytes(1, d, state_rw=0) + bench.norm_bytes(1, d)
+    assert per_tok == 2 * 1792 * 2 + (1792 + 24 + 1536) * 2 + 3 * 1536 * 2 == 23_088
+
+
+def test_scan_state_bytes_and_flops():
+    d = W.DIMS_48H
+    # one sequence's fp32 state, written once at the end of the call
+    assert bench.scan_bytes(0, d) == 48 * 64 * 128 * 4 == 1_572_864
+    # the chunked algorithm per token: per head 2 (Q P + 2 P N), per group 2 Q N
+    assert bench.scan_flops(1, d, Q=64) == 48 * 2 * (64 * 64 + 2 * 64 * 128) + 2 * 64 * 128 == 1_982_464
+    assert bench.scan_flops(1, d, Q=128) == 48 * 2 * (128 * 64 + 2 * 64 * 128) + 2 * 128 * 128 == 2_392_064
+
+
+def test_decode_bytes_per_sequence():
+    d = W.DIMS_48H
+    ssm = 2 * 48 * 64 * 128 * 4          # state read and written
+    conv = 2 * 3 * 3328 * 2              # history read and written
+    io = 3328 * 2 + 3072 * 2 + 48 * 2 + 3072 * 2  # xBC, z, dt in; output out
+    assert (ssm, conv, io) == (3_145_728, 39_936, 19_040)
+    assert bench.decode_bytes_per_seq(d) == ssm + conv + io == 3_204_704
+    # 256 sequences a step: 820.4 MB
+    assert bench.decode_bytes_per_seq(d) * 256 == 820_404_224
