@@ -454,6 +454,17 @@ const char* mamba2_last_cuda_error(void);
  */
 unsigned int mamba2_device_timeouts(void);
 
+/*
+ * Failure-detection self-test: launches one CTA that waits, through the same
+ * bounded mbarrier wait as the tensor-core kernels, on a barrier that nothing
+ * arrives at. *status_dev (device int32) becomes 2 when the wait gave up and
+ * raised the CTA's abort flag (the expected outcome, after a few seconds),
+ * 1 if the phase completed, 3 if it gave up without raising the flag. The
+ * context stays usable. MAMBA2_ERR_INVALID_ARGUMENT for a null or misaligned
+ * pointer.
+ */
+mamba2_status mamba2_selftest_bounded_wait(int32_t* status_dev, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

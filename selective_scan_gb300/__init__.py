@@ -82,6 +82,8 @@ def _lib():
         lib.mamba2_status_string.restype = ctypes.c_char_p
         lib.mamba2_last_cuda_error.restype = ctypes.c_char_p
         lib.mamba2_device_timeouts.restype = ctypes.c_uint
+        lib.mamba2_selftest_bounded_wait.argtypes = [p, p]
+        lib.mamba2_selftest_bounded_wait.restype = ctypes.c_int
         lib.mamba2_prefill_host_workspace_bytes.argtypes = [dims, ctypes.c_int, rb, i32]
         lib.mamba2_prefill_host_workspace_bytes.restype = sz
         lib.mamba2_prefill_host.argtypes = [p, p, p, p, p, p, p, p, p, p, i32, f32, p, p, i32, dims, ctypes.c_int,

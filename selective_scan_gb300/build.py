@@ -19,7 +19,7 @@ ROOT = PKG.parent
 CSRC = PKG / "csrc"
 BUILD = PKG / "_build"
 LIB = PKG / "libmamba2.so"
-SOURCES = ["api.cu", "conv1d.cu", "scan.cu", "scan_tc.cu", "norm.cu", "decode.cu", "pack.cu", "gemm_tc.cu"]
+SOURCES = ["api.cu", "conv1d.cu", "scan.cu", "scan_tc.cu", "norm.cu", "decode.cu", "pack.cu", "gemm_tc.cu", "selftest.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
               "-I", str(ROOT / "include")] + ARCH

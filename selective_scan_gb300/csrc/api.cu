@@ -299,6 +299,12 @@ const char* mamba2_status_string(mamba2_status s) {
 
 const char* mamba2_last_cuda_error(void) { return g_cuda_error; }
 
+mamba2_status mamba2_selftest_bounded_wait(int32_t* status_dev, void* stream) {
+  if (!status_dev || (reinterpret_cast<uintptr_t>(status_dev) & 3u) != 0) return MAMBA2_ERR_INVALID_ARGUMENT;
+  const cudaError_t e = launch_bounded_wait_probe(status_dev, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? MAMBA2_OK : cuda_fail(e);
+}
+
 unsigned int mamba2_device_timeouts(void) {
   const unsigned int a = read_device_timeouts(), b = read_gemm_timeouts();
   return (a == 0xffffffffu || b == 0xffffffffu) ? 0xffffffffu : a + b;

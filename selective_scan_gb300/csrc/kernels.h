@@ -138,6 +138,9 @@ struct GemmArgs {
 cudaError_t launch_gemm_tc(const GemmArgs& g, const void* A, const void* B, cudaStream_t st);
 unsigned int read_gemm_timeouts();
 
+// Failure-detection self-test: one bounded wait on a barrier nothing arrives at.
+cudaError_t launch_bounded_wait_probe(int32_t* status, cudaStream_t st);
+
 // ------------------------------------------------------------ pack ----
 constexpr int kPackThreads = 256;
 // Padded [batch, seqlen, width] <-> packed [cu[batch], width]: sequence b's tokens sit
