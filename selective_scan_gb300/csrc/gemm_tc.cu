@@ -7,24 +7,21 @@
 //   out_proj  [rows, d_inner] x W_out[d_model, d_inner]^T -> [rows, d_model]
 // bf16 operands, fp32 accumulation in tensor memory, bf16 output rounded once.
 //
-// One persistent CTA per SM; the CTAs run in clusters of two that walk pairs of
-// vertically adjacent 128 x 256 output tiles (N fastest, so the clusters working at
-// one time share the same rows of the activations in L2). The two tiles of a pair
-// need the same 256 x 64 block of B per k-block: each CTA loads 128 of its rows and
-// multicasts them to both, so a CTA reads 32 KB instead of 48 KB from L2 per
-// k-block. Roles:
-//   warp 0      TMA loads of its A (128 x 64) k-block and its half of the pair's B
-//               (128 x 64, multicast to both CTAs), 4 stages
+// One persistent CTA per SM walks 128 x 256 output tiles, N fastest, so the CTAs
+// working at one time share the same rows of the activations in L2. Each CTA loads
+// its own A and B blocks from global memory (no load is shared between CTAs).
+// Roles:
+//   warp 0      TMA loads of the A (128 x 64) and B (256 x 64) k-blocks, 4 stages
 //   warp 1      tcgen05.mma issue (one thread), M=128 N=256 K=16, into one of two
 //               256-column accumulators, so the epilogue of a tile overlaps the
 //               next tile's products
 //   warps 2-5   epilogue: tensor memory -> registers -> bf16 -> global, each
 //               thread one output row, 16-byte stores, rows and columns past the
 //               matrix skipped
-// A stage is refilled once the products of BOTH CTAs have read it (each MMA commit
-// arrives on the stage's barrier in both CTAs). Every mbarrier wait is bounded; a
-// timeout stops every role, drains what was issued, frees tensor memory and counts
-// the CTA in g_gemm_timeouts; the pair leaves through one cluster barrier.
+// A stage is refilled once the products have read it (the MMA commit arrives on the
+// stage's barrier). Every mbarrier wait is bounded; a timeout stops every role,
+// drains what was issued, frees tensor memory and counts the CTA in
+// g_gemm_timeouts.
 #include <cuda.h>
 
 #include <algorithm>
@@ -41,7 +38,6 @@ namespace {
 #include "tc.cuh"
 
 constexpr int GBM = 128, GBN = 256, GBK = 64, kGStages = 4;
-constexpr int kGCluster = 2;  // CTAs sharing one B block
 constexpr int kGThreads = 6 * 32;
 constexpr uint32_t kGTileA = GBM * GBK * 2;  // 16 KB
 constexpr uint32_t kGTileB = GBN * GBK * 2;  // 32 KB
@@ -66,39 +62,6 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
-__device__ __forceinline__ uint32_t cluster_rank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-__device__ __forceinline__ uint32_t cluster_id() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
-  return r;
-}
-__device__ __forceinline__ uint32_t cluster_count() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(r));
-  return r;
-}
-__device__ __forceinline__ void cluster_sync() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-// a TMA box into the same shared-memory offset of every CTA in `mask`, completing
-// bytes on the barrier at the same offset in each
-__device__ __forceinline__ void tma_load_2d_mc(uint32_t dst, const CUtensorMap* tm, int x, int y, uint32_t bar,
-                                               uint16_t mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
-      " [%0], [%1, {%2, %3}], [%4], %5;"
-      :: "r"(dst), "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(bar), "h"(mask) : "memory");
-}
-// arrive on the barrier at this offset in every CTA of `mask` once the issued products complete
-__device__ __forceinline__ void mma_commit_mc(uint32_t mbar, uint16_t mask) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;"
-               :: "r"(mbar), "h"(mask) : "memory");
-}
-
 __device__ __forceinline__ uint32_t bf16x2(uint32_t lo, uint32_t hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(__uint_as_float(lo), __uint_as_float(hi));
   return *reinterpret_cast<uint32_t*>(&v);
@@ -117,15 +80,13 @@ gemm_tc_kernel(const __grid_constant__ GemmArgs g, const __grid_constant__ CUten
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   const int tiles_m = (g.M + GBM - 1) / GBM, tiles_n = (g.N + GBN - 1) / GBN;
-  const int pairs = (tiles_m + kGCluster - 1) / kGCluster * tiles_n;  // (row-tile pair, column tile)
+  const int tiles = tiles_m * tiles_n;
   const int kblocks = (g.K + GBK - 1) / GBK;
-  const int rank = (int)cluster_rank(), cid = (int)cluster_id(), ncl = (int)cluster_count();
-  constexpr uint16_t kPair = (1u << kGCluster) - 1u;
-  // this cluster's pairs: cid, + ncl, ...; this CTA takes row tile 2 p + rank of pair p
-  // (past the last row tile when the count is odd: all its rows are skipped)
-  const int my_tiles = cid < pairs ? (pairs - 1 - cid) / ncl + 1 : 0;
-  auto tile_m0 = [&](int t) { return (((cid + t * ncl) / tiles_n) * kGCluster + rank) * GBM; };
-  auto tile_n0 = [&](int t) { return ((cid + t * ncl) % tiles_n) * GBN; };
+  const int cta = (int)blockIdx.x, ncta = (int)gridDim.x;
+  // this CTA's tiles: cta, + ncta, ... (N fastest)
+  const int my_tiles = cta < tiles ? (tiles - 1 - cta) / ncta + 1 : 0;
+  auto tile_m0 = [&](int t) { return ((cta + t * ncta) / tiles_n) * GBM; };
+  auto tile_n0 = [&](int t) { return ((cta + t * ncta) % tiles_n) * GBN; };
 
   if (warp == 0) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;" :: "r"(su32(s_tmem)));
@@ -134,7 +95,7 @@ gemm_tc_kernel(const __grid_constant__ GemmArgs g, const __grid_constant__ CUten
   if (threadIdx.x == 32) {
     for (int s = 0; s < kGStages; ++s) {
       mbar_init(bar(kGFull + s), 1);
-      mbar_init(bar(kGEmpty + s), kGCluster);  // the products of both CTAs
+      mbar_init(bar(kGEmpty + s), 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(bar(kGAccFull + b), 1);
@@ -146,7 +107,6 @@ gemm_tc_kernel(const __grid_constant__ GemmArgs g, const __grid_constant__ CUten
   }
   tc_fence_before();
   __syncthreads();
-  cluster_sync();  // the peer's barriers are initialised before any multicast reaches them
   tc_fence_after();
   const uint32_t tmem = *s_tmem;
 
@@ -164,10 +124,9 @@ gemm_tc_kernel(const __grid_constant__ GemmArgs g, const __grid_constant__ CUten
         }
         if (lane == 0) {
           const uint32_t dst = sbase + (uint32_t)s * kGStage;
-          mbar_expect_tx(bar(kGFull + s), kGStage);  // own A + both halves of B
+          mbar_expect_tx(bar(kGFull + s), kGStage);  // A + B
           tma_load_2d(dst, &tma, kb * GBK, m0, bar(kGFull + s));
-          const uint32_t half = (uint32_t)rank * (kGTileB / kGCluster);
-          tma_load_2d_mc(dst + kGTileA + half, &tmb, kb * GBK, n0 + rank * (GBN / kGCluster), bar(kGFull + s), kPair);
+          tma_load_2d(dst + kGTileA, &tmb, kb * GBK, n0, bar(kGFull + s));
         }
         __syncwarp();
         issued = it + 1;
@@ -200,7 +159,7 @@ gemm_tc_kernel(const __grid_constant__ GemmArgs g, const __grid_constant__ CUten
 #pragma unroll
           for (int k = 0; k < GBK / 16; ++k)  // 16 bf16 = 32 bytes along the 128-byte swizzled row
             mma_ss(d, ad + (uint64_t)(2 * k), bd + (uint64_t)(2 * k), id, (kb > 0 || k > 0) ? 1u : 0u);
-          mma_commit_mc(bar(kGEmpty + s), kPair);  // both CTAs' stage s may be refilled once read
+          mma_commit(bar(kGEmpty + s));  // stage s may be refilled once read
         }
         if (!ok) break;
         mma_commit(bar(kGAccFull + buf));
@@ -252,7 +211,6 @@ gemm_tc_kernel(const __grid_constant__ GemmArgs g, const __grid_constant__ CUten
   __syncthreads();
   if (threadIdx.x == 0 && *s_abort) atomicAdd(&g_gemm_timeouts, 1u);
   if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;" :: "r"(tmem));
-  cluster_sync();  // neither CTA leaves while the other may still write into its shared memory
 }
 
 using Encode = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*, const cuuint64_t*,
@@ -297,30 +255,20 @@ cudaError_t launch_gemm_tc(const GemmArgs& g, const void* A, const void* B, cuda
   CUtensorMap tma, tmb;
   std::memset(&tma, 0, sizeof tma);
   std::memset(&tmb, 0, sizeof tmb);
-  if (!make_kmajor_map(&tma, A, g.M, g.K, GBM) || !make_kmajor_map(&tmb, B, g.N, g.K, GBN / kGCluster))
+  if (!make_kmajor_map(&tma, A, g.M, g.K, GBM) || !make_kmajor_map(&tmb, B, g.N, g.K, GBN))
     return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGemmSmem);
   if (e != cudaSuccess) return e;
-  const int pairs = ((g.M + GBM - 1) / GBM + kGCluster - 1) / kGCluster * ((g.N + GBN - 1) / GBN);
-  cudaLaunchConfig_t cfg = {};
-  cfg.blockDim = dim3(kGThreads, 1, 1);
-  cfg.dynamicSmemBytes = kGemmSmem;
-  cfg.stream = st;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = kGCluster;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  // as many clusters as fit at once (one CTA per SM), at most one per tile pair
-  cfg.gridDim = dim3(kGCluster, 1, 1);
-  int resident = 0;
-  e = cudaOccupancyMaxActiveClusters(&resident, gemm_tc_kernel, &cfg);
+  const int tiles = ((g.M + GBM - 1) / GBM) * ((g.N + GBN - 1) / GBN);
+  int dev = 0, sms = 0;
+  e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  if (resident < 1) return cudaErrorInvalidConfiguration;
-  cfg.gridDim = dim3((unsigned)(kGCluster * std::min(pairs, resident)), 1, 1);
-  return cudaLaunchKernelEx(&cfg, gemm_tc_kernel, g, tma, tmb);
+  e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  // one CTA per SM (the shared-memory plan admits one), at most one per tile
+  const int grid = std::max(1, std::min(tiles, sms));
+  gemm_tc_kernel<<<grid, kGThreads, kGemmSmem, st>>>(g, tma, tmb);
+  return cudaGetLastError();
 }
 
 }  // namespace mamba2
