@@ -121,7 +121,9 @@ mamba2_status mamba2_causal_conv1d(void* dst, const void* x,
 /*
  * Bytes of device workspace mamba2_ssd_scan needs for this batch on the
  * current device (0 when none). Query with the same dims, rows and batch as
- * the scan call. Returns 0 for arguments the scan would reject.
+ * the scan call. The figure is the larger of the needs of the two activation
+ * types, so it suffices for the call with either (it is exact for bf16, whose
+ * need is never the smaller). Returns 0 for arguments the scan would reject.
  */
 size_t mamba2_ssd_scan_workspace_bytes(const mamba2_dims* dims, int32_t rows,
                                        const mamba2_recurrent_batch* rb);
@@ -180,13 +182,18 @@ mamba2_status mamba2_ssd_scan(void* dst, const void* xbc, const void* dt,
  * The scratch is a fixed array of MAMBA2_STATIC_SCAN_SCRATCH_BYTES (32 MiB)
  * in the library's own device memory; every GPU that loads the library holds
  * it until the process exits. This call allocates nothing: no cudaMalloc, no
- * cudaFree, no allocating library routine. The first call on each device
- * looks up the array's device address once (cudaGetSymbolAddress with that
- * device current); make that first call before any stream capture.
+ * cudaFree, no allocating library routine. The first call in each CUDA
+ * context (normally the device's primary context) looks up the array's
+ * device address with cudaGetSymbolAddress, with that device current, and
+ * caches it under the context's ID; make that first call before any stream
+ * capture. After cudaDeviceReset the device gets a new primary context with
+ * a new ID, so the next call looks the address up again.
  *
  * Arguments, semantics, results and errors are those of mamba2_ssd_scan, plus
  * MAMBA2_ERR_WORKSPACE_TOO_SMALL when the batch needs more scratch than the
- * array holds (mamba2_ssd_scan_workspace_bytes gives the need; long runs
+ * array holds (mamba2_ssd_scan_workspace_bytes gives an upper bound of the
+ * need: a batch for which it is at most the array's size is never rejected
+ * for its size; long runs
  * split into many segments and batches of many sequences need more), in
  * which case nothing is enqueued.
  *

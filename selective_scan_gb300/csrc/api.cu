@@ -359,7 +359,8 @@ size_t mamba2_ssd_scan_workspace_bytes(const mamba2_dims* dims, int32_t rows, co
   if (rb->cu_seqlens[0] != 0 || rb->cu_seqlens[rb->num_seqs] != rows) return 0;
   for (int i = 0; i < rb->num_seqs; ++i)
     if (rb->cu_seqlens[i + 1] < rb->cu_seqlens[i]) return 0;
-  return plan_scan(dims, MAMBA2_BF16, rb).ws_bytes;
+  // the larger of the two activation types' needs: enough for the call with either
+  return std::max(plan_scan(dims, MAMBA2_BF16, rb).ws_bytes, plan_scan(dims, MAMBA2_F32, rb).ws_bytes);
 }
 
 mamba2_status mamba2_ssd_scan(void* dst, const void* xbc, const void* dt, const float* A_log,
@@ -789,6 +790,8 @@ mamba2_status mamba2_prefill_host(void* out_host, const void* xBC_host, const vo
 // ---------------------------------------------------------------------------
 // Scan with the library's own scratch, for callers that cannot allocate.
 // ---------------------------------------------------------------------------
+#include <cuda.h>
+
 #include <mutex>
 
 namespace mamba2 {
@@ -799,25 +802,55 @@ namespace {
 // only a stand-in); the device address comes from cudaGetSymbolAddress.
 static __device__ __align__(256) unsigned char g_scan_scratch[MAMBA2_STATIC_SCAN_SCRATCH_BYTES];
 
-constexpr int kMaxDevices = 64;
+// The address is cached per CUDA context, identified by the driver's context
+// ID (unique for the life of the process, never reused): a device reset or a
+// new primary context gets a new ID, so a stale address is never used.
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+struct ScratchEntry {
+  unsigned long long ctx_id;
+  void* addr;
+};
+constexpr int kMaxScratchEntries = 64;
 std::mutex g_scratch_mutex;
-void* g_scratch_addr[kMaxDevices] = {};
+ScratchEntry g_scratch_cache[kMaxScratchEntries] = {};
+int g_scratch_entries = 0;
 
-// Device address of g_scan_scratch on the current device, looked up once per
-// device (with that device current).
+template <typename Fn>
+Fn driver_fn(const char* name) {
+  void* fn = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion(name, &fn, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+      q != cudaDriverEntryPointSuccess)
+    return nullptr;
+  return reinterpret_cast<Fn>(fn);
+}
+
+// Device address of g_scan_scratch in the current context. The first call in
+// each context looks it up with cudaGetSymbolAddress (which also makes the
+// current device's primary context current if none is); later calls in the
+// same context take it from the cache.
 mamba2_status scan_scratch_address(void** out) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return cuda_fail(e);
-  if (dev < 0 || dev >= kMaxDevices) return MAMBA2_ERR_INVALID_ARGUMENT;
+  static const CtxGetCurrentFn get_current = driver_fn<CtxGetCurrentFn>("cuCtxGetCurrent");
+  static const CtxGetIdFn get_id = driver_fn<CtxGetIdFn>("cuCtxGetId");
+  auto current_id = [&](unsigned long long* id) {
+    CUcontext ctx = nullptr;
+    return get_current && get_id && get_current(&ctx) == CUDA_SUCCESS && ctx && get_id(ctx, id) == CUDA_SUCCESS;
+  };
   std::lock_guard<std::mutex> lock(g_scratch_mutex);
-  if (!g_scratch_addr[dev]) {
-    void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_scan_scratch);
-    if (e != cudaSuccess) return cuda_fail(e);
-    g_scratch_addr[dev] = p;
-  }
-  *out = g_scratch_addr[dev];
+  unsigned long long id = 0;
+  if (current_id(&id))
+    for (int i = 0; i < g_scratch_entries; ++i)
+      if (g_scratch_cache[i].ctx_id == id) {
+        *out = g_scratch_cache[i].addr;
+        return MAMBA2_OK;
+      }
+  void* p = nullptr;
+  const cudaError_t e = cudaGetSymbolAddress(&p, g_scan_scratch);
+  if (e != cudaSuccess) return cuda_fail(e);
+  // without a context ID to key on, nothing is cached and every call looks the address up
+  if (current_id(&id) && g_scratch_entries < kMaxScratchEntries) g_scratch_cache[g_scratch_entries++] = {id, p};
+  *out = p;
   return MAMBA2_OK;
 }
 

@@ -50,7 +50,12 @@ def _compare_once(fn, wl, dev):
     p, b, d = wl.params, wl.batch, wl.dims
     batch = ss.Batch(b.cu_seqlens, b.slots, b.fresh)
     need = ss.ssd_scan_workspace_bytes(d, b.rows, batch=batch)
-    assert 0 < need <= MAX_SCRATCH, f"workload should be segmented and fit the scratch ({need} bytes)"
+    # the dt' region alone is rows x heads floats; anything beyond it is the
+    # segments' states and decays, which only a segmented batch has
+    dtp_bytes = b.rows * d.heads * 4
+    assert dtp_bytes < need <= MAX_SCRATCH, (
+        f"workload should be segmented (scratch beyond the {dtp_bytes}-byte dt' region) and fit the array "
+        f"({need} bytes)")
     xbc, _ = gpu_conv(wl, dev)
     dt = wl.dt.to(dev)
     prm = [p.A_log.to(dev), p.dt_bias.to(dev), p.D.to(dev)]
@@ -86,7 +91,6 @@ def test_static_scratch_rejects_oversized_batch():
     d = W.DIMS_48H
     # 199 one-chunk runs and one 65536-token run: many segments' worth of state
     lengths = [64] * 199 + [65536]
-    g = torch.Generator().manual_seed(3)
     total = sum(lengths)
     xbc = torch.zeros((total, d.conv_dim), dtype=torch.bfloat16, device=dev)
     dt = torch.zeros((total, d.heads), dtype=torch.bfloat16, device=dev)
