@@ -80,7 +80,7 @@ def _load():
             lib.mamba2_ref_ssd_scan.argtypes = [p, p, p, p, p, p, p, i32, i32, i32, i32, i32, i32, i32, i32, p, p, p, p]
             lib.mamba2_ref_gated_rmsnorm.argtypes = [p, p, p, p, i32, i32, i32, f32, i32, p]
             lib.mamba2_ref_decode_step.argtypes = [p, p, p, p, p, p, p, p, p, p, i32, f32, p, p,
-                                                  i32, i32, i32, i32, i32, i32, i32, i32, p, p]
+                                                  i32, i32, i32, i32, i32, i32, i32, i32, p, p, p]
             lib.mamba2_ref_state_bytes_per_layer.argtypes = [i32] * 6
             lib.mamba2_ref_state_bytes_per_layer.restype = ctypes.c_int64
             lib.mamba2_ref_num_threads.restype = ctypes.c_int
@@ -191,18 +191,22 @@ def gated_rmsnorm(x, z, weight, groups: int, eps: float):
 
 def decode_step(xBC, z, dt, conv_w, conv_b, A_log, dt_bias, D, norm_w, norm_groups, eps,
                 conv_state, ssm_state, dims, slots, fresh):
-    """One token per sequence through conv -> scan -> norm; states in place."""
+    """One token per sequence through conv -> scan -> norm; states in place.
+
+    Returns ``(dst, dst_f64)``: the act-typed output and the norm's unrounded values.
+    """
     H, P, N, G = dims
     n = xBC.shape[0]
     dst = torch.empty((n, H * P), dtype=xBC.dtype)
+    dst64 = torch.empty((n, H * P), dtype=torch.float64)
     sl, fr = _i32(slots), _u8(fresh)
     st = _load().mamba2_ref_decode_step(
         _ptr(dst), _ptr(xBC), _ptr(z), _ptr(dt), _ptr(conv_w), _ptr(conv_b), _ptr(A_log),
         _ptr(dt_bias), _ptr(D), _ptr(norm_w), norm_groups, float(eps), _ptr(conv_state),
         _ptr(ssm_state), ssm_state.shape[0], H, P, N, G, conv_w.shape[1], _act_code(xBC),
-        sl.numel(), _ptr(sl), _ptr(fr))
+        sl.numel(), _ptr(sl), _ptr(fr), _ptr(dst64))
     _check(st, "decode_step")
-    return dst
+    return dst, dst64
 
 
 def state_bytes_per_layer(heads, headdim, d_state, ngroups, conv_kernel, conv_act=BF16) -> int:

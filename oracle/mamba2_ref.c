@@ -299,7 +299,8 @@ int mamba2_ref_decode_step(void* dst, const void* xBC, const void* z,
                            int32_t num_slots, int32_t heads, int32_t headdim,
                            int32_t d_state, int32_t ngroups,
                            int32_t conv_kernel, int32_t act, int32_t num_seqs,
-                           const int32_t* slots, const uint8_t* fresh) {
+                           const int32_t* slots, const uint8_t* fresh,
+                           double* dst_f64) {
   if (!act_ok(act) || num_seqs < 0 || heads <= 0 || headdim <= 0 ||
       d_state <= 0 || ngroups <= 0 || heads % ngroups != 0 || conv_kernel < 1)
     return MAMBA2_REF_ERR_INVALID_ARGUMENT;
@@ -323,7 +324,7 @@ int mamba2_ref_decode_step(void* dst, const void* xBC, const void* z,
                              ngroups, act, num_seqs, cu, slots, fresh, NULL);
   if (st == MAMBA2_REF_OK)
     st = mamba2_ref_gated_rmsnorm(dst, y, z, norm_w, num_seqs, d_inner,
-                                  norm_groups, eps, act, NULL);
+                                  norm_groups, eps, act, dst_f64);
   free(xbc);
   free(y);
   free(cu);

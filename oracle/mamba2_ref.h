@@ -73,7 +73,9 @@ int mamba2_ref_gated_rmsnorm(void* dst, const void* x, const void* z,
 
 /* One token per sequence: conv -> scan -> gated norm, with the same rounding
  * points as the three ops run one after the other. xBC: [n, conv_dim],
- * z: [n, H*P], dt: [n, H]; dst: [n, H*P]. Every run length must be 1. */
+ * z: [n, H*P], dt: [n, H]; dst: [n, H*P]. Every run length must be 1.
+ * dst_f64 (optional, [n, H*P]) receives the norm's output before its
+ * rounding to act, as the gated norm's own dst_f64 does. */
 int mamba2_ref_decode_step(void* dst, const void* xBC, const void* z,
                            const void* dt, const float* conv_w,
                            const float* conv_b, const float* A_log,
@@ -83,7 +85,8 @@ int mamba2_ref_decode_step(void* dst, const void* xBC, const void* z,
                            int32_t num_slots, int32_t heads, int32_t headdim,
                            int32_t d_state, int32_t ngroups,
                            int32_t conv_kernel, int32_t act, int32_t num_seqs,
-                           const int32_t* slots, const uint8_t* fresh);
+                           const int32_t* slots, const uint8_t* fresh,
+                           double* dst_f64);
 
 /* Bytes of recurrent state one sequence holds in one layer: the fp32 SSM
  * state plus kernel-1 conv history columns at conv_act. */

@@ -55,6 +55,14 @@ def oracle_prefill(wl):
 
 
 def slot_rel_l2(got_pool, ref_pool, slots):
-    from tests.util import rel_l2
+    """Relative L2 of the named slots of a device pool against the oracle's CPU
+    pool, gathered on each side and reduced in double on the device."""
     idx = torch.tensor(list(slots), dtype=torch.long)
-    return rel_l2(got_pool.cpu()[idx], ref_pool.cpu()[idx])
+    dev = got_pool.device
+    g = got_pool[idx.to(dev)].double()
+    r = ref_pool[idx].to(dev).double()
+    den = torch.linalg.vector_norm(r).item()
+    num = torch.linalg.vector_norm(g - r).item()
+    if den == 0.0:
+        return 0.0 if num == 0.0 else float("inf")
+    return num / den

@@ -9,15 +9,20 @@ fresh flags, count) lives in device memory and is checked on the device.
   rejected step leaves every buffer but the status word bit-unchanged.
 - One captured CUDA graph replayed with a new batch each step (InfiniLM PR #575
   "feat(mamba2): integrate model loading and recurrent inference", "Summary":
-  indexed recurrent Decode replayed through Decode graphs).
+  indexed recurrent Decode replayed through Decode graphs), every replayed step
+  also checked against the oracle's decode step on the same batch: output at
+  the activation tolerance against the oracle's unrounded values, conv pool bit
+  for bit, the named slots' SSM state by relative L2, and the rejected replay
+  rejected by the oracle with the same status.
 """
 import pytest
 import torch
 
+import oracle
 import selective_scan_gb300 as ss
 import workloads as W
-from tests.gpu_util import device
-from tests.util import assert_bits_equal
+from tests.gpu_util import device, slot_rel_l2
+from tests.util import STATE_DECODE_REL_L2, assert_bits_equal, check_act
 
 pytestmark = pytest.mark.gpu
 
@@ -170,21 +175,37 @@ def test_device_batch_graph_replay():
     with torch.cuda.graph(graph):
         L.device_step()
     conv_h, ssm_h = L.conv.clone(), L.ssm.clone()
+    conv_o, ssm_o = L.conv.cpu(), L.ssm.cpu()  # the oracle's pools, carried through the replays
+    p = L.p
     for step, n in enumerate((24, 17, 10, 24, 13)):  # >= 10 sequences: one cluster shape on both paths
         slots, fresh = L.draw_step(n)
+        x, z, dt = (t[:n].cpu().contiguous() for t in (L.x, L.z, L.dt))
         if step == 3:  # a rejected replay in the middle leaves everything as it was
-            L.set_batch(slots[:2] + [slots[0]], [0, 0, 0], 3)
+            bad = slots[:2] + [slots[0]]
+            L.set_batch(bad, [0, 0, 0], 3)
             L.out.fill_(5.0)
             graph.replay()
             torch.cuda.synchronize()
             assert int(L.status.item()) == ss.ERR_SLOT_SHARED
             assert (L.out.cpu() == 5.0).all()
             assert_bits_equal(L.ssm.cpu(), ssm_h.cpu(), "ssm pool after a rejected replay")
+            with pytest.raises(oracle.OracleError) as rej:
+                oracle.decode_step(x[:3].contiguous(), z[:3].contiguous(), dt[:3].contiguous(), p.conv_w,
+                                   p.conv_b, p.A_log, p.dt_bias, p.D, p.norm_w, p.norm_groups, p.eps, conv_o,
+                                   ssm_o, L.dims.tuple4(), bad, [0, 0, 0])
+            assert rej.value.status == oracle.ERR_SLOT_SHARED
             L.set_batch(slots, fresh, n)
         out_h = L.host_step(conv_h, ssm_h, slots, fresh)
         graph.replay()
+        _, out64 = oracle.decode_step(x, z, dt, p.conv_w, p.conv_b, p.A_log, p.dt_bias, p.D, p.norm_w,
+                                      p.norm_groups, p.eps, conv_o, ssm_o, L.dims.tuple4(), slots, fresh)
         torch.cuda.synchronize()
         assert int(L.status.item()) == ss.OK, step
         assert_bits_equal(L.out[:n].cpu(), out_h.cpu(), f"graph step {step} output")
         assert_bits_equal(L.conv.cpu(), conv_h.cpu(), f"graph step {step} conv pool")
         assert_bits_equal(L.ssm.cpu(), ssm_h.cpu(), f"graph step {step} ssm pool")
+        # the replayed step against the oracle on the same batch
+        check_act(L.out[:n].cpu(), out64, f"graph step {step} output vs oracle")
+        assert_bits_equal(L.conv.cpu(), conv_o, f"graph step {step} conv pool vs oracle")
+        rl = slot_rel_l2(L.ssm, ssm_o, slots)
+        assert rl <= STATE_DECODE_REL_L2, f"graph step {step}: ssm rel L2 {rl:.3g}"

@@ -397,12 +397,14 @@ def test_decode_steps_equal_prefill():
     W.fill_resumed_slots(g, conv, ssm, slots, fresh, torch.bfloat16)
     # decode
     cd, sd = conv.clone(), ssm.clone()
-    outs = []
+    outs, outs64 = [], []
     for t in range(steps):
         fr = fresh if t == 0 else [0, 0, 0]
-        outs.append(oracle.decode_step(x[t].contiguous(), z[t].contiguous(), dt[t].contiguous(), p.conv_w,
-                                       p.conv_b, p.A_log, p.dt_bias, p.D, p.norm_w, 2, p.eps, cd, sd,
-                                       dims.tuple4(), slots, fr))
+        o_t, o64_t = oracle.decode_step(x[t].contiguous(), z[t].contiguous(), dt[t].contiguous(), p.conv_w,
+                                        p.conv_b, p.A_log, p.dt_bias, p.D, p.norm_w, 2, p.eps, cd, sd,
+                                        dims.tuple4(), slots, fr)
+        outs.append(o_t)
+        outs64.append(o64_t)
     # prefill of the same tokens, packed per sequence
     xs = torch.cat([x[:, i] for i in range(n)])
     zs = torch.cat([z[:, i] for i in range(n)])
@@ -411,10 +413,14 @@ def test_decode_steps_equal_prefill():
     cp, sp = conv.clone(), ssm.clone()
     xb, _ = oracle.causal_conv1d(xs, p.conv_w, p.conv_b, cp, cu, slots, fresh)
     y, _ = oracle.ssd_scan(xb, dts, p.A_log, p.dt_bias, p.D, sp, dims.tuple4(), cu, slots, fresh)
-    o, _ = oracle.gated_rmsnorm(y, zs, p.norm_w, 2, p.eps)
+    o, o64 = oracle.gated_rmsnorm(y, zs, p.norm_w, 2, p.eps)
     dec = torch.stack(outs)  # [steps, n, d_inner]
     pre = torch.stack([o[i * steps:(i + 1) * steps] for i in range(n)], dim=1)
     assert_bits_equal(dec, pre, "decode outputs vs prefill")
+    # the unrounded outputs too: the decode step hands back the norm's own values
+    pre64 = torch.stack([o64[i * steps:(i + 1) * steps] for i in range(n)], dim=1)
+    assert_bits_equal(torch.stack(outs64), pre64, "decode unrounded outputs vs prefill")
+    assert_bits_equal(torch.stack(outs64).to(torch.bfloat16), dec, "decode output is its unrounded value rounded")
     assert_bits_equal(cd, cp, "conv pool")
     assert_bits_equal(sd, sp, "ssm pool")
 

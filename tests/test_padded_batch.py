@@ -215,8 +215,8 @@ def test_padded_forward_and_cache_view():
         o = padded.decode(dx, dz, ddt, w, dims, cache)
         o_k = torch.empty_like(o)
         ss.decode_step(o_k, dx, dz, ddt, *wts, p.norm_groups, p.eps, conv_k, ssm_k, dims, slots, [0] * 4)
-        oo = oracle.decode_step(dx.cpu(), dz.cpu(), ddt.cpu(), p.conv_w, p.conv_b, p.A_log, p.dt_bias, p.D,
-                                p.norm_w, p.norm_groups, p.eps, conv_o, ssm_o, (H, P, N, G), slots, [0] * 4)
+        oo, _ = oracle.decode_step(dx.cpu(), dz.cpu(), ddt.cpu(), p.conv_w, p.conv_b, p.A_log, p.dt_bias, p.D,
+                                   p.norm_w, p.norm_groups, p.eps, conv_o, ssm_o, (H, P, N, G), slots, [0] * 4)
         torch.cuda.synchronize()
         assert_bits_equal(o.cpu(), o_k.cpu(), f"decode step {step} vs the plain decode call")
         assert rel_l2(o.cpu(), oo) <= 1e-2

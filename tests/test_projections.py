@@ -173,8 +173,8 @@ def test_layer_chain_matches_oracle():
     h1 = torch.randn((3, d_model), generator=g).to(torch.bfloat16)
     o1 = L.decode(h1.to(dev), conv_g, ssm_g, b.slots)
     z1, x1, dt1 = (t.to(torch.bfloat16) for t in oracle.in_proj(h1, w_in, (H, P, N, G)))
-    g1 = oracle.decode_step(x1.contiguous(), z1.contiguous(), dt1.contiguous(), p.conv_w, p.conv_b, p.A_log,
-                            p.dt_bias, p.D, p.norm_w, p.norm_groups, p.eps, conv_o, ssm_o, (H, P, N, G), b.slots,
-                            [0] * 3)
+    g1, _ = oracle.decode_step(x1.contiguous(), z1.contiguous(), dt1.contiguous(), p.conv_w, p.conv_b, p.A_log,
+                               p.dt_bias, p.D, p.norm_w, p.norm_groups, p.eps, conv_o, ssm_o, (H, P, N, G),
+                               b.slots, [0] * 3)
     torch.cuda.synchronize()
     assert rel_l2(o1.cpu(), oracle.out_proj(g1, w_out)) <= 1e-2

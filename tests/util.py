@@ -26,17 +26,14 @@ def rel_l2(got: torch.Tensor, ref: torch.Tensor) -> float:
 
 
 def check_act(got: torch.Tensor, ref64: torch.Tensor, what: str = "",
-              abs_tol: float = ABS_TOL, rel_ulp: float = REL_ULP, rel_l2_tol: float = REL_L2,
-              extra: torch.Tensor = None):
-    """Elementwise |g - r| <= abs_tol + rel_ulp*|r| (+ extra) and rel-L2 <= rel_l2_tol."""
+              abs_tol: float = ABS_TOL, rel_ulp: float = REL_ULP, rel_l2_tol: float = REL_L2):
+    """Elementwise |g - r| <= abs_tol + rel_ulp*|r| and rel-L2 <= rel_l2_tol."""
     g = got.double().cpu()
     r = ref64.double().cpu()
     assert g.shape == r.shape, (what, g.shape, r.shape)
     assert torch.isfinite(g).all(), f"{what}: non-finite output"
     err = (g - r).abs()
     bound = abs_tol + rel_ulp * r.abs()
-    if extra is not None:
-        bound = bound + extra.double().cpu()
     bad = err > bound
     if bad.any():
         idx = bad.nonzero()[0].tolist()
