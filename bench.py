@@ -70,6 +70,21 @@ def norm_bytes(T, d: W.Dims, act_b=2):
     return 3 * T * d.d_inner * act_b
 
 
+def prefill_call_bytes(wl: W.Workload, act_b=2):
+    """Algorithmic bytes of one conv -> scan -> norm call sequence over a packed
+    batch: each op's inputs and outputs once (conv, scan, norm as separate calls),
+    the conv history and SSM state of every sequence written once and, when it
+    resumes, also read once."""
+    d, b = wl.dims, wl.batch
+    T = b.rows
+    resumed = sum(1 for f in b.fresh if not f)
+    n = b.num_seqs
+    state = d.heads * d.headdim * d.d_state * 4
+    hist = (d.conv_kernel - 1) * d.conv_dim * act_b
+    return (conv_bytes(T, d, act_b) + (n + resumed) * hist + scan_bytes(T, d, act_b, state_rw=0)
+            + (n + resumed) * state + norm_bytes(T, d, act_b))
+
+
 def decode_bytes_per_seq(d: W.Dims, act_b=2):
     return (2 * d.heads * d.headdim * d.d_state * 4 + 2 * (d.conv_kernel - 1) * d.conv_dim * act_b
             + d.conv_dim * act_b + 2 * d.d_inner * act_b + d.heads * act_b)
@@ -129,6 +144,78 @@ class ClockSampler:
         reasons = sorted({names[i] for r in rows for i, v in enumerate(r[2]) if v.lower() == "active"})
         return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": max(r[1] for r in rows),
                 "reasons": reasons, "samples": len(rows)}
+
+
+class NvmlClockSampler:
+    """SM clock, power and clock-event reasons read through NVML (the driver's
+    own library, loaded with ctypes) by a background thread every `period_s`
+    seconds, so that even a timed region of a few tens of milliseconds gets ten
+    or more samples. Reads only; changes no setting. Falls back to nothing
+    (summary() returns None) when NVML cannot be loaded."""
+
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown"}
+
+    def __init__(self, device, period_s=0.002):
+        import ctypes
+        import threading
+        self.ct, self.threading = ctypes, threading
+        self.period = period_s
+        self.rows = []
+        self.lib = None
+        self.handle = None
+        try:
+            lib = ctypes.CDLL("libnvidia-ml.so.1")
+            if lib.nvmlInit_v2() != 0:
+                return
+            h = ctypes.c_void_p()
+            props = torch.cuda.get_device_properties(device)
+            bus = None
+            if all(hasattr(props, a) for a in ("pci_domain_id", "pci_bus_id", "pci_device_id")):
+                bus = f"{props.pci_domain_id:08x}:{props.pci_bus_id:02x}:{props.pci_device_id:02x}.0".encode()
+            if bus is None or lib.nvmlDeviceGetHandleByPciBusId_v2(bus, ctypes.byref(h)) != 0:
+                if lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(device.index or 0), ctypes.byref(h)) != 0:
+                    return
+            self.lib, self.handle = lib, h
+            self.get_reasons = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        except (OSError, AttributeError):
+            self.lib = None
+
+    def _sample(self):
+        ct, lib, h = self.ct, self.lib, self.handle
+        mhz, mx, mw, rs = ct.c_uint(), ct.c_uint(), ct.c_uint(), ct.c_ulonglong()
+        ok = lib.nvmlDeviceGetClockInfo(h, 1, ct.byref(mhz)) == 0  # NVML_CLOCK_SM
+        ok = ok and lib.nvmlDeviceGetMaxClockInfo(h, 1, ct.byref(mx)) == 0
+        ok = ok and self.get_reasons(h, ct.byref(rs)) == 0
+        lib.nvmlDeviceGetPowerUsage(h, ct.byref(mw))
+        if ok:
+            self.rows.append((mhz.value, mx.value, mw.value / 1000.0, rs.value))
+
+    def _loop(self):
+        while not self.stop.is_set():
+            self._sample()
+            self.stop.wait(self.period)
+
+    def __enter__(self):
+        if self.lib is not None:
+            self.stop = self.threading.Event()
+            self.thread = self.threading.Thread(target=self._loop, daemon=True)
+            self.thread.start()
+        return self
+
+    def __exit__(self, *exc):
+        if self.lib is not None:
+            self.stop.set()
+            self.thread.join(timeout=5)
+            self._sample()  # at least one sample even for a very short region
+
+    def summary(self):
+        if self.lib is None or not self.rows:
+            return None
+        reasons = sorted({name for r in self.rows for bit, name in self.REASONS.items() if r[3] & bit})
+        return {"sm_mhz": statistics.median(r[0] for r in self.rows), "sm_max_mhz": max(r[1] for r in self.rows),
+                "reasons": reasons, "samples": len(self.rows), "power_w_max": max(r[2] for r in self.rows),
+                "source": f"NVML every {self.period * 1e3:.0f} ms during the timed region"}
 
 
 # --------------------------------------------------------------------------
@@ -290,6 +377,57 @@ def time_decode_device_batch(dev, reps):
     return e0.elapsed_time(e1) * 1e3 / (reps * steps)
 
 
+def time_prefill_config(wl: W.Workload, dev, reps, hbm, tf_sus, warm_reps=10):
+    """One packed prefill call sequence (conv -> scan -> norm) of a workload, the
+    median of `reps` CUDA-event intervals around the three calls: once with L2
+    flushed before every call (a 256 MB buffer written between calls, outside
+    the interval) and once warm (the same call back to back)."""
+    import selective_scan_gb300 as ss
+    p, d, b = wl.params, wl.dims, wl.batch
+    x, z, dt = wl.xBC.to(dev), wl.z.to(dev), wl.dt.to(dev)
+    cw, cb, A, dtb, D, nw = (t.to(dev) for t in (p.conv_w, p.conv_b, p.A_log, p.dt_bias, p.D, p.norm_w))
+    conv, ssm = wl.conv_state.to(dev), wl.ssm_state.to(dev)
+    xbc = torch.empty_like(x)
+    y = torch.empty((b.rows, d.d_inner), dtype=wl.act, device=dev)
+    out = torch.empty_like(y)
+    batch = ss.Batch(b.cu_seqlens, b.slots, b.fresh)
+    dims = ss.Dims(d.heads, d.headdim, d.d_state, d.ngroups, d.conv_kernel)
+    need = ss.ssd_scan_workspace_bytes(d, b.rows, b.cu_seqlens, b.slots, b.fresh)
+    ws = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+
+    def call():
+        ss.causal_conv1d(xbc, x, cw, cb, conv, batch=batch)
+        ss.ssd_scan(y, xbc, dt, A, dtb, D, ssm, dims, workspace=ws, batch=batch)
+        ss.gated_rmsnorm(out, y, z, nw, p.norm_groups, p.eps)
+
+    for _ in range(warm_reps):
+        call()
+    res = {}
+    for mode in ("l2_flushed", "warm"):
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+        torch.cuda.synchronize()
+        for e0, e1 in evs:
+            if mode == "l2_flushed":
+                flush.fill_(1)
+            e0.record()
+            call()
+            e1.record()
+        torch.cuda.synchronize()
+        ts = sorted(e0.elapsed_time(e1) * 1e3 for e0, e1 in evs)
+        res[mode] = {"us_median": statistics.median(ts), "us_min": ts[0], "us_max": ts[-1]}
+    nbytes = prefill_call_bytes(wl)
+    fl = scan_flops(b.rows, d)
+    floor_us = max(nbytes / (hbm * 1e9), fl / (tf_sus * 1e12)) * 1e6
+    for r in res.values():
+        r["tokens_per_s"] = b.rows / (r["us_median"] * 1e-6)
+        r["GB/s"] = nbytes / (r["us_median"] * 1e-6) / 1e9
+        r["roofline_frac"] = floor_us / r["us_median"]
+    return {"workload": wl.name, "tokens": b.rows, "sequences": b.num_seqs, "algorithmic_bytes": nbytes,
+            "scan_flops": fl, "roofline_us": floor_us, "reps": reps,
+            "roofline": "max(algorithmic bytes / measured HBM, SSD flops / sustained bf16)", **res}
+
+
 def cpu_baseline(target_s=12.0):
     """The oracle, as it stands, on a bounded prefix of the same workload."""
     import oracle
@@ -311,9 +449,19 @@ def cpu_baseline(target_s=12.0):
     t = run(probe)
     tokens = int(min(TOKENS, max(probe, (target_s / max(t, 1e-3)) * probe)) // 1024 * 1024)
     t = run(tokens)
+    # the same oracle on one host thread, on a shorter prefix (about a third of the time)
+    oracle.set_num_threads(1)
+    try:
+        t1p = run(256)
+        tok1 = int(min(TOKENS, max(256, (target_s / 3 / max(t1p, 1e-3)) * 256)) // 256 * 256)
+        t1 = run(tok1)
+    finally:
+        oracle.set_num_threads(cores)
     return {"value": tokens / t, "unit": "tokens/s", "cores": cores, "kind": "oracle",
             "sample": f"prefill of the first {tokens} of the {TOKENS} tokens (conv -> scan -> norm, "
-                      f"48 heads), {t:.1f} s"}
+                      f"48 heads), {t:.1f} s",
+            "one_thread": {"value": tok1 / t1, "unit": "tokens/s", "cores": 1,
+                           "sample": f"prefill of the first {tok1} tokens, {t1:.1f} s"}}
 
 
 def output_digest(t) -> str:
@@ -335,6 +483,36 @@ def job_throughput(world, tokens_per_rank, ms):
     """Whole-job tokens/s: `world` replicas, each processing tokens_per_rank tokens, the
     slowest in `ms` milliseconds (weak scaling: the work per GPU is fixed)."""
     return world * tokens_per_rank / (ms * 1e-3)
+
+
+def time_link(dev, host_in, host_out, reps=3):
+    """The host link alone for one e2e step's bytes: every input tensor copied in
+    from pinned host memory and the output copied out, each direction on its own
+    stream, and both at once (the floor the streamed host prefill can reach)."""
+    dev_in = [torch.empty(t.shape, dtype=t.dtype, device=dev) for t in host_in]
+    dev_out = torch.empty(host_out.shape, dtype=host_out.dtype, device=dev)
+    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+    res = {}
+    for mode in ("h2d", "d2h", "both"):
+        ms = []
+        for _ in range(reps + 1):
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            if mode in ("h2d", "both"):
+                with torch.cuda.stream(s_in):
+                    for d_, h_ in zip(dev_in, host_in):
+                        d_.copy_(h_, non_blocking=True)
+            if mode in ("d2h", "both"):
+                with torch.cuda.stream(s_out):
+                    host_out.copy_(dev_out, non_blocking=True)
+            torch.cuda.synchronize()
+            ms.append((time.perf_counter() - t0) * 1e3)
+        res[mode + "_ms"] = min(ms[1:])
+    bi = sum(t.numel() * t.element_size() for t in host_in)
+    bo = host_out.numel() * host_out.element_size()
+    res["h2d_GB/s"] = bi / (res["h2d_ms"] * 1e-3) / 1e9
+    res["d2h_GB/s"] = bo / (res["d2h_ms"] * 1e-3) / 1e9
+    return res
 
 
 def time_projections(dev, T, d, reps, tf_peak):
@@ -395,7 +573,8 @@ def run_ours(args, rank, world, local_rank):
         torch.distributed.barrier()
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
     e_start, e_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with ClockSampler(local_rank) as clk:
+    nvml = NvmlClockSampler(dev)
+    with (nvml if nvml.lib is not None else ClockSampler(local_rank)) as clk:
         torch.cuda.synchronize()
         e_start.record()
         for k in range(args.steps):
@@ -409,7 +588,11 @@ def run_ours(args, rank, world, local_rank):
     t_scan = sum(e[1].elapsed_time(e[2]) for e in evs) / args.steps
     t_norm = sum(e[2].elapsed_time(e[3]) for e in evs) / args.steps
     t_tail = sum(e[3].elapsed_time(e[4]) for e in evs) / args.steps
-    t_prefill = t_conv + t_scan + t_norm
+    # the prefill: one interval from before the conv to after the norm (gaps between
+    # the launches included)
+    prefill_each = [e[0].elapsed_time(e[3]) for e in evs]
+    t_prefill = sum(prefill_each) / args.steps
+    t_prefill_median = statistics.median(prefill_each)
     total_ms, t_prefill = max_over_ranks([total_ms, t_prefill], world, dev)
     digest_timed = output_digest(pf.out)
     if digest_timed != digest_warm:
@@ -434,6 +617,13 @@ def run_ours(args, rank, world, local_rank):
     dec_us, dec_n, dec_bytes, dec_steps = time_decode_batch(dev, reps=max(2, args.steps // 100), warm=1)
     dec_gbs = dec_bytes / (dec_us * 1e-6) / 1e9
     dec_dev_us = time_decode_device_batch(dev, reps=max(2, args.steps // 100))
+
+    # the other prefill workloads (130m-shaped 2 048-token prefill, 8-sequence varlen
+    # prefill), each call timed alone: L2 flushed and warm, median of the repetitions
+    configs = {
+        "prefill_130m_2048": time_prefill_config(W.prefill_130m(), dev, args.config_reps, hbm, tf_sus),
+        "varlen_130m_8seq": time_prefill_config(W.varlen_130m(), dev, args.config_reps, hbm, tf_sus),
+    }
 
     # the layer's projections around the path (tcgen05 GEMMs), timed alone
     proj = time_projections(dev, T, d, reps=max(3, args.steps // 20), tf_peak=tf_burst)
@@ -469,6 +659,7 @@ def run_ours(args, rank, world, local_rank):
     if output_digest(hout) != e2e_digest_first:
         raise SystemExit("streamed host prefill output changed between calls")
     (e2e_ms,) = max_over_ranks([e2e_ms], world, dev)
+    link = time_link(dev, [hx, hz, hdt], hout)
 
     line = {
         "metric": METRIC,
@@ -488,6 +679,11 @@ def run_ours(args, rank, world, local_rank):
                    "decode_tail_steps": DECODE_TAIL, "chunk": 128,
                    "l2": "inputs larger than L2 (no flush)", "parallelism": f"replicas x{world}"},
         "prefill_ms": t_prefill,
+        "prefill_ms_median": t_prefill_median,
+        "prefill_roofline": {"algorithmic_bytes": prefill_call_bytes(wl), "roofline_ms": max(
+            prefill_call_bytes(wl) / (hbm * 1e9), scan_flops(T, d) / (tf_sus * 1e12)) * 1e3,
+            "frac": max(prefill_call_bytes(wl) / (hbm * 1e9), scan_flops(T, d) / (tf_sus * 1e12)) * 1e3 / t_prefill},
+        "configs": configs,
         "decode_tail_us_per_step": t_tail * 1e3 / DECODE_TAIL,
         "decode_tail_launch": "CUDA graph of the 64 steps",
         "kernels": kern,
@@ -505,7 +701,8 @@ def run_ours(args, rank, world, local_rank):
         "e2e": {"value": job_throughput(world, T, e2e_ms), "unit": "tokens/s",
                 "h2d_bytes_per_step": hx.numel() * 2 + hz.numel() * 2 + hdt.numel() * 2,
                 "d2h_bytes_per_step": hout.numel() * 2, "api": "mamba2_prefill_host",
-                "piece_rows": args.e2e_piece},
+                "piece_rows": args.e2e_piece, "ms_per_step": e2e_ms, "link": link,
+                "link_frac": link["both_ms"] / e2e_ms},
         "gpu_launches": args.steps * (1 + pf.scan_launches + 1 + DECODE_TAIL),
         "output_digest": {"prefill_sha256": digest_timed, "stable_over_timed_steps": True,
                           "e2e_sha256": e2e_digest_first, "stable_over_e2e_steps": True},
@@ -583,6 +780,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--tokens", type=int, default=TOKENS, help="prefill length (profiling captures use less)")
     ap.add_argument("--e2e-piece", type=int, default=8192, help="rows per piece of the streamed host prefill")
+    ap.add_argument("--config-reps", type=int, default=60, help="repetitions of each other prefill workload")
     args = ap.parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

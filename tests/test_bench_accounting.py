@@ -44,3 +44,16 @@ def test_decode_bytes_per_sequence():
     assert bench.decode_bytes_per_seq(d) == ssm + conv + io == 3_204_704
     # 256 sequences a step: 820.4 MB
     assert bench.decode_bytes_per_seq(d) * 256 == 820_404_224
+
+
+def test_prefill_call_bytes_with_states():
+    # the 130m-shaped prefill: one fresh sequence of 2 048 tokens; its history
+    # (3 rows of 1 792 bf16 channels) and fp32 state (24 x 64 x 128) are written once
+    wl = W.prefill_130m()
+    assert bench.prefill_call_bytes(wl) == 2048 * 23_088 + 3 * 1792 * 2 + 24 * 64 * 128 * 4 == 48_081_408
+    # the varlen batch: 8 sequences, 4 of them resuming (their history and state are
+    # also read), 16 407 tokens with seed 2
+    wl = W.varlen_130m()
+    assert wl.batch.rows == 16_407 and sum(1 for f in wl.batch.fresh if not f) == 4
+    per_seq = 3 * 1792 * 2 + 24 * 64 * 128 * 4
+    assert bench.prefill_call_bytes(wl) == 16_407 * 23_088 + (8 + 4) * per_seq
