@@ -19,33 +19,38 @@
 // Full pass: one CTA per (sequence segment, head), 20 warps in fixed roles
 // that hand work to each other through mbarriers (no CTA-wide barrier in the
 // chunk loop):
-//   warps 0-7   X o w of chunk i (bf16 hi + lo), then M(i) = CB o decay (+ D
-//               on the diagonal), bf16 hi + lo written over CB in TMEM (TMEM
-//               lane t = token row t)
-//   warps 8-15  per chunk i: the state through chunk i-1 (H = exp(total) H +
-//               dH, fp32 in registers, bf16 copy of H^T to smem; TMEM lane n =
-//               state row n), beside the other group's X o w; the output of
-//               chunk i-1, y = Y + exp(s_t) Yoff, stored from registers
-//               (two warps per TMEM lane quarter in each group, so M and the
-//               state / output work run side by side on every sub-partition)
-//   warp 16     CB = C . B^T                M=128 N=128 K=128; before it, the
-//               chunk's dt' = softplus(dt + dt_bias), cumulative log-decay and
-//               block factors (up to four chunks ahead of the element-wise warps)
-//   warp 17     Yoff = C . H^T              M=128 N=64  K=128 (H^T MN-major)
-//   warp 18     dH^T = B^T . [X o w hi | lo]  M=128 N=128 K=128;
+//   warps 0-3   M(i) = CB o decay (+ D on the diagonal) in fp16, written over
+//               the first 64 columns of chunk i's CB buffer in TMEM (one thread
+//               per token row t = TMEM lane)
+//   warps 4-7   X o w of chunk i (bf16 hi + lo) for the state product, and x
+//               converted to fp16 in place for Y = M . X
+//   warps 8-15  per chunk i: the state through chunk i (H = exp(total) H + dH,
+//               fp32 in registers; TMEM lane n = state row n), the output y = Y
+//               + exp(s_t) C . H^T(i-1) stored from registers, then H(i) as bf16
+//               hi + lo to smem (two warps per TMEM lane quarter, 32 columns p each)
+//   warp 16     the chunk's dt' = softplus(dt + dt_bias), cumulative log-decay
+//               and block factors; CB = C . B^T   M=128 N=128 K=128
+//   warp 17     Yoff = C . [H hi | H lo]^T       M=128 N=128 K=128 (H^T MN-major);
 //               also loads the C and B tiles of chunk i+2
-//   warp 19     Y = M . X (A from TMEM)     M=128 N=64  K=128 (hi and lo);
-//               also loads the X tile of chunk i+2
-// An MMA-issuing thread waits out each MMA it issues (about 100 cycles per
-// instruction at any N), so the four products run as four concurrent streams
-// from four warps. A [rows][cols] bf16 tile stored with the 128-byte swizzle
-// in 64-column blocks (the TMA box layout) is both the K-major and the
-// MN-major tcgen05 operand, so every tile is used in its load layout.
-// M and X o w are carried as bf16 hi + lo (about 16 mantissa bits): with a
-// single bf16 M the worst y error reaches 1.4x its tolerance, and a single
-// bf16 X o w gives a state error of 1.7e-3 against a 1e-3 tolerance
-// (measured on the 130m, varlen and 65 536-token workloads); a single bf16
-// copy of H costs y less than 5 % of its tolerance.
+//   warp 18     dH^T = B^T . [X o w hi | lo]     M=128 N=128 K=128
+//   warp 19     Y = M . X (fp16, A from TMEM)    M=128 N=64  K=128, into the
+//               other 64 columns of the CB buffer (so Y is double-buffered by
+//               chunk parity); also loads the X tile of chunk i+2
+// An MMA-issuing thread spends about 200 cycles on each tcgen05.mma it issues,
+// whatever its N (64 to 256): the time of a product is its instruction count,
+// so the four products run as four concurrent streams from four warps, and
+// the hi + lo splits that precision needs sit on the N side (one instruction
+// covers both halves), never on the K side. A [rows][cols] tile stored with the
+// 128-byte swizzle in 64-column blocks (the TMA box layout) is both the K-major
+// and the MN-major tcgen05 operand, so every tile is used in its load layout.
+// Precision (measured against the token loop on the 65 536-token workload):
+// H carried as a single bf16 puts the worst y error at 1.03x its tolerance,
+// as bf16 hi + lo at 5e-5 absolute; M and x in fp16 (11 significant bits) keep
+// the worst y error within 0.86 of the tolerance (most of it the output's own
+// bf16 rounding); X o w as a single bf16 gives a state error of 1.7e-3 against
+// a 1e-3 tolerance, so it stays hi + lo. fp16 holds magnitudes up to 65 504: a
+// CTA that meets a larger M entry or x recomputes its segment's y token by
+// token in fp32 (correct, slow; no workload here comes near it).
 //
 // Long runs are cut into segments. The state pass computes, per segment but
 // the last, the end state from zero (the first segment from the slot's state)
@@ -71,36 +76,56 @@ namespace {
 constexpr int TQ = 128;  // tokens per chunk
 constexpr int TP = 64;   // headdim
 constexpr int TN = 128;  // d_state
-constexpr int kMathWarps = 16;
+constexpr int kMathWarps = 16;  // element-wise warps of either pass
 constexpr int kMathThreads = 32 * kMathWarps;
-constexpr int kFullThreads = kMathThreads + 4 * 32;   // + CB (and dt), Yoff, dH, Y issuers
+constexpr int kFullThreads = kMathThreads + 4 * 32;   // + CB (and dt), Yoff (and C/B loads), dH, Y (and X loads) issuers
 constexpr int kStateThreads = kMathThreads + 4 * 32;  // + X loader, B loader, dH issuer, weight producer
+// full pass: the element-wise warps by role
+constexpr int kMWarps = 8;   // warps 0-7: X o w (bf16 hi + lo) and the fp16 copy of x, then M
+constexpr int kSWarps = 8;   // warps 8-15: state, output, H hi + lo
+static_assert(kMWarps + kSWarps == kMathWarps, "full-pass roles");
 
 // ---- full pass: TMEM columns (128 lanes each)
-constexpr uint32_t kColCB = 0;     // [0,256): CB of chunk parity b at 128 b; M hi | M lo replace it
-constexpr uint32_t kColYo = 256;   // [256,320): C . H^T
-constexpr uint32_t kColDH = 320;   // [320,448): B^T . (X o w) hi | lo, lane = n
-constexpr uint32_t kColYd = 448;   // [448,512): M . X
+// [0,256): chunk parity b at 128 b: CB = C . B^T (fp32, 128 columns), then M (fp16,
+// columns [0,64), k-step s at m_col(s)) written over it and Y = M . X (columns [64,128))
+constexpr uint32_t kColM = 0, kColY = 64;
+// TMEM column of M's k-step s (tokens [16 s, 16 s + 16)). The thread of half h =
+// s % 2 of a row computes steps h, h + 2, h + 4, h + 6 in that order and reads CB
+// columns [16 s, 16 s + 16) for each; step k of them (s = 2 k + h) goes to
+// 32 (k / 2) + 16 h + 8 (k % 2), inside CB columns that the same thread read at
+// its step k / 2 <= k. So no thread overwrites CB another thread has yet to read,
+// and M fills columns [0, 64) whole, leaving [64, 128) to Y.
+__host__ __device__ constexpr uint32_t m_col(int s) {
+  return (uint32_t)(32 * ((s >> 1) >> 1) + 16 * (s & 1) + 8 * ((s >> 1) & 1));
+}
+constexpr uint32_t kColYo = 256;   // [256,384): C . [H hi | H lo]^T, column = p (hi) or 64 + p (lo)
+constexpr uint32_t kColDH = 384;   // [384,512): B^T . [X o w hi | lo], lane = n
 
-// ---- full pass: shared memory (operand tiles 1024-byte aligned)
+// ---- full pass: shared memory (operand tiles 1024-byte aligned; the base is)
 constexpr uint32_t kTileC = TQ * TN * 2;  // 32 KB [t][n]
 constexpr uint32_t kTileB = TQ * TN * 2;  // 32 KB [j][n]
-constexpr uint32_t kTileX = TQ * TP * 2;  // 16 KB [j][p]
+constexpr uint32_t kTileX = TQ * TP * 2;  // 16 KB [j][p] (bf16 as loaded, then fp16 in place)
 constexpr uint32_t kStage = kTileC + kTileB + kTileX;  // chunk parity b at b * kStage
 constexpr uint32_t kOffXWhi = 2 * kStage;
 constexpr uint32_t kOffXWlo = kOffXWhi + kTileX;
-constexpr uint32_t kOffHT = kOffXWlo + kTileX;         // H^T bf16 [n][p]
-constexpr int kDtRing = 4;                              // dt buffers (chunk i in i % 4)
-constexpr uint32_t kOffDt = kOffHT + TN * TP * 2;      // kDtRing buffers of {s2, dt', v}[TQ] floats
-constexpr uint32_t kDtBuf = 3 * TQ * 4;
+constexpr uint32_t kOffHT = kOffXWlo + kTileX;         // H^T bf16 [n][p hi | p lo] (two 64-column blocks)
+constexpr uint32_t kTileHT = TN * 2 * TP * 2;          // 32 KB
+constexpr int kDtRing = 2;                              // dt buffers (chunk i in i % 2)
+constexpr int kDtS = 0, kDtP = TQ, kDtV = 2 * TQ;       // float offsets: S (log2), dt', v (tokens 0..95)
+constexpr uint32_t kDtBuf = (2 * TQ + 96) * 4;
+constexpr uint32_t kOffDt = kOffHT + kTileHT;
 constexpr uint32_t kOffBar = kOffDt + kDtRing * kDtBuf;
-enum FullBar : int {  // + chunk % 2 (+ chunk % 4 for kDtReady and kEpiDone)
-  kFullCB = 0, kFullX = 2, kCBDone = 4, kYoDone = 6, kDHDone = 8, kYdDone = 10,
-  kHDone = 12, kXWReady = 14, kMReady = 16, kDtReady = 18, kEpiDone = 22, kNumFullBars = 26
+enum FullBar : int {  // + chunk % 2
+  kFullCB = 0, kFullX = 2, kDtReady = 4, kDtFree = 6, kCBDone = 8, kMReady = 10, kXWReady = 12, kYdDone = 14,
+  kYoDone = 16, kDHDone = 18, kDHFree = 20, kHReady = 22, kEpiDone = 24, kYoIssued = 26, kYIssued = 28,
+  kNumFullBars = 30
 };
-constexpr uint32_t kOffMisc = kOffBar + 8 * kNumFullBars;  // TMEM base, abort flag
-constexpr uint32_t kFullSmem = kOffMisc + 16 + 1024;        // + slack to align the base to 1024
+constexpr uint32_t kOffMisc = kOffBar + 8 * kNumFullBars;  // TMEM base, abort flag, fp16 range flag
+constexpr uint32_t kFullSmem = kOffMisc + 16;
 static_assert(kFullSmem <= 232448, "full-pass shared memory plan exceeds 227 KB");
+// fp16 operands of Y = M . X: a chunk whose M or x reaches this magnitude is
+// recomputed token by token (fp16 holds up to 65 504)
+constexpr float kF16Limit = 65504.0f;
 
 // ---- state pass: shared memory (4 stages of X, 3 of B), TMEM D = [hi part | lo part] in [0,128).
 // An X stage is free once X o w has read it, a B stage once the dH product has,
@@ -146,6 +171,42 @@ __device__ __forceinline__ void split2(float a, float b, uint32_t& hi, uint32_t&
   hi = pack2(a, b);
   lo = pack2(a - __uint_as_float(hi << 16), b - __uint_as_float(hi & 0xffff0000u));
 }
+// ---- packed fp32 pairs (one instruction for two lanes of arithmetic)
+struct F2 {
+  uint64_t v;
+};
+__device__ __forceinline__ F2 f2(float lo, float hi) {
+  F2 r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r.v) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ float f2lo(F2 a) {
+  float lo, hi;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(a.v));
+  return lo;
+}
+__device__ __forceinline__ float f2hi(F2 a) {
+  float lo, hi;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(a.v));
+  return hi;
+}
+__device__ __forceinline__ F2 add2(F2 a, F2 b) {
+  F2 r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r.v) : "l"(a.v), "l"(b.v));
+  return r;
+}
+__device__ __forceinline__ F2 mul2(F2 a, F2 b) {
+  F2 r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r.v) : "l"(a.v), "l"(b.v));
+  return r;
+}
+__device__ __forceinline__ F2 fma2(F2 a, F2 b, F2 c) {
+  F2 r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r.v) : "l"(a.v), "l"(b.v), "l"(c.v));
+  return r;
+}
+// bf16 pair of a packed pair (round to nearest even), lo in the low half
+__device__ __forceinline__ uint32_t pack2(F2 a) { return pack2(f2lo(a), f2hi(a)); }
 
 // ---- tile loads
 
@@ -247,23 +308,95 @@ __device__ __forceinline__ float warp_incl_sum(float v, int lane) {
   return v;
 }
 
+// fp16 pair (lo in the low half), the TMEM A-operand packing of a k-step
+__device__ __forceinline__ uint32_t f16x2(float lo, float hi) {
+  uint32_t d;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+  return d;
+}
+__device__ __forceinline__ uint32_t f16x2(F2 a) { return f16x2(f2lo(a), f2hi(a)); }
+// bf16 hi + lo of a packed pair
+__device__ __forceinline__ void split2(F2 a, uint32_t& hi, uint32_t& lo) {
+  hi = pack2(a);
+  lo = pack2(add2(a, f2(-__uint_as_float(hi << 16), -__uint_as_float(hi & 0xffff0000u))));
+}
+
+// Seed of segment k of a sequence for state rows [p0, p0 + np) x column n: the
+// slot (zero when fresh; the state pass's copy when the last segment of the same
+// launch overwrites the slot), or the in-order fold of every piece's entry of
+// the earlier segments.
+__device__ __forceinline__ float seed_at(const ScanArgs& a, const Cta& ci, int p, int n) {
+  const int H = a.heads;
+  const int P = a.state_pieces > 0 ? a.state_pieces : 1;
+  const int64_t head_off = (int64_t)ci.h * TP * TN + (int64_t)p * TN + n;
+  auto entry = [&](int e) { return a.ws_state + (int64_t)e * H * TP * TN + head_off; };
+  if (ci.k == 0) {
+    if (ci.fresh) return 0.0f;
+    if (ci.nseg > 1) return *entry((ci.seg0 + ci.nseg - 1) * P);
+    return a.ssm_state[(int64_t)seq_slot(a.tab, ci.sq) * H * TP * TN + head_off];
+  }
+  float h = *entry(ci.seg0 * P);
+  for (int e = ci.seg0 * P + 1; e < (ci.seg0 + ci.k) * P; ++e)
+    h = fmaf(__expf(a.ws_decay[(int64_t)e * H + ci.h]), h, *entry(e));
+  return h;
+}
+
+// Token-by-token recomputation of y for this CTA's (segment, head), used when
+// a chunk's fp16 operands of Y = M . X would overflow. State in fp32 in shared
+// memory; thread (p, n-sixteenth) of 512 keeps 16 state entries in registers.
+__device__ __noinline__ void full_pass_serial_y(const ScanArgs& a, const Cta& ci, int tid) {
+  if (tid >= 512) return;
+  const int p = tid >> 3, n0 = (tid & 7) * 16;
+  const int H = a.heads;
+  float h[16];
+#pragma unroll
+  for (int e = 0; e < 16; ++e) h[e] = seed_at(a, ci, p, n0 + e);
+  const __nv_bfloat16* xbc = static_cast<const __nv_bfloat16*>(a.xbc);
+  __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(a.dst);
+  const int64_t rows_all = a.tab.cu[a.tab.n];
+  const int t0 = ci.c_begin * TQ, t1 = min(ci.c_end * TQ, ci.T);
+  for (int t = t0; t < t1; ++t) {
+    const int64_t r = ci.row0 + t;
+    const float dp = a.dtp[(int64_t)ci.h * rows_all + r];
+    const float decay = ex2(-ci.A2 * dp);
+    const __nv_bfloat16* row = xbc + r * a.conv_dim;
+    const float x = __bfloat162float(row[ci.x_col + p]);
+    const float dx = dp * x;
+    float acc = 0.0f;
+#pragma unroll
+    for (int e = 0; e < 16; ++e) {
+      const float B = __bfloat162float(row[ci.b_col + n0 + e]);
+      const float C = __bfloat162float(row[ci.c_col + n0 + e]);
+      h[e] = fmaf(h[e], decay, dx * B);
+      acc = fmaf(h[e], C, acc);
+    }
+    acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+    acc += __shfl_xor_sync(0xffffffffu, acc, 2);
+    acc += __shfl_xor_sync(0xffffffffu, acc, 4);
+    if ((tid & 7) == 0) dst[r * (int64_t)(H * TP) + ci.x_col + p] = __float2bfloat16_rn(fmaf(ci.Dh, x, acc));
+  }
+}
+
 __global__ void __launch_bounds__(kFullThreads, 1)
 ssd_tc_full(const __grid_constant__ ScanArgs a, const __grid_constant__ CUtensorMap tm, const int use_tma) {
-  extern __shared__ unsigned char smem_raw[];
-  // operand tiles need a 1024-byte aligned base (the swizzle keys on address bits 7-9)
-  const uint32_t raw_base = su32(smem_raw);
-  unsigned char* smem = smem_raw + (((raw_base + 1023u) & ~1023u) - raw_base);
+  extern __shared__ __align__(1024) unsigned char smem[];
   const uint32_t sbase = su32(smem);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if ((sbase & 1023u) != 0) {  // the swizzled operand tiles need a 1024-byte aligned base
+    if (tid == 0) atomicAdd(&g_tc_timeouts, 1u);
+    return;
+  }
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + kOffMisc);
   volatile uint32_t* s_abort = reinterpret_cast<volatile uint32_t*>(smem + kOffMisc + 4);
+  volatile uint32_t* s_range = reinterpret_cast<volatile uint32_t*>(smem + kOffMisc + 8);
   auto bar = [&](int id) { return sbase + kOffBar + 8u * (uint32_t)id; };
   auto par = [](int i) { return (uint32_t)((i >> 1) & 1); };  // phase parity of chunk i on a [2] barrier
   auto stage = [&](int i) { return sbase + (uint32_t)(i & 1) * kStage; };
+  auto dtbuf = [&](int i) { return reinterpret_cast<const float*>(smem + kOffDt + (uint32_t)(i & 1) * kDtBuf); };
 
   const Cta ci = cta_info(a, blockIdx.x);
   const int n = ci.n;
   const int H = a.heads;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const __nv_bfloat16* xbc = static_cast<const __nv_bfloat16*>(a.xbc);
 
   // ---- TMEM (warp 0) and barriers
@@ -275,19 +408,22 @@ ssd_tc_full(const __grid_constant__ ScanArgs a, const __grid_constant__ CUtensor
     for (int b = 0; b < 2; ++b) {
       mbar_init(bar(kFullCB + b), 2);  // C tile, B tile
       mbar_init(bar(kFullX + b), 1);
+      mbar_init(bar(kDtReady + b), 1);
+      mbar_init(bar(kDtFree + b), kMathWarps);
       mbar_init(bar(kCBDone + b), 1);
+      mbar_init(bar(kMReady + b), kMWarps);
+      mbar_init(bar(kXWReady + b), kMWarps);
+      mbar_init(bar(kYdDone + b), 1);
       mbar_init(bar(kYoDone + b), 1);
       mbar_init(bar(kDHDone + b), 1);
-      mbar_init(bar(kYdDone + b), 1);
-      mbar_init(bar(kHDone + b), kMathWarps / 2);
-      mbar_init(bar(kXWReady + b), kMathWarps / 2);
-      mbar_init(bar(kMReady + b), kMathWarps / 2);
-    }
-    for (int b = 0; b < 4; ++b) {
-      mbar_init(bar(kDtReady + b), 1);
-      mbar_init(bar(kEpiDone + b), kMathWarps / 2);
+      mbar_init(bar(kDHFree + b), kSWarps);
+      mbar_init(bar(kHReady + b), kSWarps);
+      mbar_init(bar(kEpiDone + b), kSWarps);
+      mbar_init(bar(kYoIssued + b), 1);
+      mbar_init(bar(kYIssued + b), 1);
     }
     *s_abort = 0u;
+    *s_range = 0u;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   tc_fence_before();
@@ -305,248 +441,234 @@ ssd_tc_full(const __grid_constant__ ScanArgs a, const __grid_constant__ CUtensor
     return s;
   };
 
-  if (warp < kMathWarps) {
-    // =================== element-wise warps: two groups of eight, two warps per
-    // TMEM lane quarter each, so that M and the state / output work of a chunk
-    // run side by side on every SM sub-partition
-    const int qrt = warp & 3;   // TMEM lane quarter = 32-row block
+  // the running state of the S warps (H^T: state row n = TMEM lane, 32 columns p),
+  // kept to the end for the slot write
+  F2 hs[16];  // pair e: columns pc0 + 2 e, pc0 + 2 e + 1
+  bool live = true;
+  const int sw = warp - kMWarps;  // S warp index when >= 0
+  const int s_half = (sw >> 2) & 1;
+  const int s_row = (warp & 3) * 32 + lane;
+  const int pc0 = 32 * s_half;
+
+  if (warp < kMWarps) {
+    // =================== per chunk i, (a) X o w (bf16 hi + lo, w_j = exp(s_end -
+    // s_j) dt'_j) for the state product and x converted to fp16 in place for Y = M .
+    // X, by the warps of TMEM lane quarters 0-2 (quarter 3 has the largest share of
+    // M); (b) M(i) = CB o exp(s_t - s_j) dt'_j (j <= t), + D on the diagonal, in fp16
+    // over the chunk's CB buffer, two threads per token row t (TMEM lane), four
+    // k-steps each (see m_col). Below the diagonal block exp(s_t - s_j) = exp(s_t -
+    // s_e) exp(s_e - s_j) with e the 32-block's last token (the second factor times
+    // dt'_j being v_j); the diagonal block exponentiates each pair; above it, zero.
+    const int qrt = warp & 3;
+    const int half = warp >> 2;
     const int row = qrt * 32 + lane;
-    const int half = (warp >> 2) & 1;  // which 16 columns of each 32-block (M) / which 32 columns (state, y)
     const uint32_t lane_off = (uint32_t)(qrt * 32) << 16;
-    auto dtbuf = [&](int i) { return reinterpret_cast<float*>(smem + kOffDt + (uint32_t)(i % kDtRing) * kDtBuf); };
-
-    if (warp < kMathWarps / 2) {
-      // ---------- group M: M(i) = CB o exp(s_t - s_j) dt'_j (j <= t), + D on the
-      // diagonal. This thread takes columns j in [32 bb + 16 half, +16) of every
-      // 32-block bb and writes, over exactly those CB columns, the 16 values as
-      // bf16 hi (8 packed pairs) then lo (8 packed pairs), so the Y product reads
-      // hi and lo as two K=16 steps against the same 16 rows of X. Above the
-      // diagonal all zero; below it exp(s_t - s_j) = exp(s_t - s_e) exp(s_e - s_j)
-      // with e the block's last token (the second factor times dt'_j being v_j);
-      // the diagonal block exponentiates each pair.
-      for (int i = 0; i < n; ++i) {
-        if (*s_abort) break;
-        // (b) X o w of chunk i (bf16 hi + lo), w_j = exp(s_end - s_j) dt'_j. Work items
-        // (row j, 16-column group g): lane quarter 0 takes groups 0 and 1, quarters 1
-        // and 2 one group each, quarter 3 (the heaviest share of M) none. Runs beside
-        // the other group's state update: both only need the previous dH.
-        bool xok = warp_wait(bar(kDtReady + (i & 3)), (uint32_t)((i >> 2) & 1), s_abort);
-        if (qrt < 3) {  // quarter 3 forms no X o w: M needs only its dt and CB
-          if (xok) xok = warp_wait(bar(kFullX + (i & 1)), par(i), s_abort);
-          if (xok && i > 0) xok = warp_wait(bar(kDHDone + ((i - 1) & 1)), par(i - 1), s_abort);  // X o w buffer read
-        }
-        if (xok && qrt < 3) {
-          const float* D0 = dtbuf(i);
-          const unsigned char* xt = smem + (uint32_t)(i & 1) * kStage + kTileC + kTileB;
-#pragma unroll 1
-          for (int it = 0; it < (qrt == 0 ? 4 : 2); ++it) {
-            const int xr = half * 32 + lane + 64 * (it & 1);
-            const int g = qrt == 0 ? (it >> 1) : qrt + 1;
-            const float w = ex2(D0[TQ - 1] - D0[xr]) * D0[TQ + xr];
-#pragma unroll
-            for (int q = 0; q < 2; ++q) {
-              const uint32_t o = tile_off(xr, 16 * g + 8 * q, TQ);
-              const uint4 xv = *reinterpret_cast<const uint4*>(xt + o);
-              const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
-              uint32_t hi[4], lo[4];
-#pragma unroll
-              for (int e = 0; e < 4; ++e)
-                split2(__uint_as_float(xw[e] << 16) * w, __uint_as_float(xw[e] & 0xffff0000u) * w, hi[e], lo[e]);
-              *reinterpret_cast<uint4*>(smem + kOffXWhi + o) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-              *reinterpret_cast<uint4*>(smem + kOffXWlo + o) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-            }
-          }
-        }
-        fence_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar(kXWReady + (i & 1)));
-
-        // (c) M(i)
-        const bool ok = xok && warp_wait(bar(kCBDone + (i & 1)), par(i), s_abort);
-        if (ok) {
-          tc_fence_after();
-          const float* D0 = dtbuf(i);
-          const float St = D0[row];
-          const uint32_t cbt = tmem + lane_off + kColCB + 128u * (uint32_t)(i & 1);
-#pragma unroll 1
-          for (int bb = 0; bb < 4; ++bb) {  // not unrolled: keeps the loop body small in the instruction cache
-            const int j0 = 32 * bb + 16 * half;
-            uint32_t hi[8], lo[8];
-            if (bb > qrt) {
-#pragma unroll
-              for (int e = 0; e < 8; ++e) hi[e] = lo[e] = 0u;
-            } else {
-              float cb[16];
-              tmem_ld16(cbt + j0, cb);
-              if (bb < qrt) {
-                const float u = ex2(St - D0[32 * bb + 31]);
-                float v[16];
-#pragma unroll
-                for (int e = 0; e < 4; ++e)
-                  *reinterpret_cast<float4*>(v + 4 * e) = *reinterpret_cast<const float4*>(D0 + 2 * TQ + j0 + 4 * e);
-#pragma unroll
-                for (int e = 0; e < 8; ++e)
-                  split2(cb[2 * e] * (u * v[2 * e]), cb[2 * e + 1] * (u * v[2 * e + 1]), hi[e], lo[e]);
-              } else {
-                float sj[16], dj[16];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                  *reinterpret_cast<float4*>(sj + 4 * e) = *reinterpret_cast<const float4*>(D0 + j0 + 4 * e);
-                  *reinterpret_cast<float4*>(dj + 4 * e) = *reinterpret_cast<const float4*>(D0 + TQ + j0 + 4 * e);
-                }
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                  const int ja = j0 + 2 * e, jb = ja + 1;
-                  float ma = ja <= row ? cb[2 * e] * ex2(St - sj[2 * e]) * dj[2 * e] : 0.f;
-                  float mb = jb <= row ? cb[2 * e + 1] * ex2(St - sj[2 * e + 1]) * dj[2 * e + 1] : 0.f;
-                  if (ja == row) ma += ci.Dh;
-                  if (jb == row) mb += ci.Dh;
-                  split2(ma, mb, hi[e], lo[e]);
-                }
-              }
-            }
-            asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};"
-                         :: "r"(cbt + j0), "r"(hi[0]), "r"(hi[1]), "r"(hi[2]), "r"(hi[3]), "r"(hi[4]), "r"(hi[5]),
-                            "r"(hi[6]), "r"(hi[7]) : "memory");
-            asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};"
-                         :: "r"(cbt + j0 + 8), "r"(lo[0]), "r"(lo[1]), "r"(lo[2]), "r"(lo[3]), "r"(lo[4]), "r"(lo[5]),
-                            "r"(lo[6]), "r"(lo[7]) : "memory");
-          }
-          asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-        }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar(kMReady + (i & 1)));
+    const int xu = qrt < 3 ? half * 96 + qrt * 32 + lane : -1;  // X o w thread index (192 of them)
+    for (int i = 0; i < n; ++i) {
+      // (a) X o w and fp16 x of chunk i
+      bool ok = warp_wait(bar(kDtReady + (i & 1)), par(i), s_abort);
+      if (ok && qrt < 3) {
+        ok = warp_wait(bar(kFullX + (i & 1)), par(i), s_abort);
+        if (ok && i > 0) ok = warp_wait(bar(kDHDone + ((i - 1) & 1)), par(i - 1), s_abort);  // X o w buffer read
       }
-    } else {
-      // ---------- group S: X o w, the running state and the output
-      const int pc0 = 32 * half;  // this thread's 32 columns (p) of the state and of y
-      // running state: H^T[n = row][p], p in [pc0, pc0 + 32)
-      const int64_t head_off = (int64_t)ci.h * TP * TN;
-      float* slot_ptr = a.ssm_state + (int64_t)seq_slot(a.tab, ci.sq) * H * TP * TN + head_off;
-      auto ws_entry = [&](int segidx) -> float* { return a.ws_state + (int64_t)segidx * H * TP * TN + head_off; };
-      float hst[32];
-      auto load_state = [&](const float* src) {
+      if (!ok) break;
+      const float* D0 = dtbuf(i);
+      if (qrt < 3) {
+        unsigned char* xt = smem + (uint32_t)(i & 1) * kStage + kTileC + kTileB;
+        const float Send = D0[kDtS + TQ - 1];
+#pragma unroll 1
+        for (int v = xu; v < TQ * TP / 8; v += 192) {  // 16-byte vector v: row v / 8, columns 8 (v % 8) ..
+          const int j = v >> 3;
+          const uint32_t o = tile_off(j, 8 * (v & 7), TQ);
+          const float w = ex2(Send - D0[kDtS + j]) * D0[kDtP + j];
+          const F2 w2 = f2(w, w);
+          const uint4 xv = *reinterpret_cast<const uint4*>(xt + o);
+          const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
+          uint32_t hi[4], lo[4], f[4];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) hst[i] = src ? src[(int64_t)(pc0 + i) * TN + row] : 0.0f;
-      };
-      const int P = a.state_pieces > 0 ? a.state_pieces : 1;
-      if (ci.k == 0) {
-        // the first segment starts from the slot (from the state pass's copy when the
-        // last segment will overwrite the slot in this same launch)
-        load_state(ci.fresh ? nullptr : (ci.nseg > 1 ? ws_entry((ci.seg0 + ci.nseg - 1) * P) : slot_ptr));
-      } else {
-        // the entries of every piece of the earlier segments, in order
-        load_state(ws_entry(ci.seg0 * P));
-        for (int e = ci.seg0 * P + 1; e < (ci.seg0 + ci.k) * P; ++e) {
-          const float d = __expf(a.ws_decay[(int64_t)e * H + ci.h]);
-          const float* src = ws_entry(e);
-#pragma unroll
-          for (int i = 0; i < 32; ++i) hst[i] = fmaf(d, hst[i], src[(int64_t)(pc0 + i) * TN + row]);
+          for (int e = 0; e < 4; ++e) {
+            const F2 x2 = f2(__uint_as_float(xw[e] << 16), __uint_as_float(xw[e] & 0xffff0000u));
+            split2(mul2(x2, w2), hi[e], lo[e]);
+            f[e] = f16x2(x2);  // an x beyond the fp16 range makes y non-finite: caught at the output
+          }
+          *reinterpret_cast<uint4*>(smem + kOffXWhi + o) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+          *reinterpret_cast<uint4*>(smem + kOffXWlo + o) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+          *reinterpret_cast<uint4*>(xt + o) = make_uint4(f[0], f[1], f[2], f[3]);
         }
       }
-      auto state_update = [&](int j) {  // H = exp(total_j) H + dH(j), dH = hi part + lo part
-        const float decay = ex2(dtbuf(j)[TQ - 1]);
-#pragma unroll
-        for (int q = 0; q < 2; ++q) {  // unrolled: hst must stay in registers
-          float dh[16], dl[16];
-          tmem_ld16x2(tmem + lane_off + kColDH + pc0 + 16 * q, tmem + lane_off + kColDH + 64 + pc0 + 16 * q, dh, dl);
-#pragma unroll
-          for (int e = 0; e < 16; ++e) hst[16 * q + e] = fmaf(decay, hst[16 * q + e], dh[e] + dl[e]);
-        }
-      };
-      // bf16 H^T (B operand of C . H^T): row n, columns [pc0, pc0 + 32)
-      auto write_ht = [&]() {
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          uint32_t hw[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) hw[e] = pack2(hst[8 * q + 2 * e], hst[8 * q + 2 * e + 1]);
-          *reinterpret_cast<uint4*>(smem + kOffHT + tile_off(row, pc0 + 8 * q, TN)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-        }
-      };
+      fence_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(kXWReady + (i & 1)));
 
-      bool live = true;
-      for (int i = 0; i <= n; ++i) {
-        if (*s_abort) {
-          live = false;
-          break;
-        }
-        if (i < n) {
-          bool ok;
-          // (a) state through chunk i-1 -> H^T for C . H^T(i); releases the dH accumulator
-          if (i > 0) {
-            ok = warp_wait(bar(kDtReady + ((i - 1) & 3)), (uint32_t)(((i - 1) >> 2) & 1), s_abort) &&
-                 warp_wait(bar(kDHDone + ((i - 1) & 1)), par(i - 1), s_abort) &&
-                 warp_wait(bar(kYoDone + ((i - 1) & 1)), par(i - 1), s_abort);  // C . H^T(i-1) has read H^T
-            if (ok) {
-              tc_fence_after();
-              state_update(i - 1);
-            }
+      // (b) M(i)
+      if (!warp_wait(bar(kCBDone + (i & 1)), par(i), s_abort)) break;
+      tc_fence_after();
+      const float St = D0[kDtS + row];
+      const uint32_t buf = tmem + lane_off + 128u * (uint32_t)(i & 1);
+#pragma unroll 1
+      for (int k = 0; k < 4; ++k) {
+        const int s = 2 * k + half, bb = s >> 1, j0 = 16 * s;
+        uint32_t m[8];
+        if (bb > qrt) {
+#pragma unroll
+          for (int e = 0; e < 8; ++e) m[e] = 0u;
+        } else {
+          float cb[16];
+          tmem_ld16(buf + (uint32_t)j0, cb);
+          if (bb < qrt) {
+            const float u = ex2(St - D0[kDtS + 32 * bb + 31]);
+            const F2 u2 = f2(u, u);
+            float v[16];
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              *reinterpret_cast<float4*>(v + 4 * e) = *reinterpret_cast<const float4*>(D0 + kDtV + j0 + 4 * e);
+#pragma unroll
+            for (int e = 0; e < 8; ++e)  // an entry beyond the fp16 range makes y non-finite: caught at the output
+              m[e] = f16x2(mul2(f2(cb[2 * e], cb[2 * e + 1]), mul2(u2, f2(v[2 * e], v[2 * e + 1]))));
           } else {
-            ok = true;
-          }
-          if (ok) write_ht();
-          fence_async_smem();
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(bar(kHDone + (i & 1)));
-        }
-        if (i > 0) {
-          // (d) output of chunk j = i-1: y = M . X + exp(s_t) C . H^T, straight to HBM
-          const int j = i - 1;
-          bool ok = warp_wait(bar(kYdDone + (j & 1)), par(j), s_abort);
-          if (i == n)  // the state step of this iteration (which waits these) does not run
-            ok = ok && warp_wait(bar(kYoDone + (j & 1)), par(j), s_abort) &&
-                 warp_wait(bar(kDtReady + (j & 3)), (uint32_t)((j >> 2) & 1), s_abort);
-          if (ok) {
-            tc_fence_after();
-            const float et = ex2(dtbuf(j)[row]);
-            const int c = ci.c_begin + j;
-            const bool in_run = row < min(TQ, ci.T - c * TQ);
-            __nv_bfloat16* ydst = static_cast<__nv_bfloat16*>(a.dst) + (ci.row0 + (int64_t)c * TQ + row) * (int64_t)(H * TP) +
-                                  ci.x_col + pc0;
-#pragma unroll 1
-            for (int q = 0; q < 2; ++q) {
-              float yd[16], yo[16];
-              tmem_ld16x2(tmem + lane_off + kColYd + pc0 + 16 * q, tmem + lane_off + kColYo + pc0 + 16 * q, yd, yo);
-              uint32_t o[8];
+            float sj[16], dj[16];
 #pragma unroll
-              for (int f = 0; f < 8; ++f) o[f] = pack2(fmaf(et, yo[2 * f], yd[2 * f]), fmaf(et, yo[2 * f + 1], yd[2 * f + 1]));
-              // one full 32-byte sector (y rows and the 16-column groups are 32-byte aligned)
-              if (in_run)
-                asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(ydst + 16 * q), "r"(o[0]), "r"(o[1]),
-                             "r"(o[2]), "r"(o[3]), "r"(o[4]), "r"(o[5]), "r"(o[6]), "r"(o[7])
-                             : "memory");
+            for (int e = 0; e < 4; ++e) {
+              *reinterpret_cast<float4*>(sj + 4 * e) = *reinterpret_cast<const float4*>(D0 + kDtS + j0 + 4 * e);
+              *reinterpret_cast<float4*>(dj + 4 * e) = *reinterpret_cast<const float4*>(D0 + kDtP + j0 + 4 * e);
+            }
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              const int ja = j0 + 2 * e, jb = ja + 1;
+              float ma = ja <= row ? cb[2 * e] * ex2(St - sj[2 * e]) * dj[2 * e] : 0.f;
+              float mb = jb <= row ? cb[2 * e + 1] * ex2(St - sj[2 * e + 1]) * dj[2 * e + 1] : 0.f;
+              if (ja == row) ma += ci.Dh;
+              if (jb == row) mb += ci.Dh;
+              m[e] = f16x2(ma, mb);
             }
           }
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(bar(kEpiDone + (j & 3)));
         }
+        asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};"
+                     :: "r"(buf + kColM + m_col(s)), "r"(m[0]), "r"(m[1]), "r"(m[2]), "r"(m[3]), "r"(m[4]),
+                        "r"(m[5]), "r"(m[6]), "r"(m[7]) : "memory");
       }
-      // ---- state after the last chunk
-      if (live) {
-        bool ok = true;
-        if (n > 0) {
-          ok = warp_wait(bar(kDHDone + ((n - 1) & 1)), par(n - 1), s_abort);
-          if (ok) {
-            tc_fence_after();
-            state_update(n - 1);
-          }
-        }
-        if (ok && ci.k == ci.nseg - 1) {
-#pragma unroll
-          for (int i = 0; i < 32; ++i) slot_ptr[(int64_t)(pc0 + i) * TN + row] = hst[i];
-        }
+      asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(bar(kMReady + (i & 1)));
+        mbar_arrive(bar(kDtFree + (i & 1)));
       }
     }
-  } else if (warp == 16) {
-    // =================== per chunk i: dt' = softplus(dt + dt_bias), log2-scaled
-    // cumulative decay S and block factors v into dt buffer i % 4 (lane l: tokens
-    // 4l .. 4l+3; the buffer last served chunk i-4, whose readers are done once
-    // chunk i-3's output is written); then CB = C . B^T (lane 0)
-    // dt' of chunks i .. i+3, loaded four chunks ahead (the loads stay in flight until used)
+  } else if (warp < kMathWarps) {
+    // =================== S warps: per chunk i, (a) the state through chunk i (H =
+    // exp(total) H + dH, dH = hi part + lo part; TMEM lane = state row n), (b) once
+    // C . H^T(i-1) is done, its value read and H(i) written to shared memory as bf16
+    // hi + lo, (c) the output y = M . X + exp(s_t) C . H^T, straight to HBM. Two
+    // warps per TMEM lane quarter, 32 columns p each.
+    const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+    const int row = s_row;
+    {
+      // the seed, staged through this thread's own places of the (not yet used)
+      // H^T region, so that seed_at is not unrolled 32 times
+      float* s_seed = reinterpret_cast<float*>(smem + kOffHT);
+#pragma unroll 1
+      for (int e = 0; e < 32; ++e) s_seed[(pc0 + e) * TN + row] = seed_at(a, ci, pc0 + e, row);
+#pragma unroll
+      for (int e = 0; e < 16; ++e) hs[e] = f2(s_seed[(pc0 + 2 * e) * TN + row], s_seed[(pc0 + 2 * e + 1) * TN + row]);
+      // every S thread has its seed before any writes the bf16 H^T over the region
+      asm volatile("bar.sync 1, %0;" :: "r"(32 * kSWarps) : "memory");
+    }
+    auto write_h = [&]() {  // bf16 hi + lo of H^T: row n, columns [pc0, +32) of each block
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        uint32_t hw[4], lw[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) split2(hs[4 * q + e], hw[e], lw[e]);
+        *reinterpret_cast<uint4*>(smem + kOffHT + tile_off(row, pc0 + 8 * q, TN)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+        *reinterpret_cast<uint4*>(smem + kOffHT + tile_off(row, TP + pc0 + 8 * q, TN)) =
+            make_uint4(lw[0], lw[1], lw[2], lw[3]);
+      }
+    };
+    write_h();
+    fence_async_smem();
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) {
+      mbar_arrive(bar(kHReady));
+      mbar_arrive(bar(kDHFree));
+    }
+    // sum of every output: not finite iff an fp16 operand of Y = M . X overflowed
+    // (an M entry or x beyond 65 504 becomes inf, and inf or inf * 0 reaches y)
+    F2 ysum = f2(0.0f, 0.0f);
+    for (int i = 0; i < n; ++i) {
+      // (a) state through chunk i; releases the dH accumulator and the dt buffer
+      if (!(warp_wait(bar(kDtReady + (i & 1)), par(i), s_abort) && warp_wait(bar(kDHDone + (i & 1)), par(i), s_abort))) {
+        live = false;
+        break;
+      }
+      tc_fence_after();
+      const float* D0 = dtbuf(i);
+      const float decay = ex2(D0[kDtS + TQ - 1]);
+      const float et = ex2(D0[kDtS + row]);
+      const F2 dec2 = f2(decay, decay), et2 = f2(et, et);
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {  // unrolled: the state must stay in registers
+        float dh[16], dl[16];
+        tmem_ld16x2(tmem + lane_off + kColDH + pc0 + 16 * q, tmem + lane_off + kColDH + TP + pc0 + 16 * q, dh, dl);
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+          hs[8 * q + e] = fma2(dec2, hs[8 * q + e], add2(f2(dh[2 * e], dh[2 * e + 1]), f2(dl[2 * e], dl[2 * e + 1])));
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(bar(kDHFree + ((i + 1) & 1)));
+        mbar_arrive(bar(kDtFree + (i & 1)));
+      }
+      // (b) the output of chunk i, y = M . X + exp(s_t) C . H^T(i-1), straight to HBM;
+      // then H(i) for C . H^T(i+1) (C . H^T(i-1) has read the previous one)
+      if (!(warp_wait(bar(kYoDone + (i & 1)), par(i), s_abort) && warp_wait(bar(kYdDone + (i & 1)), par(i), s_abort))) {
+        live = false;
+        break;
+      }
+      tc_fence_after();
+      {
+        const int c = ci.c_begin + i;
+        const bool in_run = row < min(TQ, ci.T - c * TQ);
+        __nv_bfloat16* ydst = static_cast<__nv_bfloat16*>(a.dst) +
+                              (ci.row0 + (int64_t)c * TQ + row) * (int64_t)(H * TP) + ci.x_col + pc0;
+        const uint32_t ybuf = tmem + lane_off + 128u * (uint32_t)(i & 1) + kColY + pc0;
+        const uint32_t obuf = tmem + lane_off + kColYo + pc0;
+#pragma unroll 1
+        for (int q = 0; q < 2; ++q) {  // 16 columns at a time
+          float yd[16], oh[16], ol[16];
+          tmem_ld16x2(obuf + 16 * q, obuf + TP + 16 * q, oh, ol);
+          tmem_ld16(ybuf + 16 * q, yd);
+          uint32_t o[8];
+#pragma unroll
+          for (int f = 0; f < 8; ++f) {
+            const F2 yv = fma2(et2, add2(f2(oh[2 * f], oh[2 * f + 1]), f2(ol[2 * f], ol[2 * f + 1])),
+                               f2(yd[2 * f], yd[2 * f + 1]));
+            ysum = add2(ysum, yv);
+            o[f] = pack2(yv);
+          }
+          // one full 32-byte sector (y rows and the 16-column groups are 32-byte aligned)
+          if (in_run)
+            asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(ydst + 16 * q), "r"(o[0]), "r"(o[1]),
+                         "r"(o[2]), "r"(o[3]), "r"(o[4]), "r"(o[5]), "r"(o[6]), "r"(o[7]) : "memory");
+        }
+      }
+      write_h();
+      fence_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(bar(kHReady + ((i + 1) & 1)));
+        mbar_arrive(bar(kEpiDone + (i & 1)));
+      }
+    }
+    if (!isfinite(f2lo(ysum) + f2hi(ysum))) *s_range = 1u;
+  } else if (warp == kMathWarps) {
+    // =================== per chunk i: dt' (loaded four chunks ahead), log2-scaled
+    // cumulative decay S and block factors v into dt buffer i % 2 (lane l: tokens
+    // 4l .. 4l+3; the buffer last served chunk i-2, whose readers are done); then
+    // CB = C . B^T (lane 0) into buffer i % 2 once chunk i-2's output has left it
     const int64_t rows_all = a.tab.cu[a.tab.n];
     auto load_dtp = [&](int i) {
       DtQuad r = {{0.f, 0.f, 0.f, 0.f}};
@@ -562,7 +684,7 @@ ssd_tc_full(const __grid_constant__ ScanArgs a, const __grid_constant__ CUtensor
     DtQuad r0 = load_dtp(0), r1 = load_dtp(1), r2 = load_dtp(2), r3 = load_dtp(3);
     int last = -1;
     for (int i = 0; i < n; ++i) {
-      if (i >= 3 && !warp_wait(bar(kEpiDone + ((i - 3) & 3)), (uint32_t)(((i - 3) >> 2) & 1), s_abort)) break;
+      if (i >= 2 && !warp_wait(bar(kDtFree + (i & 1)), par(i - 2), s_abort)) break;
       {
         float dp[4], S[4], run = 0.f;
 #pragma unroll
@@ -579,23 +701,26 @@ ssd_tc_full(const __grid_constant__ ScanArgs a, const __grid_constant__ CUtensor
 #pragma unroll
         for (int e = 0; e < 4; ++e) S[e] += excl;
         const float Se = __shfl_sync(0xffffffffu, S[3], (lane & ~7) | 7);  // S at the end of this 32-block
-        float* D0 = reinterpret_cast<float*>(smem + kOffDt + (uint32_t)(i % kDtRing) * kDtBuf);
-        *reinterpret_cast<float4*>(D0 + 4 * lane) = make_float4(S[0], S[1], S[2], S[3]);
-        *reinterpret_cast<float4*>(D0 + TQ + 4 * lane) = make_float4(dp[0], dp[1], dp[2], dp[3]);
-        *reinterpret_cast<float4*>(D0 + 2 * TQ + 4 * lane) =
-            make_float4(ex2(Se - S[0]) * dp[0], ex2(Se - S[1]) * dp[1], ex2(Se - S[2]) * dp[2], ex2(Se - S[3]) * dp[3]);
+        float* D0 = reinterpret_cast<float*>(smem + kOffDt + (uint32_t)(i & 1) * kDtBuf);
+        *reinterpret_cast<float4*>(D0 + kDtS + 4 * lane) = make_float4(S[0], S[1], S[2], S[3]);
+        *reinterpret_cast<float4*>(D0 + kDtP + 4 * lane) = make_float4(dp[0], dp[1], dp[2], dp[3]);
+        if (lane < 24)  // v of tokens 0..95 (the last block is never below a diagonal)
+          *reinterpret_cast<float4*>(D0 + kDtV + 4 * lane) =
+              make_float4(ex2(Se - S[0]) * dp[0], ex2(Se - S[1]) * dp[1], ex2(Se - S[2]) * dp[2], ex2(Se - S[3]) * dp[3]);
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar(kDtReady + (i & 3)));
+        if (lane == 0) mbar_arrive(bar(kDtReady + (i & 1)));
       }
       if (!warp_wait(bar(kFullCB + (i & 1)), par(i), s_abort)) break;
-      if (i >= 2 && !warp_wait(bar(kYdDone + (i & 1)), par(i - 2), s_abort)) break;  // M(i-2) consumed
+      if (i >= 2 && !warp_wait(bar(kEpiDone + (i & 1)), par(i - 2), s_abort)) break;  // buffer i % 2 free
+      // behind C . H^T(i-1) and Y(i-1) in the tensor pipe: those two gate the output
+      if (i >= 1 && !warp_wait(bar(kYIssued + ((i - 1) & 1)), par(i - 1), s_abort)) break;
       tc_fence_after();
       if (lane == 0) {
         const uint64_t a0 = sdesc(stage(i), 16, 1024), b0 = sdesc(stage(i) + kTileC, 16, 1024);
 #pragma unroll
         for (int s2 = 0; s2 < TN / 16; ++s2) {
           const uint32_t ko = ((s2 >> 2) * TQ * 128 + (s2 & 3) * 32) >> 4;
-          mma_ss(tmem + kColCB + 128u * (uint32_t)(i & 1), a0 + ko, b0 + ko, idesc128(128, 0, 0), s2 > 0);
+          mma_ss(tmem + 128u * (uint32_t)(i & 1), a0 + ko, b0 + ko, idesc128(128, 0, 0), s2 > 0);
         }
         mma_commit(bar(kCBDone + (i & 1)));
       }
@@ -603,28 +728,8 @@ ssd_tc_full(const __grid_constant__ ScanArgs a, const __grid_constant__ CUtensor
       last = i;
     }
     if (lane == 0 && last >= 0) drain_bar(bar(kCBDone + (last & 1)), par(last));
-  } else if (warp == 17) {
-    // =================== Yoff = C . H^T
-    if (lane == 0) {
-      int last = -1;
-      for (int i = 0; i < n; ++i) {
-        if (!wait_bar(bar(kFullCB + (i & 1)), par(i), s_abort)) break;
-        if (!wait_bar(bar(kHDone + (i & 1)), par(i), s_abort)) break;  // H^T through chunk i-1 written
-        if (i >= 1 && !wait_bar(bar(kEpiDone + ((i - 1) & 3)), (uint32_t)(((i - 1) >> 2) & 1), s_abort)) break;  // Yoff(i-1) read
-        tc_fence_after();
-        const uint64_t a0 = sdesc(stage(i), 16, 1024), h0 = sdesc(sbase + kOffHT, TN * 128, 1024);
-#pragma unroll
-        for (int s2 = 0; s2 < TN / 16; ++s2) {
-          const uint32_t ko = ((s2 >> 2) * TQ * 128 + (s2 & 3) * 32) >> 4;
-          mma_ss(tmem + kColYo, a0 + ko, h0 + ((s2 * 2048) >> 4), idesc128(64, 0, 1), s2 > 0);
-        }
-        mma_commit(bar(kYoDone + (i & 1)));
-        last = i;
-      }
-      if (last >= 0) drain_bar(bar(kYoDone + (last & 1)), par(last));
-    }
-  } else if (warp == 18) {
-    // =================== dH^T = B^T . (X o w); C and B tile loads
+  } else if (warp == kMathWarps + 1) {
+    // =================== Yoff = C . [H hi | H lo]^T (N = 128); C and B tile loads
     auto load_cb = [&](int i) {
       const ChunkSrc s = chunk_src(i);
       load_tile(stage(i), s, &tm, use_tma != 0, ci.c_col, TN, bar(kFullCB + (i & 1)), lane);
@@ -633,10 +738,40 @@ ssd_tc_full(const __grid_constant__ ScanArgs a, const __grid_constant__ CUtensor
     int loaded = min(n, 2), last = -1;
     for (int i = 0; i < loaded; ++i) load_cb(i);
     for (int i = 0; i < n; ++i) {
-      const bool ok = warp_wait(bar(kFullCB + (i & 1)), par(i), s_abort) &&
-                      warp_wait(bar(kHDone + (i & 1)), par(i), s_abort) &&  // dH accumulator read
-                      warp_wait(bar(kXWReady + (i & 1)), par(i), s_abort);
-      if (!ok) break;
+      if (!(warp_wait(bar(kFullCB + (i & 1)), par(i), s_abort) && warp_wait(bar(kHReady + (i & 1)), par(i), s_abort)))
+        break;
+      tc_fence_after();
+      if (lane == 0) {
+        const uint64_t a0 = sdesc(stage(i), 16, 1024), h0 = sdesc(sbase + kOffHT, TN * 128, 1024);
+#pragma unroll
+        for (int s2 = 0; s2 < TN / 16; ++s2) {
+          const uint32_t ko = ((s2 >> 2) * TQ * 128 + (s2 & 3) * 32) >> 4;
+          mma_ss(tmem + kColYo, a0 + ko, h0 + ((s2 * 2048) >> 4), idesc128(2 * TP, 0, 1), s2 > 0);
+        }
+        mma_commit(bar(kYoDone + (i & 1)));
+        mbar_arrive(bar(kYoIssued + (i & 1)));
+      }
+      __syncwarp();
+      last = i;
+      if (i + 2 < n) {
+        // chunk i's C and B tiles are spent once its three products are done
+        if (!(warp_wait(bar(kYoDone + (i & 1)), par(i), s_abort) && warp_wait(bar(kCBDone + (i & 1)), par(i), s_abort) &&
+              warp_wait(bar(kDHDone + (i & 1)), par(i), s_abort)))
+          break;
+        load_cb(i + 2);
+        loaded = i + 3;
+      }
+    }
+    if (lane == 0 && last >= 0) drain_bar(bar(kYoDone + (last & 1)), par(last));
+    if (lane == 0 && *s_abort)
+      for (int i = max(0, loaded - 2); i < loaded; ++i) drain_bar(bar(kFullCB + (i & 1)), par(i));
+  } else if (warp == kMathWarps + 2) {
+    // =================== dH^T = B^T . [X o w hi | lo] (N = 128)
+    int last = -1;
+    for (int i = 0; i < n; ++i) {
+      if (!(warp_wait(bar(kFullCB + (i & 1)), par(i), s_abort) && warp_wait(bar(kXWReady + (i & 1)), par(i), s_abort) &&
+            warp_wait(bar(kDHFree + (i & 1)), par(i), s_abort)))
+        break;
       tc_fence_after();
       if (lane == 0) {
         // B operand [X o w hi | X o w lo]: two 64-column blocks 16 KB apart
@@ -652,41 +787,30 @@ ssd_tc_full(const __grid_constant__ ScanArgs a, const __grid_constant__ CUtensor
       }
       __syncwarp();
       last = i;
-      if (i + 2 < n) {
-        // chunk i's C and B tiles are spent once its three products are done
-        if (!(warp_wait(bar(kDHDone + (i & 1)), par(i), s_abort) && warp_wait(bar(kCBDone + (i & 1)), par(i), s_abort) &&
-              warp_wait(bar(kYoDone + (i & 1)), par(i), s_abort)))
-          break;
-        load_cb(i + 2);
-        loaded = i + 3;
-      }
     }
     if (lane == 0 && last >= 0) drain_bar(bar(kDHDone + (last & 1)), par(last));
-    if (lane == 0 && *s_abort)
-      for (int i = max(0, loaded - 2); i < loaded; ++i) drain_bar(bar(kFullCB + (i & 1)), par(i));
-  } else if (warp == kMathWarps + 3) {
-    // =================== Y = M . X (A = M hi, lo from TMEM); X tile loads
+  } else {
+    // =================== Y = M . X (fp16; A = M from TMEM, 8 k-steps); X tile loads
     auto load_x = [&](int i) {
       load_tile(stage(i) + kTileC + kTileB, chunk_src(i), &tm, use_tma != 0, ci.x_col, TP, bar(kFullX + (i & 1)), lane);
     };
     int loaded = min(n, 2), last = -1;
     for (int i = 0; i < loaded; ++i) load_x(i);
     for (int i = 0; i < n; ++i) {
-      bool ok = warp_wait(bar(kMReady + (i & 1)), par(i), s_abort);
-      if (ok && i >= 1) ok = warp_wait(bar(kEpiDone + ((i - 1) & 3)), (uint32_t)(((i - 1) >> 2) & 1), s_abort);  // Y accumulator read
-      if (ok) ok = warp_wait(bar(kFullX + (i & 1)), par(i), s_abort);
-      if (!ok) break;
+      // behind C . H^T(i) in the tensor pipe (the output needs both; C . H^T(i) is on the
+      // state's critical loop)
+      if (!(warp_wait(bar(kMReady + (i & 1)), par(i), s_abort) && warp_wait(bar(kXWReady + (i & 1)), par(i), s_abort) &&
+            warp_wait(bar(kYoIssued + (i & 1)), par(i), s_abort)))
+        break;
       tc_fence_after();
       if (lane == 0) {
         const uint64_t x0 = sdesc(stage(i) + kTileC + kTileB, TQ * 128, 1024);
-        const uint32_t m = tmem + kColCB + 128u * (uint32_t)(i & 1);
+        const uint32_t buf = tmem + 128u * (uint32_t)(i & 1);
 #pragma unroll
-        for (int s2 = 0; s2 < TQ / 16; ++s2) {  // tokens [16 s2, 16 s2 + 16): hi, then lo, same 16 rows of X
-          const uint64_t xd = x0 + ((s2 * 2048) >> 4);
-          mma_ts(tmem + kColYd, m + 16 * s2, xd, idesc128(64, 0, 1), s2 > 0);
-          mma_ts(tmem + kColYd, m + 16 * s2 + 8, xd, idesc128(64, 0, 1), 1);
-        }
+        for (int s2 = 0; s2 < TQ / 16; ++s2)  // tokens [16 s2, 16 s2 + 16)
+          mma_ts(buf + kColY, buf + kColM + m_col(s2), x0 + ((s2 * 2048) >> 4), idesc128(TP, 0, 1, 0), s2 > 0);
         mma_commit(bar(kYdDone + (i & 1)));
+        mbar_arrive(bar(kYIssued + (i & 1)));
       }
       __syncwarp();
       last = i;
@@ -704,8 +828,41 @@ ssd_tc_full(const __grid_constant__ ScanArgs a, const __grid_constant__ CUtensor
   // ---- teardown: every role has drained what it issued
   tc_fence_before();
   __syncthreads();
-  if (tid == 0 && *s_abort) atomicAdd(&g_tc_timeouts, 1u);
+  const bool aborted = *s_abort != 0u;
+  if (tid == 0 && aborted) atomicAdd(&g_tc_timeouts, 1u);
   if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;" :: "r"(tmem));
+  if (aborted) return;
+  const bool s_warp = sw >= 0 && warp < kMathWarps;
+  const bool write_slot = ci.k == ci.nseg - 1;
+  float* slot_ptr = a.ssm_state + (int64_t)seq_slot(a.tab, ci.sq) * H * TP * TN + (int64_t)ci.h * TP * TN;
+  if (*s_range == 0u) {
+    // ---- state after the last chunk
+    if (s_warp && live && write_slot) {
+#pragma unroll
+      for (int e = 0; e < 16; ++e) {
+        slot_ptr[(int64_t)(pc0 + 2 * e) * TN + s_row] = f2lo(hs[e]);
+        slot_ptr[(int64_t)(pc0 + 2 * e + 1) * TN + s_row] = f2hi(hs[e]);
+      }
+    }
+    return;
+  }
+  // A chunk whose fp16 operands would overflow: y of the whole segment again,
+  // token by token. The final state waits in shared memory ([p][n] fp32 over the
+  // H^T tiles), since the recomputation may read its seed from the slot.
+  float* s_state = reinterpret_cast<float*>(smem + kOffHT);
+  static_assert(TP * TN * 4 <= kTileHT, "final state fits over the H^T tiles");
+  if (s_warp) {
+#pragma unroll
+    for (int e = 0; e < 16; ++e) {
+      s_state[(pc0 + 2 * e) * TN + s_row] = f2lo(hs[e]);
+      s_state[(pc0 + 2 * e + 1) * TN + s_row] = f2hi(hs[e]);
+    }
+  }
+  __syncthreads();
+  full_pass_serial_y(a, ci, tid);
+  __syncthreads();  // every seed has been read from the slot before it is overwritten
+  if (write_slot)
+    for (int e = tid; e < TP * TN; e += kFullThreads) slot_ptr[e] = s_state[e];
 }
 
 // State pass: end state (from zero; the first segment from the slot's state)

@@ -101,6 +101,39 @@ def test_130m_short_runs_unsegmented():
     _prefill_parity(wl)
 
 
+def test_scan_fp16_range_fallback():
+    """Inputs whose Y = M . X operands leave the fp16 range: a token whose C and
+    B rows are large and aligned (an M entry near 1.5e5, in every head's
+    segment, since the heads share one group) and one x entry of 7e4 in one head.
+    The CTAs that meet them recompute their segment's y token by token; y and
+    the state still match the oracle, and no wait times out."""
+    dev = device()
+    wl = W.make_prefill("range", 61, W.DIMS_130M, [700, 1300], torch.bfloat16, 6, [1, 0])
+    H, P, N, G = wl.dims.tuple4()
+    ref = oracle_prefill(wl)
+    xbc = ref["xbc"].clone()
+    dt = wl.dt.clone()
+    t_m = 300                                   # sequence 0: C_t . B_t = 900 * 128, dt' about 1.3
+    xbc[t_m, H * P:H * P + N] = 30.0
+    xbc[t_m, H * P + G * N:H * P + G * N + N] = 30.0
+    dt[t_m, :] = 5.0
+    t_x, h_x = 700 + 900, 5                     # sequence 1, head 5: one x of 7e4
+    xbc[t_x, h_x * P + 7] = 7.0e4
+    p, b = wl.params, wl.batch
+    lib = ss.library()
+    before = lib.mamba2_device_timeouts()
+    y, ssm = gpu_scan(wl, dev, xbc, dt=dt)
+    torch.cuda.synchronize()
+    ssm_o = wl.ssm_state.clone()
+    _, y64 = oracle.ssd_scan(xbc, dt, p.A_log, p.dt_bias, p.D, ssm_o, (H, P, N, G), b.cu_seqlens, b.slots, b.fresh)
+    assert y64.abs().max().item() > 1e5, "the planted values should make some y large"
+    check_act(y.cpu(), y64, "scan output with fp16-range fallback")
+    rl = slot_rel_l2(ssm, ssm_o, b.slots)
+    assert rl <= STATE_PREFILL_REL_L2, f"ssm state rel L2 {rl:.3g}"
+    _untouched(ssm, wl.ssm_state, b.slots, "ssm pool")
+    assert lib.mamba2_device_timeouts() == before
+
+
 def test_head_group_mapping_gpu():
     """Zeroing group 1's B and C leaves heads 2, 3 with D*x exactly and heads 0, 1 unchanged."""
     dev = device()
