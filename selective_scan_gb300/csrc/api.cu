@@ -428,17 +428,15 @@ mamba2_status mamba2_gated_rmsnorm(void* dst, const void* x, const void* z, cons
 }
 
 namespace {
-// CTAs per sequence of a decode step over n sequences. A small batch spreads each
-// sequence over 16 SMs (one sequence at 48 heads: 10.0 instead of 12.4 us a step with
-// 8). Once 16-CTA clusters would not all fit at once, each CTA takes up to 8 heads:
-// 256 sequences at 48 heads take 136 us a step in clusters of 6 against 147 with 8,
-// 143 with 7, 140 with 5 or 3 and 160 with 4 (one GB300).
-void decode_cluster(int64_t n, int heads, DecodeArgs& a) {
-  const int cl = n * kDecodeMaxCluster <= device_sm_count()
-                     ? std::min(kDecodeMaxCluster, heads)
-                     : std::min(kDecodePortableCluster, (heads + kDecodeHeadsPerCta - 1) / kDecodeHeadsPerCta);
-  a.heads_per_cta = (heads + cl - 1) / cl;
-  a.cluster = (heads + a.heads_per_cta - 1) / a.heads_per_cta;
+// Heads per CTA of the decode state kernel over n sequences: the fewest (a power
+// of two, at most 8) that keep the grid near four CTAs per SM or more, so a single
+// sequence spreads over one CTA per head and large batches take 8 heads a CTA.
+void decode_split(int64_t n, int heads, DecodeArgs& a) {
+  const int64_t target = 4 * (int64_t)std::max(1, device_sm_count());
+  int hpc = 1;
+  while (hpc < kDecodeMaxHeadsPerCta && hpc < heads && n * ((heads + hpc - 1) / hpc) > 2 * target) hpc *= 2;
+  a.heads_per_cta = hpc;
+  a.ctas_per_seq = (heads + hpc - 1) / hpc;
 }
 }  // namespace
 
@@ -488,7 +486,7 @@ mamba2_status mamba2_decode_step(void* dst, const void* xBC, const void* z, cons
   a.conv_kernel = dims->conv_kernel;
   a.norm_groups = norm_groups;
   a.eps = eps;
-  decode_cluster(n, dims->heads, a);
+  decode_split(n, dims->heads, a);
   fill_table(a.tab, rb);
   for (int i = 0; i <= n; ++i) a.tab.tile[i] = i;
   cudaError_t e = launch_decode(a, act, static_cast<cudaStream_t>(stream));
@@ -538,8 +536,8 @@ mamba2_status mamba2_decode_step_device(void* dst, const void* xBC, const void* 
   a.conv_kernel = dims->conv_kernel;
   a.norm_groups = norm_groups;
   a.eps = eps;
-  // the grid is sized for the capacity (clusters past the device count leave at once)
-  decode_cluster(capacity, dims->heads, a);
+  // the grid is sized for the capacity (CTAs past the device count leave at once)
+  decode_split(capacity, dims->heads, a);
   a.tab.n = capacity;
   a.dev_slots = slots_dev;
   a.dev_fresh = fresh_dev;

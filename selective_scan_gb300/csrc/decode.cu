@@ -10,24 +10,23 @@
 // recurrent inference" (section "Summary") runs it as indexed recurrent decode
 // over a state pool.
 //
-// Work split: a thread-block cluster per sequence (16 CTAs for batches small
-// enough that all such clusters fit on the SMs at once, else 8); CTA r of the cluster owns
-// heads [r*hpc, (r+1)*hpc). Each CTA
+// Two kernels per step. decode_step_kernel: CTA r of a sequence owns heads
+// [r*hpc, (r+1)*hpc) (hpc heads per CTA, chosen from the batch size so that the
+// grid fills the GPU: one head per CTA for a single sequence, up to 8 for large
+// batches). Each CTA
 //   1. computes the conv for its heads' x channels and for all B/C channels
 //      (B/C recomputed per CTA: 2*G*N channels, tiny), writes the new conv
 //      history of its own x channels (no other CTA touches them);
 //   2. streams its heads' fp32 SSM state once: 16-byte loads along d_state,
 //      h = h*decay + dt'*x*B, y = h.C + D*x (warp-shuffle reduction), store;
-//   3. forms g = y*silu(z) and a deterministic partial sum of g^2 per norm
-//      group in shared memory;
-//   4. cluster barrier; CTA 0 then writes the B/C conv history (every CTA has
-//      read the old one by now); each CTA sums the partials of all CTAs in
-//      rank order through distributed shared memory and writes its normed
-//      outputs; a final cluster barrier keeps shared memory alive until every
-//      CTA has read it.
+//   3. writes y, rounded to the activation type (the unfused scan's output), to dst.
+// decode_finish_kernel, one CTA per sequence, once every CTA of the first kernel
+// is done (stream order): shifts the B/C conv history (every CTA has read the old
+// one), then forms g = y*silu(z) and the gated RMSNorm over each group in a fixed
+// order, writing the output over y in dst.
 // HBM traffic per sequence: SSM state read + write (H*P*N*4 bytes each), conv
-// history read + write, the token's inputs and outputs. The state stream is
-// the roofline term.
+// history read + write, the token's inputs and outputs (y once more through the
+// second kernel). The state stream is the roofline term.
 #include "common.cuh"
 
 namespace mamba2 {
@@ -40,23 +39,10 @@ __device__ __forceinline__ uint32_t smem_addr(const void* p) {
   return (uint32_t)__cvta_generic_to_shared(p);
 }
 
-__device__ __forceinline__ void cluster_sync_all() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n" ::: "memory");
-  asm volatile("barrier.cluster.wait.acquire.aligned;\n" ::: "memory");
-}
-
-__device__ __forceinline__ float ld_dsmem_f32(const float* local, uint32_t rank) {
-  uint32_t remote;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_addr(local)), "r"(rank));
-  float v;
-  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
-  return v;
-}
-
 constexpr int kRingRows = 8;  // d_state = 128: state rows per ring stage (one float4 per lane per row)
 // float offset of the state ring in the dynamic shared memory (16-byte aligned) and its bytes
 __host__ __device__ constexpr int ring_offset(int hpc, int P, int G, int N) {
-  return (3 * hpc * P + 2 * G * N + 3 * hpc + kDecodeMaxNormGroups + kDecodeWarps + 3) & ~3;
+  return (2 * hpc * P + 2 * G * N + 3 * hpc + 3) & ~3;
 }
 constexpr int kRingBytes = kDecodeWarps * 2 * kRingRows * 32 * 16;
 
@@ -69,7 +55,7 @@ decode_step_kernel(const __grid_constant__ DecodeArgs a) {
   constexpr int HIST = K - 1;
   extern __shared__ __align__(16) float dsm[];
 
-  const int rank = blockIdx.x;  // cluster spans grid.x exactly
+  const int rank = blockIdx.x;  // CTA of the sequence
   const int s = blockIdx.y;
   const int H = a.heads, P = a.headdim, N = a.d_state, G = a.ngroups;
   const int d_inner = H * P;
@@ -79,26 +65,32 @@ decode_step_kernel(const __grid_constant__ DecodeArgs a) {
   const int nh = max(0, h1 - h0);
   const int rows = nh * P;  // state rows owned by this CTA
   const bool dev = a.dev_slots != nullptr;
-  // a device batch: every CTA of a cluster reads the same status word and count (written
-  // by the batch check before this launch), so a cluster leaves whole, before any barrier
+  // a device batch: nothing is touched unless the batch check (the launch before) passed
   if (dev && (__ldg(a.dev_status) != 0 || s >= __ldg(a.dev_n))) return;
   const bool fresh = dev ? __ldg(a.dev_fresh + s) != 0 : seq_fresh(a.tab, s);
   const int64_t slot = dev ? (int64_t)__ldg(a.dev_slots + s) : (int64_t)seq_slot(a.tab, s);
 
   float* xs = dsm;                           // [heads_per_cta * P] conv output x
-  float* ys = xs + a.heads_per_cta * P;      // [heads_per_cta * P] y, then g
+  float* ys = xs + a.heads_per_cta * P;      // [heads_per_cta * P] h . C
   float* bc = ys + a.heads_per_cta * P;      // [2 * G * N] conv output B, C
   float* hdt = bc + 2 * G * N;               // [heads_per_cta] dt'
   float* hdec = hdt + a.heads_per_cta;       // [heads_per_cta] decay
   float* hD = hdec + a.heads_per_cta;        // [heads_per_cta] D
-  float* part = hD + a.heads_per_cta;        // [kDecodeMaxNormGroups]
-  float* wsum = part + kDecodeMaxNormGroups; // [kDecodeWarps]
-  float* zs = wsum + kDecodeWarps;           // [heads_per_cta * P] silu(z) of own channels
 
   const T* xBC = static_cast<const T*>(a.xBC) + (int64_t)s * conv_dim;
   T* cst = static_cast<T*>(a.conv_state) + slot * HIST * conv_dim;
-
-  for (int i = threadIdx.x; i < kDecodeMaxNormGroups; i += kDecodeThreads) part[i] = 0.0f;
+  // the finish kernel of this step may be scheduled once every CTA has started (it
+  // waits for this grid's completion before it reads anything this grid writes)
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  // per-head constants, loaded before the conv so their latency overlaps it
+  if (threadIdx.x < nh) {
+    const int h = h0 + threadIdx.x;
+    const float v = Act<T>::to_f(static_cast<const T*>(a.dt)[(int64_t)s * H + h]) + a.dt_bias[h];
+    const float dtp = softplus_f(v);
+    hdt[threadIdx.x] = dtp;
+    hdec[threadIdx.x] = expf(-expf(a.A_log[h]) * dtp);
+    hD[threadIdx.x] = a.D[h];
+  }
 
   // ---- state-stream geometry; the first batch of state loads is issued now
   // so it is in flight while the conv phase below waits on its own inputs
@@ -164,12 +156,6 @@ decode_step_kernel(const __grid_constant__ DecodeArgs a) {
     }
     const uint4 craw = *reinterpret_cast<const uint4*>(xBC + c0);
     Vec16<T>::load(reinterpret_cast<const T*>(&craw), cur);
-    if (is_x) {  // the gate of the same channels, for the norm
-      float zv[V];
-      Vec16<T>::load(static_cast<const T*>(a.z) + (int64_t)s * d_inner + c0, zv);
-#pragma unroll
-      for (int j = 0; j < V; ++j) zs[i * V + j] = silu_f(zv[j]);
-    }
     float wv[V * K], bv[V];
     {
       const float4* wp = reinterpret_cast<const float4*>(a.conv_w + (int64_t)c0 * K);
@@ -226,14 +212,6 @@ decode_step_kernel(const __grid_constant__ DecodeArgs a) {
       if (HIST > 0)
         *reinterpret_cast<uint4*>(cst + (int64_t)(HIST > 0 ? HIST - 1 : 0) * conv_dim + c0) = craw;
     }
-  }
-  if (threadIdx.x < nh) {
-    const int h = h0 + threadIdx.x;
-    const float v = Act<T>::to_f(static_cast<const T*>(a.dt)[(int64_t)s * H + h]) + a.dt_bias[h];
-    const float dtp = softplus_f(v);
-    hdt[threadIdx.x] = dtp;
-    hdec[threadIdx.x] = expf(-expf(a.A_log[h]) * dtp);
-    hD[threadIdx.x] = a.D[h];
   }
   __syncthreads();
 
@@ -371,64 +349,104 @@ decode_step_kernel(const __grid_constant__ DecodeArgs a) {
   }
   __syncthreads();
 
-  // ---- 3. g = round(y) * silu(z); partial sums of g^2 per norm group -----
-  const int gs = d_inner / a.norm_groups;
-  for (int r = threadIdx.x; r < rows; r += kDecodeThreads) {
-    const int hl = r / P;
-    const float y = round_act<T>(ys[r] + hD[hl] * xs[r]);
-    ys[r] = y * zs[r];
-  }
-  __syncthreads();
-  if (rows > 0) {
-    const int c_lo = h0 * P, c_hi = h0 * P + rows;
-    for (int grp = c_lo / gs; grp * gs < c_hi; ++grp) {
-      const int lo = max(c_lo, grp * gs) - c_lo, hi = min(c_hi, (grp + 1) * gs) - c_lo;
-      float ss = 0.0f;
-      for (int r = lo + threadIdx.x; r < hi; r += kDecodeThreads) ss = fmaf(ys[r], ys[r], ss);
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-      if (lane == 0) wsum[warp] = ss;
-      __syncthreads();
-      if (threadIdx.x == 0) {
-        float t = 0.0f;
-        for (int w = 0; w < kDecodeWarps; ++w) t += wsum[w];
-        part[grp] = t;
-      }
-      __syncthreads();
-    }
-  }
-
-  // ---- 4. cluster: B/C history, group totals, normed output --------------
-  cluster_sync_all();
-  if (rank == 0) {
-    for (int i = threadIdx.x; i < nbcv; i += kDecodeThreads) {
-      const int c0 = d_inner + i * V;
-      const uint4 craw = *reinterpret_cast<const uint4*>(xBC + c0);
-#pragma unroll
-      for (int j = 0; j + 1 < HIST; ++j) {
-        const uint4 nxt = fresh ? make_uint4(0u, 0u, 0u, 0u)
-                                : *reinterpret_cast<const uint4*>(cst + (int64_t)(j + 1) * conv_dim + c0);
-        *reinterpret_cast<uint4*>(cst + (int64_t)j * conv_dim + c0) = nxt;
-      }
-      if (HIST > 0)
-        *reinterpret_cast<uint4*>(cst + (int64_t)(HIST > 0 ? HIST - 1 : 0) * conv_dim + c0) = craw;
-    }
-  }
+  // ---- 3. y = h.C + D*x, rounded to the activation type, to dst ------------
   if (rows > 0) {
     T* orow = static_cast<T*>(a.dst) + (int64_t)s * d_inner + h0 * P;
     for (int i = threadIdx.x; i < rows / V; i += kDecodeThreads) {
-      const int c0 = h0 * P + i * V;
-      const int grp = c0 / gs;  // V divides gs, so a vector sits in one group
-      float tot = 0.0f;
-      for (int r2 = 0; r2 < a.cluster; ++r2) tot += ld_dsmem_f32(part + grp, (uint32_t)r2);
-      const float inv = rsqrtf(tot / (float)gs + a.eps);
       float o[V];
 #pragma unroll
-      for (int j = 0; j < V; ++j) o[j] = ys[i * V + j] * inv * a.norm_w[c0 + j];
+      for (int j = 0; j < V; ++j) {
+        const int r = i * V + j;
+        o[j] = ys[r] + hD[r / P] * xs[r];
+      }
       Vec16<T>::store(orow + i * V, o);
     }
   }
-  cluster_sync_all();
+}
+
+// The rest of the step for sequence s = blockIdx.x, after every CTA of
+// decode_step_kernel is done: the B/C conv history shifted by the token, then
+// g = y * silu(z) and per norm group out = g / sqrt(mean(g^2) + eps) * weight,
+// written over y in dst. Sums of squares in a fixed order (deterministic).
+template <typename T, int K>
+__global__ void __launch_bounds__(kDecodeThreads)
+decode_finish_kernel(const __grid_constant__ DecodeArgs a) {
+  constexpr int V = Vec16<T>::n;
+  constexpr int HIST = K - 1;
+  extern __shared__ __align__(16) float gbuf[];  // [d_inner] g, then [kDecodeWarps] warp sums
+  const int s = blockIdx.x;
+  const bool dev = a.dev_slots != nullptr;
+  if (dev && (__ldg(a.dev_status) != 0 || s >= __ldg(a.dev_n))) return;
+  const bool fresh = dev ? __ldg(a.dev_fresh + s) != 0 : seq_fresh(a.tab, s);
+  const int64_t slot = dev ? (int64_t)__ldg(a.dev_slots + s) : (int64_t)seq_slot(a.tab, s);
+  const int H = a.heads, P = a.headdim, N = a.d_state, G = a.ngroups;
+  const int d_inner = H * P;
+  const int conv_dim = d_inner + 2 * G * N;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  // silu(z) first (this step's input, not written by the state kernel) ...
+  T* row = static_cast<T*>(a.dst) + (int64_t)s * d_inner;
+  const T* zrow = static_cast<const T*>(a.z) + (int64_t)s * d_inner;
+  for (int i = threadIdx.x; i < d_inner / V; i += kDecodeThreads) {
+    float zv[V];
+    Vec16<T>::load(zrow + i * V, zv);
+#pragma unroll
+    for (int j = 0; j < V; ++j) gbuf[i * V + j] = silu_f(zv[j]);
+  }
+  // ... then wait until the state kernel of this step has finished and its writes
+  // (y in dst) are visible
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+
+  // B/C conv history: older rows move up, the token's B/C becomes the newest row
+  const T* xBC = static_cast<const T*>(a.xBC) + (int64_t)s * conv_dim;
+  T* cst = static_cast<T*>(a.conv_state) + slot * HIST * conv_dim;
+  const int nbcv = 2 * G * N / V;
+  for (int i = threadIdx.x; i < nbcv && HIST > 0; i += kDecodeThreads) {
+    const int c0 = d_inner + i * V;
+    const uint4 craw = *reinterpret_cast<const uint4*>(xBC + c0);
+#pragma unroll
+    for (int j = 0; j + 1 < HIST; ++j) {
+      const uint4 nxt = fresh ? make_uint4(0u, 0u, 0u, 0u)
+                              : *reinterpret_cast<const uint4*>(cst + (int64_t)(j + 1) * conv_dim + c0);
+      *reinterpret_cast<uint4*>(cst + (int64_t)j * conv_dim + c0) = nxt;
+    }
+    *reinterpret_cast<uint4*>(cst + (int64_t)(HIST > 0 ? HIST - 1 : 0) * conv_dim + c0) = craw;
+  }
+
+  // g = y * silu(z) (each thread the same vectors it filled above)
+  for (int i = threadIdx.x; i < d_inner / V; i += kDecodeThreads) {
+    float y[V];
+    Vec16<T>::load(row + i * V, y);
+#pragma unroll
+    for (int j = 0; j < V; ++j) gbuf[i * V + j] *= y[j];
+  }
+  __syncthreads();
+  float* wsum = gbuf + d_inner;
+  const int gs = d_inner / a.norm_groups;
+  for (int grp = 0; grp < a.norm_groups; ++grp) {
+    float ss = 0.0f;
+    for (int r = grp * gs + threadIdx.x; r < (grp + 1) * gs; r += kDecodeThreads) ss = fmaf(gbuf[r], gbuf[r], ss);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    if (lane == 0) wsum[warp] = ss;
+    __syncthreads();
+    float tot = 0.0f;
+#pragma unroll
+    for (int w = 0; w < kDecodeWarps; ++w) tot += wsum[w];
+    const float inv = rsqrtf(tot / (float)gs + a.eps);
+    for (int i = grp * gs / V + threadIdx.x; i < (grp + 1) * gs / V; i += kDecodeThreads) {
+      float o[V], w[V];
+#pragma unroll
+      for (int q = 0; q < V / 4; ++q) {
+        const float4 f = __ldg(reinterpret_cast<const float4*>(a.norm_w) + (i * V) / 4 + q);
+        w[4 * q] = f.x; w[4 * q + 1] = f.y; w[4 * q + 2] = f.z; w[4 * q + 3] = f.w;
+      }
+#pragma unroll
+      for (int j = 0; j < V; ++j) o[j] = gbuf[i * V + j] * inv * w[j];
+      Vec16<T>::store(row + i * V, o);
+    }
+    __syncthreads();  // wsum is reused by the next group
+  }
 }
 
 bool decode_supported(mamba2_dtype act, const mamba2_dims& d, int norm_groups) {
@@ -490,31 +508,36 @@ __global__ void __launch_bounds__(kCheckThreads) check_device_batch_kernel(const
 
 template <typename T, int K, bool kRing>
 static cudaError_t launch_decode_tk(const DecodeArgs& a, cudaStream_t st) {
-  size_t smem = sizeof(float) * (3 * (size_t)a.heads_per_cta * a.headdim + 2 * (size_t)a.ngroups * a.d_state +
-                                 3 * (size_t)a.heads_per_cta + kDecodeMaxNormGroups + kDecodeWarps);
+  size_t smem = sizeof(float) * (2 * (size_t)a.heads_per_cta * a.headdim + 2 * (size_t)a.ngroups * a.d_state +
+                                 3 * (size_t)a.heads_per_cta);
   if (kRing) smem = sizeof(float) * (size_t)ring_offset(a.heads_per_cta, a.headdim, a.ngroups, a.d_state) + kRingBytes;
   auto kern = decode_step_kernel<T, K, kRing>;
-  if (a.cluster > kDecodePortableCluster) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-    if (e != cudaSuccess) return e;
-  }
   if (smem > 48 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
   }
+  kern<<<dim3((unsigned)a.ctas_per_seq, (unsigned)a.tab.n, 1), kDecodeThreads, smem, st>>>(a);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const size_t fsmem = sizeof(float) * ((size_t)a.heads * a.headdim + kDecodeWarps);
+  auto fin = decode_finish_kernel<T, K>;
+  if (fsmem > 48 * 1024) {
+    e = cudaFuncSetAttribute(fin, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)fsmem);
+    if (e != cudaSuccess) return e;
+  }
+  // programmatic dependent launch: the finish kernel is scheduled while the state
+  // kernel runs and waits for it (griddepcontrol.wait) before reading its output
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)a.cluster, (unsigned)a.tab.n, 1);
+  cfg.gridDim = dim3((unsigned)a.tab.n, 1, 1);
   cfg.blockDim = dim3(kDecodeThreads, 1, 1);
-  cfg.dynamicSmemBytes = smem;
+  cfg.dynamicSmemBytes = fsmem;
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = (unsigned)a.cluster;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, a);
+  return cudaLaunchKernelEx(&cfg, fin, a);
 }
 
 template <typename T, int K>

@@ -91,9 +91,7 @@ cudaError_t launch_gated_rmsnorm(const NormArgs& a, mamba2_dtype act, cudaStream
 
 // -------------------------------------------------------------- decode ----
 constexpr int kDecodeThreads = 256;
-constexpr int kDecodeMaxCluster = 16;  // CTAs per sequence when the batch leaves SMs idle (non-portable size)
-constexpr int kDecodePortableCluster = 8;  // at most this many CTAs per sequence otherwise,
-constexpr int kDecodeHeadsPerCta = 8;      // each taking up to this many heads
+constexpr int kDecodeMaxHeadsPerCta = 8;  // heads per CTA of the state kernel for large batches
 constexpr int kDecodeMaxNormGroups = 64;
 
 struct DecodeArgs {
@@ -112,7 +110,7 @@ struct DecodeArgs {
   int32_t heads, headdim, d_state, ngroups, conv_kernel;
   int32_t norm_groups;
   float eps;
-  int32_t cluster;         // CTAs per sequence
+  int32_t ctas_per_seq;    // CTAs per sequence of the state kernel
   int32_t heads_per_cta;
   SeqTable tab;            // host batch: tab.n sequences; device batch: tab.n = capacity, rest unused
   // Device batch (all null for a host batch): sequence s < *dev_n has slot dev_slots[s]

@@ -564,15 +564,33 @@ ssd_tc_full(const __grid_constant__ ScanArgs a, const __grid_constant__ CUtensor
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
     const int row = s_row;
     {
-      // the seed, staged through this thread's own places of the (not yet used)
-      // H^T region, so that seed_at is not unrolled 32 times
-      float* s_seed = reinterpret_cast<float*>(smem + kOffHT);
-#pragma unroll 1
-      for (int e = 0; e < 32; ++e) s_seed[(pc0 + e) * TN + row] = seed_at(a, ci, pc0 + e, row);
+      // the seed (seed_at's rule), entry by entry, each entry's 32 loads independent
+      const int P = a.state_pieces > 0 ? a.state_pieces : 1;
+      const int64_t col = (int64_t)pc0 * TN + row, head_off = (int64_t)ci.h * TP * TN;
+      auto entry = [&](int e) { return a.ws_state + (int64_t)e * H * TP * TN + head_off + col; };
+      auto load = [&](const float* src) {
 #pragma unroll
-      for (int e = 0; e < 16; ++e) hs[e] = f2(s_seed[(pc0 + 2 * e) * TN + row], s_seed[(pc0 + 2 * e + 1) * TN + row]);
-      // every S thread has its seed before any writes the bf16 H^T over the region
-      asm volatile("bar.sync 1, %0;" :: "r"(32 * kSWarps) : "memory");
+        for (int e = 0; e < 16; ++e) hs[e] = f2(src[(int64_t)(2 * e) * TN], src[(int64_t)(2 * e + 1) * TN]);
+      };
+      if (ci.k == 0) {
+        if (ci.fresh) {
+#pragma unroll
+          for (int e = 0; e < 16; ++e) hs[e] = f2(0.0f, 0.0f);
+        } else {
+          load(ci.nseg > 1 ? entry((ci.seg0 + ci.nseg - 1) * P)
+                           : a.ssm_state + (int64_t)seq_slot(a.tab, ci.sq) * H * TP * TN + head_off + col);
+        }
+      } else {
+        load(entry(ci.seg0 * P));
+#pragma unroll 1
+        for (int e = ci.seg0 * P + 1; e < (ci.seg0 + ci.k) * P; ++e) {
+          const float d = __expf(a.ws_decay[(int64_t)e * H + ci.h]);
+          const F2 d2 = f2(d, d);
+          const float* src = entry(e);
+#pragma unroll
+          for (int q = 0; q < 16; ++q) hs[q] = fma2(d2, hs[q], f2(src[(int64_t)(2 * q) * TN], src[(int64_t)(2 * q + 1) * TN]));
+        }
+      }
     }
     auto write_h = [&]() {  // bf16 hi + lo of H^T: row n, columns [pc0, +32) of each block
 #pragma unroll
