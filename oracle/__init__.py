@@ -27,6 +27,8 @@ import torch
 _HERE = Path(__file__).resolve().parent
 _SRC = _HERE / "mamba2_ref.c"
 _HDR = _HERE / "mamba2_ref.h"
+_SRC3 = _HERE / "mamba3_ref.c"
+_HDR3 = _HERE / "mamba3_ref.h"
 _LIB = _HERE / "libmamba2_ref.so"
 
 F32, BF16 = 0, 1
@@ -53,13 +55,13 @@ class OracleError(RuntimeError):
 
 def build(force: bool = False) -> Path:
     """Compile ``libmamba2_ref.so`` with gcc (OpenMP, no FP contraction)."""
-    newest = max(_SRC.stat().st_mtime, _HDR.stat().st_mtime)
+    newest = max(f.stat().st_mtime for f in (_SRC, _HDR, _SRC3, _HDR3))
     if not force and _LIB.exists() and _LIB.stat().st_mtime >= newest:
         return _LIB
     fd, tmp = tempfile.mkstemp(suffix=".so", dir=str(_HERE))
     os.close(fd)
     cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fopenmp",
-           "-ffp-contract=off", "-fno-fast-math", str(_SRC), "-o", tmp, "-lm"]
+           "-ffp-contract=off", "-fno-fast-math", str(_SRC), str(_SRC3), "-o", tmp, "-lm"]
     try:
         subprocess.run(cmd, check=True, capture_output=True, text=True)
         os.replace(tmp, _LIB)
@@ -84,6 +86,7 @@ def _load():
             lib.mamba2_ref_state_bytes_per_layer.argtypes = [i32] * 6
             lib.mamba2_ref_state_bytes_per_layer.restype = ctypes.c_int64
             lib.mamba2_ref_num_threads.restype = ctypes.c_int
+            lib.mamba3_ref_siso_forward.argtypes = [p] * 16 + [i32, p, i32, i32, i32, i32, p]
             lib.mamba2_ref_set_num_threads.argtypes = [ctypes.c_int]
             _lib = lib
     return _lib
@@ -207,6 +210,32 @@ def decode_step(xBC, z, dt, conv_w, conv_b, A_log, dt_bias, D, norm_w, norm_grou
         sl.numel(), _ptr(sl), _ptr(fr), _ptr(dst64))
     _check(st, "decode_step")
     return dst, dst64
+
+
+def mamba3_siso_forward(q, k, v, adt, dt, trap, q_bias, k_bias, angles, d, z, cu_seqlens):
+    """Mamba-3 SISO forward (page "Mamba-3 SISO Long-Ragged Multi-Chunk Joint States Full
+    VJP", forward steps 1-7), fp64. q, k [T, N] bf16; v, z [T, H, P] bf16; adt, dt [T, H]
+    f32; trap [T, H] bf16; q_bias, k_bias [H, N] f32; angles [T, R] bf16; d [H] f32.
+
+    Returns ``(out, final_angle, final_ssm, final_k, final_v, out_f64)``.
+    """
+    T, N = q.shape
+    H, P = v.shape[1], v.shape[2]
+    R = angles.shape[1]
+    S = len(cu_seqlens) - 1
+    out = torch.empty((T, H, P), dtype=torch.bfloat16)
+    out64 = torch.empty((T, H, P), dtype=torch.float64)
+    fa = torch.empty((S, H, R), dtype=torch.bfloat16)
+    fs = torch.empty((S, H, P, N), dtype=torch.float32)
+    fk = torch.empty((S, H, N), dtype=torch.float32)
+    fv = torch.empty((S, H, P), dtype=torch.bfloat16)
+    cu = _i32(cu_seqlens)
+    st = _load().mamba3_ref_siso_forward(
+        _ptr(out), _ptr(fa), _ptr(fs), _ptr(fk), _ptr(fv), _ptr(q), _ptr(k), _ptr(v), _ptr(adt), _ptr(dt),
+        _ptr(trap), _ptr(q_bias), _ptr(k_bias), _ptr(angles), _ptr(d), _ptr(z), S, _ptr(cu), H, P, N, R,
+        _ptr(out64))
+    _check(st, "mamba3_siso_forward")
+    return out, fa, fs, fk, fv, out64
 
 
 def state_bytes_per_layer(heads, headdim, d_state, ngroups, conv_kernel, conv_act=BF16) -> int:

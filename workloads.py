@@ -276,3 +276,76 @@ def long_prefill(seed: int = 4, tokens: int = 65536, decode_steps: int = 64,
 
 def named(i: int, **kw) -> Workload:
     return [tiny, prefill_130m, varlen_130m, decode_batch, long_prefill][i](**kw)
+
+
+# --------------------------------------------------------------------------
+# Mamba-3 SISO forward (page "Mamba-3 SISO Long-Ragged Multi-Chunk Joint States
+# Full VJP"): its frozen shapes are GQA 1 -> 32, Q/K width 128, V width 64,
+# rotary-angle width 32, three to five packed sequences of ragged lengths
+# spanning 3 to 15 chunks of 64 tokens (never a multiple of 64). The page gives
+# no value distributions; these follow the Mamba2 workloads' (activations
+# N(0, 1); dt from dt_bias = inverse-softplus U[1e-3, 0.1]; decay rate
+# A = U[1, 16] per head; D ~ N(1, 0.1^2)), with biases N(0, 0.1^2).
+# --------------------------------------------------------------------------
+
+@dataclass
+class Mamba3Batch:
+    name: str
+    heads: int
+    headdim: int
+    d_state: int
+    rot_dim: int
+    cu_seqlens: List[int]
+    q: torch.Tensor       # [T, N] bf16
+    k: torch.Tensor       # [T, N] bf16
+    v: torch.Tensor       # [T, H, P] bf16
+    adt: torch.Tensor     # [T, H] f32
+    dt: torch.Tensor      # [T, H] f32
+    trap: torch.Tensor    # [T, H] bf16
+    q_bias: torch.Tensor  # [H, N] f32
+    k_bias: torch.Tensor  # [H, N] f32
+    angles: torch.Tensor  # [T, R] bf16
+    d: torch.Tensor       # [H] f32
+    z: torch.Tensor       # [T, H, P] bf16
+
+    @property
+    def rows(self) -> int:
+        return self.cu_seqlens[-1]
+
+    def tensors(self):
+        return (self.q, self.k, self.v, self.adt, self.dt, self.trap, self.q_bias, self.k_bias, self.angles,
+                self.d, self.z)
+
+
+def mamba3_batch(seed: int = 5, lengths=None, heads: int = 32, headdim: int = 64, d_state: int = 128,
+                 rot_dim: int = 32, chunk: int = 64) -> Mamba3Batch:
+    """Three to five packed sequences, each 3 to 15 chunks long and not a multiple of the chunk
+    (drawn when `lengths` is None)."""
+    g = torch.Generator("cpu").manual_seed(seed)
+    if lengths is None:
+        n = int(torch.randint(3, 6, (1,), generator=g))
+        lengths = []
+        for _ in range(n):
+            L = int(torch.randint(2 * chunk + 1, 15 * chunk, (1,), generator=g))
+            lengths.append(L + 1 if L % chunk == 0 else L)
+    cu = [0]
+    for L in lengths:
+        cu.append(cu[-1] + int(L))
+    T, H, P, N, R = cu[-1], heads, headdim, d_state, rot_dim
+    bf = torch.bfloat16
+    q = _normal(g, (T, N), dtype=bf)
+    k = _normal(g, (T, N), dtype=bf)
+    v = _normal(g, (T, H, P), dtype=bf)
+    z = _normal(g, (T, H, P), dtype=bf)
+    y = _uniform(g, (H,), 1e-3, 0.1).double()
+    dt_bias = y + torch.log(-torch.expm1(-y))
+    dt = torch.nn.functional.softplus(_normal(g, (T, H)).double() + dt_bias).float()
+    A = _uniform(g, (H,), 1.0, 16.0)
+    adt = (-A * dt).float()
+    trap = _normal(g, (T, H), dtype=bf)
+    q_bias = _normal(g, (H, N), std=0.1)
+    k_bias = _normal(g, (H, N), std=0.1)
+    angles = _normal(g, (T, R), dtype=bf)
+    d = _normal(g, (H,), std=0.1, mean=1.0)
+    return Mamba3Batch(f"mamba3 siso {len(lengths)} seqs ({T} tok), {H} heads x {P}, N {N}, R {R}", H, P, N, R, cu,
+                       q, k, v, adt, dt, trap, q_bias, k_bias, angles, d, z)
