@@ -10,7 +10,8 @@ Entry points (same names as the C ABI without the ``mamba2_`` prefix):
 ``causal_conv1d``, ``ssd_scan`` (+ ``ssd_scan_workspace_bytes``),
 ``gated_rmsnorm``, ``decode_step``, ``decode_step_device``, ``prefill_host`` (+
 ``prefill_host_workspace_bytes``), ``padded_spans``, ``pack_rows``, ``unpack_rows``,
-``in_proj``, ``out_proj``, ``state_bytes_per_layer``. ``selective_scan_gb300.padded`` holds the padded-batch
+``in_proj``, ``out_proj``, ``state_bytes_per_layer``; and the Mamba-3 SISO forward
+``mamba3_siso_varlen_forward`` (C name unchanged). ``selective_scan_gb300.padded`` holds the padded-batch
 layer view built on them (attention mask in, HF-style cache out).
 """
 from __future__ import annotations
@@ -88,9 +89,10 @@ def _lib():
         lib.mamba2_prefill_host_workspace_bytes.restype = sz
         lib.mamba2_prefill_host.argtypes = [p, p, p, p, p, p, p, p, p, p, i32, f32, p, p, i32, dims, ctypes.c_int,
                                             rb, i32, p, sz, p]
+        lib.mamba3_siso_varlen_forward.argtypes = [p] * 16 + [p, i32, i32, i32, i32, i32, i32, p]
         for name in ("mamba2_causal_conv1d", "mamba2_ssd_scan", "mamba2_gated_rmsnorm", "mamba2_decode_step",
                      "mamba2_decode_step_device", "mamba2_prefill_host", "mamba2_padded_spans", "mamba2_pack_rows",
-                     "mamba2_unpack_rows", "mamba2_in_proj", "mamba2_out_proj"):
+                     "mamba2_unpack_rows", "mamba2_in_proj", "mamba2_out_proj", "mamba3_siso_varlen_forward"):
             getattr(lib, name).restype = ctypes.c_int
         _LIB = lib
     return _LIB
@@ -355,6 +357,25 @@ def prefill_host(out_host, xBC_host, z_host, dt_host, conv_w, conv_b, A_log, dt_
                                     workspace.numel() * workspace.element_size(), _stream(stream))
     if check:
         _check(st, "mamba2_prefill_host")
+    return st
+
+
+def mamba3_siso_varlen_forward(out, final_angle, final_ssm, final_k, final_v, q, k, v, adt, dt, trap, q_bias,
+                               k_bias, angles, d, z, cu_seqlens, stream=None, check=True) -> int:
+    """``mamba3_siso_varlen_forward`` (include/mamba3.h): the Mamba-3 SISO forward over a
+    packed batch. q, k [rows, d_state]; v, z, out [rows, heads, headdim]; adt, dt, trap
+    [rows, heads]; angles [rows, rot_dim]; biases [heads, d_state]; d [heads]; the final
+    states [num_seqs, heads, ...]; cu_seqlens a host sequence."""
+    cu = list(cu_seqlens)
+    n = len(cu) - 1
+    rows, heads, headdim = v.shape
+    arr = (ctypes.c_int32 * max(1, len(cu)))(*cu)
+    st = _lib().mamba3_siso_varlen_forward(
+        _ptr(out), _ptr(final_angle), _ptr(final_ssm), _ptr(final_k), _ptr(final_v), _ptr(q), _ptr(k), _ptr(v),
+        _ptr(adt), _ptr(dt), _ptr(trap), _ptr(q_bias), _ptr(k_bias), _ptr(angles), _ptr(d), _ptr(z), arr, n,
+        int(rows), int(heads), int(headdim), int(q.shape[1]), int(angles.shape[1]), _stream(stream))
+    if check:
+        _check(st, "mamba3_siso_varlen_forward")
     return st
 
 

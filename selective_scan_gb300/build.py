@@ -19,7 +19,7 @@ ROOT = PKG.parent
 CSRC = PKG / "csrc"
 BUILD = PKG / "_build"
 LIB = PKG / "libmamba2.so"
-SOURCES = ["api.cu", "conv1d.cu", "scan.cu", "scan_tc.cu", "norm.cu", "decode.cu", "pack.cu", "gemm_tc.cu", "selftest.cu"]
+SOURCES = ["api.cu", "conv1d.cu", "scan.cu", "scan_tc.cu", "norm.cu", "decode.cu", "pack.cu", "gemm_tc.cu", "selftest.cu", "mamba3.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
               "-I", str(ROOT / "include")] + ARCH
@@ -33,7 +33,7 @@ def _nvcc() -> str:
 
 
 def _deps() -> list[Path]:
-    return [CSRC / s for s in os.listdir(CSRC)] + [ROOT / "include" / "mamba2.h"]
+    return [CSRC / s for s in os.listdir(CSRC)] + [ROOT / "include" / "mamba2.h", ROOT / "include" / "mamba3.h"]
 
 
 def up_to_date() -> bool:

@@ -12,6 +12,7 @@
 #include <cstring>
 #include <vector>
 
+#include "../../include/mamba3.h"
 #include "kernels.h"
 
 namespace mamba2 {
@@ -306,8 +307,67 @@ mamba2_status mamba2_selftest_bounded_wait(int32_t* status_dev, void* stream) {
 }
 
 unsigned int mamba2_device_timeouts(void) {
-  const unsigned int a = read_device_timeouts(), b = read_gemm_timeouts();
-  return (a == 0xffffffffu || b == 0xffffffffu) ? 0xffffffffu : a + b;
+  const unsigned int a = read_device_timeouts(), b = read_gemm_timeouts(), c = read_m3_timeouts();
+  return (a == 0xffffffffu || b == 0xffffffffu || c == 0xffffffffu) ? 0xffffffffu : a + b + c;
+}
+
+mamba2_status mamba3_siso_varlen_forward(void* out, void* final_angle, float* final_ssm, float* final_k,
+                                         void* final_v, const void* q, const void* k, const void* v,
+                                         const float* adt, const float* dt, const void* trap, const float* q_bias,
+                                         const float* k_bias, const void* angles, const float* d, const void* z,
+                                         const int32_t* cu_seqlens, int32_t num_seqs, int32_t rows, int32_t heads,
+                                         int32_t headdim, int32_t d_state, int32_t rot_dim, void* stream) {
+  if (num_seqs < 0 || num_seqs > MAMBA2_MAX_SEQS || rows < 0 || heads <= 0 || headdim <= 0 || d_state <= 0 ||
+      rot_dim < 0 || 2 * rot_dim > d_state || (num_seqs > 0 && !cu_seqlens))
+    return MAMBA2_ERR_INVALID_ARGUMENT;
+  if (headdim != 64 || d_state != 128) return MAMBA2_ERR_NOT_IMPLEMENTED;
+  if (num_seqs > 0) {
+    const void* ptrs[] = {final_ssm, final_k, final_v, q_bias, k_bias, d};
+    for (const void* ptr : ptrs)
+      if (!ptr || !aligned16(ptr)) return MAMBA2_ERR_INVALID_ARGUMENT;
+    if (rot_dim > 0 && (!final_angle || !aligned16(final_angle))) return MAMBA2_ERR_INVALID_ARGUMENT;
+  }
+  if (rows > 0) {
+    const void* ptrs[] = {out, q, k, v, adt, dt, trap, z};
+    for (const void* ptr : ptrs)
+      if (!ptr || !aligned16(ptr)) return MAMBA2_ERR_INVALID_ARGUMENT;
+    if (rot_dim > 0 && (!angles || !aligned16(angles))) return MAMBA2_ERR_INVALID_ARGUMENT;
+  }
+  if (num_seqs == 0) return rows == 0 ? MAMBA2_OK : MAMBA2_ERR_RUNS_DONT_COVER_ROWS;
+  if (cu_seqlens[0] != 0 || cu_seqlens[num_seqs] != rows) return MAMBA2_ERR_RUNS_DONT_COVER_ROWS;
+  for (int i = 0; i < num_seqs; ++i)
+    if (cu_seqlens[i + 1] < cu_seqlens[i]) return MAMBA2_ERR_RUNS_DONT_COVER_ROWS;
+  static_assert(sizeof(Mamba3Args) < 32000, "launch parameter block");
+  Mamba3Args a;
+  a.out = out;
+  a.final_angle = final_angle;
+  a.final_ssm = final_ssm;
+  a.final_k = final_k;
+  a.final_v = final_v;
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.adt = adt;
+  a.dt = dt;
+  a.trap = trap;
+  a.q_bias = q_bias;
+  a.k_bias = k_bias;
+  a.angles = angles;
+  a.d = d;
+  a.z = z;
+  a.nseq = num_seqs;
+  a.heads = heads;
+  a.rot_dim = rot_dim;
+  for (int i = 0; i <= num_seqs; ++i) a.cu[i] = cu_seqlens[i];
+  // longest sequences first, so that the CTAs that take a second item take short ones
+  std::vector<int32_t> order(num_seqs);
+  for (int i = 0; i < num_seqs; ++i) order[i] = i;
+  std::stable_sort(order.begin(), order.end(), [&](int32_t x, int32_t y) {
+    return cu_seqlens[x + 1] - cu_seqlens[x] > cu_seqlens[y + 1] - cu_seqlens[y];
+  });
+  for (int i = 0; i < num_seqs; ++i) a.order[i] = order[i];
+  const cudaError_t e = launch_m3_forward(a, std::max(1, device_sm_count()), static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? MAMBA2_OK : cuda_fail(e);
 }
 
 int64_t mamba2_state_bytes_per_layer(const mamba2_dims* d, mamba2_dtype conv_dtype) {

@@ -136,6 +136,34 @@ struct GemmArgs {
 cudaError_t launch_gemm_tc(const GemmArgs& g, const void* A, const void* B, cudaStream_t st);
 unsigned int read_gemm_timeouts();
 
+// ------------------------------------------------------------ mamba3 ----
+// Mamba-3 SISO varlen forward (head width 64, Q/K width 128). Sequence i owns
+// rows [cu[i], cu[i+1]); order[] lists the sequences longest first (the CTAs
+// take (sequence, head) items in that order).
+struct Mamba3Args {
+  void* out;
+  void* final_angle;
+  float* final_ssm;
+  float* final_k;
+  void* final_v;
+  const void* q;
+  const void* k;
+  const void* v;
+  const float* adt;
+  const float* dt;
+  const void* trap;
+  const float* q_bias;
+  const float* k_bias;
+  const void* angles;
+  const float* d;
+  const void* z;
+  int32_t nseq, heads, rot_dim;
+  int32_t cu[MAMBA2_MAX_SEQS + 1];
+  int32_t order[MAMBA2_MAX_SEQS];
+};
+cudaError_t launch_m3_forward(const Mamba3Args& a, int num_sms, cudaStream_t st);
+unsigned int read_m3_timeouts();
+
 // Failure-detection self-test: one bounded wait on a barrier nothing arrives at.
 cudaError_t launch_bounded_wait_probe(int32_t* status, cudaStream_t st);
 

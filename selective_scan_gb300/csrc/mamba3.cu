@@ -1,0 +1,698 @@
+// Mamba-3 SISO varlen forward on the tcgen05 tensor cores, head dim 64 x
+// state 128 (the frozen shapes of the page "Mamba-3 SISO Long-Ragged
+// Multi-Chunk Joint States Full VJP": one Q/K head of width 128 serving every
+// value head of width 64, up to 64 rotary pairs).
+//
+// Semantics (that page, "What You Have", steps 1-7), per sequence and head,
+// token by token:
+//   phi_t = (sum_{s<=t} tanh(angles_s) pi dt_s) mod 2 pi          (per rotary pair)
+//   q^_t, k^_t = pairs (2i, 2i+1), i < R, of q_t + q_bias, k_t + k_bias rotated by phi_t[i]
+//   p = sigmoid(trap), sg_t = dt_{t+1} (1 - p_{t+1}) (0 at the last token),
+//   scale_t = dt_t p_t + sg_t
+//   h_t = exp(adt_t) h_{t-1} + scale_t v_t (x) k^_t
+//   y_t = h_t q^_t + d v_t - (q^_t . k^_t) sg_t v_t,   out_t = y_t z_t sigmoid(z_t)
+// and the final angle, state, rotated k and v of the sequence's last token.
+//
+// Chunked form (Q = 128 tokens, S_t = adt_0 + ... + adt_t within the chunk):
+//   y_t = exp(S_t) q^_t . H_in + sum_{s<=t} M[t][s] v_s + d v_t
+//   M[t][s] = (q^_t . k^_s) exp(S_t - S_s) scale_s    (s < t)
+//   M[t][t] = (q^_t . k^_t) dt_t p_t                   (the correction removes sg_t)
+//   H_out   = exp(S_end) H_in + sum_s exp(S_end - S_s) scale_s v_s (x) k^_s
+// The diagonal's q^ . k^ comes from the fp32 rotated values (the largest
+// entries of y are there), the rest from the tensor cores.
+//
+// One CTA of 8 warps per (sequence, head), chunk after chunk:
+//   1. per-token scalars (S in log2 units, scale, dt p), the cumulative angles
+//      (one thread per rotary pair and block of 32 tokens), q^ and k^ as fp16
+//      [token][n] tiles (128-byte swizzle) and the exact diagonal q^ . k^;
+//      v as fp16 and v o w (w_s = exp(S_end - S_s) scale_s) as fp16 tiles;
+//   2. CB = Q^ K^T (N = 128), Yoff = Q^ H^T (N = 64), dH^T = K^T (v o w)
+//      (N = 64, lane = state row n), K = 128 each;
+//   3. M written to TMEM as fp16 (the A operand of the next product), and the
+//      state H^T = exp(S_end) H^T + dH^T in fp32 registers (lane n, 32 columns
+//      per thread), its fp16 copy to shared memory for the next chunk's Yoff;
+//   4. Yd = M V (A from TMEM), then out = (Yd + exp(S_t) Yoff + d v) silu(z).
+// fp16 operands (11 significant bits) keep the worst y error about a tenth of
+// the bf16 output's own rounding. fp16 holds magnitudes up to 65 504: a CTA
+// that meets a larger operand recomputes that (sequence, head) token by token
+// in fp32 (correct, slow; no workload here comes near it).
+// Every wait is bounded: on a timeout the CTA records it in a device counter
+// (mamba2_device_timeouts), drains what it issued, frees its TMEM and returns.
+#include <cuda.h>
+
+#include "common.cuh"
+
+namespace mamba2 {
+
+__device__ unsigned int g_m3_timeouts = 0;
+
+namespace {
+
+#include "tc.cuh"
+
+constexpr int kQ = 128;  // tokens per chunk
+constexpr int kP = 64;   // value head width
+constexpr int kN = 128;  // Q/K width (state columns)
+constexpr int kThreads = 256;
+constexpr float kTwoPi = 6.283185307179586f;
+constexpr float kPiF = 3.14159265358979f;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kF16Max = 65504.0f;
+
+// ---- shared memory (operand tiles 1024-byte aligned)
+constexpr uint32_t kTileQK = kQ * kN * 2;  // 32 KB [token][n] fp16
+constexpr uint32_t kTileV = kQ * kP * 2;   // 16 KB [token][p] fp16
+constexpr uint32_t kOffQ = 0;
+constexpr uint32_t kOffK = kOffQ + kTileQK;
+constexpr uint32_t kOffV = kOffK + kTileQK;
+constexpr uint32_t kOffVW = kOffV + kTileV;
+constexpr uint32_t kOffHT = kOffVW + kTileV;  // H^T fp16 [n][p]
+// the chunk's raw inputs, row-major as in memory (copied one chunk ahead)
+constexpr uint32_t kOffRawQ = kOffHT + kN * kP * 2;  // [128][128] bf16
+constexpr uint32_t kOffRawK = kOffRawQ + kQ * kN * 2;
+constexpr uint32_t kOffRawA = kOffRawK + kQ * kN * 2;  // [128][rot_dim] bf16, rot_dim <= 64
+constexpr uint32_t kOffF = kOffRawA + kQ * 64 * 2;
+// float offsets inside the scalar block
+constexpr int kFS = 0;          // [128] cumulative log2 decay S
+constexpr int kFW = 128;        // [128] scale
+constexpr int kFDD = 256;       // [128] dt p
+constexpr int kFDG = 384;       // [128] q^ . k^ of each token (fp32)
+constexpr int kFWS = 512;       // [8] warp sums of the decay scan
+constexpr int kFAP = 520;       // [8][64] angle sums per block of 16 tokens
+constexpr int kFCar = 1032;     // [2][64] angle carried into chunk c (buffer c % 2)
+constexpr int kFDT = 1160;      // [128] dt of the head
+constexpr int kNumF = 1288;
+constexpr uint32_t kOffBar = kOffF + kNumF * 4;  // two mbarriers
+constexpr uint32_t kOffMisc = kOffBar + 16;      // TMEM base, abort flag, fp16 range flag
+constexpr uint32_t kSmemUsed = kOffMisc + 16;
+constexpr uint32_t kSmem = kSmemUsed + 1024;     // + alignment slack
+static_assert(kSmem <= 232448, "shared memory plan exceeds 227 KB");
+static_assert(kOffBar % 8 == 0, "mbarrier alignment");
+
+// ---- TMEM columns (128 lanes)
+constexpr uint32_t kColCB = 0;    // [0,128)  CB = Q^ K^T, column = token s
+constexpr uint32_t kColYo = 128;  // [128,192) Q^ H^T, column = p
+constexpr uint32_t kColDH = 192;  // [192,256) K^T (v o w), lane = n, column = p
+constexpr uint32_t kColM = 256;   // [256,320) M as fp16 pairs, k-step s at 8 s
+constexpr uint32_t kColYd = 320;  // [320,384) M V, column = p
+
+// byte offset of element (r, c) in a [128][cols] 16-bit tile, 128-byte
+// swizzle, 64-column blocks of 128 rows each
+__device__ __forceinline__ uint32_t toff(int r, int c) {
+  return (uint32_t)((c >> 6) * kQ * 128 + r * 128 + ((((c & 63) >> 3) ^ (r & 7)) << 4) + (c & 7) * 2);
+}
+
+__device__ __forceinline__ float ex2f(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+// fp16 pair (lo in the low half); `bad` set when either value is outside the fp16 range (or NaN)
+__device__ __forceinline__ uint32_t h2(float lo, float hi, bool& bad) {
+  bad |= !(fabsf(lo) <= kF16Max && fabsf(hi) <= kF16Max);
+  uint32_t d;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+  return d;
+}
+__device__ __forceinline__ float sigmoidf_(float x) { return 1.0f / (1.0f + __expf(-x)); }
+__device__ __forceinline__ float bf(const __nv_bfloat16* p, int64_t i) { return __bfloat162float(p[i]); }
+__device__ __forceinline__ float f16lo(uint32_t w) { return __half2float(__ushort_as_half((unsigned short)(w & 0xffffu))); }
+__device__ __forceinline__ float f16hi(uint32_t w) { return __half2float(__ushort_as_half((unsigned short)(w >> 16))); }
+
+__device__ __forceinline__ float wrap2pi(float x) { return x - kTwoPi * floorf(x * (1.0f / kTwoPi)); }
+// tanh(x) = 1 - 2 / (exp(2x) + 1), branch-free (absolute error a few 1e-7; |x|
+// clamped at 15, where tanh is 1 in fp32)
+__device__ __forceinline__ float tanh_fast(float x) {
+  x = fminf(fmaxf(x, -15.0f), 15.0f);
+  return 1.0f - __fdividef(2.0f, 1.0f + __expf(2.0f * x));
+}
+// (sin, cos) of phi in [0, 2 pi), taken at phi - 2 pi above pi so the hardware
+// approximation works in [-pi, pi] (absolute error about 1e-6)
+__device__ __forceinline__ void sincos_wrapped(float phi, float& sn, float& cs) {
+  __sincosf(phi > kPiF ? phi - kTwoPi : phi, &sn, &cs);
+}
+
+__device__ __forceinline__ void cp_async4(uint32_t dst, const void* src, bool valid) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;\n" ::"r"(dst), "l"(src), "r"(valid ? 4 : 0));
+}
+
+__device__ __forceinline__ float warp_incl(float v, int lane) {
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const float u = __shfl_up_sync(0xffffffffu, v, o);
+    if (lane >= o) v += u;
+  }
+  return v;
+}
+
+struct Item {
+  int s, h, row0, T;
+};
+__device__ __forceinline__ Item item_at(const Mamba3Args& a, int i) {
+  Item it;
+  it.s = a.order[i / a.heads];
+  it.h = i - (i / a.heads) * a.heads;
+  it.row0 = a.cu[it.s];
+  it.T = a.cu[it.s + 1] - it.row0;
+  return it;
+}
+
+// One (sequence, head) token by token in fp32 (256 threads; thread tid owns
+// state row p = tid / 4, columns n = 32 (tid % 4) .. + 31). Shared scratch:
+// q^, k^ [128], v [64], cos/sin [64 each], scalars.
+__device__ __noinline__ void serial_item(const Mamba3Args& a, const Item& it, float* scratch) {
+  const int tid = threadIdx.x, H = a.heads, R = a.rot_dim;
+  float* qh = scratch;
+  float* kh = scratch + 128;
+  float* vv = scratch + 256;
+  float* cs = scratch + 320;
+  float* sn = scratch + 384;
+  float* sc = scratch + 448;  // decay, scale, sg
+  const int p = tid >> 2, n0 = (tid & 3) * 32;
+  float hreg[32];
+#pragma unroll
+  for (int e = 0; e < 32; ++e) hreg[e] = 0.0f;
+  float cum = 0.0f;
+  const __nv_bfloat16* q = static_cast<const __nv_bfloat16*>(a.q);
+  const __nv_bfloat16* k = static_cast<const __nv_bfloat16*>(a.k);
+  const __nv_bfloat16* v = static_cast<const __nv_bfloat16*>(a.v);
+  const __nv_bfloat16* z = static_cast<const __nv_bfloat16*>(a.z);
+  const __nv_bfloat16* trap = static_cast<const __nv_bfloat16*>(a.trap);
+  const __nv_bfloat16* ang = static_cast<const __nv_bfloat16*>(a.angles);
+  __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out);
+  const float dh = a.d[it.h];
+  for (int t = 0; t < it.T; ++t) {
+    const int64_t r = it.row0 + t;
+    if (tid < R) {
+      cum = wrap2pi(cum + tanhf(bf(ang, r * R + tid)) * kPiF * a.dt[r * H + it.h]);
+      float s_, c_;
+      sincosf(cum, &s_, &c_);
+      cs[tid] = c_;
+      sn[tid] = s_;
+    }
+    if (tid >= 64 && tid < 128) vv[tid - 64] = bf(v, (r * H + it.h) * kP + tid - 64);
+    if (tid == 128) {
+      const float dtv = a.dt[r * H + it.h];
+      const float pp = sigmoidf_(bf(trap, r * H + it.h));
+      float sg = 0.0f;
+      if (t + 1 < it.T) sg = a.dt[(r + 1) * H + it.h] * (1.0f - sigmoidf_(bf(trap, (r + 1) * H + it.h)));
+      sc[0] = expf(a.adt[r * H + it.h]);
+      sc[1] = dtv * pp + sg;
+      sc[2] = sg;
+    }
+    __syncthreads();
+    if (tid < 64) {
+      const int c0 = 2 * tid;
+      const float q0 = bf(q, r * kN + c0) + a.q_bias[it.h * kN + c0], q1 = bf(q, r * kN + c0 + 1) + a.q_bias[it.h * kN + c0 + 1];
+      const float k0 = bf(k, r * kN + c0) + a.k_bias[it.h * kN + c0], k1 = bf(k, r * kN + c0 + 1) + a.k_bias[it.h * kN + c0 + 1];
+      const float c_ = tid < R ? cs[tid] : 1.0f, s_ = tid < R ? sn[tid] : 0.0f;
+      qh[c0] = c_ * q0 - s_ * q1;
+      qh[c0 + 1] = s_ * q0 + c_ * q1;
+      kh[c0] = c_ * k0 - s_ * k1;
+      kh[c0 + 1] = s_ * k0 + c_ * k1;
+    }
+    __syncthreads();
+    const float dec = sc[0], scl = sc[1], sg = sc[2], vp = vv[p];
+    float acc = 0.0f;
+#pragma unroll
+    for (int e = 0; e < 32; ++e) {
+      const float kv = kh[n0 + e] * vp;
+      hreg[e] = fmaf(dec, hreg[e], scl * kv);
+      acc = fmaf(hreg[e] - sg * kv, qh[n0 + e], acc);
+    }
+    acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+    acc += __shfl_xor_sync(0xffffffffu, acc, 2);
+    if ((tid & 3) == 0) {
+      const float zz = bf(z, (r * H + it.h) * kP + p);
+      out[(r * H + it.h) * kP + p] = __float2bfloat16_rn(fmaf(dh, vp, acc) * silu_f(zz));
+    }
+    __syncthreads();
+  }
+  // final states (zeros for an empty sequence)
+  const int64_t sh = (int64_t)it.s * H + it.h;
+#pragma unroll
+  for (int e = 0; e < 32; ++e) a.final_ssm[(sh * kP + p) * kN + n0 + e] = hreg[e];
+  if (tid < 128) a.final_k[sh * kN + tid] = it.T > 0 ? kh[tid] : 0.0f;
+  if (tid >= 128 && tid < 128 + kP)
+    static_cast<__nv_bfloat16*>(a.final_v)[sh * kP + tid - 128] = __float2bfloat16_rn(it.T > 0 ? vv[tid - 128] : 0.0f);
+  if (tid < R) static_cast<__nv_bfloat16*>(a.final_angle)[sh * R + tid] = __float2bfloat16_rn(cum);
+}
+
+__global__ void __launch_bounds__(kThreads, 1) m3_fwd_kernel(const __grid_constant__ Mamba3Args a) {
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  const uint32_t raw = su32(smem_raw);
+  const uint32_t sb = (raw + 1023u) & ~1023u;
+  unsigned char* smem = smem_raw + (sb - raw);
+  float* F = reinterpret_cast<float*>(smem + kOffF);
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + kOffMisc);
+  volatile uint32_t* s_abort = reinterpret_cast<volatile uint32_t*>(smem + kOffMisc + 4);
+  volatile uint32_t* s_range = reinterpret_cast<volatile uint32_t*>(smem + kOffMisc + 8);
+  const uint32_t bar0 = sb + kOffBar, bar1 = sb + kOffBar + 8;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int H = a.heads, R = a.rot_dim;
+
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;" :: "r"(su32(s_tmem)));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+  }
+  if (tid == 32) {
+    mbar_init(bar0, 1);
+    mbar_init(bar1, 1);
+    *s_abort = 0u;
+    *s_range = 0u;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *s_tmem;
+
+  const __nv_bfloat16* q = static_cast<const __nv_bfloat16*>(a.q);
+  const __nv_bfloat16* k = static_cast<const __nv_bfloat16*>(a.k);
+  const __nv_bfloat16* v = static_cast<const __nv_bfloat16*>(a.v);
+  const __nv_bfloat16* z = static_cast<const __nv_bfloat16*>(a.z);
+  const __nv_bfloat16* trap = static_cast<const __nv_bfloat16*>(a.trap);
+  const __nv_bfloat16* ang = static_cast<const __nv_bfloat16*>(a.angles);
+  __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out);
+
+  // TMEM lane quarter and column half of this thread's row (row = TMEM lane)
+  const int row = 32 * (warp & 3) + lane, half = warp >> 2;
+  const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+  // rotation role: pairs lane and lane + 32 (columns 2 pair, 2 pair + 1) of tokens
+  // 16 warp .. 16 warp + 15 (one rotated and one plain pair each when rot_dim = 32)
+  const int pA = lane, pB = lane + 32;
+  uint32_t n_bar0 = 0, n_bar1 = 0;  // completed phases waited on
+  bool aborted = false;
+
+  const int items = a.nseq * H;
+  for (int round = 0;; ++round) {
+    const int i0 = round * (int)gridDim.x;
+    if (i0 >= items) break;
+    const int item = i0 + ((round & 1) ? (int)gridDim.x - 1 - (int)blockIdx.x : (int)blockIdx.x);
+    if (item >= items) continue;
+    const Item it = item_at(a, item);
+    const int64_t sh = (int64_t)it.s * H + it.h;
+    const int nch = (it.T + kQ - 1) / kQ;
+    float hs[32];  // H^T[row][32 half + e]
+#pragma unroll
+    for (int e = 0; e < 32; ++e) hs[e] = 0.0f;
+    if (tid < 64) F[kFCar + tid] = 0.0f;
+    const float2 qbA = *reinterpret_cast<const float2*>(a.q_bias + (int64_t)it.h * kN + 2 * pA);
+    const float2 qbB = *reinterpret_cast<const float2*>(a.q_bias + (int64_t)it.h * kN + 2 * pB);
+    const float2 kbA = *reinterpret_cast<const float2*>(a.k_bias + (int64_t)it.h * kN + 2 * pA);
+    const float2 kbB = *reinterpret_cast<const float2*>(a.k_bias + (int64_t)it.h * kN + 2 * pB);
+    const float dh = a.d[it.h];
+    bool bad = false;
+
+    // raw q, k (and angles, when rot_dim is even) of the chunk starting at row
+    // rb: 16-byte (4-byte) cp.async pieces, rows past the run zero-filled
+    auto prefetch = [&](int64_t rb, int len) {
+#pragma unroll 4
+      for (int i = tid; i < 2 * kQ * 16; i += kThreads) {
+        const int which = i >> 11, rem = i & 2047, t = rem >> 4, pc = rem & 15;
+        const bool ok = t < len;
+        const __nv_bfloat16* src = (which ? k : q) + (ok ? rb + t : rb) * kN + 8 * pc;
+        cp_async16(sb + (which ? kOffRawK : kOffRawQ) + (uint32_t)(t * 256 + pc * 16), src, ok);
+      }
+      if (R > 0 && (R & 1) == 0) {
+        const int pieces = R >> 1;
+        for (int i = tid; i < kQ * pieces; i += kThreads) {
+          const int t = i / pieces, pc = i - t * pieces;
+          const bool ok = t < len;
+          cp_async4(sb + kOffRawA + (uint32_t)(t * 2 * R + 4 * pc), ang + (ok ? rb + t : rb) * R + 2 * pc, ok);
+        }
+      }
+      asm volatile("cp.async.commit_group;" ::: "memory");
+    };
+    if (nch > 0) prefetch(it.row0, min(kQ, it.T));
+    // raw per-token scalars of the chunk at row rb (thread tid < 128: token tid and
+    // the next one), loaded a chunk ahead
+    const int64_t seq_end = it.row0 + it.T;
+    float r_dt = 0.f, r_tr = 0.f, r_adt = 0.f, r_dtn = 0.f, r_trn = 0.f;
+    auto load_scalars = [&](int64_t rb, int len) {
+      r_dt = r_tr = r_adt = r_dtn = r_trn = 0.f;
+      if (tid < len) {
+        const int64_t r = rb + tid;
+        r_dt = a.dt[r * H + it.h];
+        r_tr = bf(trap, r * H + it.h);
+        r_adt = a.adt[r * H + it.h];
+        if (r + 1 < seq_end) {
+          r_dtn = a.dt[(r + 1) * H + it.h];
+          r_trn = bf(trap, (r + 1) * H + it.h);
+        }
+      }
+    };
+    if (nch > 0) load_scalars(it.row0, min(kQ, it.T));
+
+    for (int c = 0; c < nch; ++c) {
+      const int len = min(kQ, it.T - c * kQ);
+      const int64_t rb = it.row0 + (int64_t)c * kQ;  // first row of the chunk
+      const bool last_chunk = c == nch - 1;
+
+      // ---- v pieces (issued first: their latency hides behind the scalar work)
+      uint4 vraw[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int idx = tid + kThreads * e, t = idx >> 3, c8 = idx & 7;
+        vraw[e] = t < len ? *reinterpret_cast<const uint4*>(v + ((rb + t) * H + it.h) * kP + 8 * c8)
+                          : make_uint4(0u, 0u, 0u, 0u);
+      }
+      // ---- per-token scalars (warps 0-3: token tid)
+      float a2 = 0.f, incl = 0.f;
+      if (tid < kQ) {
+        float scl = 0.f, dtp = 0.f;
+        if (tid < len) {
+          const float sg = rb + tid + 1 < seq_end ? r_dtn * (1.0f - sigmoidf_(r_trn)) : 0.f;
+          a2 = r_adt * kLog2e;
+          dtp = r_dt * sigmoidf_(r_tr);
+          scl = dtp + sg;
+        }
+        F[kFW + tid] = scl;
+        F[kFDD + tid] = dtp;
+        F[kFDT + tid] = r_dt;
+        incl = warp_incl(a2, lane);
+        if (lane == 31) F[kFWS + warp] = incl;
+      }
+      if ((R & 1) != 0) {  // odd rot_dim: angles element by element
+        __nv_bfloat16* ra = reinterpret_cast<__nv_bfloat16*>(smem + kOffRawA);
+        for (int i = tid; i < kQ * R; i += kThreads) {
+          const int t = i / R;
+          ra[i] = t < len ? ang[(rb + t) * R + (i - t * R)] : __float2bfloat16_rn(0.f);
+        }
+      }
+      asm volatile("cp.async.wait_group 0;" ::: "memory");
+      __syncthreads();  // (A) raw chunk, scalars, warp sums
+      if (tid < kQ) {
+        float off = 0.f;
+        for (int w = 0; w < warp; ++w) off += F[kFWS + w];
+        F[kFS + tid] = incl + off;
+      }
+      // ---- angle increments of this thread's rotated pairs over its 16 tokens
+      const bool rotA = pA < R, rotB = pB < R;
+      float incA[16], incB[16];
+      {
+        const __nv_bfloat16* ra = reinterpret_cast<const __nv_bfloat16*>(smem + kOffRawA);
+        float partA = 0.f, partB = 0.f;
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const int t = 16 * warp + e;
+          const float pd = kPiF * F[kFDT + t];
+          incA[e] = rotA ? tanh_fast(__bfloat162float(ra[t * R + pA])) * pd : 0.f;
+          incB[e] = rotB ? tanh_fast(__bfloat162float(ra[t * R + pB])) * pd : 0.f;
+          partA += incA[e];
+          partB += incB[e];
+        }
+        F[kFAP + 64 * warp + pA] = partA;
+        F[kFAP + 64 * warp + pB] = partB;
+      }
+      __syncthreads();  // (A2) angle block sums
+      {
+        float runA = F[kFCar + 64 * (c & 1) + pA], runB = F[kFCar + 64 * (c & 1) + pB];
+        for (int j = 0; j < warp; ++j) {
+          runA += F[kFAP + 64 * j + pA];
+          runB += F[kFAP + 64 * j + pB];
+        }
+        float dv[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const int t = 16 * warp + e;
+          uint32_t qa = 0u, ka = 0u, qb = 0u, kb = 0u;
+          float d = 0.f;
+          if (t < len) {
+            runA += incA[e];
+            runB += incB[e];
+            const float phA = wrap2pi(runA), phB = wrap2pi(runB);
+            const uint32_t* rq = reinterpret_cast<const uint32_t*>(smem + kOffRawQ + t * 256);
+            const uint32_t* rk = reinterpret_cast<const uint32_t*>(smem + kOffRawK + t * 256);
+            const uint32_t qA = rq[pA], qB = rq[pB], kA = rk[pA], kB = rk[pB];
+            float snA = 0.f, csA = 1.f, snB = 0.f, csB = 1.f;
+            if (rotA) sincos_wrapped(phA, snA, csA);
+            if (rotB) sincos_wrapped(phB, snB, csB);
+            const float qa0 = __uint_as_float(qA << 16) + qbA.x, qa1 = __uint_as_float(qA & 0xffff0000u) + qbA.y;
+            const float ka0 = __uint_as_float(kA << 16) + kbA.x, ka1 = __uint_as_float(kA & 0xffff0000u) + kbA.y;
+            const float qb0 = __uint_as_float(qB << 16) + qbB.x, qb1 = __uint_as_float(qB & 0xffff0000u) + qbB.y;
+            const float kb0 = __uint_as_float(kB << 16) + kbB.x, kb1 = __uint_as_float(kB & 0xffff0000u) + kbB.y;
+            const float rqa0 = csA * qa0 - snA * qa1, rqa1 = snA * qa0 + csA * qa1;
+            const float rka0 = csA * ka0 - snA * ka1, rka1 = snA * ka0 + csA * ka1;
+            const float rqb0 = csB * qb0 - snB * qb1, rqb1 = snB * qb0 + csB * qb1;
+            const float rkb0 = csB * kb0 - snB * kb1, rkb1 = snB * kb0 + csB * kb1;
+            qa = h2(rqa0, rqa1, bad);
+            ka = h2(rka0, rka1, bad);
+            qb = h2(rqb0, rqb1, bad);
+            kb = h2(rkb0, rkb1, bad);
+            d = (rqa0 * rka0 + rqa1 * rka1) + (rqb0 * rkb0 + rqb1 * rkb1);
+            if (t == len - 1) {
+              if (rotA) F[kFCar + 64 * ((c + 1) & 1) + pA] = phA;
+              if (rotB) F[kFCar + 64 * ((c + 1) & 1) + pB] = phB;
+              if (last_chunk) {
+                *reinterpret_cast<float2*>(a.final_k + sh * kN + 2 * pA) = make_float2(rka0, rka1);
+                *reinterpret_cast<float2*>(a.final_k + sh * kN + 2 * pB) = make_float2(rkb0, rkb1);
+                __nv_bfloat16* fa = static_cast<__nv_bfloat16*>(a.final_angle) + sh * R;
+                if (rotA) fa[pA] = __float2bfloat16_rn(phA);
+                if (rotB) fa[pB] = __float2bfloat16_rn(phB);
+              }
+            }
+          }
+          *reinterpret_cast<uint32_t*>(smem + kOffQ + toff(t, 2 * pA)) = qa;
+          *reinterpret_cast<uint32_t*>(smem + kOffK + toff(t, 2 * pA)) = ka;
+          *reinterpret_cast<uint32_t*>(smem + kOffQ + toff(t, 2 * pB)) = qb;
+          *reinterpret_cast<uint32_t*>(smem + kOffK + toff(t, 2 * pB)) = kb;
+          dv[e] = d;
+        }
+        // q^ . k^ of each token: the halves of the warp first, then a transpose-
+        // reduce over the 16 tokens (lane l and l + 16 end with token 16 warp + l % 16)
+#pragma unroll
+        for (int e = 0; e < 16; ++e) dv[e] += __shfl_xor_sync(0xffffffffu, dv[e], 16);
+#pragma unroll
+        for (int o = 8; o >= 1; o >>= 1) {
+          const bool up = (lane & o) != 0;
+#pragma unroll
+          for (int e = 0; e < o; ++e) {
+            const float send = up ? dv[e] : dv[e + o];
+            const float keep = up ? dv[e + o] : dv[e];
+            dv[e] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+          }
+        }
+        if (lane < 16) F[kFDG + 16 * warp + lane] = dv[0];
+      }
+      __syncthreads();  // (B) S, diagonal partials; the raw chunk is spent
+      if (c + 1 < nch) {
+        prefetch(rb + kQ, min(kQ, it.T - (c + 1) * kQ));
+        load_scalars(rb + kQ, min(kQ, it.T - (c + 1) * kQ));
+      }
+      // ---- v (fp16) and v o w tiles; the last token's v is the final V state
+      {
+        const float s_end = F[kFS + kQ - 1];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int idx = tid + kThreads * e, t = idx >> 3, c8 = idx & 7;
+          const float w = ex2f(s_end - F[kFS + t]) * F[kFW + t];
+          const uint32_t vw4[4] = {vraw[e].x, vraw[e].y, vraw[e].z, vraw[e].w};
+          uint32_t f[4], g[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const float x0 = __uint_as_float(vw4[u] << 16), x1 = __uint_as_float(vw4[u] & 0xffff0000u);
+            f[u] = h2(x0, x1, bad);
+            g[u] = h2(x0 * w, x1 * w, bad);
+          }
+          *reinterpret_cast<uint4*>(smem + kOffV + toff(t, 8 * c8)) = make_uint4(f[0], f[1], f[2], f[3]);
+          *reinterpret_cast<uint4*>(smem + kOffVW + toff(t, 8 * c8)) = make_uint4(g[0], g[1], g[2], g[3]);
+          if (last_chunk && t == len - 1)
+            *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.final_v) + sh * kP + 8 * c8) = vraw[e];
+        }
+      }
+      fence_async_smem();
+      tc_fence_before();
+      __syncthreads();  // (C) operand tiles complete
+      if (tid == 0) {
+        tc_fence_after();
+        const uint64_t q0 = sdesc(sb + kOffQ, 16, 1024), k0 = sdesc(sb + kOffK, 16, 1024);
+#pragma unroll
+        for (int s2 = 0; s2 < kN / 16; ++s2) {
+          const uint32_t ko = ((s2 >> 2) * kQ * 128 + (s2 & 3) * 32) >> 4;
+          mma_ss(tmem + kColCB, q0 + ko, k0 + ko, idesc128(kQ, 0, 0, 0), s2 > 0);
+        }
+        if (c > 0) {
+          const uint64_t h0 = sdesc(sb + kOffHT, kN * 128, 1024);
+#pragma unroll
+          for (int s2 = 0; s2 < kN / 16; ++s2) {
+            const uint32_t ko = ((s2 >> 2) * kQ * 128 + (s2 & 3) * 32) >> 4;
+            mma_ss(tmem + kColYo, q0 + ko, h0 + ((s2 * 2048) >> 4), idesc128(kP, 0, 1, 0), s2 > 0);
+          }
+        }
+        const uint64_t kt0 = sdesc(sb + kOffK, kQ * 128, 1024), vw0 = sdesc(sb + kOffVW, kQ * 128, 1024);
+#pragma unroll
+        for (int s2 = 0; s2 < kQ / 16; ++s2)
+          mma_ss(tmem + kColDH, kt0 + ((s2 * 2048) >> 4), vw0 + ((s2 * 2048) >> 4), idesc128(kP, 1, 1, 0), s2 > 0);
+        mma_commit(bar0);
+      }
+      if (!wait_bar(bar0, n_bar0 & 1u, s_abort)) *s_abort = 1u;
+      ++n_bar0;
+      __syncthreads();
+      if (*s_abort) {
+        aborted = true;
+        break;
+      }
+      tc_fence_after();
+      // ---- M (fp16, to TMEM) and the state through this chunk
+      {
+        const float St = F[kFS + row];
+        const float diag = F[kFDD + row] * F[kFDG + row];
+#pragma unroll 1
+        for (int kk = 0; kk < 4; ++kk) {
+          const int s2 = 4 * half + kk, j0 = 16 * s2;
+          uint32_t m[8];
+          if (j0 > 32 * (warp & 3) + 31) {  // above every row of this warp (warp-uniform: the TMEM load is .aligned)
+#pragma unroll
+            for (int e = 0; e < 8; ++e) m[e] = 0u;
+          } else {
+            float cb[16];
+            tmem_ld16(tmem + lane_off + kColCB + (uint32_t)j0, cb);
+            float mv[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+              const int j = j0 + e;
+              mv[e] = j < row ? cb[e] * ex2f(St - F[kFS + j]) * F[kFW + j] : (j == row ? diag : 0.f);
+            }
+#pragma unroll
+            for (int e = 0; e < 8; ++e) m[e] = h2(mv[2 * e], mv[2 * e + 1], bad);
+          }
+          asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};"
+                       :: "r"(tmem + lane_off + kColM + 8u * (uint32_t)s2), "r"(m[0]), "r"(m[1]), "r"(m[2]),
+                          "r"(m[3]), "r"(m[4]), "r"(m[5]), "r"(m[6]), "r"(m[7]) : "memory");
+        }
+        const float dec = ex2f(F[kFS + kQ - 1]);
+        float d0[16], d1[16];
+        tmem_ld16x2(tmem + lane_off + kColDH + 32u * (uint32_t)half, tmem + lane_off + kColDH + 32u * (uint32_t)half + 16,
+                    d0, d1);
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          hs[e] = fmaf(dec, hs[e], d0[e]);
+          hs[16 + e] = fmaf(dec, hs[16 + e], d1[e]);
+        }
+        if (!last_chunk) {
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            uint32_t w[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) w[e] = h2(hs[8 * u + 2 * e], hs[8 * u + 2 * e + 1], bad);
+            *reinterpret_cast<uint4*>(smem + kOffHT + toff(row, 32 * half + 8 * u)) = make_uint4(w[0], w[1], w[2], w[3]);
+          }
+        }
+        asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+      }
+      fence_async_smem();
+      tc_fence_before();
+      __syncthreads();  // (D) M in TMEM, next H^T in shared memory
+      if (tid == 0) {
+        tc_fence_after();
+        const uint64_t v0 = sdesc(sb + kOffV, kQ * 128, 1024);
+#pragma unroll
+        for (int s2 = 0; s2 < kQ / 16; ++s2)
+          mma_ts(tmem + kColYd, tmem + kColM + 8u * (uint32_t)s2, v0 + ((s2 * 2048) >> 4), idesc128(kP, 0, 1, 0), s2 > 0);
+        mma_commit(bar1);
+      }
+      // z of this thread's row and columns while the product runs
+      uint4 zr[4];
+      const bool in_run = row < len;
+      const int64_t off = ((rb + row) * H + it.h) * kP + 32 * half;
+#pragma unroll
+      for (int u = 0; u < 4; ++u) zr[u] = in_run ? *reinterpret_cast<const uint4*>(z + off + 8 * u) : make_uint4(0u, 0u, 0u, 0u);
+      if (!wait_bar(bar1, n_bar1 & 1u, s_abort)) *s_abort = 1u;
+      ++n_bar1;
+      __syncthreads();
+      if (*s_abort) {
+        aborted = true;
+        break;
+      }
+      tc_fence_after();
+      // ---- output
+      {
+        const float et = ex2f(F[kFS + row]);
+#pragma unroll
+        for (int g = 0; g < 2; ++g) {
+          float yd[16], yo[16];
+          if (c > 0) {
+            tmem_ld16x2(tmem + lane_off + kColYd + 32u * (uint32_t)half + 16u * (uint32_t)g,
+                        tmem + lane_off + kColYo + 32u * (uint32_t)half + 16u * (uint32_t)g, yd, yo);
+          } else {
+            tmem_ld16(tmem + lane_off + kColYd + 32u * (uint32_t)half + 16u * (uint32_t)g, yd);
+#pragma unroll
+            for (int e = 0; e < 16; ++e) yo[e] = 0.f;
+          }
+          uint32_t o[8];
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            const uint4 vv = *reinterpret_cast<const uint4*>(smem + kOffV + toff(row, 32 * half + 16 * g + 8 * u));
+            const uint32_t vw[4] = {vv.x, vv.y, vv.z, vv.w};
+            const uint4 zz = zr[2 * g + u];
+            const uint32_t zw[4] = {zz.x, zz.y, zz.z, zz.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int i0 = 8 * u + 2 * e;
+              const float y0 = fmaf(et, yo[i0], yd[i0]) + dh * f16lo(vw[e]);
+              const float y1 = fmaf(et, yo[i0 + 1], yd[i0 + 1]) + dh * f16hi(vw[e]);
+              const float z0 = __uint_as_float(zw[e] << 16), z1 = __uint_as_float(zw[e] & 0xffff0000u);
+              const __nv_bfloat162 ob = __floats2bfloat162_rn(y0 * silu_f(z0), y1 * silu_f(z1));
+              o[4 * u + e] = *reinterpret_cast<const uint32_t*>(&ob);
+            }
+          }
+          if (in_run) {
+            *reinterpret_cast<uint4*>(out + off + 16 * g) = make_uint4(o[0], o[1], o[2], o[3]);
+            *reinterpret_cast<uint4*>(out + off + 16 * g + 8) = make_uint4(o[4], o[5], o[6], o[7]);
+          }
+        }
+      }
+      tc_fence_before();
+      __syncthreads();  // (E) tiles and TMEM free for the next chunk
+    }
+    if (aborted) break;
+    // ---- final state (an empty sequence has zero final states)
+    if (nch == 0) {
+      if (tid < kN) a.final_k[sh * kN + tid] = 0.f;
+      if (tid < kP) static_cast<__nv_bfloat16*>(a.final_v)[sh * kP + tid] = __float2bfloat16_rn(0.f);
+      if (tid < R) static_cast<__nv_bfloat16*>(a.final_angle)[sh * R + tid] = __float2bfloat16_rn(0.f);
+    }
+#pragma unroll
+    for (int e = 0; e < 32; ++e) a.final_ssm[(sh * kP + 32 * half + e) * kN + row] = hs[e];
+    if (bad) *s_range = 1u;
+    __syncthreads();
+    if (*s_range) {
+      // an fp16 operand overflowed: this (sequence, head) again, token by token
+      serial_item(a, it, reinterpret_cast<float*>(smem));
+      __syncthreads();
+      if (tid == 0) *s_range = 0u;
+      __syncthreads();
+    }
+  }
+  // ---- teardown
+  if (aborted && tid == 0) {
+    atomicAdd(&g_m3_timeouts, 1u);
+    // what was issued last completes before its TMEM is released
+    if (n_bar0 > 0) drain_bar(bar0, (n_bar0 - 1) & 1u);
+    if (n_bar1 > 0) drain_bar(bar1, (n_bar1 - 1) & 1u);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;" :: "r"(tmem));
+}
+
+}  // namespace
+
+unsigned int read_m3_timeouts() {
+  unsigned int v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_m3_timeouts, sizeof v) != cudaSuccess) return 0xffffffffu;
+  return v;
+}
+
+cudaError_t launch_m3_forward(const Mamba3Args& a, int num_sms, cudaStream_t st) {
+  const int items = a.nseq * a.heads;
+  if (items == 0) return cudaSuccess;
+  cudaError_t e = cudaFuncSetAttribute(m3_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem);
+  if (e != cudaSuccess) return e;
+  const int grid = items < num_sms ? items : num_sms;
+  m3_fwd_kernel<<<grid, kThreads, kSmem, st>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace mamba2

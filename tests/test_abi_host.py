@@ -1,5 +1,5 @@
 """Host-side checks of the C ABI (no GPU needed): the library loads, exports
-every function include/mamba2.h declares, and rejects malformed
+every function include/*.h declares, and rejects malformed
 RecurrentBatches before touching any device pointer, with the same status the
 oracle returns (gllm PR #85 "feat(backend): Mamba2 ops, with CPU reference
 implementations", section "Ops": out-of-range slot, shared slot, runs that do
@@ -14,18 +14,22 @@ import oracle
 import selective_scan_gb300 as ss
 import workloads as W
 
-HEADER = os.path.join(os.path.dirname(os.path.dirname(__file__)), "include", "mamba2.h")
+INCLUDE = os.path.join(os.path.dirname(os.path.dirname(__file__)), "include")
 
 
 def declared_functions():
-    text = open(HEADER).read()
-    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(mamba2_[a-z0-9_]+)\s*\(", text)))
+    names = set()
+    for h in sorted(os.listdir(INCLUDE)):
+        if h.endswith(".h"):
+            text = re.sub(r"/\*.*?\*/", "", open(os.path.join(INCLUDE, h)).read(), flags=re.S)
+            names.update(re.findall(r"\b(mamba[23]_[a-z0-9_]+)\s*\(", text))
+    return sorted(names)
 
 
 def test_exports_every_declared_symbol(product_lib):
     names = declared_functions()
-    for op in ("mamba2_causal_conv1d", "mamba2_ssd_scan", "mamba2_gated_rmsnorm", "mamba2_decode_step"):
+    for op in ("mamba2_causal_conv1d", "mamba2_ssd_scan", "mamba2_gated_rmsnorm", "mamba2_decode_step",
+               "mamba3_siso_varlen_forward"):
         assert op in names
     missing = [n for n in names if not hasattr(product_lib, n)]
     assert not missing, missing
@@ -176,3 +180,30 @@ def test_decode_device_batch_host_rejections(product_lib):
     assert call(groups=0) == ss.ERR_INVALID_ARGUMENT
     assert call(eps=-1.0) == ss.ERR_INVALID_ARGUMENT
     assert call(num_slots=-1) == ss.ERR_INVALID_ARGUMENT
+
+
+def _m3_call(lib, cu, rows=20, heads=2, headdim=64, d_state=128, rot_dim=32, ptrs=None):
+    p = ptrs if ptrs is not None else FAKE
+    arr = (ctypes.c_int32 * len(cu))(*cu)
+    return lib.mamba3_siso_varlen_forward(*p[:16], arr, len(cu) - 1, rows, heads, headdim, d_state, rot_dim, None)
+
+
+def test_mamba3_rejects_before_touching_memory(product_lib):
+    """Mamba-3 SISO forward: malformed calls return their status on the host (the fake
+    device pointers are never dereferenced)."""
+    lib = product_lib
+    assert _m3_call(lib, [0, 12, 21]) == ss.ERR_RUNS_DONT_COVER_ROWS
+    assert _m3_call(lib, [0, 12, 10, 20]) == ss.ERR_RUNS_DONT_COVER_ROWS
+    assert _m3_call(lib, [1, 12, 20]) == ss.ERR_RUNS_DONT_COVER_ROWS
+    assert _m3_call(lib, [0, 12, 20], rot_dim=65) == ss.ERR_INVALID_ARGUMENT   # 2 R > N
+    assert _m3_call(lib, [0, 12, 20], heads=0) == ss.ERR_INVALID_ARGUMENT
+    assert _m3_call(lib, [0, 12, 20], headdim=32) == ss.ERR_NOT_IMPLEMENTED
+    assert _m3_call(lib, [0, 12, 20], d_state=64, rot_dim=16) == ss.ERR_NOT_IMPLEMENTED
+    misaligned = list(FAKE)
+    misaligned[5] += 2   # q
+    assert _m3_call(lib, [0, 12, 20], ptrs=misaligned) == ss.ERR_INVALID_ARGUMENT
+    nulls = list(FAKE)
+    nulls[2] = None      # final_ssm
+    assert _m3_call(lib, [0, 12, 20], ptrs=nulls) == ss.ERR_INVALID_ARGUMENT
+    # an empty batch is a no-op
+    assert lib.mamba3_siso_varlen_forward(*([None] * 16), None, 0, 0, 2, 64, 128, 32, None) == ss.OK
