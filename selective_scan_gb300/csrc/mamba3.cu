@@ -40,6 +40,8 @@
 // (mamba2_device_timeouts), drains what it issued, frees its TMEM and returns.
 #include <cuda.h>
 
+#include <type_traits>
+
 #include "common.cuh"
 
 namespace mamba2 {
@@ -82,8 +84,8 @@ constexpr int kFAP = 520;       // [8][64] angle sums per block of 16 tokens
 constexpr int kFCar = 1032;     // [2][64] angle carried into chunk c (buffer c % 2)
 constexpr int kFDT = 1160;      // [128] dt of the head
 constexpr int kNumF = 1288;
-constexpr uint32_t kOffBar = kOffF + kNumF * 4;  // two mbarriers
-constexpr uint32_t kOffMisc = kOffBar + 16;      // TMEM base, abort flag, fp16 range flag
+constexpr uint32_t kOffBar = kOffF + kNumF * 4;  // mbarriers: products, Yd, raw q/k copy
+constexpr uint32_t kOffMisc = kOffBar + 24;      // TMEM base, abort flag, fp16 range flag
 constexpr uint32_t kSmemUsed = kOffMisc + 16;
 constexpr uint32_t kSmem = kSmemUsed + 1024;     // + alignment slack
 static_assert(kSmem <= 232448, "shared memory plan exceeds 227 KB");
@@ -107,9 +109,10 @@ __device__ __forceinline__ float ex2f(float x) {
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
-// fp16 pair (lo in the low half); `bad` set when either value is outside the fp16 range (or NaN)
-__device__ __forceinline__ uint32_t h2(float lo, float hi, bool& bad) {
-  bad |= !(fabsf(lo) <= kF16Max && fabsf(hi) <= kF16Max);
+// fp16 pair (lo in the low half); `amax` tracks the largest magnitude converted
+// (above kF16Max the pair did not fit)
+__device__ __forceinline__ uint32_t h2(float lo, float hi, float& amax) {
+  amax = fmaxf(amax, fmaxf(fabsf(lo), fabsf(hi)));
   uint32_t d;
   asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
   return d;
@@ -132,6 +135,11 @@ __device__ __forceinline__ void sincos_wrapped(float phi, float& sn, float& cs) 
   __sincosf(phi > kPiF ? phi - kTwoPi : phi, &sn, &cs);
 }
 
+// one contiguous global -> shared copy (16-byte aligned ends), completing on `bar`
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+               :: "r"(dst), "l"(src), "r"(bytes), "r"(bar) : "memory");
+}
 __device__ __forceinline__ void cp_async4(uint32_t dst, const void* src, bool valid) {
   asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;\n" ::"r"(dst), "l"(src), "r"(valid ? 4 : 0));
 }
@@ -247,7 +255,7 @@ __global__ void __launch_bounds__(kThreads, 1) m3_fwd_kernel(const __grid_consta
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + kOffMisc);
   volatile uint32_t* s_abort = reinterpret_cast<volatile uint32_t*>(smem + kOffMisc + 4);
   volatile uint32_t* s_range = reinterpret_cast<volatile uint32_t*>(smem + kOffMisc + 8);
-  const uint32_t bar0 = sb + kOffBar, bar1 = sb + kOffBar + 8;
+  const uint32_t bar0 = sb + kOffBar, bar1 = sb + kOffBar + 8, bar2 = sb + kOffBar + 16;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int H = a.heads, R = a.rot_dim;
 
@@ -258,6 +266,7 @@ __global__ void __launch_bounds__(kThreads, 1) m3_fwd_kernel(const __grid_consta
   if (tid == 32) {
     mbar_init(bar0, 1);
     mbar_init(bar1, 1);
+    mbar_init(bar2, 1);
     *s_abort = 0u;
     *s_range = 0u;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -281,7 +290,8 @@ __global__ void __launch_bounds__(kThreads, 1) m3_fwd_kernel(const __grid_consta
   // rotation role: pairs lane and lane + 32 (columns 2 pair, 2 pair + 1) of tokens
   // 16 warp .. 16 warp + 15 (one rotated and one plain pair each when rot_dim = 32)
   const int pA = lane, pB = lane + 32;
-  uint32_t n_bar0 = 0, n_bar1 = 0;  // completed phases waited on
+  uint32_t n_bar0 = 0, n_bar1 = 0, n_bar2 = 0;  // phases waited on
+  uint32_t n_pref = 0;                           // raw copies issued
   bool aborted = false;
 
   const int items = a.nseq * H;
@@ -302,19 +312,26 @@ __global__ void __launch_bounds__(kThreads, 1) m3_fwd_kernel(const __grid_consta
     const float2 kbA = *reinterpret_cast<const float2*>(a.k_bias + (int64_t)it.h * kN + 2 * pA);
     const float2 kbB = *reinterpret_cast<const float2*>(a.k_bias + (int64_t)it.h * kN + 2 * pB);
     const float dh = a.d[it.h];
-    bool bad = false;
+    float amax = 0.f;  // largest fp16 operand magnitude of the item
 
-    // raw q, k (and angles, when rot_dim is even) of the chunk starting at row
-    // rb: 16-byte (4-byte) cp.async pieces, rows past the run zero-filled
+    // raw q and k rows of the chunk starting at row rb: one bulk copy each (thread
+    // 0; rows past the run keep stale values, masked where they are read);
+    // angles likewise, or as 4-byte cp.async pieces (rows past the run zero-filled)
+    // when rot_dim is even but not a multiple of 8
+    // (rows of rot_dim a multiple of 8 are 16-byte multiples: the angles then come
+    // as one bulk copy too)
+    const bool ang_bulk = R > 0 && (R & 7) == 0;
     auto prefetch = [&](int64_t rb, int len) {
-#pragma unroll 4
-      for (int i = tid; i < 2 * kQ * 16; i += kThreads) {
-        const int which = i >> 11, rem = i & 2047, t = rem >> 4, pc = rem & 15;
-        const bool ok = t < len;
-        const __nv_bfloat16* src = (which ? k : q) + (ok ? rb + t : rb) * kN + 8 * pc;
-        cp_async16(sb + (which ? kOffRawK : kOffRawQ) + (uint32_t)(t * 256 + pc * 16), src, ok);
+      ++n_pref;
+      if (tid == 0) {
+        fence_async_smem();  // the previous chunk's reads of the staging rows come first
+        const uint32_t bytes = (uint32_t)len * kN * 2, abytes = ang_bulk ? (uint32_t)(len * R * 2) : 0u;
+        mbar_expect_tx(bar2, 2 * bytes + abytes);
+        bulk_g2s(sb + kOffRawQ, q + rb * kN, bytes, bar2);
+        bulk_g2s(sb + kOffRawK, k + rb * kN, bytes, bar2);
+        if (ang_bulk) bulk_g2s(sb + kOffRawA, ang + rb * R, abytes, bar2);
       }
-      if (R > 0 && (R & 1) == 0) {
+      if (!ang_bulk && R > 0 && (R & 1) == 0) {
         const int pieces = R >> 1;
         for (int i = tid; i < kQ * pieces; i += kThreads) {
           const int t = i / pieces, pc = i - t * pieces;
@@ -357,6 +374,12 @@ __global__ void __launch_bounds__(kThreads, 1) m3_fwd_kernel(const __grid_consta
         vraw[e] = t < len ? *reinterpret_cast<const uint4*>(v + ((rb + t) * H + it.h) * kP + 8 * c8)
                           : make_uint4(0u, 0u, 0u, 0u);
       }
+      // z of this thread's output row and columns (used at the end of the chunk)
+      uint4 zr[4];
+      const bool in_run = row < len;
+      const int64_t off = ((rb + row) * H + it.h) * kP + 32 * half;
+#pragma unroll
+      for (int u = 0; u < 4; ++u) zr[u] = in_run ? *reinterpret_cast<const uint4*>(z + off + 8 * u) : make_uint4(0u, 0u, 0u, 0u);
       // ---- per-token scalars (warps 0-3: token tid)
       float a2 = 0.f, incl = 0.f;
       if (tid < kQ) {
@@ -381,7 +404,15 @@ __global__ void __launch_bounds__(kThreads, 1) m3_fwd_kernel(const __grid_consta
         }
       }
       asm volatile("cp.async.wait_group 0;" ::: "memory");
+      if (wait_bar(bar2, n_bar2 & 1u, s_abort))
+        ++n_bar2;
+      else
+        *s_abort = 1u;
       __syncthreads();  // (A) raw chunk, scalars, warp sums
+      if (*s_abort) {
+        aborted = true;
+        break;
+      }
       if (tid < kQ) {
         float off = 0.f;
         for (int w = 0; w < warp; ++w) off += F[kFWS + w];
@@ -394,13 +425,19 @@ __global__ void __launch_bounds__(kThreads, 1) m3_fwd_kernel(const __grid_consta
         const __nv_bfloat16* ra = reinterpret_cast<const __nv_bfloat16*>(smem + kOffRawA);
         float partA = 0.f, partB = 0.f;
 #pragma unroll
+        const int iA = rotA ? pA : 0, iB = rotB ? pB : 0;  // in-range columns (R may be 0: rows are then empty)
         for (int e = 0; e < 16; ++e) {
           const int t = 16 * warp + e;
-          const float pd = kPiF * F[kFDT + t];
-          incA[e] = rotA ? tanh_fast(__bfloat162float(ra[t * R + pA])) * pd : 0.f;
-          incB[e] = rotB ? tanh_fast(__bfloat162float(ra[t * R + pB])) * pd : 0.f;
+          const float pd = kPiF * F[kFDT + t];  // 0 past the run
+          const float xa = tanh_fast(__bfloat162float(ra[t * R + iA])) * pd;
+          incA[e] = rotA ? xa : 0.f;
           partA += incA[e];
-          partB += incB[e];
+          incB[e] = 0.f;
+          if (R > 32) {  // (uniform) some second pairs rotate
+            const float xb = tanh_fast(__bfloat162float(ra[t * R + iB])) * pd;
+            incB[e] = rotB ? xb : 0.f;
+            partB += incB[e];
+          }
         }
         F[kFAP + 64 * warp + pA] = partA;
         F[kFAP + 64 * warp + pB] = partB;
@@ -413,52 +450,63 @@ __global__ void __launch_bounds__(kThreads, 1) m3_fwd_kernel(const __grid_consta
           runB += F[kFAP + 64 * j + pB];
         }
         float dv[16];
+        auto rotate_rows = [&](auto b_rotates) {
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
           const int t = 16 * warp + e;
-          uint32_t qa = 0u, ka = 0u, qb = 0u, kb = 0u;
-          float d = 0.f;
-          if (t < len) {
-            runA += incA[e];
-            runB += incB[e];
-            const float phA = wrap2pi(runA), phB = wrap2pi(runB);
-            const uint32_t* rq = reinterpret_cast<const uint32_t*>(smem + kOffRawQ + t * 256);
-            const uint32_t* rk = reinterpret_cast<const uint32_t*>(smem + kOffRawK + t * 256);
-            const uint32_t qA = rq[pA], qB = rq[pB], kA = rk[pA], kB = rk[pB];
-            float snA = 0.f, csA = 1.f, snB = 0.f, csB = 1.f;
-            if (rotA) sincos_wrapped(phA, snA, csA);
-            if (rotB) sincos_wrapped(phB, snB, csB);
-            const float qa0 = __uint_as_float(qA << 16) + qbA.x, qa1 = __uint_as_float(qA & 0xffff0000u) + qbA.y;
-            const float ka0 = __uint_as_float(kA << 16) + kbA.x, ka1 = __uint_as_float(kA & 0xffff0000u) + kbA.y;
-            const float qb0 = __uint_as_float(qB << 16) + qbB.x, qb1 = __uint_as_float(qB & 0xffff0000u) + qbB.y;
-            const float kb0 = __uint_as_float(kB << 16) + kbB.x, kb1 = __uint_as_float(kB & 0xffff0000u) + kbB.y;
-            const float rqa0 = csA * qa0 - snA * qa1, rqa1 = snA * qa0 + csA * qa1;
-            const float rka0 = csA * ka0 - snA * ka1, rka1 = snA * ka0 + csA * ka1;
-            const float rqb0 = csB * qb0 - snB * qb1, rqb1 = snB * qb0 + csB * qb1;
-            const float rkb0 = csB * kb0 - snB * kb1, rkb1 = snB * kb0 + csB * kb1;
-            qa = h2(rqa0, rqa1, bad);
-            ka = h2(rka0, rka1, bad);
-            qb = h2(rqb0, rqb1, bad);
-            kb = h2(rkb0, rkb1, bad);
-            d = (rqa0 * rka0 + rqa1 * rka1) + (rqb0 * rkb0 + rqb1 * rkb1);
-            if (t == len - 1) {
-              if (rotA) F[kFCar + 64 * ((c + 1) & 1) + pA] = phA;
-              if (rotB) F[kFCar + 64 * ((c + 1) & 1) + pB] = phB;
-              if (last_chunk) {
-                *reinterpret_cast<float2*>(a.final_k + sh * kN + 2 * pA) = make_float2(rka0, rka1);
-                *reinterpret_cast<float2*>(a.final_k + sh * kN + 2 * pB) = make_float2(rkb0, rkb1);
-                __nv_bfloat16* fa = static_cast<__nv_bfloat16*>(a.final_angle) + sh * R;
-                if (rotA) fa[pA] = __float2bfloat16_rn(phA);
-                if (rotB) fa[pB] = __float2bfloat16_rn(phB);
-              }
+          const bool live = t < len;
+          runA += incA[e];  // increments are 0 past the run
+          runB += incB[e];
+          const float phA = wrap2pi(runA), phB = wrap2pi(runB);
+          const uint32_t* rq = reinterpret_cast<const uint32_t*>(smem + kOffRawQ + t * 256);
+          const uint32_t* rk = reinterpret_cast<const uint32_t*>(smem + kOffRawK + t * 256);
+          // staging rows past the run hold stale bytes: read as zero
+          const uint32_t qA = live ? rq[pA] : 0u, qB = live ? rq[pB] : 0u;
+          const uint32_t kA = live ? rk[pA] : 0u, kB = live ? rk[pB] : 0u;
+          float snA, csA, snB = 0.f, csB = 1.f;
+          sincos_wrapped(phA, snA, csA);
+          if (!rotA) { snA = 0.f; csA = 1.f; }
+          if constexpr (decltype(b_rotates)::value) {
+            sincos_wrapped(phB, snB, csB);
+            if (!rotB) { snB = 0.f; csB = 1.f; }
+          }
+          const float qa0 = __uint_as_float(qA << 16) + qbA.x, qa1 = __uint_as_float(qA & 0xffff0000u) + qbA.y;
+          const float ka0 = __uint_as_float(kA << 16) + kbA.x, ka1 = __uint_as_float(kA & 0xffff0000u) + kbA.y;
+          const float qb0 = __uint_as_float(qB << 16) + qbB.x, qb1 = __uint_as_float(qB & 0xffff0000u) + qbB.y;
+          const float kb0 = __uint_as_float(kB << 16) + kbB.x, kb1 = __uint_as_float(kB & 0xffff0000u) + kbB.y;
+          const float rqa0 = csA * qa0 - snA * qa1, rqa1 = snA * qa0 + csA * qa1;
+          const float rka0 = csA * ka0 - snA * ka1, rka1 = snA * ka0 + csA * ka1;
+          float rqb0 = qb0, rqb1 = qb1, rkb0 = kb0, rkb1 = kb1;
+          if constexpr (decltype(b_rotates)::value) {
+            rqb0 = csB * qb0 - snB * qb1;
+            rqb1 = snB * qb0 + csB * qb1;
+            rkb0 = csB * kb0 - snB * kb1;
+            rkb1 = snB * kb0 + csB * kb1;
+          }
+          const uint32_t qa = h2(rqa0, rqa1, amax), ka = h2(rka0, rka1, amax);
+          const uint32_t qb = h2(rqb0, rqb1, amax), kb = h2(rkb0, rkb1, amax);
+          if (t == len - 1) {
+            if (rotA) F[kFCar + 64 * ((c + 1) & 1) + pA] = phA;
+            if (rotB) F[kFCar + 64 * ((c + 1) & 1) + pB] = phB;
+            if (last_chunk) {
+              *reinterpret_cast<float2*>(a.final_k + sh * kN + 2 * pA) = make_float2(rka0, rka1);
+              *reinterpret_cast<float2*>(a.final_k + sh * kN + 2 * pB) = make_float2(rkb0, rkb1);
+              __nv_bfloat16* fa = static_cast<__nv_bfloat16*>(a.final_angle) + sh * R;
+              if (rotA) fa[pA] = __float2bfloat16_rn(phA);
+              if (rotB) fa[pB] = __float2bfloat16_rn(phB);
             }
           }
-          *reinterpret_cast<uint32_t*>(smem + kOffQ + toff(t, 2 * pA)) = qa;
-          *reinterpret_cast<uint32_t*>(smem + kOffK + toff(t, 2 * pA)) = ka;
-          *reinterpret_cast<uint32_t*>(smem + kOffQ + toff(t, 2 * pB)) = qb;
-          *reinterpret_cast<uint32_t*>(smem + kOffK + toff(t, 2 * pB)) = kb;
-          dv[e] = d;
+          *reinterpret_cast<uint32_t*>(smem + kOffQ + toff(t, 2 * pA)) = live ? qa : 0u;
+          *reinterpret_cast<uint32_t*>(smem + kOffK + toff(t, 2 * pA)) = live ? ka : 0u;
+          *reinterpret_cast<uint32_t*>(smem + kOffQ + toff(t, 2 * pB)) = live ? qb : 0u;
+          *reinterpret_cast<uint32_t*>(smem + kOffK + toff(t, 2 * pB)) = live ? kb : 0u;
+          dv[e] = live ? (rqa0 * rka0 + rqa1 * rka1) + (rqb0 * rkb0 + rqb1 * rkb1) : 0.f;
         }
+        };
+        if (R > 32)
+          rotate_rows(std::true_type{});
+        else
+          rotate_rows(std::false_type{});
         // q^ . k^ of each token: the halves of the warp first, then a transpose-
         // reduce over the 16 tokens (lane l and l + 16 end with token 16 warp + l % 16)
 #pragma unroll
@@ -492,8 +540,8 @@ __global__ void __launch_bounds__(kThreads, 1) m3_fwd_kernel(const __grid_consta
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
             const float x0 = __uint_as_float(vw4[u] << 16), x1 = __uint_as_float(vw4[u] & 0xffff0000u);
-            f[u] = h2(x0, x1, bad);
-            g[u] = h2(x0 * w, x1 * w, bad);
+            f[u] = h2(x0, x1, amax);
+            g[u] = h2(x0 * w, x1 * w, amax);
           }
           *reinterpret_cast<uint4*>(smem + kOffV + toff(t, 8 * c8)) = make_uint4(f[0], f[1], f[2], f[3]);
           *reinterpret_cast<uint4*>(smem + kOffVW + toff(t, 8 * c8)) = make_uint4(g[0], g[1], g[2], g[3]);
@@ -555,7 +603,7 @@ __global__ void __launch_bounds__(kThreads, 1) m3_fwd_kernel(const __grid_consta
               mv[e] = j < row ? cb[e] * ex2f(St - F[kFS + j]) * F[kFW + j] : (j == row ? diag : 0.f);
             }
 #pragma unroll
-            for (int e = 0; e < 8; ++e) m[e] = h2(mv[2 * e], mv[2 * e + 1], bad);
+            for (int e = 0; e < 8; ++e) m[e] = h2(mv[2 * e], mv[2 * e + 1], amax);
           }
           asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};"
                        :: "r"(tmem + lane_off + kColM + 8u * (uint32_t)s2), "r"(m[0]), "r"(m[1]), "r"(m[2]),
@@ -575,7 +623,7 @@ __global__ void __launch_bounds__(kThreads, 1) m3_fwd_kernel(const __grid_consta
           for (int u = 0; u < 4; ++u) {
             uint32_t w[4];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) w[e] = h2(hs[8 * u + 2 * e], hs[8 * u + 2 * e + 1], bad);
+            for (int e = 0; e < 4; ++e) w[e] = h2(hs[8 * u + 2 * e], hs[8 * u + 2 * e + 1], amax);
             *reinterpret_cast<uint4*>(smem + kOffHT + toff(row, 32 * half + 8 * u)) = make_uint4(w[0], w[1], w[2], w[3]);
           }
         }
@@ -592,12 +640,6 @@ __global__ void __launch_bounds__(kThreads, 1) m3_fwd_kernel(const __grid_consta
           mma_ts(tmem + kColYd, tmem + kColM + 8u * (uint32_t)s2, v0 + ((s2 * 2048) >> 4), idesc128(kP, 0, 1, 0), s2 > 0);
         mma_commit(bar1);
       }
-      // z of this thread's row and columns while the product runs
-      uint4 zr[4];
-      const bool in_run = row < len;
-      const int64_t off = ((rb + row) * H + it.h) * kP + 32 * half;
-#pragma unroll
-      for (int u = 0; u < 4; ++u) zr[u] = in_run ? *reinterpret_cast<const uint4*>(z + off + 8 * u) : make_uint4(0u, 0u, 0u, 0u);
       if (!wait_bar(bar1, n_bar1 & 1u, s_abort)) *s_abort = 1u;
       ++n_bar1;
       __syncthreads();
@@ -655,7 +697,7 @@ __global__ void __launch_bounds__(kThreads, 1) m3_fwd_kernel(const __grid_consta
     }
 #pragma unroll
     for (int e = 0; e < 32; ++e) a.final_ssm[(sh * kP + 32 * half + e) * kN + row] = hs[e];
-    if (bad) *s_range = 1u;
+    if (!(amax <= kF16Max)) *s_range = 1u;
     __syncthreads();
     if (*s_range) {
       // an fp16 operand overflowed: this (sequence, head) again, token by token
@@ -666,11 +708,13 @@ __global__ void __launch_bounds__(kThreads, 1) m3_fwd_kernel(const __grid_consta
     }
   }
   // ---- teardown
+  asm volatile("cp.async.wait_group 0;" ::: "memory");
   if (aborted && tid == 0) {
     atomicAdd(&g_m3_timeouts, 1u);
     // what was issued last completes before its TMEM is released
     if (n_bar0 > 0) drain_bar(bar0, (n_bar0 - 1) & 1u);
     if (n_bar1 > 0) drain_bar(bar1, (n_bar1 - 1) & 1u);
+    if (n_bar2 < n_pref) drain_bar(bar2, n_bar2 & 1u);  // a raw copy in flight
   }
   tc_fence_before();
   __syncthreads();

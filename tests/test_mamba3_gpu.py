@@ -72,7 +72,7 @@ def test_ragged_edges():
     compare(b, run_gpu(b, dev), "ragged")
 
 
-@pytest.mark.parametrize("R", [0, 1, 64])
+@pytest.mark.parametrize("R", [0, 1, 6, 34, 40, 64])
 def test_rotary_widths(R):
     dev = device()
     b = W.mamba3_batch(seed=12, lengths=[300, 97], heads=3, rot_dim=R)
