@@ -85,6 +85,18 @@ def prefill_call_bytes(wl: W.Workload, act_b=2):
             + (n + resumed) * state + norm_bytes(T, d, act_b))
 
 
+def mamba3_bytes(b) -> int:
+    """Algorithmic bytes of one Mamba-3 SISO forward call: every input read once, the
+    output and the four final states written once (page "Mamba-3 SISO Long-Ragged
+    Multi-Chunk Joint States Full VJP", dtype paragraph: bf16 q, k, v, trap, angles, z,
+    output, final angle and v; fp32 adt, dt, biases, d, final state and k)."""
+    T, H, P, N, R = b.rows, b.heads, b.headdim, b.d_state, b.rot_dim
+    n = len(b.cu_seqlens) - 1
+    reads = 2 * T * N * 2 + 2 * T * H * P * 2 + T * H * (4 + 4 + 2) + T * R * 2 + 2 * H * N * 4 + H * 4
+    writes = T * H * P * 2 + n * H * (R * 2 + P * N * 4 + N * 4 + P * 2)
+    return reads + writes
+
+
 def decode_bytes_per_seq(d: W.Dims, act_b=2):
     return (2 * d.heads * d.headdim * d.d_state * 4 + 2 * (d.conv_kernel - 1) * d.conv_dim * act_b
             + d.conv_dim * act_b + 2 * d.d_inner * act_b + d.heads * act_b)
@@ -436,6 +448,59 @@ def time_prefill_config(wl: W.Workload, dev, reps, hbm, tf_sus, warm_reps=10):
             "roofline": "max(algorithmic bytes / measured HBM, SSD flops / sustained bf16)", **res}
 
 
+def time_mamba3(dev, reps, hbm, seed=5):
+    """The Mamba-3 SISO forward on the page's frozen shapes (one seeded batch of 3-5
+    sequences), one kernel per call replayed from a CUDA graph: L2 flushed before each
+    call and warm, median of `reps` event intervals."""
+    import selective_scan_gb300 as ss
+    b = W.mamba3_batch(seed=seed)
+    n = len(b.cu_seqlens) - 1
+    H, P, N, R = b.heads, b.headdim, b.d_state, b.rot_dim
+    ins = [t.to(dev).contiguous() for t in b.tensors()]
+    out = torch.empty((b.rows, H, P), dtype=torch.bfloat16, device=dev)
+    fa = torch.empty((n, H, R), dtype=torch.bfloat16, device=dev)
+    fs = torch.empty((n, H, P, N), dtype=torch.float32, device=dev)
+    fk = torch.empty((n, H, N), dtype=torch.float32, device=dev)
+    fv = torch.empty((n, H, P), dtype=torch.bfloat16, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+
+    def call():
+        ss.mamba3_siso_varlen_forward(out, fa, fs, fk, fv, *ins, b.cu_seqlens)
+
+    for _ in range(5):
+        call()
+    torch.cuda.synchronize()
+    digest = output_digest(out)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        call()
+    res = {}
+    for mode in ("l2_flushed", "warm"):
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+        torch.cuda.synchronize()
+        for e0, e1 in evs:
+            if mode == "l2_flushed":
+                flush.fill_(1)
+            e0.record()
+            graph.replay()
+            e1.record()
+        torch.cuda.synchronize()
+        ts = sorted(e0.elapsed_time(e1) * 1e3 for e0, e1 in evs)
+        res[mode] = {"us_median": statistics.median(ts), "us_min": ts[0], "us_max": ts[-1]}
+    if output_digest(out) != digest:
+        raise SystemExit("mamba3 output changed between calls")
+    nbytes = mamba3_bytes(b)
+    floor_us = nbytes / (hbm * 1e9) * 1e6
+    for r in res.values():
+        r["tokens_per_s"] = b.rows / (r["us_median"] * 1e-6)
+        r["GB/s"] = nbytes / (r["us_median"] * 1e-6) / 1e9
+        r["roofline_frac"] = floor_us / r["us_median"]
+    return {"workload": b.name, "tokens": b.rows, "lengths": [b.cu_seqlens[i + 1] - b.cu_seqlens[i] for i in range(n)],
+            "algorithmic_bytes": nbytes, "roofline_us": floor_us, "reps": reps,
+            "launch": "one kernel per call, replayed from a CUDA graph", "roofline": "algorithmic bytes / measured HBM",
+            "output_sha256": digest, **res}
+
+
 def cpu_baseline(target_s=12.0):
     """The oracle, as it stands, on a bounded prefix of the same workload."""
     import oracle
@@ -632,6 +697,9 @@ def run_ours(args, rank, world, local_rank):
         "prefill_130m_2048": time_prefill_config(W.prefill_130m(), dev, args.config_reps, hbm, tf_sus),
         "varlen_130m_8seq": time_prefill_config(W.varlen_130m(), dev, args.config_reps, hbm, tf_sus),
     }
+
+    # the Mamba-3 SISO forward on the page's frozen shapes, timed alone
+    configs["mamba3_siso_frozen"] = time_mamba3(dev, args.config_reps, hbm)
 
     # the layer's projections around the path (tcgen05 GEMMs), timed alone
     proj = time_projections(dev, T, d, reps=max(3, args.steps // 20), tf_peak=tf_burst)

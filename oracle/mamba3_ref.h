@@ -8,8 +8,10 @@
  * VJP", its list of the reference's forward steps (1-7) and its dtypes. Where
  * the page leaves a step open this file takes the readings listed in the
  * design notes (the form of the shifted-QK correction, the rotary pairing, the
- * final K state). All arithmetic is double; the SSM state is not rounded
- * between tokens (the page asks for no rounding there).
+ * final K state). Those three have no passage to pin against: parity unpinned
+ * for them (the tests pin this file to the readings, not to the page). All
+ * arithmetic is double; the SSM state is not rounded between tokens (the page
+ * asks for no rounding there).
  *
  *   out          [T, H, P] bf16     gated output
  *   final_angle  [S, H, R] bf16     cumulative rotary angle at each sequence's last token

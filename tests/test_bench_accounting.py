@@ -57,3 +57,17 @@ def test_prefill_call_bytes_with_states():
     assert wl.batch.rows == 16_407 and sum(1 for f in wl.batch.fresh if not f) == 4
     per_seq = 3 * 1792 * 2 + 24 * 64 * 128 * 4
     assert bench.prefill_call_bytes(wl) == 16_407 * 23_088 + (8 + 4) * per_seq
+
+
+def test_mamba3_bytes_frozen_batch():
+    # Mamba-3 SISO forward, seed-5 frozen batch: 5 sequences, 3 109 tokens, 32 heads x 64,
+    # Q/K width 128, 32 angles. Inputs: q, k [T,128] bf16; v, z [T,32,64] bf16; adt, dt
+    # [T,32] f32; trap [T,32] bf16; angles [T,32] bf16; biases [32,128] f32; d [32] f32.
+    # Outputs: out [T,32,64] bf16; per (sequence, head) angle 32 bf16, state 64x128 f32,
+    # k 128 f32, v 64 bf16.
+    b = W.mamba3_batch(seed=5)
+    assert b.rows == 3109 and len(b.cu_seqlens) == 6
+    reads = 2 * 3109 * 128 * 2 + 2 * 3109 * 32 * 64 * 2 + 3109 * 32 * (4 + 4 + 2) + 3109 * 32 * 2 + 2 * 32 * 128 * 4 + 32 * 4
+    writes = 3109 * 32 * 64 * 2 + 5 * 32 * (32 * 2 + 64 * 128 * 4 + 128 * 4 + 64 * 2)
+    assert (reads, writes) == (28_287_488, 18_089_984)
+    assert bench.mamba3_bytes(b) == 46_377_472
