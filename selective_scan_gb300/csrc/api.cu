@@ -113,6 +113,8 @@ ScanPlan plan_scan(const mamba2_dims* d, mamba2_dtype act, const mamba2_recurren
   // about two chunks of fill and drain per CTA. On the tcgen05 path the state
   // pass may cut each segment into several pieces (one entry each, folded in
   // order by the full pass), so that its CTAs fill the SMs the segments leave.
+  // the tcgen05 state pass serves two heads of one group per CTA
+  const int64_t state_ctas_per_piece = (tc && (d->heads / d->ngroups) % 2 == 0) ? d->heads / 2 : d->heads;
   std::vector<int64_t> ch(n);
   for (int i = 0; i < n; ++i) ch[i] = (rb->cu_seqlens[i + 1] - rb->cu_seqlens[i] + Q - 1) / Q;
   std::sort(ch.begin(), ch.end(), std::greater<int64_t>());
@@ -129,7 +131,7 @@ ScanPlan plan_scan(const mamba2_dims* d, mamba2_dtype act, const mamba2_recurren
     if (extra > 0) {
       state_cost = 1e300;
       for (int P = 1; P <= (tc ? std::min<int64_t>(kMaxStatePieces, sc) : 1); ++P) {  // no empty piece
-        const int64_t state_waves = (d->heads * extra * P + nsm - 1) / nsm;
+        const int64_t state_waves = (state_ctas_per_piece * extra * P + nsm - 1) / nsm;
         const double c = (double)state_waves * (0.35 * (double)((sc + P - 1) / P) + 1.0);
         if (c < state_cost - 1e-9) {
           state_cost = c;

@@ -127,22 +127,24 @@ static_assert(kFullSmem <= 232448, "full-pass shared memory plan exceeds 227 KB"
 // recomputed token by token (fp16 holds up to 65 504)
 constexpr float kF16Limit = 65504.0f;
 
-// ---- state pass: shared memory (4 stages of X, 3 of B), TMEM D = [hi part | lo part] in [0,128).
-// An X stage is free once X o w has read it, a B stage once the dH product has,
-// so the X loads (from HBM) run a chunk further ahead than the B loads (L2).
-constexpr int kStNX = 4;                               // X stages (chunk i in i % 4)
-constexpr int kStNB = 3;                               // B stages (chunk i in i % 3)
-constexpr int kStNW = 2;                               // token-weight buffers (chunk i in i % 2)
-constexpr uint32_t kStOffB = kStNX * kTileX;
-constexpr uint32_t kStOffXW = kStOffB + kStNB * kTileB;  // [2][hi, lo] X o w tiles
-constexpr uint32_t kStOffW = kStOffXW + 4 * kTileX;      // [kStNW][TQ] token weights
-constexpr uint32_t kStOffR = kStOffW + kStNW * TQ * 4;   // total log2 decay of the segment
+// ---- state pass: two heads of one group per CTA (they share the B tile and
+// one N = 256 product per chunk); TMEM D = [head 0 hi | lo | head 1 hi | lo].
+// A stage holds, per head, the X tile (X o w hi is written over it in place)
+// and the X o w lo tile: four 64-column blocks 16 KB apart, which is the
+// product's B operand as it stands. A stage is free once the product of its
+// chunk is done.
+constexpr int kStStages = 2;                            // chunk i in stage i % 2
+constexpr uint32_t kStHeadTile = 2 * kTileX;            // [X, then X o w hi | X o w lo] of one head
+constexpr uint32_t kStStage = 2 * kStHeadTile;          // two heads
+constexpr uint32_t kStOffB = kStStages * kStStage;      // B stages
+constexpr uint32_t kStOffW = kStOffB + kStStages * kTileB;  // [2 buffers][2 heads][TQ] token weights
+constexpr uint32_t kStOffR = kStOffW + 2 * 2 * TQ * 4;  // [2 heads] total log2 decay of the piece
 constexpr uint32_t kStOffBar = kStOffR + 16;
-enum StateBar : int {  // + chunk % 4 (X stages, X o w ready), % 3 (B stages, dH done) or % 2 (weights)
-  kStFullX = 0, kStFullB = 4, kStDHDone = 7, kStXWReady = 10, kStWReady = 14, kNumStateBars = 16
+enum StateBar : int {  // + chunk % 2
+  kStFullX = 0, kStFullB = 2, kStDHDone = 4, kStXWReady = 6, kStWReady = 8, kNumStateBars = 10
 };
 constexpr uint32_t kStOffMisc = kStOffBar + 8 * kNumStateBars;
-constexpr uint32_t kStateSmem = kStOffMisc + 16 + 1024;
+constexpr uint32_t kStateSmem = kStOffMisc + 16;  // the base is 1024-byte aligned (checked)
 static_assert(kStateSmem <= 232448, "state-pass shared memory plan exceeds 227 KB");
 
 
@@ -884,23 +886,33 @@ ssd_tc_full(const __grid_constant__ ScanArgs a, const __grid_constant__ CUtensor
 }
 
 // State pass: end state (from zero; the first segment from the slot's state)
-// and total log-decay of every segment but the last. Chunks are read last to
-// first; with R the log2 decay of the chunks already read, token j's weight is
-// w_j = 2^(R + S_end - S_j) dt'_j (S the chunk's cumulative log2 decay), so
-// B^T . (X o w) of every chunk accumulates into the same TMEM columns.
-//   warps 0-15  X o w (bf16 hi + lo); at the end, the segment's state
-//   warp 16     X tile loads (four stages)
-//   warp 17     B tile loads (three stages)
-//   warp 18     dH^T += B^T . [X o w hi | lo]  (M=128 N=128 K=128 per chunk)
-//   warp 19     dt' and the token weights, up to two chunks ahead
+// and total log-decay of every segment but the last, for two heads of one
+// group per CTA (heads 2 y and 2 y + 1; one head when the group has an odd
+// number of heads). Chunks are read last to first; with R the log2 decay of
+// the chunks already read, token j's weight is w_j = 2^(R + S_end - S_j) dt'_j
+// (S the chunk's cumulative log2 decay, per head), so B^T . (X o w) of every
+// chunk accumulates into the same TMEM columns.
+//   warps 0-15  X o w (bf16 hi + lo) of both heads; at the end, the pieces' states
+//   warp 16     X tile loads (two heads, two stages)
+//   warp 17     B tile loads (two stages)
+//   warp 18     dH^T += B^T . [X o w hi | lo | X o w hi | lo]  (M=128 N=256 K=128 per chunk)
+//   warp 19     dt' and the token weights of both heads, up to two chunks ahead
 __global__ void __launch_bounds__(kStateThreads, 1)
 ssd_tc_state(const __grid_constant__ ScanArgs a, const __grid_constant__ CUtensorMap tm, const int use_tma) {
-  // CTA b: piece q = b % P of segment b / P, an equal share of the segment's
-  // chunks; its entry (index b) is the piece's end state from zero (the first
-  // piece of a sequence's first segment from the slot) and total log-decay
+  // CTA (b, y): piece q = b % P of segment b / P, an equal share of the segment's
+  // chunks, for heads h0 = hpc y and h0 + 1; its entry (index b) is the piece's end
+  // state from zero (the first piece of a sequence's first segment from the slot)
+  // and total log-decay
   const int P = a.state_pieces > 0 ? a.state_pieces : 1;
   const int entry = blockIdx.x, q = entry % P;
+  const int H = a.heads;
+  const int hpc = ((H / a.ngroups) & 1) == 0 ? 2 : 1;  // heads per CTA (never across a group)
+  const int h0 = hpc * (int)blockIdx.y;
+  const int nh = hpc;                                   // heads this CTA writes
   Cta ci = cta_info(a, entry / P);
+  ci.h = h0;
+  ci.x_col = h0 * TP;
+  ci.b_col = H * TP + (h0 / (H / a.ngroups)) * TN;  // both heads' group
   if (ci.k == ci.nseg - 1) return;  // the last segment has no entry (the full pass ends it)
   {
     // balanced shares: sizes differ by at most one chunk, none empty while P <= chunks
@@ -910,45 +922,48 @@ ssd_tc_state(const __grid_constant__ ScanArgs a, const __grid_constant__ CUtenso
     ci.c_end = pe;
     ci.n = pe - pb;
   }
-  const int H = a.heads;
+  const int x_col1 = (h0 + nh - 1) * TP;  // the second head's x columns (the first's again when one head)
+  float A2h[2];
+  A2h[0] = expf(a.A_log[h0]) * 1.4426950408889634f;
+  A2h[1] = expf(a.A_log[h0 + nh - 1]) * 1.4426950408889634f;
   if (ci.n == 0) {  // an empty piece (only when a segment has fewer than P chunks): zero state, zero decay
-    float* dst = a.ws_state + ((int64_t)entry * H + ci.h) * TP * TN;
-    for (int i = threadIdx.x; i < TP * TN; i += blockDim.x) dst[i] = 0.0f;
-    if (threadIdx.x == 0) a.ws_decay[(int64_t)entry * H + ci.h] = 0.0f;
+    for (int hh = 0; hh < nh; ++hh) {
+      float* dst = a.ws_state + ((int64_t)entry * H + h0 + hh) * TP * TN;
+      for (int i = threadIdx.x; i < TP * TN; i += blockDim.x) dst[i] = 0.0f;
+      if (threadIdx.x == 0) a.ws_decay[(int64_t)entry * H + h0 + hh] = 0.0f;
+    }
     return;
   }
-  extern __shared__ unsigned char smem_raw[];
-  const uint32_t raw_base = su32(smem_raw);
-  unsigned char* smem = smem_raw + (((raw_base + 1023u) & ~1023u) - raw_base);
+  extern __shared__ __align__(1024) unsigned char smem[];
   const uint32_t sbase = su32(smem);
+  if ((sbase & 1023u) != 0) {  // the swizzled operand tiles need a 1024-byte aligned base
+    if (threadIdx.x == 0) atomicAdd(&g_tc_timeouts, 1u);
+    return;
+  }
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + kStOffMisc);
   volatile uint32_t* s_abort = reinterpret_cast<volatile uint32_t*>(smem + kStOffMisc + 4);
   float* s_w = reinterpret_cast<float*>(smem + kStOffW);
   float* s_R = reinterpret_cast<float*>(smem + kStOffR);
   auto bar = [&](int id) { return sbase + kStOffBar + 8u * (uint32_t)id; };
-  auto stg_x = [&](int i) { return sbase + (uint32_t)(i % kStNX) * kTileX; };
-  auto stg_b = [&](int i) { return sbase + kStOffB + (uint32_t)(i % kStNB) * kTileB; };
-  auto p3 = [](int i) { return (uint32_t)((i / 3) & 1); };   // phase parity on a [3] barrier
-  auto p4 = [](int i) { return (uint32_t)((i >> 2) & 1); };  // phase parity on a [4] barrier
+  auto stg_x = [&](int i) { return sbase + (uint32_t)(i & 1) * kStStage; };
+  auto stg_b = [&](int i) { return sbase + kStOffB + (uint32_t)(i & 1) * kTileB; };
   auto p2 = [](int i) { return (uint32_t)((i >> 1) & 1); };  // phase parity on a [2] barrier
 
   const int n = ci.n;  // >= 1 here
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
   if (warp == 0) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 128;" :: "r"(su32(s_tmem)));
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 256;" :: "r"(su32(s_tmem)));
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
   }
   if (tid == kMathThreads) {
-    for (int s = 0; s < kStNB; ++s) {
-      mbar_init(bar(kStFullB + s), 1);
-      mbar_init(bar(kStDHDone + s), 1);
-    }
-    for (int b = 0; b < kStNX; ++b) {
-      mbar_init(bar(kStFullX + b), 1);
+    for (int b = 0; b < kStStages; ++b) {
+      mbar_init(bar(kStFullX + b), 2);  // one tile per head
+      mbar_init(bar(kStFullB + b), 1);
+      mbar_init(bar(kStDHDone + b), 1);
       mbar_init(bar(kStXWReady + b), kMathWarps);
+      mbar_init(bar(kStWReady + b), 1);
     }
-    for (int b = 0; b < kStNW; ++b) mbar_init(bar(kStWReady + b), 1);
     *s_abort = 0u;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -969,142 +984,153 @@ ssd_tc_state(const __grid_constant__ ScanArgs a, const __grid_constant__ CUtenso
   };
 
   if (warp < kMathWarps) {
-    // =================== X o w of every chunk, then the segment's state
+    // =================== X o w of every chunk (both heads), then the pieces' states
     const int row = tid & 127, cg = tid >> 7, qrt = warp & 3;
     const uint32_t lane_off = (uint32_t)(qrt * 32) << 16;
-    const int64_t head_off = (int64_t)ci.h * TP * TN;
-    auto ws_entry = [&](int segidx) -> float* { return a.ws_state + (int64_t)segidx * H * TP * TN + head_off; };
     bool live = true;
     for (int i = 0; i < n; ++i) {
-      bool ok = warp_wait(bar(kStFullX + (i & 3)), p4(i), s_abort) &&
-                warp_wait(bar(kStWReady + (i & 1)), p2(i), s_abort);
-      if (ok && i >= 2) ok = warp_wait(bar(kStDHDone + (i - 2) % kStNB), p3(i - 2), s_abort);  // X o w buffer read
-      if (!ok) {
+      if (!(warp_wait(bar(kStFullX + (i & 1)), p2(i), s_abort) && warp_wait(bar(kStWReady + (i & 1)), p2(i), s_abort))) {
         live = false;
         break;
       }
-      const float w = s_w[(i & 1) * TQ + row];
-      const unsigned char* xt = smem + (uint32_t)(i % kStNX) * kTileX;
-      unsigned char* xw = smem + kStOffXW + (uint32_t)(i & 1) * 2 * kTileX;
 #pragma unroll
-      for (int q = 0; q < 2; ++q) {
-        const uint32_t o = tile_off(row, 16 * cg + 8 * q, TQ);
-        const uint4 xv = *reinterpret_cast<const uint4*>(xt + o);
-        const uint32_t xr[4] = {xv.x, xv.y, xv.z, xv.w};
-        uint32_t hi[4], lo[4];
+      for (int hh = 0; hh < 2; ++hh) {
+        const float w = s_w[((i & 1) * 2 + hh) * TQ + row];
+        unsigned char* xt = smem + (uint32_t)(i & 1) * kStStage + (uint32_t)hh * kStHeadTile;
 #pragma unroll
-        for (int e = 0; e < 4; ++e)
-          split2(__uint_as_float(xr[e] << 16) * w, __uint_as_float(xr[e] & 0xffff0000u) * w, hi[e], lo[e]);
-        *reinterpret_cast<uint4*>(xw + o) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-        *reinterpret_cast<uint4*>(xw + kTileX + o) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+        for (int qq = 0; qq < 2; ++qq) {
+          const uint32_t o = tile_off(row, 16 * cg + 8 * qq, TQ);
+          const uint4 xv = *reinterpret_cast<const uint4*>(xt + o);
+          const uint32_t xr[4] = {xv.x, xv.y, xv.z, xv.w};
+          uint32_t hi[4], lo[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            split2(__uint_as_float(xr[e] << 16) * w, __uint_as_float(xr[e] & 0xffff0000u) * w, hi[e], lo[e]);
+          // in place: each element is read and rewritten by this thread only
+          *reinterpret_cast<uint4*>(xt + o) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+          *reinterpret_cast<uint4*>(xt + kTileX + o) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+        }
       }
       fence_async_smem();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(kStXWReady + (i & 3)));
+      if (lane == 0) mbar_arrive(bar(kStXWReady + (i & 1)));
     }
-    if (live && warp_wait(bar(kStDHDone + (n - 1) % kStNB), p3(n - 1), s_abort)) {
+    if (live && warp_wait(bar(kStDHDone + ((n - 1) & 1)), p2(n - 1), s_abort)) {
       tc_fence_after();
-      float dhi[16], dlo[16];
-      tmem_ld16x2(tmem + lane_off + 16 * cg, tmem + lane_off + 64 + 16 * cg, dhi, dlo);
-      const float Rt = *s_R;  // written before the weights of the last chunk were published
-      float* dst = ws_entry(entry);
-      if (ci.k == 0 && q == 0 && !ci.fresh) {
-        // the first piece starts from the slot's state: add its decayed share, and
-        // leave a copy of it for the full pass (whose last segment overwrites the slot)
-        // in the first entry of the last segment, which has no entries of its own
-        const float d = ex2(Rt);
-        const float* slot_ptr = a.ssm_state + (int64_t)seq_slot(a.tab, ci.sq) * H * TP * TN + head_off;
-        float* copy = ws_entry((ci.seg0 + ci.nseg - 1) * P);
+      for (int hh = 0; hh < nh; ++hh) {
+        const int h = h0 + hh;
+        float dhi[16], dlo[16];
+        tmem_ld16x2(tmem + lane_off + 128u * (uint32_t)hh + 16 * cg, tmem + lane_off + 128u * (uint32_t)hh + 64 + 16 * cg,
+                    dhi, dlo);
+        const float Rt = s_R[hh];  // written before the weights of the last chunk were published
+        const int64_t head_off = (int64_t)h * TP * TN;
+        float* dst = a.ws_state + (int64_t)entry * H * TP * TN + head_off;
+        if (ci.k == 0 && q == 0 && !ci.fresh) {
+          // the first piece starts from the slot's state: add its decayed share, and
+          // leave a copy of it for the full pass (whose last segment overwrites the slot)
+          // in the first entry of the last segment, which has no entries of its own
+          const float d = ex2(Rt);
+          const float* slot_ptr = a.ssm_state + (int64_t)seq_slot(a.tab, ci.sq) * H * TP * TN + head_off;
+          float* copy = a.ws_state + (int64_t)((ci.seg0 + ci.nseg - 1) * P) * H * TP * TN + head_off;
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const float h0 = slot_ptr[(int64_t)(16 * cg + i) * TN + row];
-          copy[(int64_t)(16 * cg + i) * TN + row] = h0;
-          dst[(int64_t)(16 * cg + i) * TN + row] = fmaf(d, h0, dhi[i] + dlo[i]);
+          for (int i = 0; i < 16; ++i) {
+            const float hv = slot_ptr[(int64_t)(16 * cg + i) * TN + row];
+            copy[(int64_t)(16 * cg + i) * TN + row] = hv;
+            dst[(int64_t)(16 * cg + i) * TN + row] = fmaf(d, hv, dhi[i] + dlo[i]);
+          }
+        } else {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) dst[(int64_t)(16 * cg + i) * TN + row] = dhi[i] + dlo[i];
         }
-      } else {
-#pragma unroll
-        for (int i = 0; i < 16; ++i) dst[(int64_t)(16 * cg + i) * TN + row] = dhi[i] + dlo[i];
+        if (tid == 0) a.ws_decay[(int64_t)entry * H + h] = Rt * 0.6931471805599453f;
       }
-      if (tid == 0) a.ws_decay[(int64_t)entry * H + ci.h] = Rt * 0.6931471805599453f;
     }
   } else if (warp == kMathWarps) {
-    // =================== X tile loads: stage i % 4 is free once X o w of chunk i - 4 is done
+    // =================== X tile loads of both heads: stage i % 2 is free once the product of chunk i - 2 is done
     int loaded = 0;
     for (int i = 0; i < n; ++i) {
-      if (i >= kStNX && !warp_wait(bar(kStXWReady + (i & 3)), p4(i - kStNX), s_abort)) break;
-      load_tile(stg_x(i), chunk_src(i), &tm, use_tma != 0, ci.x_col, TP, bar(kStFullX + (i & 3)), lane);
+      if (i >= kStStages && !warp_wait(bar(kStDHDone + (i & 1)), p2(i - kStStages), s_abort)) break;
+      load_tile(stg_x(i), chunk_src(i), &tm, use_tma != 0, ci.x_col, TP, bar(kStFullX + (i & 1)), lane);
+      load_tile(stg_x(i) + kStHeadTile, chunk_src(i), &tm, use_tma != 0, x_col1, TP, bar(kStFullX + (i & 1)), lane);
       loaded = i + 1;
     }
     if (lane == 0 && *s_abort)
-      for (int i = max(0, loaded - kStNX); i < loaded; ++i) drain_bar(bar(kStFullX + (i & 3)), p4(i));
+      for (int i = max(0, loaded - kStStages); i < loaded; ++i) drain_bar(bar(kStFullX + (i & 1)), p2(i));
   } else if (warp == kMathWarps + 1) {
-    // =================== B tile loads: stage i % 3 is free once the dH product of chunk i - 3 is done
+    // =================== B tile loads: stage i % 2 is free once the product of chunk i - 2 is done
     int loaded = 0;
     for (int i = 0; i < n; ++i) {
-      if (i >= kStNB && !warp_wait(bar(kStDHDone + i % kStNB), p3(i - kStNB), s_abort)) break;
-      load_tile(stg_b(i), chunk_src(i), &tm, use_tma != 0, ci.b_col, TN, bar(kStFullB + i % kStNB), lane);
+      if (i >= 2 && !warp_wait(bar(kStDHDone + (i & 1)), p2(i - 2), s_abort)) break;
+      load_tile(stg_b(i), chunk_src(i), &tm, use_tma != 0, ci.b_col, TN, bar(kStFullB + (i & 1)), lane);
       loaded = i + 1;
     }
     if (lane == 0 && *s_abort)
-      for (int i = max(0, loaded - kStNB); i < loaded; ++i) drain_bar(bar(kStFullB + i % kStNB), p3(i));
+      for (int i = max(0, loaded - 2); i < loaded; ++i) drain_bar(bar(kStFullB + (i & 1)), p2(i));
   } else if (warp == kMathWarps + 2) {
-    // =================== dH^T += B^T . [X o w hi | X o w lo] (one N=128 product per chunk)
+    // =================== dH^T += B^T . [X o w hi | lo | hi | lo] (one N=256 product per chunk)
     if (lane == 0) {
       int last = -1;
       for (int i = 0; i < n; ++i) {
-        if (!wait_bar(bar(kStFullB + i % kStNB), p3(i), s_abort)) break;
-        if (!wait_bar(bar(kStXWReady + (i & 3)), p4(i), s_abort)) break;
+        if (!wait_bar(bar(kStFullB + (i & 1)), p2(i), s_abort)) break;
+        if (!wait_bar(bar(kStXWReady + (i & 1)), p2(i), s_abort)) break;
         tc_fence_after();
         const uint64_t bt0 = sdesc(stg_b(i), TQ * 128, 1024);
-        const uint64_t xw0 = sdesc(sbase + kStOffXW + (uint32_t)(i & 1) * 2 * kTileX, kTileX, 1024);  // hi | lo blocks
+        const uint64_t xw0 = sdesc(stg_x(i), kTileX, 1024);  // four 64-column blocks 16 KB apart
 #pragma unroll
         for (int s2 = 0; s2 < TQ / 16; ++s2) {
           const uint32_t jk = (s2 * 2048) >> 4;
-          mma_ss(tmem, bt0 + jk, xw0 + jk, idesc128(128, 1, 1), (i > 0 || s2 > 0) ? 1u : 0u);
+          mma_ss(tmem, bt0 + jk, xw0 + jk, idesc128(256, 1, 1), (i > 0 || s2 > 0) ? 1u : 0u);
         }
-        mma_commit(bar(kStDHDone + i % kStNB));
+        mma_commit(bar(kStDHDone + (i & 1)));
         last = i;
       }
-      if (last >= 0) drain_bar(bar(kStDHDone + last % kStNB), p3(last));
+      if (last >= 0) drain_bar(bar(kStDHDone + (last & 1)), p2(last));
     }
   } else {
-    // =================== dt' and token weights of chunk i into buffer i % 2
-    // (lane l: tokens 4l .. 4l+3); buffer i % 2 last served chunk i-2
-    // dt' of chunks i .. i+3, loaded four chunks ahead
+    // =================== dt' and token weights of chunk i, both heads, into buffer
+    // i % 2 (lane l: tokens 4l .. 4l+3); buffer i % 2 last served chunk i-2
     const int64_t rows_all = a.tab.cu[a.tab.n];
-    auto load_dtp = [&](int i) {
+    auto load_dtp = [&](int i, int h) {
       DtQuad r = {{0.f, 0.f, 0.f, 0.f}};
       if (i < n) {
         const int c = ci.c_end - 1 - i, len = min(TQ, ci.T - c * TQ);
-        const float* src = a.dtp + (int64_t)ci.h * rows_all + ci.row0 + (int64_t)c * TQ;
+        const float* src = a.dtp + (int64_t)h * rows_all + ci.row0 + (int64_t)c * TQ;
 #pragma unroll
         for (int e = 0; e < 4; ++e)
           if (4 * lane + e < len) r.v[e] = src[4 * lane + e];
       }
       return r;
     };
-    float R = 0.f;  // log2 decay from the end of the chunks already read to the segment end
-    DtQuad r0 = load_dtp(0), r1 = load_dtp(1), r2 = load_dtp(2), r3 = load_dtp(3);
+    const int hB = h0 + nh - 1;
+    float R[2] = {0.f, 0.f};  // log2 decay from the end of the chunks already read to the piece's end
+    DtQuad a0 = load_dtp(0, h0), a1 = load_dtp(1, h0), b0 = load_dtp(0, hB), b1 = load_dtp(1, hB);
     for (int i = 0; i < n; ++i) {
-      if (i >= kStNW && !warp_wait(bar(kStXWReady + ((i - kStNW) & 3)), p4(i - kStNW), s_abort)) break;
-      float dp[4], S[4], run = 0.f;
+      if (i >= 2 && !warp_wait(bar(kStXWReady + (i & 1)), p2(i - 2), s_abort)) break;
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        dp[e] = r0.v[e];
-        run -= ci.A2 * dp[e];
-        S[e] = run;
+      for (int hh = 0; hh < 2; ++hh) {
+        const DtQuad& r = hh == 0 ? a0 : b0;
+        float dp[4], S[4], run = 0.f;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          dp[e] = r.v[e];
+          run -= A2h[hh] * dp[e];
+          S[e] = run;
+        }
+        const float incl = warp_incl_sum(run, lane);
+        const float tot = __shfl_sync(0xffffffffu, incl, 31);
+        const float base = R[hh] + (tot - (incl - run));  // R + S_end - (S before this lane's tokens)
+        *reinterpret_cast<float4*>(s_w + ((i & 1) * 2 + hh) * TQ + 4 * lane) = make_float4(
+            ex2(base - S[0]) * dp[0], ex2(base - S[1]) * dp[1], ex2(base - S[2]) * dp[2], ex2(base - S[3]) * dp[3]);
+        R[hh] += tot;
       }
-      r0 = r1;
-      r1 = r2;
-      r2 = r3;
-      r3 = load_dtp(i + 4);
-      const float incl = warp_incl_sum(run, lane);
-      const float tot = __shfl_sync(0xffffffffu, incl, 31);
-      const float base = R + (tot - (incl - run));  // R + S_end - (S before this lane's tokens)
-      *reinterpret_cast<float4*>(s_w + (i & 1) * TQ + 4 * lane) =
-          make_float4(ex2(base - S[0]) * dp[0], ex2(base - S[1]) * dp[1], ex2(base - S[2]) * dp[2], ex2(base - S[3]) * dp[3]);
-      R += tot;
-      if (i == n - 1 && lane == 0) *s_R = R;
+      a0 = a1;
+      b0 = b1;
+      a1 = load_dtp(i + 2, h0);
+      b1 = load_dtp(i + 2, hB);
+      if (i == n - 1 && lane == 0) {
+        s_R[0] = R[0];
+        s_R[1] = R[1];
+      }
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(kStWReady + (i & 1)));
     }
@@ -1113,7 +1139,7 @@ ssd_tc_state(const __grid_constant__ ScanArgs a, const __grid_constant__ CUtenso
   tc_fence_before();
   __syncthreads();
   if (tid == 0 && *s_abort) atomicAdd(&g_tc_timeouts, 1u);
-  if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 128;" :: "r"(tmem));
+  if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 256;" :: "r"(tmem));
 }
 
 // Tensor map over xbc [rows][conv_dim] bf16: boxes of 64 columns x TQ rows,
@@ -1170,7 +1196,9 @@ cudaError_t launch_scan_tc(const ScanArgs& a, cudaStream_t st) {
   if (segmented) {
     cudaError_t e = cudaFuncSetAttribute(ssd_tc_state, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kStateSmem);
     if (e != cudaSuccess) return e;
-    const dim3 sgrid((unsigned)(segs * (a.state_pieces > 0 ? a.state_pieces : 1)), (unsigned)a.heads);
+    // two heads of one group per CTA (one when a group has an odd number of heads)
+    const int hpc = ((a.heads / a.ngroups) & 1) == 0 ? 2 : 1;
+    const dim3 sgrid((unsigned)(segs * (a.state_pieces > 0 ? a.state_pieces : 1)), (unsigned)(a.heads / hpc));
     ssd_tc_state<<<sgrid, kStateThreads, kStateSmem, st>>>(a, tm, use_tma);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;

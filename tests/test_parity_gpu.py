@@ -101,6 +101,17 @@ def test_130m_short_runs_unsegmented():
     _prefill_parity(wl)
 
 
+@pytest.mark.parametrize("H,G", [(8, 2), (6, 2), (5, 1)])
+def test_state_pass_head_pairs(H, G):
+    """Runs long enough to be cut into segments, so the state pass runs: with 8
+    heads in 2 groups its CTAs take heads in pairs that never cross a group; with
+    6 heads in 2 groups or 5 in 1 (an odd number of heads per group) one head each.
+    A resumed sequence seeds the first piece from its slot."""
+    d = W.Dims(H, 64, 128, G, 4)
+    wl = W.make_prefill(f"pairs-{H}x{G}", 71, d, [2600, 1700, 90], torch.bfloat16, 6, [0, 1, 0])
+    _prefill_parity(wl)
+
+
 def test_scan_fp16_range_fallback():
     """Inputs whose Y = M . X operands leave the fp16 range: a token whose C and
     B rows are large and aligned (an M entry near 1.5e5, in every head's
