@@ -32,6 +32,7 @@
 namespace mamba2 {
 
 constexpr int kDecodeWarps = kDecodeThreads / 32;
+static_assert(kDecodeWarps % 4 == 0, "the finish kernel's norm-weight buffer follows the warp sums 16-byte aligned");
 constexpr int kDecodeUnroll = 16;  // state rows in flight per lane (16-byte loads)
 static_assert(kDecodeUnroll == 16, "the d_state = 128 path reduces 16 rows by recursive halving");
 
@@ -65,6 +66,26 @@ decode_step_kernel(const __grid_constant__ DecodeArgs a) {
   const int nh = max(0, h1 - h0);
   const int rows = nh * P;  // state rows owned by this CTA
   const bool dev = a.dev_slots != nullptr;
+  // Launched as a programmatic dependent of whatever precedes it on the stream
+  // (the previous step's finish kernel lets it be scheduled early): only the
+  // model's parameters may be read before this wait; the batch, the token's
+  // inputs, both pools and dst come after it.
+  float A_h = 0.f, D_h = 0.f, bias_h = 0.f;
+  if (threadIdx.x < nh) {
+    A_h = a.A_log[h0 + threadIdx.x];
+    D_h = a.D[h0 + threadIdx.x];
+    bias_h = a.dt_bias[h0 + threadIdx.x];
+  }
+  {
+    // the conv taps and bias of this thread's first conv vector into L1
+    const int nxv0 = rows / V, i0 = threadIdx.x;
+    if (i0 < nxv0 + 2 * G * N / V) {
+      const int c0 = i0 < nxv0 ? h0 * P + i0 * V : d_inner + (i0 - nxv0) * V;
+      asm volatile("prefetch.global.L1 [%0];" ::"l"(a.conv_w + (int64_t)c0 * K));
+      asm volatile("prefetch.global.L1 [%0];" ::"l"(a.conv_b + c0));
+    }
+  }
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   // a device batch: nothing is touched unless the batch check (the launch before) passed
   if (dev && (__ldg(a.dev_status) != 0 || s >= __ldg(a.dev_n))) return;
   const bool fresh = dev ? __ldg(a.dev_fresh + s) != 0 : seq_fresh(a.tab, s);
@@ -85,11 +106,11 @@ decode_step_kernel(const __grid_constant__ DecodeArgs a) {
   // per-head constants, loaded before the conv so their latency overlaps it
   if (threadIdx.x < nh) {
     const int h = h0 + threadIdx.x;
-    const float v = Act<T>::to_f(static_cast<const T*>(a.dt)[(int64_t)s * H + h]) + a.dt_bias[h];
+    const float v = Act<T>::to_f(static_cast<const T*>(a.dt)[(int64_t)s * H + h]) + bias_h;
     const float dtp = softplus_f(v);
     hdt[threadIdx.x] = dtp;
-    hdec[threadIdx.x] = expf(-expf(a.A_log[h]) * dtp);
-    hD[threadIdx.x] = a.D[h];
+    hdec[threadIdx.x] = expf(-expf(A_h) * dtp);
+    hD[threadIdx.x] = D_h;
   }
 
   // ---- state-stream geometry; the first batch of state loads is issued now
@@ -373,7 +394,7 @@ __global__ void __launch_bounds__(kDecodeThreads)
 decode_finish_kernel(const __grid_constant__ DecodeArgs a) {
   constexpr int V = Vec16<T>::n;
   constexpr int HIST = K - 1;
-  extern __shared__ __align__(16) float gbuf[];  // [d_inner] g, then [kDecodeWarps] warp sums
+  extern __shared__ __align__(16) float gbuf[];  // [d_inner] g, [kDecodeWarps] warp sums, [d_inner] norm weight
   const int s = blockIdx.x;
   const bool dev = a.dev_slots != nullptr;
   if (dev && (__ldg(a.dev_status) != 0 || s >= __ldg(a.dev_n))) return;
@@ -384,7 +405,14 @@ decode_finish_kernel(const __grid_constant__ DecodeArgs a) {
   const int conv_dim = d_inner + 2 * G * N;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-  // silu(z) first (this step's input, not written by the state kernel) ...
+  // the next step's state kernel may be scheduled now (it waits for this grid's
+  // completion before it reads anything this grid writes)
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  // the norm weight (a parameter) and silu(z) (this step's input, not written by
+  // the state kernel) first ...
+  float* wbuf = gbuf + d_inner + kDecodeWarps;  // [d_inner] norm weight
+  for (int i = threadIdx.x; i < d_inner / 4; i += kDecodeThreads)
+    reinterpret_cast<float4*>(wbuf)[i] = __ldg(reinterpret_cast<const float4*>(a.norm_w) + i);
   T* row = static_cast<T*>(a.dst) + (int64_t)s * d_inner;
   const T* zrow = static_cast<const T*>(a.z) + (int64_t)s * d_inner;
   for (int i = threadIdx.x; i < d_inner / V; i += kDecodeThreads) {
@@ -397,11 +425,35 @@ decode_finish_kernel(const __grid_constant__ DecodeArgs a) {
   // (y in dst) are visible
   asm volatile("griddepcontrol.wait;" ::: "memory");
 
-  // B/C conv history: older rows move up, the token's B/C becomes the newest row
+  // B/C conv history: older rows move up, the token's B/C becomes the newest row.
+  // Each thread's history rows are loaded first and stored after its y vectors
+  // are loaded, so the two round trips overlap.
   const T* xBC = static_cast<const T*>(a.xBC) + (int64_t)s * conv_dim;
   T* cst = static_cast<T*>(a.conv_state) + slot * HIST * conv_dim;
   const int nbcv = 2 * G * N / V;
-  for (int i = threadIdx.x; i < nbcv && HIST > 0; i += kDecodeThreads) {
+  const int i_bc = threadIdx.x;  // this thread's first history vector
+  uint4 hrow[HIST > 0 ? HIST : 1];
+  if (HIST > 0 && i_bc < nbcv) {
+    const int c0 = d_inner + i_bc * V;
+#pragma unroll
+    for (int j = 0; j + 1 < HIST; ++j)
+      hrow[j] = fresh ? make_uint4(0u, 0u, 0u, 0u) : *reinterpret_cast<const uint4*>(cst + (int64_t)(j + 1) * conv_dim + c0);
+    hrow[HIST > 0 ? HIST - 1 : 0] = *reinterpret_cast<const uint4*>(xBC + c0);
+  }
+
+  // g = y * silu(z) (each thread the same vectors it filled above)
+  for (int i = threadIdx.x; i < d_inner / V; i += kDecodeThreads) {
+    float y[V];
+    Vec16<T>::load(row + i * V, y);
+#pragma unroll
+    for (int j = 0; j < V; ++j) gbuf[i * V + j] *= y[j];
+  }
+  if (HIST > 0 && i_bc < nbcv) {
+    const int c0 = d_inner + i_bc * V;
+#pragma unroll
+    for (int j = 0; j < HIST; ++j) *reinterpret_cast<uint4*>(cst + (int64_t)j * conv_dim + c0) = hrow[j];
+  }
+  for (int i = i_bc + kDecodeThreads; i < nbcv && HIST > 0; i += kDecodeThreads) {  // wider B/C: the rest
     const int c0 = d_inner + i * V;
     const uint4 craw = *reinterpret_cast<const uint4*>(xBC + c0);
 #pragma unroll
@@ -411,14 +463,6 @@ decode_finish_kernel(const __grid_constant__ DecodeArgs a) {
       *reinterpret_cast<uint4*>(cst + (int64_t)j * conv_dim + c0) = nxt;
     }
     *reinterpret_cast<uint4*>(cst + (int64_t)(HIST > 0 ? HIST - 1 : 0) * conv_dim + c0) = craw;
-  }
-
-  // g = y * silu(z) (each thread the same vectors it filled above)
-  for (int i = threadIdx.x; i < d_inner / V; i += kDecodeThreads) {
-    float y[V];
-    Vec16<T>::load(row + i * V, y);
-#pragma unroll
-    for (int j = 0; j < V; ++j) gbuf[i * V + j] *= y[j];
   }
   __syncthreads();
   float* wsum = gbuf + d_inner;
@@ -435,14 +479,9 @@ decode_finish_kernel(const __grid_constant__ DecodeArgs a) {
     for (int w = 0; w < kDecodeWarps; ++w) tot += wsum[w];
     const float inv = rsqrtf(tot / (float)gs + a.eps);
     for (int i = grp * gs / V + threadIdx.x; i < (grp + 1) * gs / V; i += kDecodeThreads) {
-      float o[V], w[V];
+      float o[V];
 #pragma unroll
-      for (int q = 0; q < V / 4; ++q) {
-        const float4 f = __ldg(reinterpret_cast<const float4*>(a.norm_w) + (i * V) / 4 + q);
-        w[4 * q] = f.x; w[4 * q + 1] = f.y; w[4 * q + 2] = f.z; w[4 * q + 3] = f.w;
-      }
-#pragma unroll
-      for (int j = 0; j < V; ++j) o[j] = gbuf[i * V + j] * inv * w[j];
+      for (int j = 0; j < V; ++j) o[j] = gbuf[i * V + j] * inv * wbuf[i * V + j];
       Vec16<T>::store(row + i * V, o);
     }
     __syncthreads();  // wsum is reused by the next group
@@ -516,10 +555,22 @@ static cudaError_t launch_decode_tk(const DecodeArgs& a, cudaStream_t st) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
   }
-  kern<<<dim3((unsigned)a.ctas_per_seq, (unsigned)a.tab.n, 1), kDecodeThreads, smem, st>>>(a);
-  cudaError_t e = cudaGetLastError();
+  // programmatic dependent launch: scheduled while the kernel before it (the
+  // previous step's finish kernel) runs; it waits (griddepcontrol.wait) before
+  // reading anything but the parameters
+  cudaLaunchConfig_t scfg = {};
+  scfg.gridDim = dim3((unsigned)a.ctas_per_seq, (unsigned)a.tab.n, 1);
+  scfg.blockDim = dim3(kDecodeThreads, 1, 1);
+  scfg.dynamicSmemBytes = smem;
+  scfg.stream = st;
+  cudaLaunchAttribute sattr[1];
+  sattr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  sattr[0].val.programmaticStreamSerializationAllowed = 1;
+  scfg.attrs = sattr;
+  scfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&scfg, kern, a);
   if (e != cudaSuccess) return e;
-  const size_t fsmem = sizeof(float) * ((size_t)a.heads * a.headdim + kDecodeWarps);
+  const size_t fsmem = sizeof(float) * (2 * (size_t)a.heads * a.headdim + kDecodeWarps);
   auto fin = decode_finish_kernel<T, K>;
   if (fsmem > 48 * 1024) {
     e = cudaFuncSetAttribute(fin, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)fsmem);
