@@ -300,6 +300,46 @@ __global__ void __launch_bounds__(256) dt_prime_kernel(const __nv_bfloat16* __re
     if (r < rows && h < heads) dtp[(int64_t)h * rows + r] = tile[tx][k];
   }
 }
+// The same, 64 rows x every head per CTA: the rows' dt are one contiguous run
+// (read with coalesced loads), and each head's 64 dt' one contiguous 256-byte
+// run (written with coalesced stores); [head][row] staging in shared memory.
+constexpr int kDtRows = 64;
+__global__ void __launch_bounds__(256) dt_prime_rows_kernel(const __nv_bfloat16* __restrict__ dt,
+                                                           const float* __restrict__ dt_bias, float* __restrict__ dtp,
+                                                           int rows, int heads) {
+  extern __shared__ float dts[];  // [heads][kDtRows + 1]
+  const int r0 = blockIdx.x * kDtRows;
+  const int nr = min(kDtRows, rows - r0);
+  const __nv_bfloat16* src = dt + (int64_t)r0 * heads;
+  // thread t: head t % heads of rows t / heads, + rpp, + 2 rpp, ... (rpp rows a pass)
+  const int rpp = max(1, 256 / heads);
+  if (threadIdx.x < rpp * heads) {
+    const int h = (int)threadIdx.x % heads;
+    const float bias = dt_bias[h];
+    for (int r = (int)threadIdx.x / heads; r < nr; r += rpp) {
+      // softplus(v) = max(v, 0) + log(1 + e^-|v|), with the hardware base-2
+      // exponential and logarithm (absolute error about 1e-7)
+      const float v = __bfloat162float(src[(int64_t)r * heads + h]) + bias;
+      float e, l;
+      asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e) : "f"(-fabsf(v) * 1.4426950408889634f));
+      asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(l) : "f"(1.0f + e));
+      dts[h * (kDtRows + 1) + r] = fmaxf(v, 0.0f) + l * 0.6931471805599453f;
+    }
+  }
+  // (heads above 256: the remaining heads, one per thread and row)
+  for (int h = 256; h < heads; h += 256) {
+    const int hh = h + (int)threadIdx.x;
+    if (hh < heads)
+      for (int r = 0; r < nr; ++r) dts[hh * (kDtRows + 1) + r] = softplus_f(__bfloat162float(src[(int64_t)r * heads + hh]) + dt_bias[hh]);
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < heads * kDtRows; e += 256) {
+    const int h = e / kDtRows, r = e - h * kDtRows;
+    if (r < nr) dtp[(int64_t)h * rows + r0 + r] = dts[h * (kDtRows + 1) + r];
+  }
+}
+constexpr int kDtRowsMaxHeads = 768;  // shared memory [heads][65] floats within 200 KB
+
 // inclusive warp scan
 __device__ __forceinline__ float warp_incl_sum(float v, int lane) {
 #pragma unroll
@@ -1185,8 +1225,18 @@ cudaError_t launch_scan_tc(const ScanArgs& a, cudaStream_t st) {
   const int use_tma = make_xbc_map(&tm, a) ? 1 : 0;
   const int rows = a.tab.cu[a.tab.n];
   if (rows > 0) {
-    const dim3 pg((unsigned)((rows + 31) / 32), (unsigned)((a.heads + 31) / 32));
-    dt_prime_kernel<<<pg, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(a.dt), a.dt_bias, a.dtp, rows, a.heads);
+    if (a.heads <= kDtRowsMaxHeads) {
+      const size_t dsm = sizeof(float) * (size_t)a.heads * (kDtRows + 1);
+      if (dsm > 48 * 1024) {
+        const cudaError_t ea = cudaFuncSetAttribute(dt_prime_rows_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dsm);
+        if (ea != cudaSuccess) return ea;
+      }
+      dt_prime_rows_kernel<<<(unsigned)((rows + kDtRows - 1) / kDtRows), 256, dsm, st>>>(
+          static_cast<const __nv_bfloat16*>(a.dt), a.dt_bias, a.dtp, rows, a.heads);
+    } else {
+      const dim3 pg((unsigned)((rows + 31) / 32), (unsigned)((a.heads + 31) / 32));
+      dt_prime_kernel<<<pg, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(a.dt), a.dt_bias, a.dtp, rows, a.heads);
+    }
     const cudaError_t e0 = cudaGetLastError();
     if (e0 != cudaSuccess) return e0;
   }
