@@ -45,6 +45,9 @@ gated_rmsnorm_kernel(const NormArgs a, const int w_smem) {
                    "l"(wg + 4 * i));
   }
   asm volatile("cp.async.commit_group;\n" ::: "memory");
+  // launched as a programmatic dependent of the kernel before it (the scan that
+  // writes x): the weights above are a parameter; x and z come after this wait
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const float* w = w_smem ? wsm : wg;
   const int64_t base = row * a.dim + (int64_t)grp * gs;
   const T* x = static_cast<const T*>(a.x) + base;
@@ -130,11 +133,18 @@ cudaError_t launch_gated_rmsnorm(const NormArgs& a, mamba2_dtype act, cudaStream
   const int gs = a.dim / a.groups;
   const int w_smem = gs <= kNormSmemW ? 1 : 0;
   const size_t smem = w_smem ? (size_t)gs * sizeof(float) : 0;
-  if (act == MAMBA2_BF16)
-    gated_rmsnorm_kernel<__nv_bfloat16><<<(unsigned)items, kNormThreads * kNormRows, smem, st>>>(a, w_smem);
-  else
-    gated_rmsnorm_kernel<float><<<(unsigned)items, kNormThreads * kNormRows, smem, st>>>(a, w_smem);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)items, 1, 1);
+  cfg.blockDim = dim3(kNormThreads * kNormRows, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (act == MAMBA2_BF16) return cudaLaunchKernelEx(&cfg, gated_rmsnorm_kernel<__nv_bfloat16>, a, w_smem);
+  return cudaLaunchKernelEx(&cfg, gated_rmsnorm_kernel<float>, a, w_smem);
 }
 
 }  // namespace mamba2

@@ -288,6 +288,7 @@ struct DtQuad {
 __global__ void __launch_bounds__(256) dt_prime_kernel(const __nv_bfloat16* __restrict__ dt, const float* __restrict__ dt_bias,
                                                       float* __restrict__ dtp, int rows, int heads) {
   __shared__ float tile[32][33];
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");  // the state pass may be scheduled
   const int r0 = blockIdx.x * 32, h0 = blockIdx.y * 32;
   const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
   for (int k = ty; k < 32; k += 8) {
@@ -308,6 +309,7 @@ __global__ void __launch_bounds__(256) dt_prime_rows_kernel(const __nv_bfloat16*
                                                            const float* __restrict__ dt_bias, float* __restrict__ dtp,
                                                            int rows, int heads) {
   extern __shared__ float dts[];  // [heads][kDtRows + 1]
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");  // the state pass may be scheduled
   const int r0 = blockIdx.x * kDtRows;
   const int nr = min(kDtRows, rows - r0);
   const __nv_bfloat16* src = dt + (int64_t)r0 * heads;
@@ -472,6 +474,12 @@ ssd_tc_full(const __grid_constant__ ScanArgs a, const __grid_constant__ CUtensor
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *s_tmem;
+  // Launched as a programmatic dependent of the state pass (or of the dt'
+  // pre-pass): the tile loaders (warps 17 and 19) read only the conv's output
+  // and start at once; every other role reads dt', the state entries or the
+  // slot, or writes dst, after this wait.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");  // the norm may be scheduled
+  if (warp != kMathWarps + 1 && warp != kMathWarps + 3) asm volatile("griddepcontrol.wait;" ::: "memory");
 
   auto chunk_src = [&](int i) {
     ChunkSrc s;
@@ -1011,6 +1019,11 @@ ssd_tc_state(const __grid_constant__ ScanArgs a, const __grid_constant__ CUtenso
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *s_tmem;
+  // Launched as a programmatic dependent of the dt' pre-pass: the tile loaders
+  // (warps 16, 17) and the product issuer start at once; the weight producer
+  // (dt') and the element-wise warps (the slot) wait.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");  // the full pass may be scheduled
+  if (warp < kMathWarps || warp == kMathWarps + 3) asm volatile("griddepcontrol.wait;" ::: "memory");
 
   // local chunk i is chunk c_end - 1 - i
   auto chunk_src = [&](int i) {
@@ -1217,6 +1230,25 @@ unsigned int read_device_timeouts() {
   return v;
 }
 
+// A launch as a programmatic dependent of the previous kernel on the stream: it
+// may be scheduled while that kernel runs, and waits (griddepcontrol.wait)
+// before it touches what that kernel writes.
+template <typename Kern>
+cudaError_t launch_dependent(Kern kern, dim3 grid, int threads, size_t smem, cudaStream_t st, const ScanArgs& a,
+                             const CUtensorMap& tm, int use_tma) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3((unsigned)threads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, a, tm, use_tma);
+}
+
 cudaError_t launch_scan_tc(const ScanArgs& a, cudaStream_t st) {
   const int segs = a.tab.tile[a.tab.n];
   if (segs == 0) return cudaSuccess;
@@ -1249,14 +1281,12 @@ cudaError_t launch_scan_tc(const ScanArgs& a, cudaStream_t st) {
     // two heads of one group per CTA (one when a group has an odd number of heads)
     const int hpc = ((a.heads / a.ngroups) & 1) == 0 ? 2 : 1;
     const dim3 sgrid((unsigned)(segs * (a.state_pieces > 0 ? a.state_pieces : 1)), (unsigned)(a.heads / hpc));
-    ssd_tc_state<<<sgrid, kStateThreads, kStateSmem, st>>>(a, tm, use_tma);
-    e = cudaGetLastError();
+    e = launch_dependent(ssd_tc_state, sgrid, kStateThreads, kStateSmem, st, a, tm, use_tma);
     if (e != cudaSuccess) return e;
   }
   cudaError_t e = cudaFuncSetAttribute(ssd_tc_full, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kFullSmem);
   if (e != cudaSuccess) return e;
-  ssd_tc_full<<<grid, kFullThreads, kFullSmem, st>>>(a, tm, use_tma);
-  return cudaGetLastError();
+  return launch_dependent(ssd_tc_full, grid, kFullThreads, kFullSmem, st, a, tm, use_tma);
 }
 
 }  // namespace mamba2
