@@ -153,20 +153,115 @@ __device__ __forceinline__ float conv_silu_bf16_fast(float bias, const float (&w
   return __bfloat162float(__float2bfloat16_rn(v));
 }
 
+// ---- double-float (pair of fp32) arithmetic: Dekker's and Knuth's error-free
+// transformations (two-sum, two-product with a fused multiply-add), about 46
+// significant bits
+struct DF {
+  float hi, lo;
+};
+__device__ __forceinline__ DF df_two_sum(float a, float b) {
+  const float s = __fadd_rn(a, b);
+  const float bb = __fsub_rn(s, a);
+  return {s, __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb))};
+}
+__device__ __forceinline__ DF df_fast_two_sum(float a, float b) {  // |a| >= |b|
+  const float s = __fadd_rn(a, b);
+  return {s, __fsub_rn(b, __fsub_rn(s, a))};
+}
+__device__ __forceinline__ DF df_add(DF x, DF y) {
+  const DF s = df_two_sum(x.hi, y.hi);
+  return df_fast_two_sum(s.hi, __fadd_rn(s.lo, __fadd_rn(x.lo, y.lo)));
+}
+__device__ __forceinline__ DF df_mul(DF x, DF y) {
+  const float p = __fmul_rn(x.hi, y.hi);
+  const float e = __fmaf_rn(x.hi, y.hi, -p);
+  return df_fast_two_sum(p, __fmaf_rn(x.hi, y.lo, __fmaf_rn(x.lo, y.hi, e)));
+}
+__device__ __forceinline__ DF df_div(DF x, DF y) {
+  const float q1 = __fdiv_rn(x.hi, y.hi);
+  const DF r = df_add(x, df_mul(y, DF{-q1, 0.0f}));
+  return df_fast_two_sum(q1, __fdiv_rn(r.hi, y.hi));
+}
+// 1/k! as a double-float constant
+__host__ __device__ constexpr DF df_inv_fact(int k) {
+  double f = 1.0;
+  for (int i = 2; i <= k; ++i) f *= (double)i;
+  const double v = 1.0 / f;
+  const float hi = (float)v;
+  return {hi, (float)(v - (double)hi)};
+}
+
+// Middle tier of the rounding test: silu(bias + sum_k w_k u_k) in double-float
+// (exact products and sums; e^-p by range reduction to |r| <= ln2/2 and its
+// Taylor series to degree 12, then 2^n), rounded as the double-precision
+// definition rounds it: to fp32, then to bf16. Undecided (left to fp64) when the
+// value lies within its error bound of the edge of the fp32 rounding interval of
+// the bf16 midpoint, or outside the range handled here.
+template <int K>
+__device__ __forceinline__ float conv_silu_bf16_df(float bias, const float* w, const float* u, bool& undecided) {
+  DF p = {bias, 0.0f};
+  float psum = fabsf(bias);
+#pragma unroll
+  for (int k = 0; k < K; ++k) {
+    const float m = __fmul_rn(w[k], u[k]);
+    p = df_add(p, DF{m, __fmaf_rn(w[k], u[k], -m)});
+    psum += fabsf(p.hi);
+  }
+  undecided = true;
+  if (!(fabsf(p.hi) <= 80.0f) || !(fabsf(p.hi) >= 0x1p-60f)) return 0.0f;
+  // e^-p = 2^n e^r, r = -p - n ln 2 (ln 2 as 0.693145751953125 + its remainder, so
+  // that n times the first part is exact for |n| <= 128)
+  const float n = rintf(__fmul_rn(-p.hi, 1.4426950408889634f));
+  const float ln2a = 0.693145751953125f, ln2b = (float)(0.69314718055994530942 - 0.693145751953125);
+  DF r = df_add(DF{-p.hi, -p.lo}, DF{__fmul_rn(-n, ln2a), 0.0f});
+  const float nb = __fmul_rn(-n, ln2b);
+  r = df_add(r, DF{nb, __fmaf_rn(-n, ln2b, -nb)});
+  DF e = df_inv_fact(12);
+#pragma unroll
+  for (int k = 11; k >= 0; --k) e = df_add(df_mul(e, r), df_inv_fact(k));
+  const float sc = __int_as_float((127 + (int)n) << 23);  // 2^n, |n| <= 116 here
+  e = DF{__fmul_rn(e.hi, sc), __fmul_rn(e.lo, sc)};
+  const DF v = df_div(p, df_add(DF{1.0f, 0.0f}, e));
+  // the bf16 midpoint m nearest v, and the half-width h of m's fp32 rounding interval
+  const float m = __uint_as_float((__float_as_uint(v.hi) & 0xffff0000u) | 0x8000u);
+  const uint32_t ex = (__float_as_uint(m) >> 23) & 0xffu;
+  if (ex <= 30u) return 0.0f;  // near the subnormal range: fp64 decides
+  const float h = __uint_as_float((ex - 24u) << 23);
+  // |v - (the definition's double value)| <= E: 2^-38 |v| covers this tier's
+  // arithmetic and the definition's own rounding, 2^-44 psum the cancellation
+  // of the sum's partial values in either evaluation
+  const float E = fmaf(0x1p-38f, fabsf(v.hi), 0x1p-44f * psum);
+  const float d = fabsf(__fadd_rn(__fsub_rn(v.hi, m), v.lo));
+  if (d < h - E) {  // the value rounds to m in fp32: a tie, to even in bf16
+    undecided = false;
+    return __bfloat162float(__float2bfloat16_rn(m));
+  }
+  if (d > h + E) {  // strictly on one side of m's interval
+    undecided = false;
+    const float x = __fadd_rn(v.hi, v.lo);
+    return __bfloat162float(__float2bfloat16_rn(x));
+  }
+  return 0.0f;
+}
+
 // Conv output rounded to bf16 as the double-precision definition rounds it.
 //
 // The value silu(bias + sum_k w_k u_k) is computed in fp32 together with a
 // bound on its error; when the fp32 value lies farther than that bound from
 // the bf16 rounding boundary nearest to it, its bf16 rounding equals that of
 // the exact value rounded first to fp32 and then to bf16. Otherwise (about
-// one element in a thousand) the value is recomputed in fp64. This is Ziv's
-// rounding test; it keeps the conv output, and so the state it feeds,
-// independent of fp32 rounding noise.
+// one element in two thousand) the value is recomputed in double-float, and in
+// fp64 when that is still too close to call (which no workload here has shown).
+// This is Ziv's rounding test; it keeps the conv output, and so the state it
+// feeds, independent of fp32 rounding noise.
 template <int K>
 __device__ __forceinline__ float conv_silu_bf16_exact(float bias, const float (&w)[K], const float (&u)[K]) {
   bool retry;
   const float v = conv_silu_bf16_fast<K>(bias, w, u, retry);
-  return retry ? conv_silu_bf16_fp64<K>(bias, w, u) : v;
+  if (!retry) return v;
+  bool undecided;
+  const float v2 = conv_silu_bf16_df<K>(bias, w, u, undecided);
+  return undecided ? conv_silu_bf16_fp64<K>(bias, w, u) : v2;
 }
 
 // Conv output for one channel at the activation type: bf16 through the exact

@@ -212,7 +212,7 @@ decode_step_kernel(const __grid_constant__ DecodeArgs a) {
     float* o = is_x ? xs + i * V : bc + (c0 - d_inner);
 #pragma unroll
     for (int j = 0; j < V; ++j) o[j] = out[j];
-    // fp64 retry of the outputs the fast rounding test could not decide
+    // retry of the outputs the fast rounding test could not decide
     // (inputs re-read; this thread has not yet rewritten its history rows)
     while (retry_mask) {
       const int j = __ffs(retry_mask) - 1;
@@ -224,7 +224,9 @@ decode_step_kernel(const __grid_constant__ DecodeArgs a) {
         wk[k] = a.conv_w[(int64_t)c * K + k];
         uk[k] = k < HIST ? (fresh ? 0.f : Act<T>::to_f(cst[(int64_t)k * conv_dim + c])) : Act<T>::to_f(xBC[c]);
       }
-      o[j] = conv_silu_bf16_fp64<K>(a.conv_b[c], wk, uk);
+      bool undecided;  // double-float first (fp64 is slow on this part), fp64 when that cannot decide
+      const float v2 = conv_silu_bf16_df<K>(a.conv_b[c], wk, uk, undecided);
+      o[j] = undecided ? conv_silu_bf16_fp64<K>(a.conv_b[c], wk, uk) : v2;
     }
     if (is_x) {  // own channels: shift the history now
 #pragma unroll
