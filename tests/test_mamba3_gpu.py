@@ -110,3 +110,11 @@ def test_rejects_bad_batches_before_launch():
     assert st == ss.ERR_RUNS_DONT_COVER_ROWS
     st = ss.mamba3_siso_varlen_forward(*outs, *ins, [0, 12, 10], check=False)
     assert st == ss.ERR_RUNS_DONT_COVER_ROWS
+
+
+def test_long_sequence_many_chunks():
+    """A 4 000-token sequence (32 chunks of 128: the angle carry and the state cross
+    31 chunk boundaries), one head and a run of one-token sequences beside it."""
+    dev = device()
+    b = W.mamba3_batch(seed=16, lengths=[4000, 1, 1, 3, 130], heads=1)
+    compare(b, run_gpu(b, dev), "4000 tokens, 1 head")
