@@ -64,12 +64,14 @@ def test_frozen_shapes(seed):
     compare(b, run_gpu(b, dev), f"seed {seed}")
 
 
-def test_ragged_edges():
+@pytest.mark.parametrize("heads", [5, 8])
+def test_ragged_edges(heads):
     """An empty sequence, one token, a whole 128-token chunk, one past it, and a
-    long one, packed together."""
+    long one, packed together. With 8 heads the per-token scalars come by TMA
+    (rows of 16-byte multiples), with 5 by strided loads."""
     dev = device()
-    b = W.mamba3_batch(seed=11, lengths=[0, 1, 128, 129, 700, 255], heads=5)
-    compare(b, run_gpu(b, dev), "ragged")
+    b = W.mamba3_batch(seed=11, lengths=[0, 1, 128, 129, 700, 255], heads=heads)
+    compare(b, run_gpu(b, dev), f"ragged, {heads} heads")
 
 
 @pytest.mark.parametrize("R", [0, 1, 6, 34, 40, 64])
@@ -112,9 +114,11 @@ def test_rejects_bad_batches_before_launch():
     assert st == ss.ERR_RUNS_DONT_COVER_ROWS
 
 
-def test_long_sequence_many_chunks():
+@pytest.mark.parametrize("heads", [1, 8])
+def test_long_sequence_many_chunks(heads):
     """A 4 000-token sequence (32 chunks of 128: the angle carry and the state cross
-    31 chunk boundaries), one head and a run of one-token sequences beside it."""
+    31 chunk boundaries) and a run of one-token sequences beside it; the last rows
+    of the batch end inside the final chunk's boxes (read as zero past the tensor)."""
     dev = device()
-    b = W.mamba3_batch(seed=16, lengths=[4000, 1, 1, 3, 130], heads=1)
-    compare(b, run_gpu(b, dev), "4000 tokens, 1 head")
+    b = W.mamba3_batch(seed=16, lengths=[4000, 1, 1, 3, 130], heads=heads)
+    compare(b, run_gpu(b, dev), f"4000 tokens, {heads} heads")
