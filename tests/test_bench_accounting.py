@@ -71,3 +71,11 @@ def test_mamba3_bytes_frozen_batch():
     writes = 3109 * 32 * 64 * 2 + 5 * 32 * (32 * 2 + 64 * 128 * 4 + 128 * 4 + 64 * 2)
     assert (reads, writes) == (28_287_488, 18_089_984)
     assert bench.mamba3_bytes(b) == 46_377_472
+
+
+def test_prefill_fused_bytes():
+    """The fused minimum at the 65 536-token shape: 19 040 bytes a token (xBC 6 656,
+    z 6 144, dt 96, output 6 144) plus one fresh sequence's conv history and SSM
+    state written once."""
+    wl = W.long_prefill(tokens=65536, decode_steps=1)
+    assert bench.prefill_fused_bytes(wl) == 65536 * 19_040 + 3 * 3328 * 2 + 48 * 64 * 128 * 4
