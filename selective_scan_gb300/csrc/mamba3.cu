@@ -41,9 +41,13 @@
 // Strided per-thread loads of [rows, heads] columns, 32 lines a warp instruction,
 // held the load pipe for thousands of cycles a chunk, and every warp behind them.
 // fp16 operands (11 significant bits) keep the worst y error about a tenth of
-// the bf16 output's own rounding. fp16 holds magnitudes up to 65 504: a CTA
-// that meets a larger operand recomputes that (sequence, head) token by token
-// in fp32 (correct, slow; no workload here comes near it).
+// the bf16 output's own rounding. fp16 holds magnitudes up to 65 504: a larger
+// operand converts to inf, which reaches the y it feeds or the state (inf, or
+// NaN through inf * 0). Each thread sums the y it stores and its final state
+// entries; a CTA whose sums are not finite recomputes that (sequence, head) token
+// by token in fp32 (correct, slow; no workload here comes near it). An operand
+// that overflows where no product uses it (q^ of a chunk's first token before any
+// state exists) changes nothing and is not caught, which is also correct.
 // Every wait is bounded: on a timeout the CTA records it in a device counter
 // (mamba2_device_timeouts), drains what it issued, frees its TMEM and returns.
 #include <cuda.h>
@@ -69,7 +73,6 @@ constexpr int kThreads = 512;
 constexpr float kTwoPi = 6.283185307179586f;
 constexpr float kPiF = 3.14159265358979f;
 constexpr float kLog2e = 1.4426950408889634f;
-constexpr float kF16Max = 65504.0f;
 
 // ---- shared memory (operand tiles 1024-byte aligned)
 constexpr uint32_t kTileQK = kQ * kN * 2;  // 32 KB [token][n] fp16
@@ -129,10 +132,9 @@ __device__ __forceinline__ float ex2f(float x) {
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
-// fp16 pair (lo in the low half); `amax` tracks the largest magnitude converted
-// (above kF16Max the pair did not fit)
-__device__ __forceinline__ uint32_t h2(float lo, float hi, float& amax) {
-  amax = fmaxf(amax, fmaxf(fabsf(lo), fabsf(hi)));
+// fp16 pair (lo in the low half); a value beyond the fp16 range becomes inf, and
+// inf (or inf * 0) reaches y or the state it feeds: caught there
+__device__ __forceinline__ uint32_t h2(float lo, float hi) {
   uint32_t d;
   asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
   return d;
@@ -348,7 +350,9 @@ m3_fwd_kernel(const __grid_constant__ Mamba3Args a, const __grid_constant__ CUte
     const float2 kbA = *reinterpret_cast<const float2*>(a.k_bias + (int64_t)it.h * kN + 2 * pA);
     const float2 kbB = *reinterpret_cast<const float2*>(a.k_bias + (int64_t)it.h * kN + 2 * pB);
     const float dh = a.d[it.h];
-    float amax = 0.f;  // largest fp16 operand magnitude of the item
+    // sum of every stored y and of the final state: not finite iff an fp16 operand
+    // of the products overflowed (or an input was not finite)
+    float fsum = 0.f;
 
     // raw q and k rows of the chunk starting at row rb: one bulk copy each (rows
     // past the run keep stale values, masked where they are read);
@@ -526,8 +530,8 @@ m3_fwd_kernel(const __grid_constant__ Mamba3Args a, const __grid_constant__ CUte
             rkb0 = csB * kb0 - snB * kb1;
             rkb1 = snB * kb0 + csB * kb1;
           }
-          const uint32_t qa = h2(rqa0, rqa1, amax), ka = h2(rka0, rka1, amax);
-          const uint32_t qb = h2(rqb0, rqb1, amax), kb = h2(rkb0, rkb1, amax);
+          const uint32_t qa = h2(rqa0, rqa1), ka = h2(rka0, rka1);
+          const uint32_t qb = h2(rqb0, rqb1), kb = h2(rkb0, rkb1);
           if (t == len - 1) {
             if (rotA) F[kFCar + 64 * ((c + 1) & 1) + pA] = phA;
             if (rotB) F[kFCar + 64 * ((c + 1) & 1) + pB] = phB;
@@ -591,8 +595,8 @@ m3_fwd_kernel(const __grid_constant__ Mamba3Args a, const __grid_constant__ CUte
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
             const float x0 = __uint_as_float(vw4[u] << 16), x1 = __uint_as_float(vw4[u] & 0xffff0000u);
-            f[u] = h2(x0, x1, amax);
-            g[u] = h2(x0 * w, x1 * w, amax);
+            f[u] = h2(x0, x1);
+            g[u] = h2(x0 * w, x1 * w);
           }
           *reinterpret_cast<uint4*>(smem + kOffV + toff(t, 8 * c8)) = make_uint4(f[0], f[1], f[2], f[3]);
           *reinterpret_cast<uint4*>(smem + kOffVW + toff(t, 8 * c8)) = make_uint4(g[0], g[1], g[2], g[3]);
@@ -659,7 +663,7 @@ m3_fwd_kernel(const __grid_constant__ Mamba3Args a, const __grid_constant__ CUte
               mv[e] = j < row ? cb[e] * ex2f(St - F[kFS + j]) * F[kFW + j] : (j == row ? diag : 0.f);
             }
 #pragma unroll
-            for (int e = 0; e < 8; ++e) m[e] = h2(mv[2 * e], mv[2 * e + 1], amax);
+            for (int e = 0; e < 8; ++e) m[e] = h2(mv[2 * e], mv[2 * e + 1]);
           }
           asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};"
                        :: "r"(tmem + lane_off + kColM + 8u * (uint32_t)s2), "r"(m[0]), "r"(m[1]), "r"(m[2]),
@@ -675,7 +679,7 @@ m3_fwd_kernel(const __grid_constant__ Mamba3Args a, const __grid_constant__ CUte
           for (int u = 0; u < 2; ++u) {
             uint32_t w[4];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) w[e] = h2(hs[8 * u + 2 * e], hs[8 * u + 2 * e + 1], amax);
+            for (int e = 0; e < 4; ++e) w[e] = h2(hs[8 * u + 2 * e], hs[8 * u + 2 * e + 1]);
             *reinterpret_cast<uint4*>(smem + kOffHT + toff(row, 16 * cq + 8 * u)) = make_uint4(w[0], w[1], w[2], w[3]);
           }
         }
@@ -727,6 +731,7 @@ m3_fwd_kernel(const __grid_constant__ Mamba3Args a, const __grid_constant__ CUte
             const int i0 = 8 * u + 2 * e;
             const float y0 = fmaf(et, yo[i0], yd[i0]) + dh * f16lo(vw[e]);
             const float y1 = fmaf(et, yo[i0 + 1], yd[i0 + 1]) + dh * f16hi(vw[e]);
+            if (in_run) fsum += y0 + y1;
             const float z0 = __uint_as_float(zw[e] << 16), z1 = __uint_as_float(zw[e] & 0xffff0000u);
             const __nv_bfloat162 ob = __floats2bfloat162_rn(y0 * silu_f(z0), y1 * silu_f(z1));
             o[4 * u + e] = *reinterpret_cast<const uint32_t*>(&ob);
@@ -750,7 +755,9 @@ m3_fwd_kernel(const __grid_constant__ Mamba3Args a, const __grid_constant__ CUte
     }
 #pragma unroll
     for (int e = 0; e < 16; ++e) a.final_ssm[(sh * kP + 16 * cq + e) * kN + row] = hs[e];
-    if (!(amax <= kF16Max)) *s_range = 1u;
+#pragma unroll
+    for (int e = 0; e < 16; ++e) fsum += hs[e];
+    if (!isfinite(fsum)) *s_range = 1u;
     __syncthreads();
     if (*s_range) {
       // an fp16 operand overflowed: this (sequence, head) again, token by token
