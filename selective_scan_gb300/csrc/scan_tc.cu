@@ -123,9 +123,6 @@ enum FullBar : int {  // + chunk % 2
 constexpr uint32_t kOffMisc = kOffBar + 8 * kNumFullBars;  // TMEM base, abort flag, fp16 range flag
 constexpr uint32_t kFullSmem = kOffMisc + 16;
 static_assert(kFullSmem <= 232448, "full-pass shared memory plan exceeds 227 KB");
-// fp16 operands of Y = M . X: a chunk whose M or x reaches this magnitude is
-// recomputed token by token (fp16 holds up to 65 504)
-constexpr float kF16Limit = 65504.0f;
 
 // ---- state pass: two heads of one group per CTA (they share the B tile and
 // one N = 256 product per chunk); TMEM D = [head 0 hi | lo | head 1 hi | lo].
@@ -183,13 +180,13 @@ __device__ __forceinline__ F2 f2(float lo, float hi) {
   return r;
 }
 __device__ __forceinline__ float f2lo(F2 a) {
-  float lo, hi;
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(a.v));
+  float lo;
+  asm("{\n .reg .f32 t;\n mov.b64 {%0, t}, %1;\n}" : "=f"(lo) : "l"(a.v));
   return lo;
 }
 __device__ __forceinline__ float f2hi(F2 a) {
-  float lo, hi;
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(a.v));
+  float hi;
+  asm("{\n .reg .f32 t;\n mov.b64 {t, %0}, %1;\n}" : "=f"(hi) : "l"(a.v));
   return hi;
 }
 __device__ __forceinline__ F2 add2(F2 a, F2 b) {
