@@ -74,11 +74,13 @@ def test_ragged_edges(heads):
     compare(b, run_gpu(b, dev), f"ragged, {heads} heads")
 
 
-@pytest.mark.parametrize("R", [0, 1, 6, 34, 40, 64])
-def test_rotary_widths(R):
+@pytest.mark.parametrize("R,heads", [(0, 3), (1, 3), (6, 3), (34, 3), (40, 3), (64, 3), (0, 8), (34, 8), (64, 8)])
+def test_rotary_widths(R, heads):
+    """Rotary widths from none to every pair (above 32 each thread's second pair turns
+    too); with 8 heads the per-token scalars come by TMA, with 3 by strided loads."""
     dev = device()
-    b = W.mamba3_batch(seed=12, lengths=[300, 97], heads=3, rot_dim=R)
-    compare(b, run_gpu(b, dev), f"rot_dim {R}")
+    b = W.mamba3_batch(seed=12, lengths=[300, 97], heads=heads, rot_dim=R)
+    compare(b, run_gpu(b, dev), f"rot_dim {R}, {heads} heads")
 
 
 def test_more_items_than_sms():
