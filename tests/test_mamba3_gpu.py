@@ -83,6 +83,19 @@ def test_rotary_widths(R, heads):
     compare(b, run_gpu(b, dev), f"rot_dim {R}, {heads} heads")
 
 
+def test_all_sequences_empty():
+    """Sequences but no rows: the kernel still runs every (sequence, head) item and
+    writes zero final states (NaN-poisoned before), issuing no copy."""
+    dev = device()
+    b = W.mamba3_batch(seed=17, lengths=[0, 0, 0], heads=8)
+    assert b.rows == 0
+    out, fa, fs, fk, fv = run_gpu(b, dev)
+    for t, name in ((fa, "final angle"), (fs, "final ssm"), (fk, "final k"), (fv, "final v")):
+        assert torch.equal(t.float(), torch.zeros_like(t.float())), f"{name} not zero"
+    assert out.numel() == 0
+    assert ss.library().mamba2_device_timeouts() == 0
+
+
 def test_more_items_than_sms():
     """More (sequence, head) items than SMs: CTAs take a second item."""
     dev = device()
