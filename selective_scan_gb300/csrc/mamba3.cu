@@ -461,9 +461,9 @@ m3_fwd_kernel(const __grid_constant__ Mamba3Args a, const __grid_constant__ CUte
         break;
       }
       if (tid < kQ) {
-        float off = 0.f;
-        for (int w = 0; w < warp; ++w) off += F[kFWS + w];
-        F[kFS + tid] = incl + off;
+        float before = 0.f;  // decay of the warps' earlier tokens
+        for (int w = 0; w < warp; ++w) before += F[kFWS + w];
+        F[kFS + tid] = incl + before;
       }
       // ---- angle increments of this thread's rotated pairs over its 8 tokens
       const bool rotA = pA < R, rotB = pB < R;
