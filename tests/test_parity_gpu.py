@@ -112,6 +112,14 @@ def test_state_pass_head_pairs(H, G):
     _prefill_parity(wl)
 
 
+def test_many_heads_dt_prime_by_head_tiles():
+    """800 heads (above the 768 whose dt' rows fit one CTA's shared memory): the
+    scan's dt' pre-pass runs as 32 x 32 tiles instead of 64-row blocks."""
+    d = W.Dims(800, 64, 128, 2, 4)
+    wl = W.make_prefill("heads-800", 83, d, [300, 129], torch.bfloat16, 3, [1, 0])
+    _prefill_parity(wl)
+
+
 def test_scan_fp16_range_fallback():
     """Inputs whose Y = M . X operands leave the fp16 range: a token whose C and
     B rows are large and aligned (an M entry near 1.5e5, in every head's
