@@ -79,7 +79,7 @@ constexpr int TN = 128;  // d_state
 constexpr int kMathWarps = 16;  // element-wise warps of either pass
 constexpr int kMathThreads = 32 * kMathWarps;
 constexpr int kFullThreads = kMathThreads + 4 * 32;   // + CB (and dt), Yoff (and C/B loads), dH, Y (and X loads) issuers
-constexpr int kStateThreads = kMathThreads + 4 * 32;  // + X loader, B loader, dH issuer, weight producer
+constexpr int kStateThreads = kMathThreads + 5 * 32;  // + X loader, B loader, hi issuer, weight producer, lo issuer
 // full pass: the element-wise warps by role
 constexpr int kMWarps = 8;   // warps 0-7: X o w (bf16 hi + lo) and the fp16 copy of x, then M
 constexpr int kSWarps = 8;   // warps 8-15: state, output, H hi + lo
@@ -124,24 +124,28 @@ constexpr uint32_t kOffMisc = kOffBar + 8 * kNumFullBars;  // TMEM base, abort f
 constexpr uint32_t kFullSmem = kOffMisc + 16;
 static_assert(kFullSmem <= 232448, "full-pass shared memory plan exceeds 227 KB");
 
-// ---- state pass: two heads of one group per CTA (they share the B tile and
-// one N = 256 product per chunk); TMEM D = [head 0 hi | lo | head 1 hi | lo].
-// A stage holds, per head, the X tile (X o w hi is written over it in place)
-// and the X o w lo tile: four 64-column blocks 16 KB apart, which is the
-// product's B operand as it stands. A stage is free once the product of its
-// chunk is done.
-constexpr int kStStages = 2;                            // chunk i in stage i % 2
-constexpr uint32_t kStHeadTile = 2 * kTileX;            // [X, then X o w hi | X o w lo] of one head
-constexpr uint32_t kStStage = 2 * kStHeadTile;          // two heads
-constexpr uint32_t kStOffB = kStStages * kStStage;      // B stages
+// ---- state pass: two heads of one group per CTA (they share the B tile). The
+// product is D = (X o w)^T . B with X o w (bf16 hi and lo) written to TMEM by the
+// element-wise warps as the A operand (lane = column p of head 0, then head 1), so
+// shared memory holds only the loaded X and B tiles, three chunks deep: an X stage
+// is free once X o w of its chunk is formed, a B stage once its chunk's products
+// are done.
+constexpr int kStStages = 3;                            // X and B rings: chunk i in stage i % 3
+constexpr uint32_t kStXStage = 2 * kTileX;              // the X tiles of both heads
+constexpr uint32_t kStOffB = kStStages * kStXStage;     // B stages
 constexpr uint32_t kStOffW = kStOffB + kStStages * kTileB;  // [2 buffers][2 heads][TQ] token weights
 constexpr uint32_t kStOffR = kStOffW + 2 * 2 * TQ * 4;  // [2 heads] total log2 decay of the piece
 constexpr uint32_t kStOffBar = kStOffR + 16;
-enum StateBar : int {  // + chunk % 2
-  kStFullX = 0, kStFullB = 2, kStDHDone = 4, kStXWReady = 6, kStWReady = 8, kNumStateBars = 10
+enum StateBar : int {  // + chunk % 3 on the rings of three, + chunk % 2 on the rings of two
+  kStFullX = 0, kStFullB = 3, kStXFree = 6, kStBFree = 9, kStXWReady = 12, kStDHDone = 14, kStWReady = 16,
+  kNumStateBars = 18
 };
 constexpr uint32_t kStOffMisc = kStOffBar + 8 * kNumStateBars;
 constexpr uint32_t kStateSmem = kStOffMisc + 16;  // the base is 1024-byte aligned (checked)
+// TMEM: D = (X o w)^T . B as hi and lo accumulators (lane = p of head 0 then head 1,
+// column = n), and X o w itself, the products' A operand, in two stages (lane = p,
+// column j / 2 holds tokens j and j + 1 as a bf16 pair): hi, then lo
+constexpr uint32_t kStColDHi = 0, kStColDLo = 128, kStColXW = 256;
 static_assert(kStateSmem <= 232448, "state-pass shared memory plan exceeds 227 KB");
 
 
@@ -937,11 +941,14 @@ ssd_tc_full(const __grid_constant__ ScanArgs a, const __grid_constant__ CUtensor
 // the chunks already read, token j's weight is w_j = 2^(R + S_end - S_j) dt'_j
 // (S the chunk's cumulative log2 decay, per head), so B^T . (X o w) of every
 // chunk accumulates into the same TMEM columns.
-//   warps 0-15  X o w (bf16 hi + lo) of both heads; at the end, the pieces' states
-//   warp 16     X tile loads (two heads, two stages)
-//   warp 17     B tile loads (two stages)
-//   warp 18     dH^T += B^T . [X o w hi | lo | X o w hi | lo]  (M=128 N=256 K=128 per chunk)
+//   warps 0-15  X o w (bf16 hi + lo) of both heads into TMEM (warp w: lanes of
+//               quarter w % 4, tokens [32 (w / 4), +32)); at the end, the pieces' states
+//   warp 16     X tile loads (two heads, three stages)
+//   warp 17     B tile loads (three stages)
+//   warp 18     D hi += (X o w hi)^T . B  (A from TMEM; M=128 N=128 K=128 per chunk)
 //   warp 19     dt' and the token weights of both heads, up to two chunks ahead
+//   warp 20     D lo += (X o w lo)^T . B  (the two accumulators are summed at the end;
+//               one issuing thread per half, so the two halves' instructions overlap)
 __global__ void __launch_bounds__(kStateThreads, 1)
 ssd_tc_state(const __grid_constant__ ScanArgs a, const __grid_constant__ CUtensorMap tm, const int use_tma) {
   // CTA (b, y): piece q = b % P of segment b / P, an equal share of the segment's
@@ -990,23 +997,28 @@ ssd_tc_state(const __grid_constant__ ScanArgs a, const __grid_constant__ CUtenso
   float* s_w = reinterpret_cast<float*>(smem + kStOffW);
   float* s_R = reinterpret_cast<float*>(smem + kStOffR);
   auto bar = [&](int id) { return sbase + kStOffBar + 8u * (uint32_t)id; };
-  auto stg_x = [&](int i) { return sbase + (uint32_t)(i & 1) * kStStage; };
-  auto stg_b = [&](int i) { return sbase + kStOffB + (uint32_t)(i & 1) * kTileB; };
-  auto p2 = [](int i) { return (uint32_t)((i >> 1) & 1); };  // phase parity on a [2] barrier
+  auto stg_x = [&](int i) { return sbase + (uint32_t)(i % kStStages) * kStXStage; };
+  auto stg_b = [&](int i) { return sbase + kStOffB + (uint32_t)(i % kStStages) * kTileB; };
+  auto p2 = [](int i) { return (uint32_t)((i >> 1) & 1); };          // phase parity on a [2] barrier
+  auto p3 = [](int i) { return (uint32_t)((i / kStStages) & 1); };   // phase parity on a [3] barrier
 
   const int n = ci.n;  // >= 1 here
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
   if (warp == 0) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 256;" :: "r"(su32(s_tmem)));
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;" :: "r"(su32(s_tmem)));
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
   }
   if (tid == kMathThreads) {
     for (int b = 0; b < kStStages; ++b) {
       mbar_init(bar(kStFullX + b), 2);  // one tile per head
       mbar_init(bar(kStFullB + b), 1);
-      mbar_init(bar(kStDHDone + b), 1);
+      mbar_init(bar(kStXFree + b), kMathWarps);
+      mbar_init(bar(kStBFree + b), 2);  // one commit from each issuer
+    }
+    for (int b = 0; b < 2; ++b) {
       mbar_init(bar(kStXWReady + b), kMathWarps);
+      mbar_init(bar(kStDHDone + b), 2);
       mbar_init(bar(kStWReady + b), 1);
     }
     *s_abort = 0u;
@@ -1034,104 +1046,127 @@ ssd_tc_state(const __grid_constant__ ScanArgs a, const __grid_constant__ CUtenso
   };
 
   if (warp < kMathWarps) {
-    // =================== X o w of every chunk (both heads), then the pieces' states
-    const int row = tid & 127, cg = tid >> 7, qrt = warp & 3;
+    // =================== X o w of every chunk into TMEM (lane = p: head 0's columns in
+    // lane quarters 0-1, head 1's in 2-3; warp group tg takes tokens [32 tg, +32)),
+    // then the pieces' states
+    const int qrt = warp & 3, tg = warp >> 2;
+    const int hq = qrt >> 1, p = 32 * (qrt & 1) + lane;
     const uint32_t lane_off = (uint32_t)(qrt * 32) << 16;
     bool live = true;
     for (int i = 0; i < n; ++i) {
-      if (!(warp_wait(bar(kStFullX + (i & 1)), p2(i), s_abort) && warp_wait(bar(kStWReady + (i & 1)), p2(i), s_abort))) {
+      if (!(warp_wait(bar(kStFullX + i % kStStages), p3(i), s_abort) &&
+            warp_wait(bar(kStWReady + (i & 1)), p2(i), s_abort) &&
+            (i < 2 || warp_wait(bar(kStDHDone + (i & 1)), p2(i - 2), s_abort)))) {  // TMEM stage i % 2 read
         live = false;
         break;
       }
+      const unsigned char* xt = smem + (uint32_t)(i % kStStages) * kStXStage + (uint32_t)hq * kTileX;
+      const float* w = s_w + ((i & 1) * 2 + hq) * TQ;
+      uint32_t hw[16], lw[16];
 #pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        const float w = s_w[((i & 1) * 2 + hh) * TQ + row];
-        unsigned char* xt = smem + (uint32_t)(i & 1) * kStStage + (uint32_t)hh * kStHeadTile;
-#pragma unroll
-        for (int qq = 0; qq < 2; ++qq) {
-          const uint32_t o = tile_off(row, 16 * cg + 8 * qq, TQ);
-          const uint4 xv = *reinterpret_cast<const uint4*>(xt + o);
-          const uint32_t xr[4] = {xv.x, xv.y, xv.z, xv.w};
-          uint32_t hi[4], lo[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e)
-            split2(__uint_as_float(xr[e] << 16) * w, __uint_as_float(xr[e] & 0xffff0000u) * w, hi[e], lo[e]);
-          // in place: each element is read and rewritten by this thread only
-          *reinterpret_cast<uint4*>(xt + o) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-          *reinterpret_cast<uint4*>(xt + kTileX + o) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-        }
+      for (int k = 0; k < 16; ++k) {
+        const int j = 32 * tg + 2 * k;
+        const float x0 = __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(xt + tile_off(j, p, TQ)));
+        const float x1 = __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(xt + tile_off(j + 1, p, TQ)));
+        split2(x0 * w[j], x1 * w[j + 1], hw[k], lw[k]);
       }
-      fence_async_smem();
+      fence_async_smem();  // the X tile's reads come before its refill
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(kStXFree + i % kStStages));
+      const uint32_t ta = tmem + lane_off + kStColXW + 128u * (uint32_t)(i & 1) + 16u * (uint32_t)tg;
+      asm volatile("tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};"
+                   :: "r"(ta), "r"(hw[0]), "r"(hw[1]), "r"(hw[2]), "r"(hw[3]), "r"(hw[4]), "r"(hw[5]), "r"(hw[6]),
+                      "r"(hw[7]), "r"(hw[8]), "r"(hw[9]), "r"(hw[10]), "r"(hw[11]), "r"(hw[12]), "r"(hw[13]),
+                      "r"(hw[14]), "r"(hw[15]) : "memory");
+      asm volatile("tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};"
+                   :: "r"(ta + 64u), "r"(lw[0]), "r"(lw[1]), "r"(lw[2]), "r"(lw[3]), "r"(lw[4]), "r"(lw[5]), "r"(lw[6]),
+                      "r"(lw[7]), "r"(lw[8]), "r"(lw[9]), "r"(lw[10]), "r"(lw[11]), "r"(lw[12]), "r"(lw[13]),
+                      "r"(lw[14]), "r"(lw[15]) : "memory");
+      asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+      tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(kStXWReady + (i & 1)));
     }
     if (live && warp_wait(bar(kStDHDone + ((n - 1) & 1)), p2(n - 1), s_abort)) {
       tc_fence_after();
-      for (int hh = 0; hh < nh; ++hh) {
-        const int h = h0 + hh;
+      // D row p (this lane), columns n = [32 tg, +32): hi + lo
+      float dsum[32];
+#pragma unroll
+      for (int g = 0; g < 2; ++g) {
         float dhi[16], dlo[16];
-        tmem_ld16x2(tmem + lane_off + 128u * (uint32_t)hh + 16 * cg, tmem + lane_off + 128u * (uint32_t)hh + 64 + 16 * cg,
-                    dhi, dlo);
-        const float Rt = s_R[hh];  // written before the weights of the last chunk were published
-        const int64_t head_off = (int64_t)h * TP * TN;
-        float* dst = a.ws_state + (int64_t)entry * H * TP * TN + head_off;
+        tmem_ld16x2(tmem + lane_off + kStColDHi + 32u * (uint32_t)tg + 16u * (uint32_t)g,
+                    tmem + lane_off + kStColDLo + 32u * (uint32_t)tg + 16u * (uint32_t)g, dhi, dlo);
+#pragma unroll
+        for (int e = 0; e < 16; ++e) dsum[16 * g + e] = dhi[e] + dlo[e];
+      }
+      if (hq < nh) {
+        const int h = h0 + hq;
+        const float Rt = s_R[hq];  // written before the weights of the last chunk were published
+        const int64_t head_off = (int64_t)h * TP * TN, row_off = (int64_t)p * TN + 32 * tg;
+        float* dst = a.ws_state + (int64_t)entry * H * TP * TN + head_off + row_off;
         if (ci.k == 0 && q == 0 && !ci.fresh) {
           // the first piece starts from the slot's state: add its decayed share, and
           // leave a copy of it for the full pass (whose last segment overwrites the slot)
           // in the first entry of the last segment, which has no entries of its own
           const float d = ex2(Rt);
-          const float* slot_ptr = a.ssm_state + (int64_t)seq_slot(a.tab, ci.sq) * H * TP * TN + head_off;
-          float* copy = a.ws_state + (int64_t)((ci.seg0 + ci.nseg - 1) * P) * H * TP * TN + head_off;
+          const float* slot_ptr = a.ssm_state + (int64_t)seq_slot(a.tab, ci.sq) * H * TP * TN + head_off + row_off;
+          float* copy = a.ws_state + (int64_t)((ci.seg0 + ci.nseg - 1) * P) * H * TP * TN + head_off + row_off;
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const float hv = slot_ptr[(int64_t)(16 * cg + i) * TN + row];
-            copy[(int64_t)(16 * cg + i) * TN + row] = hv;
-            dst[(int64_t)(16 * cg + i) * TN + row] = fmaf(d, hv, dhi[i] + dlo[i]);
+          for (int e = 0; e < 32; e += 4) {
+            const float4 hv = *reinterpret_cast<const float4*>(slot_ptr + e);
+            *reinterpret_cast<float4*>(copy + e) = hv;
+            *reinterpret_cast<float4*>(dst + e) = make_float4(fmaf(d, hv.x, dsum[e]), fmaf(d, hv.y, dsum[e + 1]),
+                                                              fmaf(d, hv.z, dsum[e + 2]), fmaf(d, hv.w, dsum[e + 3]));
           }
         } else {
 #pragma unroll
-          for (int i = 0; i < 16; ++i) dst[(int64_t)(16 * cg + i) * TN + row] = dhi[i] + dlo[i];
+          for (int e = 0; e < 32; e += 4)
+            *reinterpret_cast<float4*>(dst + e) = make_float4(dsum[e], dsum[e + 1], dsum[e + 2], dsum[e + 3]);
         }
-        if (tid == 0) a.ws_decay[(int64_t)entry * H + h] = Rt * 0.6931471805599453f;
       }
+      if (tid == 0)
+        for (int hh = 0; hh < nh; ++hh) a.ws_decay[(int64_t)entry * H + h0 + hh] = s_R[hh] * 0.6931471805599453f;
     }
   } else if (warp == kMathWarps) {
-    // =================== X tile loads of both heads: stage i % 2 is free once the product of chunk i - 2 is done
+    // =================== X tile loads of both heads: stage i % 3 is free once X o w of chunk i - 3 is formed
     int loaded = 0;
     for (int i = 0; i < n; ++i) {
-      if (i >= kStStages && !warp_wait(bar(kStDHDone + (i & 1)), p2(i - kStStages), s_abort)) break;
-      load_tile(stg_x(i), chunk_src(i), &tm, use_tma != 0, ci.x_col, TP, bar(kStFullX + (i & 1)), lane);
-      load_tile(stg_x(i) + kStHeadTile, chunk_src(i), &tm, use_tma != 0, x_col1, TP, bar(kStFullX + (i & 1)), lane);
+      if (i >= kStStages && !warp_wait(bar(kStXFree + i % kStStages), p3(i - kStStages), s_abort)) break;
+      load_tile(stg_x(i), chunk_src(i), &tm, use_tma != 0, ci.x_col, TP, bar(kStFullX + i % kStStages), lane);
+      load_tile(stg_x(i) + kTileX, chunk_src(i), &tm, use_tma != 0, x_col1, TP, bar(kStFullX + i % kStStages), lane);
       loaded = i + 1;
     }
     if (lane == 0 && *s_abort)
-      for (int i = max(0, loaded - kStStages); i < loaded; ++i) drain_bar(bar(kStFullX + (i & 1)), p2(i));
+      for (int i = max(0, loaded - kStStages); i < loaded; ++i) drain_bar(bar(kStFullX + i % kStStages), p3(i));
   } else if (warp == kMathWarps + 1) {
-    // =================== B tile loads: stage i % 2 is free once the product of chunk i - 2 is done
+    // =================== B tile loads: stage i % 3 is free once the products of chunk i - 3 are done
     int loaded = 0;
     for (int i = 0; i < n; ++i) {
-      if (i >= 2 && !warp_wait(bar(kStDHDone + (i & 1)), p2(i - 2), s_abort)) break;
-      load_tile(stg_b(i), chunk_src(i), &tm, use_tma != 0, ci.b_col, TN, bar(kStFullB + (i & 1)), lane);
+      if (i >= kStStages && !warp_wait(bar(kStBFree + i % kStStages), p3(i - kStStages), s_abort)) break;
+      load_tile(stg_b(i), chunk_src(i), &tm, use_tma != 0, ci.b_col, TN, bar(kStFullB + i % kStStages), lane);
       loaded = i + 1;
     }
     if (lane == 0 && *s_abort)
-      for (int i = max(0, loaded - 2); i < loaded; ++i) drain_bar(bar(kStFullB + (i & 1)), p2(i));
-  } else if (warp == kMathWarps + 2) {
-    // =================== dH^T += B^T . [X o w hi | lo | hi | lo] (one N=256 product per chunk)
+      for (int i = max(0, loaded - kStStages); i < loaded; ++i) drain_bar(bar(kStFullB + i % kStStages), p3(i));
+  } else if (warp == kMathWarps + 2 || warp == kMathWarps + 4) {
+    // =================== D += (X o w)^T . B, the hi part from one thread and the lo
+    // part from another (two accumulators, summed at the end)
     if (lane == 0) {
+      const bool lo = warp == kMathWarps + 4;
+      const uint32_t dcol = lo ? kStColDLo : kStColDHi, acol = kStColXW + (lo ? 64u : 0u);
       int last = -1;
       for (int i = 0; i < n; ++i) {
-        if (!wait_bar(bar(kStFullB + (i & 1)), p2(i), s_abort)) break;
+        if (!wait_bar(bar(kStFullB + i % kStStages), p3(i), s_abort)) break;
         if (!wait_bar(bar(kStXWReady + (i & 1)), p2(i), s_abort)) break;
         tc_fence_after();
-        const uint64_t bt0 = sdesc(stg_b(i), TQ * 128, 1024);
-        const uint64_t xw0 = sdesc(stg_x(i), kTileX, 1024);  // four 64-column blocks 16 KB apart
+        const uint64_t b0 = sdesc(stg_b(i), TQ * 128, 1024);
+        const uint32_t a0 = tmem + acol + 128u * (uint32_t)(i & 1);
 #pragma unroll
-        for (int s2 = 0; s2 < TQ / 16; ++s2) {
-          const uint32_t jk = (s2 * 2048) >> 4;
-          mma_ss(tmem, bt0 + jk, xw0 + jk, idesc128(256, 1, 1), (i > 0 || s2 > 0) ? 1u : 0u);
-        }
+        for (int s2 = 0; s2 < TQ / 16; ++s2)
+          mma_ts(tmem + dcol, a0 + 8u * (uint32_t)s2, b0 + ((s2 * 2048) >> 4), idesc128(TN, 0, 1),
+                 (i > 0 || s2 > 0) ? 1u : 0u);
         mma_commit(bar(kStDHDone + (i & 1)));
+        mma_commit(bar(kStBFree + i % kStStages));
         last = i;
       }
       if (last >= 0) drain_bar(bar(kStDHDone + (last & 1)), p2(last));
@@ -1189,7 +1224,7 @@ ssd_tc_state(const __grid_constant__ ScanArgs a, const __grid_constant__ CUtenso
   tc_fence_before();
   __syncthreads();
   if (tid == 0 && *s_abort) atomicAdd(&g_tc_timeouts, 1u);
-  if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 256;" :: "r"(tmem));
+  if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;" :: "r"(tmem));
 }
 
 // Tensor map over xbc [rows][conv_dim] bf16: boxes of 64 columns x TQ rows,
