@@ -26,6 +26,16 @@ mamba2_status cuda_fail(cudaError_t e) {
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+// the streamed prefill's internal copy streams and events, kept per host thread and
+// CUDA context (see mamba2_prefill_host)
+struct CopyLanes {
+  unsigned long long ctx;
+  cudaStream_t s_in, s_out;
+  cudaEvent_t ev[9];
+};
+// the driver's ID of the current CUDA context (unique for the life of the process,
+// never reused); false when there is none or the driver cannot say
+bool current_context_id(unsigned long long* id);
 
 size_t act_size(mamba2_dtype a) { return a == MAMBA2_F32 ? 4 : 2; }
 bool act_ok(mamba2_dtype a) { return a == MAMBA2_F32 || a == MAMBA2_BF16; }
@@ -771,23 +781,49 @@ mamba2_status mamba2_prefill_host(void* out_host, const void* xBC_host, const vo
   if (!workspace || workspace_bytes < L.total) return MAMBA2_ERR_WORKSPACE_TOO_SMALL;
   if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return MAMBA2_ERR_INVALID_ARGUMENT;
 
-  // ---- two copy streams and their events, made for this call and released at its end
-  // (destruction waits for the work already enqueued on them)
-  cudaStream_t cs = static_cast<cudaStream_t>(stream), s_in = nullptr, s_out = nullptr;
-  cudaEvent_t ev[9] = {};  // start, in_ready[2], in_free[2], out_ready[2], out_free[2]
+  // ---- two copy streams and their events: made on a host thread's first call in a
+  // CUDA context and kept for that thread (a new context, as after a device reset, gets
+  // new ones), so a call creates nothing; without a context ID to key on, each call
+  // makes its own and releases them at its end (destruction waits for the work already
+  // enqueued on them). Every use is stream-ordered, so a later call may re-record an
+  // event an earlier call's work has yet to reach.
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  CopyLanes lanes = {};
+  bool cached = false;
+  static thread_local std::vector<CopyLanes> t_lanes;
+  unsigned long long ctx = 0;
+  const bool keyed = current_context_id(&ctx);
+  if (keyed)
+    for (const CopyLanes& l : t_lanes)
+      if (l.ctx == ctx) {
+        lanes = l;
+        cached = true;
+        break;
+      }
   auto release = [&]() {
-    for (cudaEvent_t& e : ev)
-      if (e) cudaEventDestroy(e);
-    if (s_in) cudaStreamDestroy(s_in);
-    if (s_out) cudaStreamDestroy(s_out);
+    if (cached) return;
+    for (cudaEvent_t& ev : lanes.ev)
+      if (ev) cudaEventDestroy(ev);
+    if (lanes.s_in) cudaStreamDestroy(lanes.s_in);
+    if (lanes.s_out) cudaStreamDestroy(lanes.s_out);
   };
-  cudaError_t e = cudaStreamCreateWithFlags(&s_in, cudaStreamNonBlocking);
-  if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&s_out, cudaStreamNonBlocking);
-  for (int i = 0; i < 9 && e == cudaSuccess; ++i) e = cudaEventCreateWithFlags(&ev[i], cudaEventDisableTiming);
-  if (e != cudaSuccess) {
-    release();
-    return cuda_fail(e);
+  cudaError_t e = cudaSuccess;
+  if (!cached) {
+    e = cudaStreamCreateWithFlags(&lanes.s_in, cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&lanes.s_out, cudaStreamNonBlocking);
+    for (int i = 0; i < 9 && e == cudaSuccess; ++i) e = cudaEventCreateWithFlags(&lanes.ev[i], cudaEventDisableTiming);
+    if (e != cudaSuccess) {
+      release();
+      return cuda_fail(e);
+    }
+    if (keyed) {
+      lanes.ctx = ctx;
+      t_lanes.push_back(lanes);
+      cached = true;
+    }
   }
+  cudaStream_t s_in = lanes.s_in, s_out = lanes.s_out;
+  cudaEvent_t* ev = lanes.ev;  // start, in_ready[2], in_free[2], out_ready[2], out_free[2]
   cudaEvent_t ev_start = ev[0], *in_ready = ev + 1, *in_free = ev + 3, *out_ready = ev + 5, *out_free = ev + 7;
 
   char* ws = static_cast<char*>(workspace);
@@ -886,20 +922,21 @@ Fn driver_fn(const char* name) {
   return reinterpret_cast<Fn>(fn);
 }
 
+bool current_context_id(unsigned long long* id) {
+  static const CtxGetCurrentFn get_current = driver_fn<CtxGetCurrentFn>("cuCtxGetCurrent");
+  static const CtxGetIdFn get_id = driver_fn<CtxGetIdFn>("cuCtxGetId");
+  CUcontext ctx = nullptr;
+  return get_current && get_id && get_current(&ctx) == CUDA_SUCCESS && ctx && get_id(ctx, id) == CUDA_SUCCESS;
+}
+
 // Device address of g_scan_scratch in the current context. The first call in
 // each context looks it up with cudaGetSymbolAddress (which also makes the
 // current device's primary context current if none is); later calls in the
 // same context take it from the cache.
 mamba2_status scan_scratch_address(void** out) {
-  static const CtxGetCurrentFn get_current = driver_fn<CtxGetCurrentFn>("cuCtxGetCurrent");
-  static const CtxGetIdFn get_id = driver_fn<CtxGetIdFn>("cuCtxGetId");
-  auto current_id = [&](unsigned long long* id) {
-    CUcontext ctx = nullptr;
-    return get_current && get_id && get_current(&ctx) == CUDA_SUCCESS && ctx && get_id(ctx, id) == CUDA_SUCCESS;
-  };
   std::lock_guard<std::mutex> lock(g_scratch_mutex);
   unsigned long long id = 0;
-  if (current_id(&id))
+  if (current_context_id(&id))
     for (int i = 0; i < g_scratch_entries; ++i)
       if (g_scratch_cache[i].ctx_id == id) {
         *out = g_scratch_cache[i].addr;
@@ -909,7 +946,7 @@ mamba2_status scan_scratch_address(void** out) {
   const cudaError_t e = cudaGetSymbolAddress(&p, g_scan_scratch);
   if (e != cudaSuccess) return cuda_fail(e);
   // without a context ID to key on, nothing is cached and every call looks the address up
-  if (current_id(&id) && g_scratch_entries < kMaxScratchEntries) g_scratch_cache[g_scratch_entries++] = {id, p};
+  if (current_context_id(&id) && g_scratch_entries < kMaxScratchEntries) g_scratch_cache[g_scratch_entries++] = {id, p};
   *out = p;
   return MAMBA2_OK;
 }
