@@ -339,9 +339,13 @@ size_t mamba2_prefill_host_workspace_bytes(const mamba2_dims* dims, mamba2_dtype
  * Asynchronous like the other calls: it returns once everything is enqueued
  * and `stream` completes after the last output copy. Read out_host, and
  * reuse or free the host inputs and the workspace, only after that. The two
- * copy streams and their events are created by the call and released at its
- * end (their release waits for the enqueued work), so no state is kept
- * between calls. Errors: the checks of the three ops for the whole batch,
+ * internal copy streams and their nine events are created on a host thread's
+ * first call in a CUDA context and kept for that thread's later calls in the
+ * same context (a new context, as after a device reset, gets new ones); they
+ * hold no data between calls, and every use of them is ordered after the
+ * previous call's. Calls from one host thread on different caller streams
+ * therefore share those copy streams and run their copies one after the
+ * other. Errors: the checks of the three ops for the whole batch,
  * then MAMBA2_ERR_WORKSPACE_TOO_SMALL, all before anything is enqueued;
  * MAMBA2_ERR_CUDA if a copy, launch or stream/event creation fails.
  */
