@@ -19,8 +19,10 @@
  *  - Device buffers are caller-owned device pointers, row-major and
  *    contiguous, 16-byte aligned (mamba2_prefill_host alone takes its
  *    activations and output in host memory). The library allocates no device
- *    memory and keeps no state between calls; only `dst`, the named slots of
- *    the state pools and a caller-provided workspace are written.
+ *    memory and keeps no data between calls (the streamed prefill's copy
+ *    streams and the static scan scratch's address are kept, per context);
+ *    only `dst`, the named slots of the state pools and a caller-provided
+ *    workspace are written.
  *  - Batch metadata (mamba2_recurrent_batch) is HOST memory. It is validated
  *    on the host and passed to the kernels by value in their launch
  *    parameters, so the host arrays may be reused as soon as the call returns.
